@@ -1,0 +1,543 @@
+#!/usr/bin/env python
+"""Benchmark of the per-layer n-gram embedding (PLE / Engram) path on GB300.
+
+One step = one pass of the whole hot path over one batch: n-gram ids ->
+row gather -> kv_proj -> gate + short conv (four libple launches), on the
+8192-token prefill workload (16 ragged requests, 16 heads x 128 over an 8.2 GB
+bf16 table in HBM, hidden 4096, kv_proj 2048 -> 2 x 4096, conv K=4 d=3).
+Metric: PLE tokens/sec/layer (one step processes one layer).
+
+Steps rotate over 4 independent layer parameter sets (table, kv_proj weight,
+gammas, conv taps, hash multipliers, hidden states, token ids): one rotation
+touches far more than the 129 MB L2, so no step finds its inputs cached by an
+earlier one and no L2 flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill8k|decode256x4|tiny|uva32g|fp8x8]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step on one node's replicas); rank 0 prints one
+JSON line with the whole-job rate, timed as the max over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PLE tokens/sec/layer"
+UNIT = "tokens/s/layer"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NUM_SETS = 4
+KERNELS = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: barrier + max-over-ranks timing only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_setup(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value, device="cpu"):
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        peaks = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = data.get(key)
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v is not None:
+                peaks[key] = float(v)
+        if "hbm_gbs" in peaks and "bf16_tflops" in peaks:
+            return peaks, "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": float(np.median(power)) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """dram bytes per launch from the committed ncu summary of ``kernel``,
+    or None when the summary is missing or the kernel source changed since."""
+    summary = os.path.join(ROOT, "profiles", f"{kernel}_prefill8k.md")
+    src = os.path.join(ROOT, "hashed_gram_embedding_gb300", "csrc",
+                       {"kv_proj": "kv_proj.cu", "lookup": "lookup.cu",
+                        "gate_conv": "gate_conv.cu", "ngram_ids": "ngram_ids.cu"}[kernel])
+    try:
+        text = open(summary).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("source_sha256", "dram_bytes_per_launch")):
+            k, _, v = line.strip().partition(":")
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256") != source_hash(src):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workload set-up
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(w):
+    """Bytes (or flops) one launch of each kernel must move (or do)."""
+    T, H, D, C, E = w.num_tokens, w.num_heads, w.head_dim, w.hidden, w.emb_dim
+    elem = 1 if w.table_dtype == "fp8" else 2
+    row_read = H * D * elem + (H * 4 if w.table_dtype == "fp8" else 0)
+    return {
+        "ngram_ids": ("hbm", T * 4 + T * H * 8 + (w.num_reqs + 1) * 4),
+        "lookup": ("hbm", T * (H * 8 + row_read + H * D * 2)),
+        "kv_proj": ("tensor", 2.0 * T * E * 2 * C),
+        "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2)),
+    }
+
+
+def make_sets(torch, w, device, num_sets):
+    from hashed_gram_embedding_gb300 import workloads as wl
+    sets = []
+    for s in range(num_sets):
+        host = wl.host_inputs(w, step=s)
+        dense = wl.dense_inputs(torch, w, device, layer=s, step=s, random_gamma=True)
+        table, row_scale = wl.make_table(torch, w, device, layer=s)
+        sets.append({
+            "host": host,
+            "input_ids": torch.from_numpy(host["input_ids"]).to(device),
+            "qsl": torch.from_numpy(host["query_start_loc"]).to(device),
+            "ctx": None if host["ngram_context"] is None else torch.from_numpy(host["ngram_context"]).to(device),
+            "mult": wl.layer_multipliers(w, s),
+            "table": table, "row_scale": row_scale, **dense,
+        })
+    return sets
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from hashed_gram_embedding_gb300 import build as build_mod
+    from hashed_gram_embedding_gb300 import _lib
+    from hashed_gram_embedding_gb300 import workloads as wl
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist_setup("nccl")
+    if rank == 0 or not os.path.exists(_lib.LIB_PATH):
+        build_mod.build()
+    barrier()
+
+    w = wl.WORKLOADS[args.workload]
+    # one step = one layer; multi-layer workloads rotate over their layers
+    num_sets = w.num_layers if w.num_layers > 1 else (NUM_SETS if w.table_loc == "hbm" else 1)
+    sets = make_sets(torch, w, device, num_sets)
+    T, H, C = w.num_tokens, w.num_heads, w.hidden
+    ids = torch.empty((T, H), dtype=torch.int64, device=device)
+    emb = torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device)
+    kv = torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device)
+    y = torch.empty((T, C), dtype=torch.bfloat16, device=device)
+    ctx_out = torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device)
+    st_out = (torch.empty_like(sets[0]["conv_state"]) if w.decode else None)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(s, ev=None):
+        p = sets[s % num_sets]
+        if ev is not None:
+            ev[0].record(stream)
+        _lib.ple_ngram_ids(p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"],
+                           p["host"]["O"], w.eos_token_id, w.heads_per_ngram, ids,
+                           ctx_out if w.decode else None, err, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"],
+                           w.dilation, y, conv_state=p.get("conv_state"), conv_state_out=st_out,
+                           dev_err=err, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+
+    # ---- timed region: K steps, device events on the launching stream ----
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(i, events[i])
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = events[0][0].elapsed_time(events[-1][4])
+    per_kernel = {k: [] for k in KERNELS}
+    for ev in events:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k].append(ev[j].elapsed_time(ev[j + 1]))
+    total_ms = max_over_ranks(total_ms, device)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+
+    # ---- end to end through PLELayer with host buffers ----
+    from hashed_gram_embedding_gb300 import PLELayer
+    p0 = sets[0]
+    layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
+                     w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
+                     p0["conv_w"], w.dilation)
+    h_ids = torch.from_numpy(p0["host"]["input_ids"]).pin_memory()
+    h_qsl = torch.from_numpy(p0["host"]["query_start_loc"]).pin_memory()
+    h_hidden = p0["hidden"].cpu().pin_memory()
+    h_y = torch.empty((T, C), dtype=torch.bfloat16).pin_memory()
+    d_ids = torch.empty_like(p0["input_ids"])
+    d_qsl = torch.empty_like(p0["qsl"])
+    d_hidden = torch.empty_like(p0["hidden"])
+    h2d = h_ids.numel() * 4 + h_qsl.numel() * 4 + h_hidden.numel() * 2
+    d2h = h_y.numel() * 2
+
+    def e2e_step():
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_qsl.copy_(h_qsl, non_blocking=True)
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        out = layer.forward(d_ids, d_qsl, d_hidden, ngram_context=p0["ctx"],
+                            ngram_context_out=ctx_out if w.decode else None,
+                            conv_state=p0.get("conv_state"), conv_state_out=st_out,
+                            dev_err=err, stream=stream)
+        h_y.copy_(out, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3) or 1):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device)
+    clocks = sampler.stop()
+
+    if rank != 0:
+        return None
+    peaks, peak_kind = load_peaks()
+    work = algorithmic_work(w)
+    kernels = {}
+    for k in KERNELS:
+        avg_ms = float(np.mean(per_kernel[k]))
+        bound, amount = work[k]
+        if bound == "tensor":
+            achieved = amount / (avg_ms * 1e-3) / 1e12
+            peak = peaks["bf16_tflops"]
+            unit = "TFLOP/s"
+        else:
+            achieved = amount / (avg_ms * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        kernels[k] = {"us": round(avg_ms * 1e3, 2), "bound": bound, "achieved": round(achieved, 1),
+                      "unit": unit, "frac": round(achieved / peak, 4),
+                      "share": round(avg_ms / float(np.mean([sum(per_kernel[x][i] for x in KERNELS)
+                                                           for i in range(args.steps)])), 4)}
+    dominant = max(KERNELS, key=lambda k: kernels[k]["us"])
+    dk = kernels[dominant]
+    bound, amount = work[dominant]
+    traffic = ncu_traffic(dominant) if args.workload == "prefill8k" else None
+    roofline = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
+                "peak": peaks["bf16_tflops"] if dk["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": dk["unit"], "frac": dk["frac"], "peak_source": peak_kind,
+                "algorithmic_per_launch": amount, "traffic": traffic}
+    value = world * args.steps * T / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.table_dtype == "bf16" else "fp8->bf16",
+        "data": "synthetic (seeded workload recipe; no dataset)",
+        "config": {"workload": w.name, "num_tokens": T, "num_reqs": w.num_reqs, "heads": H,
+                   "head_dim": w.head_dim, "table_rows": int(sets[0]["table"].shape[0]),
+                   "table_loc": w.table_loc, "table_dtype": w.table_dtype, "hidden": C,
+                   "conv_kernel": w.conv_k, "dilation": w.dilation,
+                   "layer_sets": num_sets,
+                   "l2": f"inputs rotate over {num_sets} layer sets (> 129 MB L2 per rotation); no flush",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gather": {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]},
+        "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, p, req_range, max_tokens, bits):
+    """Time the oracle over requests req_range (truncated to max_tokens tokens)."""
+    import torch
+    import oracle
+
+    host = p["host"]
+    qsl = host["query_start_loc"]
+    r0, r1 = req_range
+    start, end = int(qsl[r0]), int(min(qsl[r1], qsl[r0] + max_tokens))
+    sub_qsl = [q - start for q in qsl[r0:r1 + 1]]
+    sub_qsl = [min(q, end - start) for q in sub_qsl]
+    tokens = host["input_ids"][start:end]
+    ctx = None if host["ngram_context"] is None else host["ngram_context"][r0:r1]
+    t = {}
+    t0 = time.perf_counter()
+    ids, _ = oracle.ngram_ids(tokens, sub_qsl, ctx, p["mult"], host["V"], host["O"],
+                              w.eos_token_id, w.heads_per_ngram)
+    t["ngram_ids"] = time.perf_counter() - t0
+    ids = np.asarray(ids, dtype=np.int64).reshape(len(tokens), -1)
+    # input staging, not timed: the rows the sample names, as a compact table
+    uniq, inv = np.unique(ids, return_inverse=True)
+    rows = p["table"][torch.from_numpy(uniq).to(p["table"].device)]
+    hidden = bits(p["hidden"][start:end])
+    w_kv, gh, gk, cw = (bits(p[k]) for k in ("w_kv", "gamma_h", "gamma_k", "conv_w"))
+    t0 = time.perf_counter()
+    if p["row_scale"] is None:
+        emb = oracle.lookup_bf16(inv.reshape(ids.shape), bits(rows))
+    else:
+        scale = p["row_scale"][torch.from_numpy(uniq).to(p["row_scale"].device)].cpu().numpy()
+        emb = oracle.lookup_fp8(inv.reshape(ids.shape), rows.cpu().numpy(), scale)
+    t["lookup"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    kv = oracle.kv_proj(emb, w_kv)
+    t["kv_proj"] = time.perf_counter() - t0
+    state = None if p.get("conv_state") is None else bits(p["conv_state"][r0:r1])
+    t0 = time.perf_counter()
+    oracle.gate_conv(hidden, kv, gh, gk, 1e-6, sub_qsl, cw, w.dilation, state)
+    t["gate_conv"] = time.perf_counter() - t0
+    return len(tokens), t
+
+
+def _bits(t):
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(w, p, budget_s=15.0):
+    """The oracle as it stands on this host, over whole requests until the
+    time budget is spent (at least one request)."""
+    qsl = p["host"]["query_start_loc"]
+    tokens = 0
+    stages = {k: 0.0 for k in KERNELS}
+    r = 0
+    while r < len(qsl) - 1:
+        n, t = oracle_sample(w, p, (r, r + 1), 1 << 30, _bits)
+        tokens += n
+        for k in KERNELS:
+            stages[k] += t[k]
+        r += 1
+        if sum(stages.values()) > budget_s:
+            break
+    total = sum(stages.values())
+    return {"value": round(tokens / total, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"requests 0..{r - 1} of {w.name} ({tokens} of {w.num_tokens} tokens), "
+                      f"float64 NumPy / Python-int oracle, inputs staged outside the timed region",
+            "stage_seconds": {k: round(v, 3) for k, v in stages.items()}}
+
+
+def run_reference(args):
+    """The reference arm: the oracle timed on the host cores, rank 0 only."""
+    import torch
+    from hashed_gram_embedding_gb300 import workloads as wl
+
+    rank, world, local_rank = dist_env()
+    if rank != 0:
+        return None
+    device = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    w = wl.WORKLOADS[args.workload]
+    p = make_sets(torch, w, device, 1)[0]
+    qsl = p["host"]["query_start_loc"]
+    max_tokens = args.ref_tokens
+    times = []
+    toks = []
+    for i in range(args.warmup + args.steps):
+        r = i % (len(qsl) - 1)
+        n, t = oracle_sample(w, p, (r, r + 1), max_tokens, _bits)
+        if i >= args.warmup:
+            times.append(sum(t.values()))
+            toks.append(n)
+    total_s = sum(times)
+    value = sum(toks) / total_s
+    sample = (f"per step one request of {w.name} truncated to {max_tokens} tokens "
+              f"({int(np.mean(toks))} tokens on average)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_s * 1e3 / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded workload recipe; no dataset)",
+            "config": {"workload": w.name, "num_tokens": w.num_tokens, "num_reqs": w.num_reqs,
+                       "parallelism": "single"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill8k")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

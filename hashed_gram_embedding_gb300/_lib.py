@@ -1,0 +1,182 @@
+"""ctypes binding of libple (the C ABI declared in include/ple.h).
+
+Argument marshalling only: every step of the path runs in libple's CUDA
+kernels. Functions take torch tensors for device buffers (their data
+pointers are passed through) and raise PleError on a non-OK status. There is
+no fallback: if libple.so is missing the first call raises.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libple.so")
+
+PLE_OK = 0
+PLE_ERR_INVALID_ARG = 1
+PLE_ERR_UNSUPPORTED = 2
+PLE_ERR_CUDA = 3
+PLE_ERR_TIMEOUT = 4
+PLE_ERR_BOUNDS = 5
+STATUS_NAMES = {0: "PLE_OK", 1: "PLE_ERR_INVALID_ARG", 2: "PLE_ERR_UNSUPPORTED",
+                3: "PLE_ERR_CUDA", 4: "PLE_ERR_TIMEOUT", 5: "PLE_ERR_BOUNDS"}
+
+PLE_DEVERR_BOUNDS = 1
+PLE_DEVERR_QSL = 2
+PLE_DEVERR_TIMEOUT = 4
+
+PLE_BF16 = 0
+PLE_FP8_E4M3 = 1
+PLE_HBM = 0
+PLE_HOST_UVA = 1
+
+# Every entry point of include/ple.h with its ctypes signature.
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F32 = ctypes.c_float
+_I64P = ctypes.POINTER(ctypes.c_int64)
+SIGNATURES = {
+    "ple_ngram_ids": [_P, _I64, _P, _I32, _P, _I32, _I64P, _I64P, _I64P, _I32, _I32, _P, _P, _P, _P],
+    "ple_lookup": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32, _P, _P],
+    "ple_lookup_prefetch": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32,
+                            _P, _P, _P],
+    "ple_wait": [_P, _P, _I32],
+    "ple_kv_proj": [_P, _P, _I64, _I32, _I32, _P, _P, _P],
+    "ple_gate": [_P, _P, _P, _P, _F32, _I64, _I32, _P, _P, _P],
+    "ple_conv": [_P, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P],
+    "ple_gate_conv": [_P, _P, _P, _P, _F32, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P],
+    "ple_last_error": [],
+    "ple_version": [],
+}
+
+
+class PleError(RuntimeError):
+    def __init__(self, func, status, detail):
+        self.status = status
+        super().__init__(f"{func} -> {STATUS_NAMES.get(status, status)}: {detail}")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libple (built in-tree); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m hashed_gram_embedding_gb300.build` (there is no non-CUDA path)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, args in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_char_p if name in ("ple_last_error", "ple_version") else ctypes.c_int
+        _lib = handle
+    return _lib
+
+
+def _check(name, status):
+    if status != PLE_OK:
+        detail = lib().ple_last_error().decode(errors="replace")
+        raise PleError(name, status, detail)
+    return status
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _i64_array(values):
+    a = np.ascontiguousarray(np.asarray(values, dtype=np.int64))
+    return a, a.ctypes.data_as(_I64P)
+
+
+def ple_ngram_ids(input_ids, query_start_loc, ngram_context, layer_multipliers,
+                  vocab_sizes, offsets, eos_token_id, heads_per_ngram, out,
+                  ngram_context_out=None, dev_err=None, stream=None):
+    """Device tensors: input_ids int32 [T], query_start_loc int32 [R+1],
+    ngram_context int32 [R, L] or None, out int64 [T, H], ngram_context_out
+    int32 [R, L] or None, dev_err int32 [1] or None. Host arrays:
+    layer_multipliers [L+1], vocab_sizes [H], offsets [H] (int64)."""
+    mult, mult_p = _i64_array(layer_multipliers)
+    V, V_p = _i64_array(vocab_sizes)
+    O, O_p = _i64_array(offsets)
+    return _check("ple_ngram_ids", lib().ple_ngram_ids(
+        _ptr(input_ids), input_ids.numel(), _ptr(query_start_loc), query_start_loc.numel() - 1,
+        _ptr(ngram_context), len(mult) - 1, mult_p, V_p, O_p, int(eos_token_id),
+        int(heads_per_ngram), _ptr(out), _ptr(ngram_context_out), _ptr(dev_err), _stream(stream)))
+
+
+def _lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc):
+    dtype = PLE_FP8_E4M3 if row_scale is not None else PLE_BF16
+    if loc is None:
+        loc = PLE_HBM if table.is_cuda else PLE_HOST_UVA
+    T, H = ids.shape
+    return (_ptr(ids), T, H, _ptr(table), table.shape[0], table.shape[1], dtype, _ptr(row_scale),
+            loc, _ptr(out), int(max_ctas), _ptr(dev_err))
+
+
+def ple_lookup(ids, table, out, row_scale=None, max_ctas=0, dev_err=None, loc=None, stream=None):
+    """ids int64 [T, H]; table [rows, D] bf16 (or uint8 e4m3 codes with
+    row_scale float32 [rows]), on the device or pinned on the host; out bf16
+    [T, H*D]."""
+    return _check("ple_lookup", lib().ple_lookup(
+        *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
+
+
+def ple_lookup_prefetch(ids, table, out, side_stream, done_event, row_scale=None, max_ctas=0,
+                        dev_err=None, loc=None):
+    """ple_lookup on ``side_stream``, then ``done_event`` (torch.cuda.Event) recorded there."""
+    return _check("ple_lookup_prefetch", lib().ple_lookup_prefetch(
+        *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc),
+        ctypes.c_void_p(side_stream.cuda_stream), ctypes.c_void_p(done_event.cuda_event)))
+
+
+def ple_wait(done_event, consumer_stream=None, timeout_ms=0):
+    return _check("ple_wait", lib().ple_wait(ctypes.c_void_p(done_event.cuda_event),
+                                             _stream(consumer_stream), int(timeout_ms)))
+
+
+def ple_kv_proj(emb, w, kv, dev_err=None, stream=None):
+    """emb bf16 [T, E], w bf16 [2C, E], kv bf16 [T, 2C]."""
+    T, E = emb.shape
+    return _check("ple_kv_proj", lib().ple_kv_proj(
+        _ptr(emb), _ptr(w), T, E, w.shape[0] // 2, _ptr(kv), _ptr(dev_err), _stream(stream)))
+
+
+def ple_gate(hidden, kv, gamma_h, gamma_k, out, eps=1e-6, gate_out=None, stream=None):
+    T, C = hidden.shape
+    return _check("ple_gate", lib().ple_gate(
+        _ptr(hidden), _ptr(kv), _ptr(gamma_h), _ptr(gamma_k), float(eps), T, C, _ptr(out),
+        _ptr(gate_out), _stream(stream)))
+
+
+def ple_conv(x, query_start_loc, w, dilation, out, conv_state=None, conv_state_out=None,
+             dev_err=None, stream=None):
+    T, C = x.shape
+    return _check("ple_conv", lib().ple_conv(
+        _ptr(x), _ptr(query_start_loc), query_start_loc.numel() - 1, T, C, _ptr(w), w.shape[1],
+        int(dilation), _ptr(conv_state), _ptr(conv_state_out), _ptr(out), _ptr(dev_err),
+        _stream(stream)))
+
+
+def ple_gate_conv(hidden, kv, gamma_h, gamma_k, query_start_loc, w, dilation, out, eps=1e-6,
+                  conv_state=None, conv_state_out=None, gate_out=None, dev_err=None, stream=None):
+    T, C = hidden.shape
+    return _check("ple_gate_conv", lib().ple_gate_conv(
+        _ptr(hidden), _ptr(kv), _ptr(gamma_h), _ptr(gamma_k), float(eps), _ptr(query_start_loc),
+        query_start_loc.numel() - 1, T, C, _ptr(w), w.shape[1], int(dilation), _ptr(conv_state),
+        _ptr(conv_state_out), _ptr(out), _ptr(gate_out), _ptr(dev_err), _stream(stream)))
+
+
+def ple_version():
+    return lib().ple_version().decode()

@@ -1,0 +1,397 @@
+// ple_kv_proj: the merged key/value projection kv = emb @ W^T on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
+// operands staged by TMA.
+//
+// Source: PR#54517 report ("Fuse Qwen4Exp PLE kernels"), 实现拆解 item 1:
+// key_proj and value_proj merged into one MergedColumnParallelLinear, so one
+// GEMM [T, E] x [2C, E]^T produces k (columns [0, C)) and v ([C, 2C)).
+//
+// Design (dense contraction, tensor-bound at serving sizes):
+//   * CTA tile 128 x 256 (M x N), K step 64 = one 128-byte swizzle atom of
+//     bf16. A = emb and B = W are both K-major, exactly the canonical
+//     SWIZZLE_128B K-major layout TMA writes and tcgen05 reads, so no
+//     transposes anywhere. tcgen05.mma.cta_group::1.kind::f16, M=128 N=256
+//     K=16, fp32 accumulate.
+//   * 4-stage smem ring (48 KB per stage) fed by TMA; mbarriers full/empty.
+//   * Persistent: one CTA per SM walks tiles tile = blockIdx.x + i*gridDim.x
+//     (consecutive CTAs share A rows; all of W stays hot in the 129 MB L2).
+//   * Two 256-column fp32 accumulators in TMEM (all 512 columns): the
+//     epilogue of tile i drains one while the MMAs of tile i+1 fill the other.
+//   * Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and
+//     lane 0 issues MMAs, warps 2-5 (one per TMEM lane quadrant) read the
+//     accumulator with tcgen05.ld, round to bf16 and store rows to global.
+//   * Every mbarrier wait is bounded (1 s of %globaltimer). On expiry the
+//     kernel raises PLE_DEVERR_TIMEOUT, stops issuing, waits (bounded) for its
+//     own TMA copies and MMAs in flight, frees TMEM and returns.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace ple {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int A_STAGE = BM * BK * 2;     // 16 KB
+constexpr int B_STAGE = BN * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int ACC_COLS = BN;             // fp32 columns per accumulator
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr int kNumBars = 2 * STAGES + 4 + 1;
+constexpr size_t kSmemBytes = size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
+// B bf16 (10-12 = 1), A and B K-major (15, 16 = 0), N >> 3 at 17-22,
+// M >> 4 at 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete. Gives up after
+// kWaitLimitNs, or early when `abort_flag` is set (if non-null).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                       const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// tile whose rows are 128 bytes and whose 8-row groups are 1024 bytes apart:
+// start address >> 4 (bits 0-13), leading byte offset (16-29; not used by
+// swizzled K-major layouts, set to 1), stride byte offset 1024 >> 4 (32-45),
+// fixed 0b001 at 46-48, base offset 0 (tiles are 1024-byte aligned),
+// swizzle mode 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      // the wait sits in the same statement so no use of r[] can move above it
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               ple_bf16_t* __restrict__ out, int M, int N, int K, int32_t* dev_err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* a_smem = smem;
+  uint8_t* b_smem = smem + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = (N + BN - 1) / BN;
+  const int num_tiles = ((M + BM - 1) / BM) * n_tiles;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpilogueThreads);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;        // stages holding a copy this thread issued
+    uint32_t armed_parity = 0; // parity of that copy's full-barrier phase
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles) * BM;
+      const int n0 = (tile % n_tiles) * BN;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+        tma_load_2d(smem_u32(a_smem + stage * A_STAGE), &map_a, full_bar(stage), kb * BK, m0);
+        tma_load_2d(smem_u32(b_smem + stage * B_STAGE), &map_b, full_bar(stage), kb * BK, n0);
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+    // Never leave with a copy in flight into this CTA's shared memory.
+    for (int s = 0; s < STAGES; ++s)
+      if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u, nullptr);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_desc(smem_u32(a_smem + stage * A_STAGE));
+          const uint64_t b_desc = sw128_desc(smem_u32(b_smem + stage * B_STAGE));
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advance 16 elements (32 bytes) along K inside the swizzle atom
+            const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
+            umma_bf16(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(acc));        // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+      // Every MMA this thread issued has completed once done_bar flips.
+      umma_commit(done_bar);
+      mbar_wait(done_bar, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> bf16 -> global ----------------
+    const int quad = warp & 3;                 // TMEM lanes this warp may read
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag));
+      if (!ok) {
+        if (lane == 0) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+        break;
+      }
+      tc_fence_after();
+      const int m = (tile / n_tiles) * BM + row_in_tile;
+      const int n_base = (tile % n_tiles) * BN;
+      ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
+#pragma unroll 1
+      for (int chunk = 0; chunk < BN / 32; ++chunk) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                      static_cast<uint32_t>(acc * ACC_COLS + chunk * 32),
+                  r);
+        const int n = n_base + chunk * 32;
+        if (m < M && n < N) {
+          uint4* dst = reinterpret_cast<uint4*>(row_out + n);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(r[8 * q + 0], r[8 * q + 1]);
+            v.y = pack_bf16x2(r[8 * q + 2], r[8 * q + 3]);
+            v.z = pack_bf16x2(r[8 * q + 4], r[8 * q + 5]);
+            v.w = pack_bf16x2(r[8 * q + 6], r[8 * q + 7]);
+            dst[q] = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acce_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D K-major bf16 matrix [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
+ple_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return fail(PLE_ERR_CUDA, "ple_kv_proj: cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                      strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PLE_ERR_CUDA, "ple_kv_proj: cuTensorMapEncodeTiled failed (%d)",
+                                     static_cast<int>(r));
+  return PLE_OK;
+}
+
+}  // namespace
+}  // namespace ple
+
+PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, int64_t num_tokens,
+                                  int32_t emb_dim, int32_t hidden, ple_bf16_t* kv,
+                                  int32_t* dev_err, cudaStream_t stream) {
+  using namespace ple;
+  if (num_tokens < 0 || emb_dim < 1 || hidden < 1)
+    return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: bad sizes");
+  if (emb_dim % 8 != 0 || hidden % 16 != 0)
+    return fail(PLE_ERR_UNSUPPORTED, "ple_kv_proj: emb_dim %% 8 and hidden %% 16 must be 0");
+  if (num_tokens > 0x7fffffffLL - BM || 2LL * hidden > 0x7fffffffLL)
+    return fail(PLE_ERR_UNSUPPORTED, "ple_kv_proj: sizes exceed 32-bit tile indexing");
+  if (num_tokens == 0) return PLE_OK;
+  if (!emb || !w || !kv) return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: null pointer");
+  if (!aligned16(emb) || !aligned16(w) || !aligned16(kv))
+    return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: buffers must be 16-byte aligned");
+  const int M = static_cast<int>(num_tokens);
+  const int N = 2 * hidden;
+  const int K = emb_dim;
+  CUtensorMap map_a, map_b;
+  ple_status s = make_map(&map_a, emb, M, K, BM);
+  if (s != PLE_OK) return s;
+  s = make_map(&map_b, w, N, K, BN);
+  if (s != PLE_OK) return s;
+  cudaError_t err = cudaFuncSetAttribute(kv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+  if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj: smem attribute");
+  const int num_tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = num_tiles < num_sms() ? num_tiles : num_sms();
+  kv_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, kv, M, N, K, dev_err);
+  return check_cuda(cudaGetLastError(), "ple_kv_proj launch");
+}

@@ -1,0 +1,275 @@
+/*
+ * ple.h -- C ABI of libple: the per-layer n-gram embedding (PLE / Engram)
+ * lookup path for one GB300 (sm_103a) GPU.
+ *
+ * The path (one transformer layer):
+ *   ple_ngram_ids  ragged n-gram hash ids        -> ids [T][H] int64
+ *   ple_lookup     multi-head row gather         -> emb [T][H*D] bf16
+ *   ple_kv_proj    merged key/value projection   -> kv  [T][2C] bf16
+ *   ple_gate_conv  RMSNorm + sigmoid gate, then the dilated causal depthwise
+ *                  short conv                    -> y   [T][C] bf16
+ * with ple_gate / ple_conv as the two halves of ple_gate_conv, and
+ * ple_lookup_prefetch / ple_wait for a gather on a side stream (a table in
+ * pinned host memory read over UVA, overlapped with other work).
+ *
+ * Sources (page titles abbreviated):
+ *   PR#54517 report "[Qwen3.8-Flash-Next] Fuse Qwen4Exp PLE kernels":
+ *     section 关键源码片段 (compute_ngram_ids and its CPU branch; the
+ *     _ple_ngram_ids_kernel signature and skeleton), 实现拆解 items 1, 2, 4
+ *     (merged kv_proj; ple_ngram_ids / ple_gate / ple_conv; short-conv state).
+ *   PR#54371 report "[Qwen4Exp] Support UVA PLE-offload and Engram tensor
+ *     parallelism": 实现拆解 items 1 and 4, 关键源码片段 (device and
+ *     pinned-host embedding backends, start_prefetch, BF16/FP8 weights).
+ *   PR#56512 report "[DS V4.1][Engram] Support async prefetch ...":
+ *     功能与动机 and 实现拆解 item 4 (side-stream prefetch with a reduced grid,
+ *     the consumer waiting on the side stream), 关键源码片段 (pinned check).
+ *
+ * Conventions for every entry point:
+ *   - Buffers are caller-owned. Unless a comment says "host", a pointer is
+ *     device memory (or any memory the GPU can address, e.g. managed).
+ *     The one exception is the table of ple_lookup in PLE_HOST_UVA mode,
+ *     which must be pinned (cudaHostAlloc) or registered (cudaHostRegister)
+ *     host memory.
+ *   - Calls are asynchronous on the given stream (0 = legacy default stream)
+ *     and never synchronise it, except ple_wait with a host timeout.
+ *   - The library allocates no device or host memory and keeps no state
+ *     between calls other than the thread-local error text.
+ *   - bf16 data is passed as 16-bit containers (ple_bf16_t): IEEE binary32
+ *     truncated to its high half, row-major.
+ *   - A call returns PLE_OK when its work was enqueued. Argument errors found
+ *     on the host return PLE_ERR_INVALID_ARG / PLE_ERR_UNSUPPORTED and enqueue
+ *     nothing. Errors that only the GPU can see (an id outside the table,
+ *     invalid query_start_loc contents, a pipeline wait that gave up) are
+ *     OR-ed as PLE_DEVERR_* bits into the optional device word `dev_err`
+ *     (pass NULL to ignore them); the kernel then writes zeros for the
+ *     affected rows instead of touching memory out of range. The caller
+ *     clears *dev_err before the call when it wants a fresh reading.
+ *   - num_tokens == 0 is a no-op returning PLE_OK (a zero-token prefetch
+ *     returns early, PR#54371 report, start_prefetch); carry-over outputs
+ *     (ngram_context_out, conv_state_out) are then copied from their inputs.
+ *   - ple_last_error() gives a human-readable reason for the last non-OK
+ *     status returned on the calling host thread.
+ */
+#ifndef PLE_H_
+#define PLE_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ple_bf16_t;
+
+typedef enum {
+  PLE_OK = 0,
+  PLE_ERR_INVALID_ARG = 1,  /* bad pointer / size / layout found on the host */
+  PLE_ERR_UNSUPPORTED = 2,  /* valid but not handled (e.g. row not 16-byte sized) */
+  PLE_ERR_CUDA = 3,         /* a CUDA runtime call failed (text in ple_last_error) */
+  PLE_ERR_TIMEOUT = 4,      /* ple_wait gave up before the event completed */
+  PLE_ERR_BOUNDS = 5        /* reserved for callers mapping PLE_DEVERR_BOUNDS */
+} ple_status;
+
+/* Bits OR-ed into the optional device word `dev_err`. */
+#define PLE_DEVERR_BOUNDS 1   /* an id was outside [0, table_rows): row zeroed */
+#define PLE_DEVERR_QSL 2      /* query_start_loc not 0-based / non-decreasing / <= T */
+#define PLE_DEVERR_TIMEOUT 4  /* a kernel pipeline wait exceeded its limit */
+
+typedef enum { PLE_BF16 = 0, PLE_FP8_E4M3 = 1 } ple_dtype;
+typedef enum { PLE_HBM = 0, PLE_HOST_UVA = 1 } ple_table_loc;
+
+/* Limits of ple_ngram_ids (constants travel in the kernel's parameter block). */
+#define PLE_MAX_CTX_LEN 7     /* NGRAM_CONTEXT_LEN: n-gram orders 2 .. ctx_len + 1 */
+#define PLE_MAX_HEADS 64      /* ctx_len * heads_per_ngram */
+
+/*
+ * ple_ngram_ids -- ragged n-gram hash ids of every token.
+ * (PR#54517 report, 关键源码片段: compute_ngram_ids, _ple_ngram_ids_kernel.)
+ *
+ * For token t of request r, over r's virtual sequence
+ * S = ngram_context[r] ++ input_ids[segment of r] (history oldest first;
+ * NULL history = ctx_len EOS tokens, the EOS padding at request starts),
+ * with x_s the token s places back (s = 0 current):
+ *   - EOS crossing: an EOS at lag j >= 1 is kept, every lag > j becomes EOS;
+ *   - mixed_1 = x_0 * m_0 and mixed_{s+1} = mixed_s XOR (x_s * m_s), all in
+ *     wrapping int64 arithmetic (tokens are sign-extended int32);
+ *   - order n = s + 1 (s = 1 .. ctx_len) emits heads
+ *     h = (n - 2) * heads_per_ngram + j, j < heads_per_ngram:
+ *     out[t][h] = floor_mod(mixed_n, V_h) + O_h  (torch.remainder semantics).
+ * Token t belongs to the last request whose start is <= t, so empty requests
+ * own nothing and tokens at or past query_start_loc[num_reqs] continue the
+ * last request (padding of a captured graph).
+ *
+ *   input_ids          [num_tokens] int32, device.
+ *   query_start_loc    [num_reqs + 1] int32, device; must be 0 at [0],
+ *                      non-decreasing, and <= num_tokens at [num_reqs]
+ *                      (checked on the GPU -> PLE_DEVERR_QSL; ids are then
+ *                      still written, from clamped positions).
+ *   ngram_context      [num_reqs][ctx_len] int32 device, oldest first, or NULL.
+ *   ctx_len            1 .. PLE_MAX_CTX_LEN.
+ *   layer_multipliers  [ctx_len + 1] int64, HOST (copied at the call).
+ *   vocab_sizes        [H] int64 HOST, each >= 1; H = ctx_len * heads_per_ngram
+ *                      <= PLE_MAX_HEADS.
+ *   offsets            [H] int64 HOST.
+ *   out                [num_tokens][H] int64, device.
+ *   ngram_context_out  [num_reqs][ctx_len] int32 device or NULL: the last
+ *                      ctx_len tokens of each S (carry-over for the next step);
+ *                      must not overlap ngram_context (ping-pong two buffers).
+ *   dev_err            optional device word (see conventions).
+ * Errors: num_reqs < 1 with num_tokens > 0, bad sizes, overlapping
+ * context buffers, V_h < 1 -> PLE_ERR_INVALID_ARG.
+ */
+ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens,
+                         const int32_t* query_start_loc, int32_t num_reqs,
+                         const int32_t* ngram_context, int32_t ctx_len,
+                         const int64_t* layer_multipliers,
+                         const int64_t* vocab_sizes, const int64_t* offsets,
+                         int32_t eos_token_id, int32_t heads_per_ngram,
+                         int64_t* out, int32_t* ngram_context_out,
+                         int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * ple_lookup -- multi-head row gather, bf16 or fp8 e4m3 with a per-row scale.
+ * (PR#54371 report: device / pinned-host embedding backends, F.embedding;
+ * BF16 / FP8 weight methods. PR#53899 page: FP8 table with weight_scale.)
+ *
+ *   out[t][h*D + c] = table[ids[t][h]][c]                         (bf16)
+ *   out[t][h*D + c] = bf16_rn(float(e4m3(table[id][c])) * row_scale[id])  (fp8)
+ * A global scale is row_scale filled with one value.
+ *
+ *   ids          [num_tokens][num_heads] int64 device (offsets already added).
+ *   table        [table_rows][head_dim] (bf16 or uint8 e4m3 codes). In
+ *                PLE_HBM mode device memory; in PLE_HOST_UVA mode pinned or
+ *                registered host memory (checked with cudaPointerGetAttributes,
+ *                else PLE_ERR_INVALID_ARG), read in place over the host link.
+ *                16-byte aligned.
+ *   row_scale    [table_rows] float32 device, fp8 only (NULL for bf16).
+ *   out          [num_tokens][num_heads * head_dim] bf16 device, 16-byte aligned.
+ *   max_ctas     0 = a full-GPU grid; > 0 caps the grid (e.g. half the SMs
+ *                for a side-stream prefetch that overlaps other kernels).
+ * A row's byte size (head_dim * element size) must be a multiple of 16
+ * (else PLE_ERR_UNSUPPORTED). Ids outside [0, table_rows) give a zero row
+ * and PLE_DEVERR_BOUNDS.
+ */
+ple_status ple_lookup(const int64_t* ids, int64_t num_tokens, int32_t num_heads,
+                      const void* table, int64_t table_rows, int32_t head_dim,
+                      ple_dtype dtype, const float* row_scale,
+                      ple_table_loc loc, ple_bf16_t* out, int32_t max_ctas,
+                      int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * ple_lookup_prefetch -- ple_lookup enqueued on `side_stream`, after which
+ * `done` is recorded on that stream. The consumer later calls ple_wait
+ * (or cudaStreamWaitEvent) before reading `out`.
+ * (PR#54371 report: start_prefetch on a prefetch stream; PR#56512 report:
+ * lookup on a side stream with a reduced grid, embed() waits on it.)
+ * `done` is created by the caller (cudaEventCreateWithFlags, timing disabled
+ * is fine). The inputs (ids) must be ready on side_stream: record an event
+ * on the producer stream and make side_stream wait on it first.
+ */
+ple_status ple_lookup_prefetch(const int64_t* ids, int64_t num_tokens,
+                               int32_t num_heads, const void* table,
+                               int64_t table_rows, int32_t head_dim,
+                               ple_dtype dtype, const float* row_scale,
+                               ple_table_loc loc, ple_bf16_t* out,
+                               int32_t max_ctas, int32_t* dev_err,
+                               cudaStream_t side_stream, cudaEvent_t done);
+
+/*
+ * ple_wait -- make `consumer` wait for `done`.
+ *   timeout_ms <= 0: enqueue a device-side wait only (cudaStreamWaitEvent);
+ *                    the host does not block.
+ *   timeout_ms  > 0: first poll the event from the host for at most
+ *                    timeout_ms; if it has not completed, return
+ *                    PLE_ERR_TIMEOUT without touching `consumer`; else
+ *                    enqueue the device-side wait and return PLE_OK.
+ */
+ple_status ple_wait(cudaEvent_t done, cudaStream_t consumer, int32_t timeout_ms);
+
+/*
+ * ple_kv_proj -- merged key/value projection, kv = emb @ W^T.
+ * (PR#54517 report, 实现拆解 item 1: key_proj and value_proj merged into one
+ * MergedColumnParallelLinear.) W = [W_k; W_v]: rows [0, C) give k, rows
+ * [C, 2C) give v. fp32 accumulation on the tensor cores, bf16 result
+ * (round to nearest even).
+ *
+ *   emb   [num_tokens][emb_dim] bf16 device, 16-byte aligned.
+ *   w     [2 * hidden][emb_dim] bf16 device, 16-byte aligned.
+ *   kv    [num_tokens][2 * hidden] bf16 device.
+ * emb_dim must be a multiple of 8 and hidden a multiple of 16
+ * (else PLE_ERR_UNSUPPORTED).
+ */
+ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w,
+                       int64_t num_tokens, int32_t emb_dim, int32_t hidden,
+                       ple_bf16_t* kv, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * ple_gate -- RMSNorm + sigmoid gate ("PLE gating and normalisation",
+ * PR#54517 report 实现拆解 item 2; the pages give no formula, this is the
+ * reading the library implements):
+ *   g_t = sigmoid( <rms(h_t) * gamma_h, rms(k_t) * gamma_k> / sqrt(C) ),
+ *   rms(x) = x / sqrt(mean(x^2) + eps),   u_t = bf16_rn(g_t * v_t).
+ *
+ *   hidden      [num_tokens][C] bf16.   kv [num_tokens][2C] bf16 (k | v).
+ *   gamma_h/k   [C] bf16.                out (u) [num_tokens][C] bf16.
+ *   gate_out    [num_tokens] float32 or NULL (the scalar gates).
+ * C must be a multiple of 8.
+ */
+ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
+                    const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k,
+                    float eps, int64_t num_tokens, int32_t hidden_size,
+                    ple_bf16_t* out, float* gate_out, cudaStream_t stream);
+
+/*
+ * ple_conv -- dilated causal depthwise short conv over ragged requests
+ * (PR#54517 report 实现拆解 items 2 and 4: _ple_conv_kernel, prefill and
+ * decode with a cached state). For token t of request r, channel c:
+ *   y_t[c] = sum_{i<K} w[c][i] * x_{t - (K-1-i)*dilation}[c]
+ * over r's virtual sequence conv_state[r] ++ x[segment of r]; positions
+ * before it read zeros (conv_state == NULL means all-zero history).
+ *
+ *   x               [num_tokens][C] bf16.      w [C][K] bf16.
+ *   query_start_loc [num_reqs + 1] int32 device (same rules as ple_ngram_ids).
+ *   conv_state      [num_reqs][(K-1)*dilation][C] bf16 (history, oldest first)
+ *                   or NULL.
+ *   conv_state_out  same shape or NULL: the last (K-1)*dilation inputs of
+ *                   each virtual sequence. Must not overlap conv_state.
+ *   out             [num_tokens][C] bf16.
+ * K in 1 .. 8, dilation >= 1, (K-1)*dilation <= 64, C a multiple of 8.
+ */
+ple_status ple_conv(const ple_bf16_t* x, const int32_t* query_start_loc,
+                    int32_t num_reqs, int64_t num_tokens, int32_t hidden_size,
+                    const ple_bf16_t* w, int32_t kernel_size, int32_t dilation,
+                    const ple_bf16_t* conv_state, ple_bf16_t* conv_state_out,
+                    ple_bf16_t* out, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * ple_gate_conv -- ple_gate followed by ple_conv in one kernel: the gate
+ * scalars of a token tile (and its dilation halo) are reduced on chip, the
+ * gated values u = bf16_rn(g * v) are staged in shared memory and never
+ * written to global memory. Same results as ple_gate then ple_conv.
+ * Arguments as in those two calls; gate_out optional.
+ */
+ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* kv,
+                         const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k,
+                         float eps, const int32_t* query_start_loc,
+                         int32_t num_reqs, int64_t num_tokens,
+                         int32_t hidden_size, const ple_bf16_t* w,
+                         int32_t kernel_size, int32_t dilation,
+                         const ple_bf16_t* conv_state,
+                         ple_bf16_t* conv_state_out, ple_bf16_t* out,
+                         float* gate_out, int32_t* dev_err,
+                         cudaStream_t stream);
+
+/* Text of the last non-OK status on this host thread ("" if none). */
+const char* ple_last_error(void);
+
+/* Library version string. */
+const char* ple_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLE_H_ */

@@ -1,0 +1,77 @@
+"""Shared test utilities: bf16 bit conversions, tolerances, case builders.
+
+Tolerances (float stages; ids and gathered rows are compared bit for bit):
+  |gpu - ref| <= rtol * |ref| + atol_frac * rms(ref), elementwise,
+with rtol = atol_frac = 1e-2 for bf16 tables and 3e-2 for the fp8 chain.
+The absolute part is scaled by the data's rms because the synthetic
+activations are far below 1 (kv ~ 2e-2): a plain 1e-2 absolute bound would
+accept anything. One bf16 rounding step is 2^-8 relative, so an honest result
+sits well inside 1e-2.
+"""
+
+import numpy as np
+import torch
+
+from hashed_gram_embedding_gb300 import workloads as wl
+
+
+def bits(t):
+    """torch bf16 tensor -> numpy uint16 bit patterns (on the host)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(a, device="cpu"):
+    """numpy uint16 bf16 bits -> torch bf16 tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def bf16_values(a):
+    b = np.asarray(a, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def assert_close(gpu_bits, ref_bits, rtol=1e-2, atol_frac=1e-2, what=""):
+    g = bf16_values(gpu_bits)
+    r = bf16_values(ref_bits)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    if r.size == 0:
+        return
+    rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
+    tol = rtol * np.abs(r) + atol_frac * max(rms, 1e-30)
+    err = np.abs(g - r)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {r.size} elements out of tolerance; first at "
+            f"{idx.tolist()}: gpu {g[bad][:5]} ref {r[bad][:5]} (rms {rms:.3g})")
+
+
+def dev_err_word(device="cuda"):
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def tiny_case(w=None, seed_step=0, random_gamma=True, decode=None):
+    """A small workload with every input on the host (numpy) and the device.
+
+    Dense tensors are drawn on the CPU so that the oracle and the GPU see the
+    same bits; the table is small enough to hold on both sides.
+    """
+    w = w or wl.WORKLOADS["tiny"]
+    if decode is not None:
+        w = wl.scaled(w, decode=decode)
+    host = wl.host_inputs(w, step=seed_step)
+    dense = wl.dense_inputs(torch, w, "cpu", step=seed_step, random_gamma=random_gamma)
+    rows = wl.table_rows(w)
+    if w.table_dtype == "fp8":
+        codes = torch.empty((rows, w.head_dim), dtype=torch.uint8)
+        scale = torch.empty((rows,), dtype=torch.float32)
+        wl.fill_table_fp8(torch, codes, scale, w.seed, 10)
+        table, row_scale = codes, scale
+    else:
+        table = torch.empty((rows, w.head_dim), dtype=torch.bfloat16)
+        g = torch.Generator().manual_seed(w.seed * 1009 + 10)
+        table.copy_(torch.randn((rows, w.head_dim), generator=g).mul_(0.02).to(torch.bfloat16))
+        row_scale = None
+    return w, host, dense, table, row_scale

@@ -1,0 +1,111 @@
+"""The C ABI: libple builds, loads and exports what include/ple.h declares;
+host-side argument checks reject bad calls before any CUDA work (no GPU)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ple.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ple_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hashed_gram_embedding_gb300 import build, _lib
+    build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ["ple_ngram_ids", "ple_lookup", "ple_lookup_prefetch", "ple_wait",
+                     "ple_kv_proj", "ple_gate", "ple_conv", "ple_gate_conv",
+                     "ple_last_error", "ple_version"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from hashed_gram_embedding_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_version_string(lib):
+    assert b"libple" in lib.ple_version()
+
+
+def _ngram(lib, **kw):
+    args = dict(input_ids=None, T=4, qsl=None, R=1, ctx=None, ctx_len=2, mult=[1, 2, 3],
+                V=[7, 11], O=[0, 7], eos=2, hpn=1, out=None, ctx_out=None, err=None)
+    args.update(kw)
+    I64P = ctypes.POINTER(ctypes.c_int64)
+    keep = [np.asarray(args[k], dtype=np.int64) for k in ("mult", "V", "O")]
+    return lib.ple_ngram_ids(args["input_ids"], args["T"], args["qsl"], args["R"], args["ctx"],
+                             args["ctx_len"], *(a.ctypes.data_as(I64P) for a in keep),
+                             args["eos"], args["hpn"], args["out"], args["ctx_out"], args["err"],
+                             None)
+
+
+def test_ngram_ids_rejects_empty_head_shard(lib):
+    assert _ngram(lib, hpn=0) == 1
+    assert b"empty head" in lib.ple_last_error()
+
+
+def test_ngram_ids_rejects_bad_sizes(lib):
+    assert _ngram(lib, ctx_len=0, mult=[1]) == 1
+    assert _ngram(lib, ctx_len=8, mult=[1] * 9, V=[7] * 8, O=[0] * 8) == 1
+    assert _ngram(lib, R=0) == 1                       # tokens but no request
+    assert _ngram(lib, V=[7, 0]) == 1                  # empty vocab
+    assert _ngram(lib, hpn=40, V=[7] * 80, O=[0] * 80) == 1  # too many heads
+    assert _ngram(lib, T=-1) == 1
+
+
+def test_ngram_ids_zero_tokens_is_a_noop(lib):
+    assert _ngram(lib, T=0) == 0
+
+
+def test_ngram_ids_rejects_overlapping_context_buffers(lib):
+    buf = (ctypes.c_int32 * 8)()
+    p = ctypes.addressof(buf)
+    assert _ngram(lib, ctx=p, ctx_out=p + 4, R=2, T=0) == 1
+    assert b"overlaps" in lib.ple_last_error()
+
+
+def test_lookup_rejects_unaligned_rows_and_bad_enums(lib):
+    # 12 bf16 = 24 bytes per row: not a multiple of 16
+    assert lib.ple_lookup(None, 1, 1, None, 10, 12, 0, None, 0, None, 0, None, None) == 2
+    assert lib.ple_lookup(None, 1, 1, None, 10, 64, 7, None, 0, None, 0, None, None) == 1
+    assert lib.ple_lookup(None, 1, 1, None, 10, 64, 0, None, 9, None, 0, None, None) == 1
+    assert lib.ple_lookup(None, 1, 0, None, 10, 64, 0, None, 0, None, 0, None, None) == 1
+    assert lib.ple_lookup(None, 0, 1, None, 10, 64, 0, None, 0, None, 0, None, None) == 0
+    # fp8 without scales
+    assert lib.ple_lookup(ctypes.c_void_p(16), 1, 1, ctypes.c_void_p(16), 10, 64, 1, None, 0,
+                          ctypes.c_void_p(16), 0, None, None) == 1
+
+
+def test_kv_proj_rejects_unsupported_shapes(lib):
+    assert lib.ple_kv_proj(None, None, 4, 12, 64, None, None, None) == 2   # E % 8
+    assert lib.ple_kv_proj(None, None, 4, 64, 24, None, None, None) == 2   # C % 16
+    assert lib.ple_kv_proj(None, None, 0, 64, 64, None, None, None) == 0
+
+
+def test_conv_and_gate_reject_bad_shapes(lib):
+    assert lib.ple_gate(None, None, None, None, 1e-6, 4, 12, None, None, None) == 1
+    assert lib.ple_conv(None, None, 1, 4, 64, None, 9, 1, None, None, None, None, None) == 1
+    assert lib.ple_conv(None, None, 1, 4, 64, None, 4, 30, None, None, None, None, None) == 1
+    assert lib.ple_gate_conv(None, None, None, None, 1e-6, None, 0, 4, 64, None, 4, 3, None,
+                             None, None, None, None, None) == 1
+
+
+def test_wait_rejects_null_event(lib):
+    assert lib.ple_wait(None, None, 0) == 1

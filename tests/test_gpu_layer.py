@@ -1,0 +1,116 @@
+"""GPU parity of the whole per-layer chain (PLELayer.forward: ids -> gather ->
+kv_proj -> gate + conv, four libple launches) against the oracle's
+layer_forward: the tiny workload with a bf16 and with an fp8 table (every
+token), the decode workload's carry-over outputs, and the 8k prefill at full
+size (sampled tokens with their conv windows)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hashed_gram_embedding_gb300 import PLELayer
+from hashed_gram_embedding_gb300 import workloads as wl
+
+from _helpers import assert_close, bits, dev_err_word, tiny_case
+
+pytestmark = pytest.mark.gpu
+
+
+def build_layer(w, host, dense, table, row_scale, layer=0):
+    return PLELayer(table, row_scale, host["multipliers"][layer], host["V"], host["O"],
+                    w.eos_token_id, w.heads_per_ngram, dense["w_kv"], dense["gamma_h"],
+                    dense["gamma_k"], dense["conv_w"], w.dilation)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_tiny_chain_every_token(dtype):
+    w = wl.scaled(wl.WORKLOADS["tiny"], table_dtype=dtype)
+    w, host, dense, table, row_scale = tiny_case(w)
+    d_dense = {k: v.cuda() for k, v in dense.items()}
+    layer = build_layer(w, host, d_dense, table.cuda(),
+                        None if row_scale is None else row_scale.cuda())
+    err = dev_err_word()
+    qsl = torch.from_numpy(host["query_start_loc"]).cuda()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), qsl, d_dense["hidden"],
+                      dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    host_table = bits(table) if row_scale is None else table.numpy()
+    ref = oracle.layer_forward(host["input_ids"], host["query_start_loc"], None,
+                               host["multipliers"][0], host["V"], host["O"], w.eos_token_id,
+                               w.heads_per_ngram, host_table,
+                               None if row_scale is None else row_scale.numpy(),
+                               bits(dense["hidden"]), bits(dense["w_kv"]), bits(dense["gamma_h"]),
+                               bits(dense["gamma_k"]), 1e-6, bits(dense["conv_w"]), w.dilation)
+    b = layer.buffers(w.num_tokens, y.device)
+    assert np.array_equal(b["ids"].cpu().numpy(), ref["ids"])
+    assert np.array_equal(bits(b["emb"]), ref["emb"])
+    tol = 1e-2 if dtype == "bf16" else 3e-2
+    assert_close(bits(b["kv"]), ref["kv"], rtol=tol, atol_frac=tol, what="kv")
+    assert_close(bits(y), ref["y"], rtol=tol, atol_frac=tol, what="y")
+
+
+def test_decode_chain_carry_over():
+    w = wl.scaled(wl.WORKLOADS["decode256x4"], hidden=256, vocab_start=5000, num_reqs=64,
+                  num_tokens=256, fixed_lengths=(4,) * 64)
+    host = wl.host_inputs(w)
+    dense = wl.dense_inputs(torch, w, "cpu", random_gamma=True)
+    rows = wl.table_rows(w)
+    g = torch.Generator().manual_seed(5)
+    table = (torch.randn((rows, w.head_dim), generator=g) * 0.02).to(torch.bfloat16)
+    d = {k: v.cuda() for k, v in dense.items()}
+    layer = build_layer(w, host, d, table.cuda(), None)
+    ctx_in = torch.from_numpy(host["ngram_context"]).cuda()
+    ctx_out = torch.empty_like(ctx_in)
+    st_out = torch.empty_like(d["conv_state"])
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(),
+                      torch.from_numpy(host["query_start_loc"]).cuda(), d["hidden"],
+                      ngram_context=ctx_in, ngram_context_out=ctx_out,
+                      conv_state=d["conv_state"], conv_state_out=st_out)
+    torch.cuda.synchronize()
+    ref = oracle.layer_forward(host["input_ids"], host["query_start_loc"], host["ngram_context"],
+                               host["multipliers"][0], host["V"], host["O"], w.eos_token_id,
+                               w.heads_per_ngram, bits(table), None, bits(dense["hidden"]),
+                               bits(dense["w_kv"]), bits(dense["gamma_h"]), bits(dense["gamma_k"]),
+                               1e-6, bits(dense["conv_w"]), w.dilation, bits(dense["conv_state"]))
+    assert np.array_equal(ctx_out.cpu().numpy(), np.asarray(ref["ngram_context_out"]))
+    assert_close(bits(y), ref["y"], what="decode y")
+    assert_close(bits(st_out), ref["conv_state_out"], what="decode state")
+
+
+def test_prefill_8k_chain_sampled():
+    w = wl.WORKLOADS["prefill8k"]
+    host = wl.host_inputs(w)
+    table, _ = wl.make_table(torch, w, "cuda")
+    dense = wl.dense_inputs(torch, w, "cuda", random_gamma=True)
+    layer = build_layer(w, host, dense, table, None)
+    qsl = host["query_start_loc"]
+    err = dev_err_word()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), torch.from_numpy(qsl).cuda(),
+                      dense["hidden"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ids, _ = oracle.ngram_ids(host["input_ids"], qsl, None, host["multipliers"][0], host["V"],
+                              host["O"], w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64)
+    assert np.array_equal(layer.buffers(w.num_tokens, y.device)["ids"].cpu().numpy(), ids)
+    rng = np.random.default_rng(2)
+    sample = np.unique(np.concatenate([s + np.arange(4) for s in qsl[:-1]] +
+                                      [rng.integers(0, w.num_tokens, 56), [w.num_tokens - 1]]))
+    req_of = np.searchsorted(qsl, sample, side="right") - 1
+    wkv, gh, gk, cw = (bits(dense[k]) for k in ("w_kv", "gamma_h", "gamma_k", "conv_w"))
+    hid = dense["hidden"]
+    yb = bits(y)
+    for t, r in zip(sample, req_of):
+        lo = max(int(qsl[r]), int(t) - 9)
+        win_ids = ids[lo:t + 1]
+        uniq, inv = np.unique(win_ids, return_inverse=True)
+        compact = bits(table[torch.from_numpy(uniq).cuda()])
+        emb = oracle.lookup_bf16(inv.reshape(win_ids.shape), compact)
+        kv = oracle.kv_proj(emb, wkv)
+        ref_y, _, _ = oracle.gate_conv(bits(hid[lo:t + 1]), kv, gh, gk, 1e-6,
+                                       [0, int(t) + 1 - lo], cw, w.dilation)
+        assert_close(yb[t:t + 1], ref_y[-1:], what=f"token {t}")
+    del table
+    torch.cuda.empty_cache()

@@ -1,0 +1,196 @@
+"""GPU parity of ple_lookup / ple_lookup_prefetch / ple_wait against the
+oracle: bit-exact bf16 rows (HBM and pinned-host UVA tables, several row
+sizes, ragged token counts, capped grids), bit-exact fp8 e4m3 dequant with a
+per-row scale over all 256 codes, out-of-range ids flagged and zeroed, the
+side-stream prefetch, the bounded host wait, and the 8 GB 8k-prefill table at
+full size."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import lookup_bf16, lookup_fp8, ngram_ids as oracle_ids
+from hashed_gram_embedding_gb300 import _lib
+from hashed_gram_embedding_gb300 import workloads as wl
+
+from _helpers import bits, dev_err_word
+
+pytestmark = pytest.mark.gpu
+
+
+def random_table_bits(rng, rows, D):
+    return rng.integers(0, 1 << 16, size=(rows, D), dtype=np.uint16)
+
+
+def to_dev_bf16(a, pinned=False):
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    if pinned:
+        return t.pin_memory()
+    return t.cuda()
+
+
+@pytest.mark.parametrize("T,H,D,rows", [(1, 1, 64, 10), (37, 5, 64, 1000), (513, 16, 128, 4096),
+                                        (29, 3, 8, 77), (31, 2, 24, 50), (1000, 8, 256, 333)])
+def test_bf16_gather_bit_exact(T, H, D, rows):
+    rng = np.random.default_rng(T * 7 + D)
+    table = random_table_bits(rng, rows, D)
+    ids = rng.integers(0, rows, size=(T, H))
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), to_dev_bf16(table), out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(bits(out), lookup_bf16(ids, table))
+
+
+@pytest.mark.parametrize("max_ctas", [1, 3, 152])
+def test_capped_grid_and_uva_table(max_ctas):
+    rng = np.random.default_rng(max_ctas)
+    rows, D, T, H = 5000, 128, 300, 16
+    table = random_table_bits(rng, rows, D)
+    ids = rng.integers(0, rows, size=(T, H))
+    ref = lookup_bf16(ids, table)
+    d_ids = torch.from_numpy(ids).cuda()
+    for pinned in (False, True):
+        out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+        _lib.ple_lookup(d_ids, to_dev_bf16(table, pinned=pinned), out, max_ctas=max_ctas)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), ref), f"pinned={pinned}"
+
+
+def test_uva_requires_pinned_host_memory():
+    table = torch.zeros((10, 64), dtype=torch.bfloat16)  # pageable host memory
+    ids = torch.zeros((1, 1), dtype=torch.int64, device="cuda")
+    out = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(_lib.PleError, match="PLE_ERR_INVALID_ARG"):
+        _lib.ple_lookup(ids, table, out, loc=_lib.PLE_HOST_UVA)
+    with pytest.raises(_lib.PleError, match="PLE_ERR_INVALID_ARG"):
+        _lib.ple_lookup(ids, table.pin_memory(), out, loc=_lib.PLE_HBM)
+
+
+def test_fp8_all_codes_bit_exact():
+    rng = np.random.default_rng(3)
+    D = 128
+    rows = 64
+    codes = np.concatenate([np.arange(256, dtype=np.uint8).reshape(2, 128),
+                            rng.integers(0, 256, size=(rows - 2, D), dtype=np.uint8)])
+    scale = np.concatenate([[1.0, 0.5], np.abs(rng.standard_normal(rows - 2)) * 1e-3 + 1e-7]
+                           ).astype(np.float32)
+    ids = rng.integers(0, rows, size=(50, 4))
+    ids[0] = [0, 1, 0, 1]
+    out = torch.empty((50, 4 * D), dtype=torch.bfloat16, device="cuda")
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), torch.from_numpy(codes).cuda(), out,
+                    row_scale=torch.from_numpy(scale).cuda())
+    torch.cuda.synchronize()
+    got = bits(out)
+    ref = lookup_fp8(ids, codes, scale)
+    nan_g = (got & 0x7FFF) > 0x7F80
+    nan_r = (ref & 0x7FFF) > 0x7F80
+    assert np.array_equal(nan_g, nan_r)
+    assert np.array_equal(got[~nan_r], ref[~nan_r])
+
+
+def test_fp8_workload_rows_bit_exact():
+    w = wl.scaled(wl.WORKLOADS["fp8x8"], vocab_start=1000, num_tokens=200, num_reqs=3)
+    rows = wl.table_rows(w)
+    codes = torch.empty((rows, w.head_dim), dtype=torch.uint8, device="cuda")
+    scale = torch.empty((rows,), dtype=torch.float32, device="cuda")
+    wl.fill_table_fp8(torch, codes, scale, w.seed, 10)
+    rng = np.random.default_rng(4)
+    ids = rng.integers(0, rows, size=(200, 16))
+    out = torch.empty((200, 16 * w.head_dim), dtype=torch.bfloat16, device="cuda")
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), codes, out, row_scale=scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), lookup_fp8(ids, codes.cpu().numpy(), scale.cpu().numpy()))
+
+
+def test_out_of_range_ids_are_zeroed_and_flagged():
+    rng = np.random.default_rng(5)
+    rows, D = 100, 64
+    table = random_table_bits(rng, rows, D)
+    ids = rng.integers(0, rows, size=(20, 3))
+    ids[4, 1] = rows
+    ids[7, 0] = -1
+    ids[9, 2] = 1 << 40
+    out = torch.full((20, 3 * D), 1.0, dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), to_dev_bf16(table), out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & _lib.PLE_DEVERR_BOUNDS
+    got = bits(out)
+    bad = [(4, 1), (7, 0), (9, 2)]
+    for t, h in bad:
+        assert np.all(got[t, h * D:(h + 1) * D] == 0)
+    ok_ids = ids.copy()
+    for t, h in bad:
+        ok_ids[t, h] = 0
+    ref = lookup_bf16(ok_ids, table)
+    for t, h in bad:
+        ref[t, h * D:(h + 1) * D] = 0
+    assert np.array_equal(got, ref)
+
+
+def test_prefetch_on_side_stream_then_wait():
+    rng = np.random.default_rng(6)
+    rows, D, T, H = 20000, 128, 1024, 16
+    table = random_table_bits(rng, rows, D)
+    ids = rng.integers(0, rows, size=(T, H))
+    d_ids = torch.from_numpy(ids).cuda()
+    host_table = to_dev_bf16(table, pinned=True)
+    side = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    ready = torch.cuda.Event()
+    ready.record(torch.cuda.current_stream())
+    side.wait_event(ready)
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    _lib.ple_lookup_prefetch(d_ids, host_table, out, side, done, max_ctas=76)
+    _lib.ple_wait(done, torch.cuda.current_stream(), timeout_ms=0)
+    result = out.clone()  # ordered after the wait on the consumer stream
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(result), lookup_bf16(ids, table))
+
+
+def test_wait_times_out_then_completes():
+    side = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    ids = torch.zeros((1, 1), dtype=torch.int64, device="cuda")
+    table = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        a = torch.randn((8192, 8192), device="cuda", dtype=torch.bfloat16)
+        for _ in range(40):
+            a = (a @ a).clamp_(-1, 1)  # tens of milliseconds of work before the event
+    _lib.ple_lookup_prefetch(ids, table, out, side, done)
+    with pytest.raises(_lib.PleError, match="PLE_ERR_TIMEOUT"):
+        _lib.ple_wait(done, torch.cuda.current_stream(), timeout_ms=1)
+    _lib.ple_wait(done, torch.cuda.current_stream(), timeout_ms=60000)
+    torch.cuda.synchronize()
+
+
+def test_prefill_8k_full_size_table():
+    w = wl.WORKLOADS["prefill8k"]
+    h = wl.host_inputs(w)
+    table, _ = wl.make_table(torch, w, "cuda")
+    ids, _ = oracle_ids(h["input_ids"], h["query_start_loc"], None, h["multipliers"][0], h["V"],
+                        h["O"], w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64)
+    d_ids = torch.from_numpy(ids).cuda()
+    out = torch.empty((w.num_tokens, w.emb_dim), dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_lookup(d_ids, table, out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # every row: a plain index_select of the input table (library routine)
+    assert torch.equal(out, table.index_select(0, d_ids.reshape(-1)).reshape(out.shape))
+    # a sample through the oracle on the host
+    rng = np.random.default_rng(8)
+    sample = np.unique(np.concatenate([rng.integers(0, w.num_tokens, 256),
+                                       h["query_start_loc"][:-1]]))
+    sub_ids = ids[sample]
+    uniq, inv = np.unique(sub_ids, return_inverse=True)
+    compact = bits(table[torch.from_numpy(uniq).cuda()])
+    ref = lookup_bf16(inv.reshape(sub_ids.shape), compact)
+    assert np.array_equal(bits(out)[sample], ref)
+    del table
+    torch.cuda.empty_cache()
