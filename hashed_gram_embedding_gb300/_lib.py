@@ -133,15 +133,26 @@ def ple_lookup(ids, table, out, row_scale=None, max_ctas=0, dev_err=None, loc=No
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
 
 
+def _event_handle(event, stream):
+    """Raw cudaEvent_t of a torch.cuda.Event (torch creates it lazily, on the
+    first record: record it once on ``stream`` if it does not exist yet)."""
+    if event.cuda_event == 0:
+        event.record(stream)
+    return ctypes.c_void_p(event.cuda_event)
+
+
 def ple_lookup_prefetch(ids, table, out, side_stream, done_event, row_scale=None, max_ctas=0,
                         dev_err=None, loc=None):
     """ple_lookup on ``side_stream``, then ``done_event`` (torch.cuda.Event) recorded there."""
+    done = _event_handle(done_event, side_stream)
     return _check("ple_lookup_prefetch", lib().ple_lookup_prefetch(
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc),
-        ctypes.c_void_p(side_stream.cuda_stream), ctypes.c_void_p(done_event.cuda_event)))
+        ctypes.c_void_p(side_stream.cuda_stream), done))
 
 
 def ple_wait(done_event, consumer_stream=None, timeout_ms=0):
+    if done_event.cuda_event == 0:
+        return PLE_OK  # never recorded: nothing to wait for
     return _check("ple_wait", lib().ple_wait(ctypes.c_void_p(done_event.cuda_event),
                                              _stream(consumer_stream), int(timeout_ms)))
 

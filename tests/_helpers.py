@@ -7,12 +7,21 @@ The absolute part is scaled by the data's rms because the synthetic
 activations are far below 1 (kv ~ 2e-2): a plain 1e-2 absolute bound would
 accept anything. One bf16 rounding step is 2^-8 relative, so an honest result
 sits well inside 1e-2.
+
+Outputs downstream of kv_proj in the whole chain use CHAIN_ATOL_FRAC = 2e-2:
+the kernel's fp32-accumulated kv and the oracle's float64 kv may land one bf16
+ulp apart; that moves the gate scalar slightly and can flip the rounding of
+a gated value u (one more ulp); y sums K = 4 taps w_i * u_i with |w| ~ 0.5 and
+cancels, so |dy| <= sum_i |w_i| * 2 ulp(u_i) ~ 4 * 0.5 * 2 * 2^-8 * rms(u),
+about 1.6e-2 * rms(y) at the worst, where rms(y) ~ rms(u).
 """
 
 import numpy as np
 import torch
 
 from hashed_gram_embedding_gb300 import workloads as wl
+
+CHAIN_ATOL_FRAC = 2e-2
 
 
 def bits(t):

@@ -12,7 +12,7 @@ import oracle
 from hashed_gram_embedding_gb300 import PLELayer
 from hashed_gram_embedding_gb300 import workloads as wl
 
-from _helpers import assert_close, bits, dev_err_word, tiny_case
+from _helpers import CHAIN_ATOL_FRAC, assert_close, bits, dev_err_word, tiny_case
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def test_tiny_chain_every_token(dtype):
     assert np.array_equal(bits(b["emb"]), ref["emb"])
     tol = 1e-2 if dtype == "bf16" else 3e-2
     assert_close(bits(b["kv"]), ref["kv"], rtol=tol, atol_frac=tol, what="kv")
-    assert_close(bits(y), ref["y"], rtol=tol, atol_frac=tol, what="y")
+    assert_close(bits(y), ref["y"], rtol=tol, atol_frac=max(tol, CHAIN_ATOL_FRAC), what="y")
 
 
 def test_decode_chain_carry_over():
@@ -75,8 +75,9 @@ def test_decode_chain_carry_over():
                                bits(dense["w_kv"]), bits(dense["gamma_h"]), bits(dense["gamma_k"]),
                                1e-6, bits(dense["conv_w"]), w.dilation, bits(dense["conv_state"]))
     assert np.array_equal(ctx_out.cpu().numpy(), np.asarray(ref["ngram_context_out"]))
-    assert_close(bits(y), ref["y"], what="decode y")
-    assert_close(bits(st_out), ref["conv_state_out"], what="decode state")
+    assert_close(bits(y), ref["y"], atol_frac=CHAIN_ATOL_FRAC, what="decode y")
+    assert_close(bits(st_out), ref["conv_state_out"], atol_frac=CHAIN_ATOL_FRAC,
+                 what="decode state")
 
 
 def test_prefill_8k_chain_sampled():
@@ -111,6 +112,6 @@ def test_prefill_8k_chain_sampled():
         kv = oracle.kv_proj(emb, wkv)
         ref_y, _, _ = oracle.gate_conv(bits(hid[lo:t + 1]), kv, gh, gk, 1e-6,
                                        [0, int(t) + 1 - lo], cw, w.dilation)
-        assert_close(yb[t:t + 1], ref_y[-1:], what=f"token {t}")
+        assert_close(yb[t:t + 1], ref_y[-1:], atol_frac=CHAIN_ATOL_FRAC, what=f"token {t}")
     del table
     torch.cuda.empty_cache()
