@@ -242,8 +242,12 @@ def run_ours(args):
     barrier()
 
     w = wl.WORKLOADS[args.workload]
+    if args.vocab_start:
+        w = wl.scaled(w, vocab_start=args.vocab_start)  # smaller table (profiling cases)
     # one step = one layer; multi-layer workloads rotate over their layers
     num_sets = w.num_layers if w.num_layers > 1 else (NUM_SETS if w.table_loc == "hbm" else 1)
+    if args.layer_sets:
+        num_sets = args.layer_sets
     sets = make_sets(torch, w, device, num_sets)
     T, H, C = w.num_tokens, w.num_heads, w.hidden
     ids = torch.empty((T, H), dtype=torch.int64, device=device)
@@ -525,6 +529,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer-sets", type=int, default=0,
+                    help="layer parameter sets to rotate over (0 = workload default)")
+    ap.add_argument("--vocab-start", type=int, default=0,
+                    help="first per-head vocab prime (smaller table for profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

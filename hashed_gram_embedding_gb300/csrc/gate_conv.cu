@@ -25,13 +25,14 @@
 // re-read from L2 by the neighbouring tile), v once, y written once.
 #include "common.cuh"
 
+#include <cooperative_groups.h>
+#include <cstdlib>
+
 namespace ple {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 512;          // channels staged per pass
-constexpr int kChunkVecs = kChunk / 8;
 constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
 
@@ -121,6 +122,22 @@ gate_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict_
 
 // ---------------------------------------------------------------------------
 // ple_conv (GATED = false, input x) and ple_gate_conv (GATED = true).
+//
+// Grid: one thread-block cluster of CL CTAs per tile of TT tokens; CTA
+// `part` of the cluster owns channels [part*slice, (part+1)*slice).
+//   0. the tile's request boundaries (binary search) go to shared memory;
+//   1. one thread issues bulk async copies of the v rows of the tile and its
+//      halo (only rows of the first tile token's request or later) into
+//      shared memory -- they land while step 2 runs;
+//   2. (gated) warps reduce sum h^2, sum k^2, sum h*gh*k*gk over the CTA's
+//      channel slice for every row; a cluster barrier publishes these partial
+//      sums and every CTA adds the CL partials of each row through
+//      distributed shared memory to get the gate scalars;
+//   3. after the copies land, each thread produces 8 channels of one token:
+//      u = bf16(g * v) for the K dilated taps (from shared memory, or the
+//      carry-over state before the request's first token), fp32 FMA with
+//      the taps, bf16 out; the CTA holding a request's last token writes that
+//      request's new state for its channels.
 // ---------------------------------------------------------------------------
 struct ConvArgs {
   const ple_bf16_t* hidden;   // gated only
@@ -140,30 +157,62 @@ struct ConvArgs {
   ple_bf16_t* out;
   float* gate_out;
   int32_t* dev_err;
-  int TT;
+  int TT;      // tokens per tile
+  int CL;      // CTAs per tile (channel split; the cluster size when gated)
+  int slice;   // channels per CTA (multiple of 8)
 };
+
+struct ConvSmem {
+  // offsets in bytes from the dynamic shared-memory base
+  size_t v, w, part, g, start, end, req, bar, total;
+};
+
+__host__ __device__ inline ConvSmem conv_smem_layout(int TT, int K, int dil, int slice) {
+  ConvSmem L;
+  const int rows = TT + (K - 1) * dil;
+  size_t off = 0;
+  L.v = off;      off += static_cast<size_t>(rows) * slice * 2;          // staged v rows
+  off = (off + 15) & ~size_t(15);
+  L.w = off;      off += static_cast<size_t>(K) * slice * 4;             // taps, [K][slice] f32
+  L.part = off;   off += static_cast<size_t>(rows) * 4 * 4;              // partial sums
+  L.g = off;      off += static_cast<size_t>(rows) * 4;                  // gate scalars
+  off = (off + 7) & ~size_t(7);
+  L.start = off;  off += static_cast<size_t>(TT) * 8;
+  L.end = off;    off += static_cast<size_t>(TT) * 8;
+  L.req = off;    off += static_cast<size_t>(TT) * 4;
+  off = (off + 7) & ~size_t(7);
+  L.bar = off;    off += 8;
+  L.total = off;
+  return L;
+}
 
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads)
 conv_kernel(const __grid_constant__ ConvArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int W = (a.K - 1) * a.dil;
   const int rows = a.TT + W;
   const int C = a.C;
   const int64_t T = a.T;
-  // shared layout: u_s [rows][kChunk] bf16 | w_s [K][kChunk] f32 | g_s [rows] f32
-  //                | start_s, end_s [TT] i64 | req_s [TT] i32
-  uint4* u_s = reinterpret_cast<uint4*>(smem);
-  float* w_s = reinterpret_cast<float*>(smem + static_cast<size_t>(rows) * kChunk * 2);
-  float* g_s = w_s + a.K * kChunk;
-  int64_t* start_s = reinterpret_cast<int64_t*>(g_s + ((rows + 1) & ~1));
-  int64_t* end_s = start_s + a.TT;
-  int* req_s = reinterpret_cast<int*>(end_s + a.TT);
+  const int slice = a.slice;
+  const int ng = slice / 8;                      // 16-byte channel groups per CTA
+  const ConvSmem L = conv_smem_layout(a.TT, a.K, a.dil, slice);
+  uint4* v_s = reinterpret_cast<uint4*>(smem + L.v);
+  float* w_s = reinterpret_cast<float*>(smem + L.w);
+  float4* part_s = reinterpret_cast<float4*>(smem + L.part);
+  float* g_s = reinterpret_cast<float*>(smem + L.g);
+  int64_t* start_s = reinterpret_cast<int64_t*>(smem + L.start);
+  int64_t* end_s = reinterpret_cast<int64_t*>(smem + L.end);
+  int* req_s = reinterpret_cast<int*>(smem + L.req);
+  const uint32_t bar = smem_u32(smem + L.bar);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * a.TT;
+  const int tile = blockIdx.x / a.CL;
+  const int part = blockIdx.x % a.CL;
+  const int c0 = part * slice;
+  const int64_t t0 = static_cast<int64_t>(tile) * a.TT;
   const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
   const int64_t src_off = GATED ? C : 0;  // v sits after k in kv
 
@@ -171,6 +220,7 @@ conv_kernel(const __grid_constant__ ConvArgs a) {
     for (int i = tid; i < a.num_reqs + 1; i += kThreads)
       check_qsl(a.qsl, a.num_reqs, T, i, a.dev_err);
 
+  // 0. request of every tile token; taps of this CTA's channels
   for (int i = tid; i < a.TT; i += kThreads) {
     const int64_t t = t0 + i;
     int r = 0;
@@ -183,125 +233,195 @@ conv_kernel(const __grid_constant__ ConvArgs a) {
     start_s[i] = s;
     end_s[i] = e;
   }
+  for (int idx = tid; idx < a.K * slice; idx += kThreads) {
+    const int i = idx / slice;
+    const int c = c0 + idx - i * slice;
+    w_s[idx] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.w)[static_cast<int64_t>(c) * a.K + i]);
+  }
+  for (int i = tid; i < rows; i += kThreads) part_s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
   __syncthreads();
   // Halo rows are needed only back to the start of the first tile token's
   // request; earlier rows belong to other requests.
   const int64_t lo = start_s[0];
+  const int i_lo = static_cast<int>(max(static_cast<int64_t>(0), lo - (t0 - W)));
+  const int i_hi = static_cast<int>(min(static_cast<int64_t>(rows), T - (t0 - W)));
 
-  if constexpr (GATED) {
-    for (int i = warp; i < rows; i += kWarps) {
+  // 1. stage v rows [i_lo, i_hi) of this CTA's channels
+  if (tid == 0) {
+    const uint32_t row_bytes = static_cast<uint32_t>(slice) * 2;
+    const int n = i_hi > i_lo ? i_hi - i_lo : 0;
+    mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(n));
+    for (int i = i_lo; i < i_hi; ++i) {
       const int64_t j = t0 - W + i;
-      float g = 0.f;
-      if (j >= lo && j < T) {
-        g = gate_scalar(a.hidden + j * C, a.src + j * src_pitch, a.gamma_h, a.gamma_k, C,
-                        a.eps, lane);
-        if (lane == 0 && a.gate_out != nullptr && i >= W) a.gate_out[j] = g;
-      }
-      if (lane == 0) g_s[i] = g;
+      bulk_copy_g2s(smem_u32(v_s) + static_cast<uint32_t>(i) * row_bytes,
+                    a.src + j * src_pitch + src_off + c0, row_bytes, bar);
     }
-    __syncthreads();
   }
 
-  for (int c0 = 0; c0 < C; c0 += kChunk) {
-    for (int idx = tid; idx < a.K * kChunk; idx += kThreads) {
-      const int i = idx / kChunk;
-      const int c = c0 + idx % kChunk;
-      w_s[idx] = (c < C) ? __bfloat162float(
-                               reinterpret_cast<const __nv_bfloat16*>(a.w)[static_cast<int64_t>(c) * a.K + i])
-                         : 0.f;
-    }
-    for (int idx = tid; idx < rows * kChunkVecs; idx += kThreads) {
-      const int i = idx / kChunkVecs;
-      const int cv = idx - i * kChunkVecs;
+  // 2. gate scalars
+  if constexpr (GATED) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int per_lane = (ng + 31) / 32;
+    for (int i = i_lo + warp; i < i_hi; i += kWarps) {
       const int64_t j = t0 - W + i;
-      const int c = c0 + cv * 8;
-      if (c < C && j >= lo && j < T) {
-        uint4 v = ldg16(a.src + j * src_pitch + src_off + c);
-        if constexpr (GATED) {
-          float f[8];
-          unpack8(v, f);
-          const float g = g_s[i];
+      const ple_bf16_t* h_row = a.hidden + j * C + c0;
+      const ple_bf16_t* k_row = a.src + j * src_pitch + c0;
+      float sh = 0.f, sk = 0.f, sd = 0.f;
+      for (int m = 0; m < per_lane; ++m) {
+        const int cv = lane + 32 * m;
+        if (cv < ng) {
+          float h[8], k[8], gh[8], gk[8];
+          unpack8(ldg16(h_row + cv * 8), h);
+          unpack8(ldg16(k_row + cv * 8), k);
+          unpack8(ldg16(a.gamma_h + c0 + cv * 8), gh);
+          unpack8(ldg16(a.gamma_k + c0 + cv * 8), gk);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= g;
-          v = pack8(f);
+          for (int e = 0; e < 8; ++e) {
+            sh = fmaf(h[e], h[e], sh);
+            sk = fmaf(k[e], k[e], sk);
+            sd = fmaf(h[e] * gh[e], k[e] * gk[e], sd);
+          }
         }
-        u_s[static_cast<size_t>(i) * kChunkVecs + cv] = v;
       }
+      sh = warp_sum(sh);
+      sk = warp_sum(sk);
+      sd = warp_sum(sd);
+      if (lane == 0) part_s[i] = make_float4(sh, sk, sd, 0.f);
     }
-    __syncthreads();
+    cluster.sync();  // every CTA's partial sums are now visible cluster-wide
+    const float inv_c = 1.0f / static_cast<float>(C);
+    const float inv_sqrt_c = 1.0f / sqrtf(static_cast<float>(C));
+    for (int i = i_lo + tid; i < i_hi; i += kThreads) {
+      float sh = 0.f, sk = 0.f, sd = 0.f;
+      for (int r = 0; r < a.CL; ++r) {
+        const float4 p = *cluster.map_shared_rank(part_s + i, r);
+        sh += p.x;
+        sk += p.y;
+        sd += p.z;
+      }
+      const float score = sd / (sqrtf(fmaf(sh, inv_c, a.eps)) * sqrtf(fmaf(sk, inv_c, a.eps))) *
+                          inv_sqrt_c;
+      const float g = 1.0f / (1.0f + expf(-score));
+      g_s[i] = g;
+      const int64_t j = t0 - W + i;
+      if (part == 0 && a.gate_out != nullptr && i >= W) a.gate_out[j] = g;
+    }
+  }
 
-    for (int idx = tid; idx < a.TT * kChunkVecs; idx += kThreads) {
-      const int tt = idx / kChunkVecs;
-      const int cv = idx - tt * kChunkVecs;
+  // 3. wait for the staged rows (bounded), then the dilated taps
+  const bool staged = mbar_wait(bar, 0, nullptr);
+  if (!staged && tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
+  __syncthreads();
+
+  if (staged) {
+    for (int idx = tid; idx < a.TT * ng; idx += kThreads) {
+      const int tt = idx / ng;
+      const int cv = idx - tt * ng;
       const int64_t t = t0 + tt;
+      if (t >= T) continue;
       const int c = c0 + cv * 8;
-      if (t >= T || c >= C) continue;
       const int r = req_s[tt];
       const int64_t start = start_s[tt];
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int i = 0; i < a.K; ++i) {
         const int64_t j = t - static_cast<int64_t>(a.K - 1 - i) * a.dil;
-        uint4 uv = make_uint4(0, 0, 0, 0);
-        if (j >= start) {
-          uv = u_s[static_cast<size_t>(j - t0 + W) * kChunkVecs + cv];
-        } else if (a.state != nullptr) {
-          const int64_t hp = W + (j - start);  // history row, oldest first
-          if (hp >= 0) uv = ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
-        }
         float u[8];
-        unpack8(uv, u);
-        const float* wi = w_s + i * kChunk + cv * 8;
+        if (j >= start) {
+          const int row = static_cast<int>(j - t0 + W);
+          unpack8(v_s[static_cast<size_t>(row) * ng + cv], u);
+          if constexpr (GATED) {
+            const float g = g_s[row];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wi[e], u[e], acc[e]);
+            for (int e = 0; e < 8; ++e) u[e] = g * u[e];
+            unpack8(pack8(u), u);  // u is rounded to bf16 before the conv
+          }
+        } else {
+          const int64_t hp = W + (j - start);  // history row, oldest first
+          uint4 hv = make_uint4(0, 0, 0, 0);
+          if (a.state != nullptr && hp >= 0)
+            hv = ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
+          unpack8(hv, u);
+        }
+        const float4 w0 = *reinterpret_cast<const float4*>(w_s + i * slice + cv * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(w_s + i * slice + cv * 8 + 4);
+        acc[0] = fmaf(w0.x, u[0], acc[0]);
+        acc[1] = fmaf(w0.y, u[1], acc[1]);
+        acc[2] = fmaf(w0.z, u[2], acc[2]);
+        acc[3] = fmaf(w0.w, u[3], acc[3]);
+        acc[4] = fmaf(w1.x, u[4], acc[4]);
+        acc[5] = fmaf(w1.y, u[5], acc[5]);
+        acc[6] = fmaf(w1.z, u[6], acc[6]);
+        acc[7] = fmaf(w1.w, u[7], acc[7]);
       }
       *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
 
-      // Carry-over: the block holding a request's last token writes its state.
+      // Carry-over: the CTA holding a request's last token writes its state.
       if (a.state_out != nullptr && W > 0 && t == end_s[tt] - 1) {
         for (int jj = 0; jj < W; ++jj) {
-          const int64_t srcj = t - W + 1 + jj;
-          uint4 uv = make_uint4(0, 0, 0, 0);
-          if (srcj >= start) {
-            uv = u_s[static_cast<size_t>(srcj - t0 + W) * kChunkVecs + cv];
-          } else if (a.state != nullptr && W + (srcj - start) >= 0) {
-            uv = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (srcj - start)) * C + c);
+          const int64_t sj = t - W + 1 + jj;
+          uint4 sv = make_uint4(0, 0, 0, 0);
+          if (sj >= start) {
+            const int row = static_cast<int>(sj - t0 + W);
+            sv = v_s[static_cast<size_t>(row) * ng + cv];
+            if constexpr (GATED) {
+              float u[8];
+              unpack8(sv, u);
+              const float g = g_s[row];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) u[e] = g * u[e];
+              sv = pack8(u);
+            }
+          } else if (a.state != nullptr && W + (sj - start) >= 0) {
+            sv = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (sj - start)) * C + c);
           }
-          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = uv;
+          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = sv;
         }
       }
     }
-    __syncthreads();
   }
 
-  // Requests with no tokens keep their state (block 0 copies it through).
-  if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
-    const int vecs = C / 8;
+  // Requests with no tokens keep their state (tile 0 copies it through).
+  if (a.state_out != nullptr && W > 0 && tile == 0) {
     for (int r = 0; r < a.num_reqs; ++r) {
       int64_t s, e;
       request_span(a.qsl, a.num_reqs, T, r, &s, &e);
       if (e != s) continue;
-      for (int idx = tid; idx < W * vecs; idx += kThreads) {
-        const int64_t off = (static_cast<int64_t>(r) * W + idx / vecs) * C + (idx % vecs) * 8;
+      for (int idx = tid; idx < W * ng; idx += kThreads) {
+        const int64_t off = (static_cast<int64_t>(r) * W + idx / ng) * C + c0 + (idx % ng) * 8;
         const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(a.state_out + off) = v;
       }
     }
   }
+
+  if constexpr (GATED) {
+    // No CTA leaves while a peer may still read its partial sums.
+    cooperative_groups::this_cluster().sync();
+  }
 }
 
-size_t conv_smem_bytes(int TT, int K, int dil) {
-  const int W = (K - 1) * dil;
-  const int rows = TT + W;
-  return static_cast<size_t>(rows) * kChunk * 2 + static_cast<size_t>(K) * kChunk * 4 +
-         static_cast<size_t>((rows + 1) & ~1) * 4 + static_cast<size_t>(TT) * 16 +
-         static_cast<size_t>(TT) * 4;
-}
-
-int pick_tile(int64_t T) {
-  const int64_t target = 2 * static_cast<int64_t>(num_sms());
-  int tt = 32;
-  while (tt > 4 && (T + tt - 1) / tt < target) tt >>= 1;
-  return tt;
+// Launch shape: CL CTAs per tile splitting the channels (slices of >= 512
+// channels, a multiple of 8), TT tokens per tile so that the grid has at
+// least ~3 CTAs per SM. PLE_CONV_TILE / PLE_CONV_SPLIT override the choice
+// (launch-shape sweeps).
+void pick_conv_shape(int64_t T, int C, int* TT, int* CL) {
+  int cl = 8;
+  while (cl > 1 && (C % (cl * 8) != 0 || C / cl < 512)) cl >>= 1;
+  int tt = 64;
+  const int64_t target = 3 * static_cast<int64_t>(num_sms());
+  while (tt > 8 && ((T + tt - 1) / tt) * cl < target) tt >>= 1;
+  if (const char* e = getenv("PLE_CONV_TILE")) { int v = atoi(e); if (v >= 1 && v <= 256) tt = v; }
+  if (const char* e = getenv("PLE_CONV_SPLIT")) {
+    int v = atoi(e);
+    if (v >= 1 && v <= 8 && C % (v * 8) == 0) cl = v;
+  }
+  *TT = tt;
+  *CL = cl;
 }
 
 ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_t C,
@@ -380,15 +500,31 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   a.out = out;
   a.gate_out = gate_out;
   a.dev_err = dev_err;
-  a.TT = pick_tile(T);
-  const size_t smem = conv_smem_bytes(a.TT, K, dil);
+  pick_conv_shape(T, C, &a.TT, &a.CL);
+  a.slice = C / a.CL;
+  const ConvSmem L = conv_smem_layout(a.TT, K, dil, a.slice);
+  if (L.total > 227 * 1024)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: %zu bytes of shared memory needed", name, L.total);
   auto kernel = gated ? conv_kernel<true> : conv_kernel<false>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(L.total));
   if (err != cudaSuccess) return check_cuda(err, name);
-  const int64_t blocks = (T + a.TT - 1) / a.TT;
-  if (blocks > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
-  kernel<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(a);
+  const int64_t tiles = (T + a.TT - 1) / a.TT;
+  if (tiles * a.CL > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * a.CL));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = gated ? a.CL : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kernel, a);
+  if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
 }
 

@@ -23,6 +23,8 @@
 namespace ple {
 namespace {
 
+constexpr int kStagedBounds = 4096;  // query_start_loc entries staged in shared memory
+
 struct NgramConsts {
   int64_t mult[PLE_MAX_CTX_LEN + 1];
   int64_t vocab[PLE_MAX_HEADS];
@@ -50,6 +52,15 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
                  int32_t* dev_err, const __grid_constant__ NgramConsts k) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
 
+  // Request boundaries staged once per block (one coalesced load) so that
+  // every thread's binary search runs in shared memory, not through L1 misses.
+  __shared__ int32_t qsl_s[kStagedBounds];
+  const bool staged = num_reqs < kStagedBounds;
+  if (staged) {
+    for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
+  }
+  __syncthreads();
+
   check_qsl(qsl, num_reqs, num_tokens, i, dev_err);
 
   // Carry-over: last ctx_len tokens of each request's virtual sequence.
@@ -71,8 +82,18 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   const int h = static_cast<int>(i - t * num_heads);
   const int order_lags = h / heads_per_ngram + 1;  // n - 1 for this head
 
-  const int r = find_request(qsl, num_reqs, t);
-  const int64_t start = __ldg(qsl + r);
+  int r;
+  if (staged) {
+    int lo = 0, hi = num_reqs + 1;  // count of boundaries <= t lies in [lo, hi]
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int64_t>(qsl_s[mid]) <= t) lo = mid + 1; else hi = mid;
+    }
+    r = lo - 1 < 0 ? 0 : (lo - 1 >= num_reqs ? num_reqs - 1 : lo - 1);
+  } else {
+    r = find_request(qsl, num_reqs, t);
+  }
+  const int64_t start = staged ? qsl_s[r] : __ldg(qsl + r);
   const int64_t pos = t - start;  // position inside the request
 
   int64_t mixed = 0;

@@ -138,3 +138,13 @@ def test_invalid_query_start_loc_is_flagged_not_faulted():
 def test_empty_head_shard_rejected():
     with pytest.raises(_lib.PleError):
         run_gpu([1, 2], [0, 2], None, [1, 2, 3], [], [], 2, 0)
+
+
+def test_many_requests_search_outside_shared_memory():
+    # more boundaries than the kernel stages in shared memory
+    rng = np.random.default_rng(11)
+    lengths = rng.integers(0, 4, size=5000)
+    qsl = [0] + [int(x) for x in np.cumsum(lengths)]
+    tokens = [int(t) for t in rng.integers(0, 50, size=qsl[-1])]
+    ctx = rng.integers(0, 50, size=(5000, 2))
+    check(tokens, qsl, ctx, [7, -11, 13], [101, 103], [0, 101], 2, 1)
