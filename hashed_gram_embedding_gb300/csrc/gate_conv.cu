@@ -11,28 +11,31 @@
 //   y_t[c] = sum_{i<K} w[c][i] * u_{t-(K-1-i)*d}[c]
 // over each request's virtual sequence (conv state ++ segment, zeros before).
 //
-// Design (HBM-bound): the gate is one scalar per token, a reduction over the
-// full hidden row; the conv is per channel along the token axis. The fused
-// kernel takes a tile of TT consecutive tokens and
-//   1. reduces the gate scalars of the tile and of its dilation halo (the
-//      (K-1)*d previous tokens of the same request) with one warp per token
-//      (16-byte loads, warp-shuffle reductions) into shared memory;
-//   2. walks the channels in chunks of CH: stages u = bf16(g * v) for the
-//      tile + halo in shared memory (the dilation window), then every thread
-//      produces 8 channels of one token from the K staged taps;
-//   3. writes the carry-over state of every request that ends in the tile.
-// u never goes to global memory; h and k are read once (halo rows are
-// re-read from L2 by the neighbouring tile), v once, y written once.
+// Design (HBM-bound: read h, k, v once, write y once; u never leaves the SM).
+// One 768-thread CTA per SM owns a contiguous token range [t0, t1):
+//   1. gate: one warp per row reduces sum h^2, sum k^2 and sum h*k*gh*gk over
+//      the full hidden row (16-byte loads, four 256-channel blocks of loads in
+//      flight per lane, warp-shuffle reductions) for the range and its
+//      dilation halo (the (K-1)*d previous tokens of the same request); the
+//      gate scalars go to shared memory;
+//   2. conv: a walker owns 8 channels and one residue class mod d of a
+//      segment of the range; since the taps of y_t are t, t-d, ..., t-(K-1)d,
+//      a ring of K gated values in registers holds the whole dilation window
+//      whatever d is: u = bf16(g*v) is computed once per token and every tap
+//      is a register read. Crossing into a new request reloads the ring from
+//      that request's carry-over state (or zeros); the walker holding a
+//      request's last token writes the new state.
 #include "common.cuh"
 
-#include <cooperative_groups.h>
 #include <cstdlib>
 
 namespace ple {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kGateThreads = 256;
+constexpr int kGateWarps = kGateThreads / 32;
+constexpr int kConvThreads = 768;
+constexpr int kConvWarps = kConvThreads / 32;
 constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
 
@@ -58,10 +61,26 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
   return v;
 }
 
+// u = bf16(g * v) for 8 packed bf16 values.
+__device__ __forceinline__ uint4 gate8(uint4 v, float g) {
+  float f[8];
+  unpack8(v, f);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] *= g;
+  return pack8(f);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+__device__ __forceinline__ float gate_of(float sh, float sk, float sd, int C, float eps) {
+  const float inv_c = 1.0f / static_cast<float>(C);
+  const float score = sd / (sqrtf(fmaf(sh, inv_c, eps)) * sqrtf(fmaf(sk, inv_c, eps))) /
+                      sqrtf(static_cast<float>(C));
+  return 1.0f / (1.0f + expf(-score));
 }
 
 // Gate scalar of one token, computed by a whole warp; every lane gets it.
@@ -85,25 +104,19 @@ __device__ __forceinline__ float gate_scalar(const ple_bf16_t* __restrict__ h_ro
       sd = fmaf(h[e] * gh[e], k[e] * gk[e], sd);
     }
   }
-  sh = warp_sum(sh);
-  sk = warp_sum(sk);
-  sd = warp_sum(sd);
-  const float inv_c = 1.0f / static_cast<float>(C);
-  const float score = sd / (sqrtf(fmaf(sh, inv_c, eps)) * sqrtf(fmaf(sk, inv_c, eps))) /
-                      sqrtf(static_cast<float>(C));
-  return 1.0f / (1.0f + expf(-score));
+  return gate_of(warp_sum(sh), warp_sum(sk), warp_sum(sd), C, eps);
 }
 
 // ---------------------------------------------------------------------------
 // ple_gate: one warp per token.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kGateThreads)
 gate_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
             const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
             float eps, int64_t T, int C, ple_bf16_t* __restrict__ out,
             float* __restrict__ gate_out) {
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5);
   if (t >= T) return;
   const ple_bf16_t* h_row = hidden + t * C;
   const ple_bf16_t* k_row = kv + t * 2 * C;
@@ -111,33 +124,12 @@ gate_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict_
   if (gate_out != nullptr && lane == 0) gate_out[t] = g;
   const ple_bf16_t* v_row = k_row + C;
 #pragma unroll 4
-  for (int c = lane * 8; c < C; c += 32 * 8) {
-    float v[8];
-    unpack8(ldg16(v_row + c), v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] *= g;
-    *reinterpret_cast<uint4*>(out + t * C + c) = pack8(v);
-  }
+  for (int c = lane * 8; c < C; c += 32 * 8)
+    *reinterpret_cast<uint4*>(out + t * C + c) = gate8(ldg16(v_row + c), g);
 }
 
 // ---------------------------------------------------------------------------
 // ple_conv (GATED = false, input x) and ple_gate_conv (GATED = true).
-//
-// Grid: one thread-block cluster of CL CTAs per tile of TT tokens; CTA
-// `part` of the cluster owns channels [part*slice, (part+1)*slice).
-//   0. the tile's request boundaries (binary search) go to shared memory;
-//   1. one thread issues bulk async copies of the v rows of the tile and its
-//      halo (only rows of the first tile token's request or later) into
-//      shared memory -- they land while step 2 runs;
-//   2. (gated) warps reduce sum h^2, sum k^2, sum h*gh*k*gk over the CTA's
-//      channel slice for every row; a cluster barrier publishes these partial
-//      sums and every CTA adds the CL partials of each row through
-//      distributed shared memory to get the gate scalars;
-//   3. after the copies land, each thread produces 8 channels of one token:
-//      u = bf16(g * v) for the K dilated taps (from shared memory, or the
-//      carry-over state before the request's first token), fp32 FMA with
-//      the taps, bf16 out; the CTA holding a request's last token writes that
-//      request's new state for its channels.
 // ---------------------------------------------------------------------------
 struct ConvArgs {
   const ple_bf16_t* hidden;   // gated only
@@ -157,271 +149,173 @@ struct ConvArgs {
   ple_bf16_t* out;
   float* gate_out;
   int32_t* dev_err;
-  int TT;      // tokens per tile
-  int CL;      // CTAs per tile (channel split; the cluster size when gated)
-  int slice;   // channels per CTA (multiple of 8)
 };
 
-struct ConvSmem {
-  // offsets in bytes from the dynamic shared-memory base
-  size_t v, w, part, g, start, end, req, bar, total;
+// Walks one (8-channel group, residue class rho mod d, token segment) of the
+// CTA's range: tokens t = s0 + rho, s0 + rho + d, ... < s1. The taps of y_t
+// sit at t, t-d, ..., t-(K-1)d -- all in the walker's own residue class -- so
+// a ring of K gated values (registers) holds the whole dilation window:
+// ring[i] = u of token t - (K-1-i)*d, and y_t = sum_i w[i] * ring[i].
+template <bool GATED, int KT>
+struct ConvWalker {
+  const ConvArgs& a;
+  const float* g_s;      // gate scalars, row i <-> token row0 + i
+  int64_t row0;          // t0 - W
+  int W, dil, C, c;
+  int64_t src_pitch, src_off;
+  uint4 wt[KT];          // taps of this thread's 8 channels, packed bf16
+
+  __device__ ConvWalker(const ConvArgs& args, const float* g, int64_t t0, int c_)
+      : a(args), g_s(g), c(c_) {
+    dil = a.dil;
+    W = (KT - 1) * dil;
+    C = a.C;
+    row0 = t0 - W;
+    src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
+    src_off = GATED ? C : 0;
+    const uint16_t* w = reinterpret_cast<const uint16_t*>(a.w);
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+      uint32_t p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        p[e] = static_cast<uint32_t>(__ldg(w + static_cast<int64_t>(c + 2 * e) * KT + i)) |
+               (static_cast<uint32_t>(__ldg(w + static_cast<int64_t>(c + 2 * e + 1) * KT + i)) << 16);
+      wt[i] = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+  }
+
+  // gated (or plain) input of token j of request r whose first token is start
+  __device__ __forceinline__ uint4 input(int64_t j, int r, int64_t start) const {
+    if (j >= start) {
+      const uint4 v = ldg16(a.src + j * src_pitch + src_off + c);
+      if constexpr (GATED) return gate8(v, g_s[j - row0]);
+      return v;
+    }
+    const int64_t hp = W + (j - start);  // history row, oldest first
+    if (a.state != nullptr && hp >= 0)
+      return ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
+    return make_uint4(0, 0, 0, 0);
+  }
+
+  __device__ __forceinline__ static void fma8(float acc[8], uint4 w, uint4 u) {
+    float f[8], g[8];
+    unpack8(u, f);
+    unpack8(w, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(g[e], f[e], acc[e]);
+  }
+
+  // Next request that owns token t (skips empty requests).
+  __device__ __forceinline__ void advance(int64_t t, int* r, int64_t* start, int64_t* end) const {
+    do {
+      ++*r;
+      request_span(a.qsl, a.num_reqs, a.T, *r, start, end);
+    } while (*end <= t && *r + 1 < a.num_reqs);
+  }
+
+  __device__ void run(int64_t s0, int64_t s1, int rho) {
+    int64_t t = s0 + rho;
+    if (t >= s1) return;
+    int r = find_request(a.qsl, a.num_reqs, t);
+    int64_t start, end;
+    request_span(a.qsl, a.num_reqs, a.T, r, &start, &end);
+    uint4 ring[KT];
+#pragma unroll
+    for (int i = 0; i < KT - 1; ++i)
+      ring[i + 1] = input(t - static_cast<int64_t>(KT - 1 - i) * dil, r, start);
+    for (; t < s1; t += dil) {
+      if (t >= end) {  // a new request: reload the window from its history
+        advance(t, &r, &start, &end);
+#pragma unroll
+        for (int i = 0; i < KT - 1; ++i)
+          ring[i + 1] = input(t - static_cast<int64_t>(KT - 1 - i) * dil, r, start);
+      }
+#pragma unroll
+      for (int i = 0; i < KT - 1; ++i) ring[i] = ring[i + 1];
+      ring[KT - 1] = input(t, r, start);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < KT; ++i) fma8(acc, wt[i], ring[i]);
+      *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
+      // The walker holding a request's last token writes its new state: the
+      // last W inputs of the request's virtual sequence (any residue class).
+      if (a.state_out != nullptr && W > 0 && t == end - 1) {
+        for (int jj = 0; jj < W; ++jj) {
+          const uint4 u = input(t - W + 1 + jj, r, start);
+          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
+        }
+      }
+    }
+  }
 };
 
-__host__ __device__ inline ConvSmem conv_smem_layout(int TT, int K, int dil, int slice) {
-  ConvSmem L;
-  const int rows = TT + (K - 1) * dil;
-  size_t off = 0;
-  L.v = off;      off += static_cast<size_t>(rows) * slice * 2;          // staged v rows
-  off = (off + 15) & ~size_t(15);
-  L.w = off;      off += static_cast<size_t>(K) * slice * 4;             // taps, [K][slice] f32
-  L.part = off;   off += static_cast<size_t>(rows) * 4 * 4;              // partial sums
-  L.g = off;      off += static_cast<size_t>(rows) * 4;                  // gate scalars
-  off = (off + 7) & ~size_t(7);
-  L.start = off;  off += static_cast<size_t>(TT) * 8;
-  L.end = off;    off += static_cast<size_t>(TT) * 8;
-  L.req = off;    off += static_cast<size_t>(TT) * 4;
-  off = (off + 7) & ~size_t(7);
-  L.bar = off;    off += 8;
-  L.total = off;
-  return L;
-}
-
-template <bool GATED>
-__global__ void __launch_bounds__(kThreads)
+template <bool GATED, int KT>
+__global__ void __launch_bounds__(kConvThreads, 1)
 conv_kernel(const __grid_constant__ ConvArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int W = (a.K - 1) * a.dil;
-  const int rows = a.TT + W;
+  extern __shared__ float g_s[];
+  const int dil = a.dil;
+  const int W = (KT - 1) * dil;
   const int C = a.C;
   const int64_t T = a.T;
-  const int slice = a.slice;
-  const int ng = slice / 8;                      // 16-byte channel groups per CTA
-  const ConvSmem L = conv_smem_layout(a.TT, a.K, a.dil, slice);
-  uint4* v_s = reinterpret_cast<uint4*>(smem + L.v);
-  float* w_s = reinterpret_cast<float*>(smem + L.w);
-  float4* part_s = reinterpret_cast<float4*>(smem + L.part);
-  float* g_s = reinterpret_cast<float*>(smem + L.g);
-  int64_t* start_s = reinterpret_cast<int64_t*>(smem + L.start);
-  int64_t* end_s = reinterpret_cast<int64_t*>(smem + L.end);
-  int* req_s = reinterpret_cast<int*>(smem + L.req);
-  const uint32_t bar = smem_u32(smem + L.bar);
-
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int tile = blockIdx.x / a.CL;
-  const int part = blockIdx.x % a.CL;
-  const int c0 = part * slice;
-  const int64_t t0 = static_cast<int64_t>(tile) * a.TT;
-  const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
-  const int64_t src_off = GATED ? C : 0;  // v sits after k in kv
+  const int64_t t0 = T * blockIdx.x / gridDim.x;
+  const int64_t t1 = T * (blockIdx.x + 1) / gridDim.x;
 
   if (blockIdx.x == 0)
-    for (int i = tid; i < a.num_reqs + 1; i += kThreads)
+    for (int i = tid; i < a.num_reqs + 1; i += kConvThreads)
       check_qsl(a.qsl, a.num_reqs, T, i, a.dev_err);
 
-  // 0. request of every tile token; taps of this CTA's channels
-  for (int i = tid; i < a.TT; i += kThreads) {
-    const int64_t t = t0 + i;
-    int r = 0;
-    int64_t s = 0, e = 0;
-    if (t < T) {
-      r = find_request(a.qsl, a.num_reqs, t);
-      request_span(a.qsl, a.num_reqs, T, r, &s, &e);
-    }
-    req_s[i] = r;
-    start_s[i] = s;
-    end_s[i] = e;
-  }
-  for (int idx = tid; idx < a.K * slice; idx += kThreads) {
-    const int i = idx / slice;
-    const int c = c0 + idx - i * slice;
-    w_s[idx] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.w)[static_cast<int64_t>(c) * a.K + i]);
-  }
-  for (int i = tid; i < rows; i += kThreads) part_s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  // Halo rows are needed only back to the start of the first tile token's
-  // request; earlier rows belong to other requests.
-  const int64_t lo = start_s[0];
-  const int i_lo = static_cast<int>(max(static_cast<int64_t>(0), lo - (t0 - W)));
-  const int i_hi = static_cast<int>(min(static_cast<int64_t>(rows), T - (t0 - W)));
+  // Rows before the start of t0's request belong to other requests.
+  int64_t lo, lo_end;
+  request_span(a.qsl, a.num_reqs, T, find_request(a.qsl, a.num_reqs, t0), &lo, &lo_end);
+  const int64_t row0 = t0 - W;
 
-  // 1. stage v rows [i_lo, i_hi) of this CTA's channels
-  if (tid == 0) {
-    const uint32_t row_bytes = static_cast<uint32_t>(slice) * 2;
-    const int n = i_hi > i_lo ? i_hi - i_lo : 0;
-    mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(n));
-    for (int i = i_lo; i < i_hi; ++i) {
-      const int64_t j = t0 - W + i;
-      bulk_copy_g2s(smem_u32(v_s) + static_cast<uint32_t>(i) * row_bytes,
-                    a.src + j * src_pitch + src_off + c0, row_bytes, bar);
-    }
-  }
-
-  // 2. gate scalars
+  // 1. gate scalars of rows [max(lo, row0), t1), one warp per row
   if constexpr (GATED) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int per_lane = (ng + 31) / 32;
-    for (int i = i_lo + warp; i < i_hi; i += kWarps) {
-      const int64_t j = t0 - W + i;
-      const ple_bf16_t* h_row = a.hidden + j * C + c0;
-      const ple_bf16_t* k_row = a.src + j * src_pitch + c0;
-      float sh = 0.f, sk = 0.f, sd = 0.f;
-      for (int m = 0; m < per_lane; ++m) {
-        const int cv = lane + 32 * m;
-        if (cv < ng) {
-          float h[8], k[8], gh[8], gk[8];
-          unpack8(ldg16(h_row + cv * 8), h);
-          unpack8(ldg16(k_row + cv * 8), k);
-          unpack8(ldg16(a.gamma_h + c0 + cv * 8), gh);
-          unpack8(ldg16(a.gamma_k + c0 + cv * 8), gk);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sh = fmaf(h[e], h[e], sh);
-            sk = fmaf(k[e], k[e], sk);
-            sd = fmaf(h[e] * gh[e], k[e] * gk[e], sd);
-          }
-        }
+    const int64_t first = lo > row0 ? lo : row0;
+    for (int64_t j = first + warp; j < t1; j += kConvWarps) {
+      const float g = gate_scalar(a.hidden + j * C, a.src + j * 2 * static_cast<int64_t>(C),
+                                  a.gamma_h, a.gamma_k, C, a.eps, lane);
+      if (lane == 0) {
+        g_s[j - row0] = g;
+        if (a.gate_out != nullptr && j >= t0) a.gate_out[j] = g;
       }
-      sh = warp_sum(sh);
-      sk = warp_sum(sk);
-      sd = warp_sum(sd);
-      if (lane == 0) part_s[i] = make_float4(sh, sk, sd, 0.f);
     }
-    cluster.sync();  // every CTA's partial sums are now visible cluster-wide
-    const float inv_c = 1.0f / static_cast<float>(C);
-    const float inv_sqrt_c = 1.0f / sqrtf(static_cast<float>(C));
-    for (int i = i_lo + tid; i < i_hi; i += kThreads) {
-      float sh = 0.f, sk = 0.f, sd = 0.f;
-      for (int r = 0; r < a.CL; ++r) {
-        const float4 p = *cluster.map_shared_rank(part_s + i, r);
-        sh += p.x;
-        sk += p.y;
-        sd += p.z;
-      }
-      const float score = sd / (sqrtf(fmaf(sh, inv_c, a.eps)) * sqrtf(fmaf(sk, inv_c, a.eps))) *
-                          inv_sqrt_c;
-      const float g = 1.0f / (1.0f + expf(-score));
-      g_s[i] = g;
-      const int64_t j = t0 - W + i;
-      if (part == 0 && a.gate_out != nullptr && i >= W) a.gate_out[j] = g;
-    }
+    __syncthreads();
   }
 
-  // 3. wait for the staged rows (bounded), then the dilated taps
-  const bool staged = mbar_wait(bar, 0, nullptr);
-  if (!staged && tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
-  __syncthreads();
-
-  if (staged) {
-    for (int idx = tid; idx < a.TT * ng; idx += kThreads) {
-      const int tt = idx / ng;
-      const int cv = idx - tt * ng;
-      const int64_t t = t0 + tt;
-      if (t >= T) continue;
-      const int c = c0 + cv * 8;
-      const int r = req_s[tt];
-      const int64_t start = start_s[tt];
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int i = 0; i < a.K; ++i) {
-        const int64_t j = t - static_cast<int64_t>(a.K - 1 - i) * a.dil;
-        float u[8];
-        if (j >= start) {
-          const int row = static_cast<int>(j - t0 + W);
-          unpack8(v_s[static_cast<size_t>(row) * ng + cv], u);
-          if constexpr (GATED) {
-            const float g = g_s[row];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = g * u[e];
-            unpack8(pack8(u), u);  // u is rounded to bf16 before the conv
-          }
-        } else {
-          const int64_t hp = W + (j - start);  // history row, oldest first
-          uint4 hv = make_uint4(0, 0, 0, 0);
-          if (a.state != nullptr && hp >= 0)
-            hv = ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
-          unpack8(hv, u);
-        }
-        const float4 w0 = *reinterpret_cast<const float4*>(w_s + i * slice + cv * 8);
-        const float4 w1 = *reinterpret_cast<const float4*>(w_s + i * slice + cv * 8 + 4);
-        acc[0] = fmaf(w0.x, u[0], acc[0]);
-        acc[1] = fmaf(w0.y, u[1], acc[1]);
-        acc[2] = fmaf(w0.z, u[2], acc[2]);
-        acc[3] = fmaf(w0.w, u[3], acc[3]);
-        acc[4] = fmaf(w1.x, u[4], acc[4]);
-        acc[5] = fmaf(w1.y, u[5], acc[5]);
-        acc[6] = fmaf(w1.z, u[6], acc[6]);
-        acc[7] = fmaf(w1.w, u[7], acc[7]);
-      }
-      *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
-
-      // Carry-over: the CTA holding a request's last token writes its state.
-      if (a.state_out != nullptr && W > 0 && t == end_s[tt] - 1) {
-        for (int jj = 0; jj < W; ++jj) {
-          const int64_t sj = t - W + 1 + jj;
-          uint4 sv = make_uint4(0, 0, 0, 0);
-          if (sj >= start) {
-            const int row = static_cast<int>(sj - t0 + W);
-            sv = v_s[static_cast<size_t>(row) * ng + cv];
-            if constexpr (GATED) {
-              float u[8];
-              unpack8(sv, u);
-              const float g = g_s[row];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) u[e] = g * u[e];
-              sv = pack8(u);
-            }
-          } else if (a.state != nullptr && W + (sj - start) >= 0) {
-            sv = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (sj - start)) * C + c);
-          }
-          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = sv;
-        }
-      }
-    }
+  // 2. the conv: walkers (channel group, residue class, segment)
+  const int ng = C / 8;
+  const int64_t n = t1 - t0;
+  const int64_t per_seg = static_cast<int64_t>(ng) * dil;
+  int64_t segs = kConvThreads / per_seg;
+  if (segs < 1) segs = 1;
+  const int64_t max_segs = (n + dil - 1) / dil;
+  if (segs > max_segs) segs = max_segs > 0 ? max_segs : 1;
+  for (int64_t item = tid; item < per_seg * segs; item += kConvThreads) {
+    const int cg = static_cast<int>(item % ng);
+    const int rho = static_cast<int>((item / ng) % dil);
+    const int64_t seg = item / per_seg;
+    ConvWalker<GATED, KT> walker(a, g_s, t0, cg * 8);
+    walker.run(t0 + n * seg / segs, t0 + n * (seg + 1) / segs, rho);
   }
 
-  // Requests with no tokens keep their state (tile 0 copies it through).
-  if (a.state_out != nullptr && W > 0 && tile == 0) {
+  // Requests with no tokens keep their state (CTA 0 copies it through).
+  if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
     for (int r = 0; r < a.num_reqs; ++r) {
       int64_t s, e;
       request_span(a.qsl, a.num_reqs, T, r, &s, &e);
       if (e != s) continue;
-      for (int idx = tid; idx < W * ng; idx += kThreads) {
-        const int64_t off = (static_cast<int64_t>(r) * W + idx / ng) * C + c0 + (idx % ng) * 8;
+      for (int idx = tid; idx < W * ng; idx += kConvThreads) {
+        const int64_t off = (static_cast<int64_t>(r) * W + idx / ng) * C + (idx % ng) * 8;
         const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(a.state_out + off) = v;
       }
     }
   }
-
-  if constexpr (GATED) {
-    // No CTA leaves while a peer may still read its partial sums.
-    cooperative_groups::this_cluster().sync();
-  }
-}
-
-// Launch shape: CL CTAs per tile splitting the channels (slices of >= 512
-// channels, a multiple of 8), TT tokens per tile so that the grid has at
-// least ~3 CTAs per SM. PLE_CONV_TILE / PLE_CONV_SPLIT override the choice
-// (launch-shape sweeps).
-void pick_conv_shape(int64_t T, int C, int* TT, int* CL) {
-  int cl = 8;
-  while (cl > 1 && (C % (cl * 8) != 0 || C / cl < 512)) cl >>= 1;
-  int tt = 64;
-  const int64_t target = 3 * static_cast<int64_t>(num_sms());
-  while (tt > 8 && ((T + tt - 1) / tt) * cl < target) tt >>= 1;
-  if (const char* e = getenv("PLE_CONV_TILE")) { int v = atoi(e); if (v >= 1 && v <= 256) tt = v; }
-  if (const char* e = getenv("PLE_CONV_SPLIT")) {
-    int v = atoi(e);
-    if (v >= 1 && v <= 8 && C % (v * 8) == 0) cl = v;
-  }
-  *TT = tt;
-  *CL = cl;
 }
 
 ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_t C,
@@ -442,6 +336,45 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   return PLE_OK;
 }
 
+// CTAs of the conv grid: one per SM, fewer when there are under 16 tokens per
+// SM. PLE_CONV_CTAS overrides the count (launch-shape sweeps).
+int conv_grid(int64_t T) {
+  int64_t g = num_sms();
+  const int64_t by_tokens = (T + 15) / 16;
+  if (by_tokens < g) g = by_tokens;
+  if (const char* e = getenv("PLE_CONV_CTAS")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 65535) g = v;
+  }
+  if (g > T) g = T;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <bool GATED>
+ple_status launch_conv(const ConvArgs& a, cudaStream_t stream, const char* name) {
+  const int grid = conv_grid(a.T);
+  const int64_t rows_max = (a.T + grid - 1) / grid + 1 + static_cast<int64_t>(a.K - 1) * a.dil;
+  const size_t smem = GATED ? static_cast<size_t>(rows_max) * sizeof(float) : 0;
+  if (smem > 200 * 1024)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: %zu bytes of gate scalars per CTA", name, smem);
+  void (*kernel)(ConvArgs) = nullptr;
+  switch (a.K) {
+    case 1: kernel = conv_kernel<GATED, 1>; break;
+    case 2: kernel = conv_kernel<GATED, 2>; break;
+    case 3: kernel = conv_kernel<GATED, 3>; break;
+    case 4: kernel = conv_kernel<GATED, 4>; break;
+    case 5: kernel = conv_kernel<GATED, 5>; break;
+    case 6: kernel = conv_kernel<GATED, 6>; break;
+    case 7: kernel = conv_kernel<GATED, 7>; break;
+    default: kernel = conv_kernel<GATED, 8>; break;
+  }
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return check_cuda(err, name);
+  kernel<<<grid, kConvThreads, smem, stream>>>(a);
+  return check_cuda(cudaGetLastError(), name);
+}
+
 }  // namespace
 }  // namespace ple
 
@@ -459,8 +392,8 @@ PLE_EXPORT ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
   if (!aligned16(hidden) || !aligned16(kv) || !aligned16(gamma_h) || !aligned16(gamma_k) ||
       !aligned16(out))
     return fail(PLE_ERR_INVALID_ARG, "ple_gate: buffers must be 16-byte aligned");
-  const int64_t blocks = (num_tokens + kWarps - 1) / kWarps;
-  gate_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+  const int64_t blocks = (num_tokens + kGateWarps - 1) / kGateWarps;
+  gate_kernel<<<static_cast<unsigned>(blocks), kGateThreads, 0, stream>>>(
       hidden, kv, gamma_h, gamma_k, eps, num_tokens, hidden_size, out, gate_out);
   return check_cuda(cudaGetLastError(), "ple_gate launch");
 }
@@ -500,32 +433,7 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   a.out = out;
   a.gate_out = gate_out;
   a.dev_err = dev_err;
-  pick_conv_shape(T, C, &a.TT, &a.CL);
-  a.slice = C / a.CL;
-  const ConvSmem L = conv_smem_layout(a.TT, K, dil, a.slice);
-  if (L.total > 227 * 1024)
-    return fail(PLE_ERR_UNSUPPORTED, "%s: %zu bytes of shared memory needed", name, L.total);
-  auto kernel = gated ? conv_kernel<true> : conv_kernel<false>;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(L.total));
-  if (err != cudaSuccess) return check_cuda(err, name);
-  const int64_t tiles = (T + a.TT - 1) / a.TT;
-  if (tiles * a.CL > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles * a.CL));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L.total;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = gated ? a.CL : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kernel, a);
-  if (err != cudaSuccess) return check_cuda(err, name);
-  return check_cuda(cudaGetLastError(), name);
+  return gated ? launch_conv<true>(a, stream, name) : launch_conv<false>(a, stream, name);
 }
 
 PLE_EXPORT ple_status ple_conv(const ple_bf16_t* x, const int32_t* query_start_loc,
