@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kGateThreads = 256;
 constexpr int kGateWarps = kGateThreads / 32;
-constexpr int kConvThreads = 768;
+constexpr int kConvThreads = 512;
 constexpr int kConvWarps = kConvThreads / 32;
 constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
@@ -83,25 +83,50 @@ __device__ __forceinline__ float gate_of(float sh, float sk, float sd, int C, fl
   return 1.0f / (1.0f + expf(-score));
 }
 
+// gamma_h[c] * gamma_k[c] for 8 channels, from the two bf16 vectors in
+// global memory (standalone gate) ...
+struct GammaFromGlobal {
+  const ple_bf16_t* gh;
+  const ple_bf16_t* gk;
+  __device__ __forceinline__ void operator()(int c, float out[8]) const {
+    float a[8], b[8];
+    unpack8(ldg16(gh + c), a);
+    unpack8(ldg16(gk + c), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[e] = a[e] * b[e];
+  }
+};
+
+// ... or precomputed once per CTA in shared memory (fused kernel). Both give
+// the same float32 products, so the two kernels agree bit for bit.
+struct GammaFromShared {
+  const float* gg;
+  __device__ __forceinline__ void operator()(int c, float out[8]) const {
+    const float4 x = *reinterpret_cast<const float4*>(gg + c);
+    const float4 y = *reinterpret_cast<const float4*>(gg + c + 4);
+    out[0] = x.x; out[1] = x.y; out[2] = x.z; out[3] = x.w;
+    out[4] = y.x; out[5] = y.y; out[6] = y.z; out[7] = y.w;
+  }
+};
+
 // Gate scalar of one token, computed by a whole warp; every lane gets it.
+// <rms(h)*gh, rms(k)*gk> = sum(h*k*gh*gk) / (rms_h * rms_k).
+template <class Gamma>
 __device__ __forceinline__ float gate_scalar(const ple_bf16_t* __restrict__ h_row,
                                              const ple_bf16_t* __restrict__ k_row,
-                                             const ple_bf16_t* __restrict__ gamma_h,
-                                             const ple_bf16_t* __restrict__ gamma_k,
-                                             int C, float eps, int lane) {
+                                             const Gamma& gamma, int C, float eps, int lane) {
   float sh = 0.f, sk = 0.f, sd = 0.f;
 #pragma unroll 4
   for (int c = lane * 8; c < C; c += 32 * 8) {
-    float h[8], k[8], gh[8], gk[8];
+    float h[8], k[8], g[8];
     unpack8(ldg16(h_row + c), h);
     unpack8(ldg16(k_row + c), k);
-    unpack8(ldg16(gamma_h + c), gh);
-    unpack8(ldg16(gamma_k + c), gk);
+    gamma(c, g);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       sh = fmaf(h[e], h[e], sh);
       sk = fmaf(k[e], k[e], sk);
-      sd = fmaf(h[e] * gh[e], k[e] * gk[e], sd);
+      sd = fmaf(h[e] * k[e], g[e], sd);
     }
   }
   return gate_of(warp_sum(sh), warp_sum(sk), warp_sum(sd), C, eps);
@@ -120,7 +145,7 @@ gate_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict_
   if (t >= T) return;
   const ple_bf16_t* h_row = hidden + t * C;
   const ple_bf16_t* k_row = kv + t * 2 * C;
-  const float g = gate_scalar(h_row, k_row, gamma_h, gamma_k, C, eps, lane);
+  const float g = gate_scalar(h_row, k_row, GammaFromGlobal{gamma_h, gamma_k}, C, eps, lane);
   if (gate_out != nullptr && lane == 0) gate_out[t] = g;
   const ple_bf16_t* v_row = k_row + C;
 #pragma unroll 4
@@ -151,164 +176,275 @@ struct ConvArgs {
   int32_t* dev_err;
 };
 
-// Walks one (8-channel group, residue class rho mod d, token segment) of the
-// CTA's range: tokens t = s0 + rho, s0 + rho + d, ... < s1. The taps of y_t
-// sit at t, t-d, ..., t-(K-1)d -- all in the walker's own residue class -- so
-// a ring of K gated values (registers) holds the whole dilation window:
-// ring[i] = u of token t - (K-1-i)*d, and y_t = sum_i w[i] * ring[i].
-template <bool GATED, int KT>
-struct ConvWalker {
-  const ConvArgs& a;
-  const float* g_s;      // gate scalars, row i <-> token row0 + i
-  int64_t row0;          // t0 - W
-  int W, dil, C, c;
-  int64_t src_pitch, src_off;
-  uint4 wt[KT];          // taps of this thread's 8 channels, packed bf16
+// Request boundaries of the requests a CTA touches, staged in shared memory
+// (falls back to global memory when there are too many).
+struct Bounds {
+  const int32_t* qsl;    // global
+  const int32_t* s;      // shared copy of qsl[r0 .. r0 + n], or nullptr
+  int r0, n, num_reqs;
+  int64_t T;
 
-  __device__ ConvWalker(const ConvArgs& args, const float* g, int64_t t0, int c_)
-      : a(args), g_s(g), c(c_) {
-    dil = a.dil;
-    W = (KT - 1) * dil;
-    C = a.C;
-    row0 = t0 - W;
-    src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
-    src_off = GATED ? C : 0;
-    const uint16_t* w = reinterpret_cast<const uint16_t*>(a.w);
-#pragma unroll
-    for (int i = 0; i < KT; ++i) {
-      uint32_t p[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        p[e] = static_cast<uint32_t>(__ldg(w + static_cast<int64_t>(c + 2 * e) * KT + i)) |
-               (static_cast<uint32_t>(__ldg(w + static_cast<int64_t>(c + 2 * e + 1) * KT + i)) << 16);
-      wt[i] = make_uint4(p[0], p[1], p[2], p[3]);
+  __device__ __forceinline__ int find(int64_t t) const {
+    if (s == nullptr) return find_request(qsl, num_reqs, t);
+    int lo = 0, hi = n + 1;  // count of staged boundaries <= t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int64_t>(s[mid]) <= t) lo = mid + 1; else hi = mid;
     }
+    int r = r0 + lo - 1;
+    r = r < r0 ? r0 : r;
+    return r >= num_reqs ? num_reqs - 1 : r;
   }
-
-  // gated (or plain) input of token j of request r whose first token is start
-  __device__ __forceinline__ uint4 input(int64_t j, int r, int64_t start) const {
-    if (j >= start) {
-      const uint4 v = ldg16(a.src + j * src_pitch + src_off + c);
-      if constexpr (GATED) return gate8(v, g_s[j - row0]);
-      return v;
+  __device__ __forceinline__ void span(int r, int64_t* start, int64_t* end) const {
+    if (s == nullptr || r < r0 || r >= r0 + n) {
+      request_span(qsl, num_reqs, T, r, start, end);
+      return;
     }
-    const int64_t hp = W + (j - start);  // history row, oldest first
-    if (a.state != nullptr && hp >= 0)
-      return ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
-    return make_uint4(0, 0, 0, 0);
-  }
-
-  __device__ __forceinline__ static void fma8(float acc[8], uint4 w, uint4 u) {
-    float f[8], g[8];
-    unpack8(u, f);
-    unpack8(w, g);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(g[e], f[e], acc[e]);
-  }
-
-  // Next request that owns token t (skips empty requests).
-  __device__ __forceinline__ void advance(int64_t t, int* r, int64_t* start, int64_t* end) const {
-    do {
-      ++*r;
-      request_span(a.qsl, a.num_reqs, a.T, *r, start, end);
-    } while (*end <= t && *r + 1 < a.num_reqs);
-  }
-
-  __device__ void run(int64_t s0, int64_t s1, int rho) {
-    int64_t t = s0 + rho;
-    if (t >= s1) return;
-    int r = find_request(a.qsl, a.num_reqs, t);
-    int64_t start, end;
-    request_span(a.qsl, a.num_reqs, a.T, r, &start, &end);
-    uint4 ring[KT];
-#pragma unroll
-    for (int i = 0; i < KT - 1; ++i)
-      ring[i + 1] = input(t - static_cast<int64_t>(KT - 1 - i) * dil, r, start);
-    for (; t < s1; t += dil) {
-      if (t >= end) {  // a new request: reload the window from its history
-        advance(t, &r, &start, &end);
-#pragma unroll
-        for (int i = 0; i < KT - 1; ++i)
-          ring[i + 1] = input(t - static_cast<int64_t>(KT - 1 - i) * dil, r, start);
-      }
-#pragma unroll
-      for (int i = 0; i < KT - 1; ++i) ring[i] = ring[i + 1];
-      ring[KT - 1] = input(t, r, start);
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < KT; ++i) fma8(acc, wt[i], ring[i]);
-      *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
-      // The walker holding a request's last token writes its new state: the
-      // last W inputs of the request's virtual sequence (any residue class).
-      if (a.state_out != nullptr && W > 0 && t == end - 1) {
-        for (int jj = 0; jj < W; ++jj) {
-          const uint4 u = input(t - W + 1 + jj, r, start);
-          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
-        }
-      }
-    }
+    int64_t st = s[r - r0];
+    int64_t e = (r + 1 < num_reqs) ? static_cast<int64_t>(s[r + 1 - r0]) : T;
+    st = st < 0 ? 0 : (st > T ? T : st);
+    e = e < st ? st : (e > T ? T : e);
+    *start = st;
+    *end = e;
   }
 };
 
-template <bool GATED, int KT>
+constexpr int kStagedBounds = 1024;  // request boundaries staged per CTA
+constexpr int kMaxTileTokens = 64;   // tokens per CTA (bounds the staged window)
+
+// Shared-memory layout of conv_kernel (byte offsets).
+struct ConvLayout {
+  size_t gg, bounds, g, tok, w, buf0, buf_bytes, bars, total;
+  int rows, chunk;
+};
+
+__host__ __device__ inline ConvLayout conv_layout(int C, int W, int tile_tokens, bool gated,
+                                                  int chunk) {
+  ConvLayout L;
+  L.rows = tile_tokens + W;
+  L.chunk = chunk;
+  size_t off = 0;
+  L.gg = off;      off += gated ? static_cast<size_t>(C) * 4 : 0;       // gamma_h * gamma_k
+  L.bounds = off;  off += kStagedBounds * 4;                            // query_start_loc slice
+  L.g = off;       off += static_cast<size_t>(L.rows) * 4;              // gate scalars
+  off = (off + 15) & ~size_t(15);
+  L.tok = off;     off += static_cast<size_t>(tile_tokens) * 16;        // per-token (start, end, req)
+  L.w = off;       off += static_cast<size_t>(kMaxK) * chunk * 4;       // taps of the chunk, f32
+  off = (off + 127) & ~size_t(127);
+  L.buf0 = off;
+  L.buf_bytes = static_cast<size_t>(L.rows) * chunk * 2;                // one window buffer
+  off += 2 * L.buf_bytes;
+  off = (off + 7) & ~size_t(7);
+  L.bars = off;    off += 16;
+  L.total = off;
+  return L;
+}
+
+// Channel chunk of the staged window: the widest of 512/256/128/64/.../8
+// channels dividing C whose two buffers fit next to the rest.
+__host__ __device__ inline int conv_chunk(int C, int W, int tile_tokens, bool gated) {
+  for (int ch = 512; ch >= 8; ch >>= 1) {
+    if (C % ch != 0) continue;
+    if (conv_layout(C, W, tile_tokens, gated, ch).total <= 200 * 1024) return ch;
+  }
+  return 0;
+}
+
+template <bool GATED>
 __global__ void __launch_bounds__(kConvThreads, 1)
-conv_kernel(const __grid_constant__ ConvArgs a) {
-  extern __shared__ float g_s[];
+conv_kernel(const __grid_constant__ ConvArgs a, int tile_tokens, int chunk) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int K = a.K;
   const int dil = a.dil;
-  const int W = (KT - 1) * dil;
+  const int W = (K - 1) * dil;
   const int C = a.C;
   const int64_t T = a.T;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int64_t t0 = T * blockIdx.x / gridDim.x;
-  const int64_t t1 = T * (blockIdx.x + 1) / gridDim.x;
+  const ConvLayout L = conv_layout(C, W, tile_tokens, GATED, chunk);
+  float* gg_s = reinterpret_cast<float*>(smem + L.gg);
+  int32_t* qsl_s = reinterpret_cast<int32_t*>(smem + L.bounds);
+  float* g_s = reinterpret_cast<float*>(smem + L.g);
+  int4* tok_s = reinterpret_cast<int4*>(smem + L.tok);   // (start - t0, end - t0, request) per token
+  float* w_s = reinterpret_cast<float*>(smem + L.w);      // [K][chunk]
+  const uint32_t bar0 = smem_u32(smem + L.bars);
+  auto buffer = [&](int bsel) {
+    return reinterpret_cast<uint4*>(smem + L.buf0 + static_cast<size_t>(bsel) * L.buf_bytes);
+  };
+
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tile_tokens;
+  const int64_t t1 = t0 + tile_tokens < T ? t0 + tile_tokens : T;
+  const int n_tok = static_cast<int>(t1 - t0);
+  const int64_t row0 = t0 - W;              // window row i <-> token row0 + i
+  const int vecs = chunk / 8;                // 16-byte vectors per window row
+  const int n_chunks = C / chunk;
+  const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
+  const int64_t src_off = GATED ? C : 0;    // v sits after k in kv
 
   if (blockIdx.x == 0)
     for (int i = tid; i < a.num_reqs + 1; i += kConvThreads)
       check_qsl(a.qsl, a.num_reqs, T, i, a.dev_err);
 
-  // Rows before the start of t0's request belong to other requests.
-  int64_t lo, lo_end;
-  request_span(a.qsl, a.num_reqs, T, find_request(a.qsl, a.num_reqs, t0), &lo, &lo_end);
-  const int64_t row0 = t0 - W;
-
-  // 1. gate scalars of rows [max(lo, row0), t1), one warp per row
+  // Boundaries of the requests the tile and its halo touch.
+  const int r_lo = find_request(a.qsl, a.num_reqs, row0 > 0 ? row0 : 0);
+  const int r_hi = find_request(a.qsl, a.num_reqs, t1 - 1);
+  const int nb = r_hi - r_lo + 1;
+  const bool staged = nb >= 1 && nb + 1 <= kStagedBounds;
+  if (staged)
+    for (int i = tid; i <= nb; i += kConvThreads)
+      qsl_s[i] = (r_lo + i <= a.num_reqs) ? __ldg(a.qsl + r_lo + i) : static_cast<int32_t>(T);
   if constexpr (GATED) {
-    const int64_t first = lo > row0 ? lo : row0;
-    for (int64_t j = first + warp; j < t1; j += kConvWarps) {
-      const float g = gate_scalar(a.hidden + j * C, a.src + j * 2 * static_cast<int64_t>(C),
-                                  a.gamma_h, a.gamma_k, C, a.eps, lane);
+    for (int c = tid; c < C; c += kConvThreads)
+      gg_s[c] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.gamma_h)[c]) *
+                __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.gamma_k)[c]);
+  }
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const Bounds b{a.qsl, staged ? qsl_s : nullptr, r_lo, nb, a.num_reqs, T};
+  for (int i = tid; i < n_tok; i += kConvThreads) {
+    const int r = b.find(t0 + i);
+    int64_t st, en;
+    b.span(r, &st, &en);
+    tok_s[i] = make_int4(static_cast<int>(st - t0), static_cast<int>(en - t0), r, 0);
+  }
+  // Window rows before the start of t0's request belong to other requests.
+  int64_t lo, lo_end;
+  b.span(b.find(t0), &lo, &lo_end);
+  const int i_lo = static_cast<int>(lo > row0 ? lo - row0 : 0);
+  const int i_hi = W + n_tok;
+  const uint32_t row_bytes = static_cast<uint32_t>(chunk) * 2;
+
+  // Issue the bulk copies of window chunk k (rows [i_lo, i_hi)) into buffer k % 2.
+  int issued[2] = {0, 0};  // copies issued into each buffer (uniform over the CTA)
+  auto issue = [&](int k) {
+    const int bsel = k & 1;
+    ++issued[bsel];
+    if (warp == 0) {
+      const uint32_t bar = bar0 + 8u * bsel;
+      if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(i_hi - i_lo));
+      __syncwarp();
+      const int c0 = k * chunk;
+      for (int i = i_lo + lane; i < i_hi; i += 32)
+        bulk_copy_g2s(smem_u32(buffer(bsel)) + static_cast<uint32_t>(i) * row_bytes,
+                      a.src + (row0 + i) * src_pitch + src_off + c0, row_bytes, bar);
+    }
+  };
+  issue(0);
+  if (n_chunks > 1) issue(1);
+
+  // 1. gate scalars of window rows [i_lo, i_hi), one warp per row (overlaps the copies)
+  if constexpr (GATED) {
+    const GammaFromShared gamma{gg_s};
+    for (int i = i_lo + warp; i < i_hi; i += kConvWarps) {
+      const int64_t j = row0 + i;
+      const float g = gate_scalar(a.hidden + j * C, a.src + j * src_pitch, gamma, C, a.eps, lane);
       if (lane == 0) {
-        g_s[j - row0] = g;
-        if (a.gate_out != nullptr && j >= t0) a.gate_out[j] = g;
+        g_s[i] = g;
+        if (a.gate_out != nullptr && i >= W) a.gate_out[j] = g;
       }
     }
-    __syncthreads();
   }
+  __syncthreads();
 
-  // 2. the conv: walkers (channel group, residue class, segment)
-  const int ng = C / 8;
-  const int64_t n = t1 - t0;
-  const int64_t per_seg = static_cast<int64_t>(ng) * dil;
-  int64_t segs = kConvThreads / per_seg;
-  if (segs < 1) segs = 1;
-  const int64_t max_segs = (n + dil - 1) / dil;
-  if (segs > max_segs) segs = max_segs > 0 ? max_segs : 1;
-  for (int64_t item = tid; item < per_seg * segs; item += kConvThreads) {
-    const int cg = static_cast<int>(item % ng);
-    const int rho = static_cast<int>((item / ng) % dil);
-    const int64_t seg = item / per_seg;
-    ConvWalker<GATED, KT> walker(a, g_s, t0, cg * 8);
-    walker.run(t0 + n * seg / segs, t0 + n * (seg + 1) / segs, rho);
+  // 2. per channel chunk: wait for the window, gate it in place, convolve
+  bool ok = true;
+  for (int k = 0; k < n_chunks && ok; ++k) {
+    const int bsel = k & 1;
+    const uint32_t parity = static_cast<uint32_t>(k >> 1) & 1u;
+    ok = mbar_wait(bar0 + 8u * bsel, parity, nullptr);
+    if (!ok) {
+      if (tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
+      break;
+    }
+    uint4* win = buffer(bsel);
+    const int c0 = k * chunk;
+    if constexpr (GATED) {
+      for (int idx = i_lo * vecs + tid; idx < i_hi * vecs; idx += kConvThreads)
+        win[idx] = gate8(win[idx], g_s[idx / vecs]);
+    }
+    for (int idx = tid; idx < K * chunk; idx += kConvThreads) {
+      const int i = idx / chunk;
+      const int cc = idx - i * chunk;
+      w_s[idx] = __uint_as_float(static_cast<uint32_t>(__ldg(
+                     reinterpret_cast<const uint16_t*>(a.w) + static_cast<int64_t>(c0 + cc) * K + i)) << 16);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < n_tok * vecs; idx += kConvThreads) {
+      const int tt = idx / vecs;
+      const int cv = idx - tt * vecs;
+      const int c = c0 + cv * 8;
+      const int64_t t = t0 + tt;
+      const int4 sr = tok_s[tt];
+      const int64_t start = t0 + sr.x;
+      const int64_t end = t0 + sr.y;
+      const int r = sr.z;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int i = 0; i < K; ++i) {
+        const int64_t j = t - static_cast<int64_t>(K - 1 - i) * dil;
+        uint4 u;
+        if (j >= start) {
+          u = win[static_cast<int>(j - row0) * vecs + cv];
+        } else {
+          const int64_t hp = W + (j - start);  // history row, oldest first
+          u = (a.state != nullptr && hp >= 0)
+                  ? ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c)
+                  : make_uint4(0, 0, 0, 0);
+        }
+        float f[8];
+        unpack8(u, f);
+        const float4 w0 = *reinterpret_cast<const float4*>(w_s + i * chunk + cv * 8);
+        const float4 w1 = *reinterpret_cast<const float4*>(w_s + i * chunk + cv * 8 + 4);
+        acc[0] = fmaf(w0.x, f[0], acc[0]);
+        acc[1] = fmaf(w0.y, f[1], acc[1]);
+        acc[2] = fmaf(w0.z, f[2], acc[2]);
+        acc[3] = fmaf(w0.w, f[3], acc[3]);
+        acc[4] = fmaf(w1.x, f[4], acc[4]);
+        acc[5] = fmaf(w1.y, f[5], acc[5]);
+        acc[6] = fmaf(w1.z, f[6], acc[6]);
+        acc[7] = fmaf(w1.w, f[7], acc[7]);
+      }
+      *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
+      // Carry-over: the thread holding a request's last token writes its state.
+      if (a.state_out != nullptr && W > 0) {
+        if (t == end - 1) {
+          for (int jj = 0; jj < W; ++jj) {
+            const int64_t sj = t - W + 1 + jj;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (sj >= start) u = win[static_cast<int>(sj - row0) * vecs + cv];
+            else if (a.state != nullptr && W + (sj - start) >= 0)
+              u = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (sj - start)) * C + c);
+            *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
+          }
+        }
+      }
+    }
+    // The buffer was written by generic stores (the gating) and is about to
+    // be refilled by async-proxy copies: every writer fences before the
+    // barrier that precedes the refill.
+    if (k + 2 < n_chunks) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();  // every access to this buffer is done
+    if (k + 2 < n_chunks) issue(k + 2);
+  }
+  if (!ok) {
+    // never leave with copies in flight into this CTA's shared memory: wait
+    // (bounded) for the last fill of each buffer
+    for (int bsel = 0; bsel < 2; ++bsel)
+      if (issued[bsel] > 0)
+        mbar_wait(bar0 + 8u * bsel, static_cast<uint32_t>(issued[bsel] - 1) & 1u, nullptr);
   }
 
   // Requests with no tokens keep their state (CTA 0 copies it through).
   if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
+    const int ng = C / 8;
     for (int r = 0; r < a.num_reqs; ++r) {
-      int64_t s, e;
-      request_span(a.qsl, a.num_reqs, T, r, &s, &e);
-      if (e != s) continue;
+      int64_t s0, e0;
+      request_span(a.qsl, a.num_reqs, T, r, &s0, &e0);
+      if (e0 != s0) continue;
       for (int idx = tid; idx < W * ng; idx += kConvThreads) {
         const int64_t off = (static_cast<int64_t>(r) * W + idx / ng) * C + (idx % ng) * 8;
         const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
@@ -336,42 +472,32 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   return PLE_OK;
 }
 
-// CTAs of the conv grid: one per SM, fewer when there are under 16 tokens per
-// SM. PLE_CONV_CTAS overrides the count (launch-shape sweeps).
-int conv_grid(int64_t T) {
-  int64_t g = num_sms();
-  const int64_t by_tokens = (T + 15) / 16;
-  if (by_tokens < g) g = by_tokens;
-  if (const char* e = getenv("PLE_CONV_CTAS")) {
+// Tokens per CTA: enough CTAs for every SM, at most kMaxTileTokens.
+// PLE_CONV_TILE overrides (launch-shape sweeps).
+int conv_tile_tokens(int64_t T) {
+  int64_t per = (T + num_sms() - 1) / num_sms();
+  if (per < 4) per = 4;
+  if (per > kMaxTileTokens) per = kMaxTileTokens;
+  if (const char* e = getenv("PLE_CONV_TILE")) {
     const int v = atoi(e);
-    if (v >= 1 && v <= 65535) g = v;
+    if (v >= 1 && v <= kMaxTileTokens) per = v;
   }
-  if (g > T) g = T;
-  return static_cast<int>(g < 1 ? 1 : g);
+  return static_cast<int>(per);
 }
 
 template <bool GATED>
 ple_status launch_conv(const ConvArgs& a, cudaStream_t stream, const char* name) {
-  const int grid = conv_grid(a.T);
-  const int64_t rows_max = (a.T + grid - 1) / grid + 1 + static_cast<int64_t>(a.K - 1) * a.dil;
-  const size_t smem = GATED ? static_cast<size_t>(rows_max) * sizeof(float) : 0;
-  if (smem > 200 * 1024)
-    return fail(PLE_ERR_UNSUPPORTED, "%s: %zu bytes of gate scalars per CTA", name, smem);
-  void (*kernel)(ConvArgs) = nullptr;
-  switch (a.K) {
-    case 1: kernel = conv_kernel<GATED, 1>; break;
-    case 2: kernel = conv_kernel<GATED, 2>; break;
-    case 3: kernel = conv_kernel<GATED, 3>; break;
-    case 4: kernel = conv_kernel<GATED, 4>; break;
-    case 5: kernel = conv_kernel<GATED, 5>; break;
-    case 6: kernel = conv_kernel<GATED, 6>; break;
-    case 7: kernel = conv_kernel<GATED, 7>; break;
-    default: kernel = conv_kernel<GATED, 8>; break;
-  }
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  const int W = (a.K - 1) * a.dil;
+  const int tile = conv_tile_tokens(a.T);
+  const int chunk = conv_chunk(a.C, W, tile, GATED);
+  if (chunk == 0) return fail(PLE_ERR_UNSUPPORTED, "%s: window does not fit in shared memory", name);
+  const ConvLayout L = conv_layout(a.C, W, tile, GATED, chunk);
+  cudaError_t err = cudaFuncSetAttribute(conv_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L.total));
   if (err != cudaSuccess) return check_cuda(err, name);
-  kernel<<<grid, kConvThreads, smem, stream>>>(a);
+  const int64_t grid = (a.T + tile - 1) / tile;
+  if (grid > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
+  conv_kernel<GATED><<<static_cast<unsigned>(grid), kConvThreads, L.total, stream>>>(a, tile, chunk);
   return check_cuda(cudaGetLastError(), name);
 }
 

@@ -194,3 +194,38 @@ def test_prefill_8k_full_size_table():
     assert np.array_equal(bits(out)[sample], ref)
     del table
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_uva_gather_in_windows(dtype, monkeypatch):
+    """Host tables are gathered one address window at a time; with 1 MB
+    windows over a ~10 MB table every row must still land exactly once."""
+    monkeypatch.setenv("PLE_UVA_WINDOW_MB", "1")
+    rng = np.random.default_rng(12)
+    D, T, H = 128, 700, 16
+    if dtype == "bf16":
+        rows = 40000
+        table = random_table_bits(rng, rows, D)
+        host = to_dev_bf16(table, pinned=True)
+        scale = None
+    else:
+        rows = 80000
+        codes = rng.integers(0, 0x7E, size=(rows, D), dtype=np.uint8)
+        sc = (np.abs(rng.standard_normal(rows)) * 1e-3 + 1e-6).astype(np.float32)
+        host = torch.from_numpy(codes).pin_memory()
+        scale = torch.from_numpy(sc).cuda()
+    ids = rng.integers(0, rows, size=(T, H))
+    ids[3, 2] = rows + 5          # outside the table: zero row + flag
+    ids[9, 0] = -7
+    out = torch.full((T, H * D), 3.0, dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), host, out, row_scale=scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & _lib.PLE_DEVERR_BOUNDS
+    ok = ids.copy()
+    ok[3, 2] = 0
+    ok[9, 0] = 0
+    ref = lookup_bf16(ok, table) if dtype == "bf16" else lookup_fp8(ok, codes, sc)
+    ref[3, 2 * D:3 * D] = 0
+    ref[9, 0:D] = 0
+    assert np.array_equal(bits(out), ref)
