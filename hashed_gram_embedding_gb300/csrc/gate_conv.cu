@@ -209,6 +209,83 @@ struct Bounds {
   }
 };
 
+// One walker: tokens tt = first, first + d, ... < s1 of the tile (tile-relative),
+// for 8 channels c..c+7 of the current window chunk.
+template <bool GATED, int K>
+struct ConvWalker {
+  static __device__ __forceinline__ void load_u(const ConvArgs& a, const uint4* win, const float* g_s,
+                                                int vecs, int cv, int c, int64_t j, int64_t start,
+                                                int r, int64_t row0, int W, float u[8]) {
+    if (j >= start) {
+      const int row = static_cast<int>(j - row0);
+      unpack8(win[row * vecs + cv], u);
+      if constexpr (GATED) {
+        const float g = g_s[row];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = g * u[e];
+        unpack8(pack8(u), u);  // u is a bf16 value (a step boundary)
+      }
+    } else {
+      const int64_t hp = W + (j - start);  // history row, oldest first
+      uint4 h = make_uint4(0, 0, 0, 0);
+      if (a.state != nullptr && hp >= 0)
+        h = ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * a.C + c);
+      unpack8(h, u);
+    }
+  }
+
+  static __device__ void run(const ConvArgs& a, const uint4* win, const float* g_s,
+                             const float* w_col, int chunk, int vecs, int cv, int c,
+                             const int4* tok_s, int64_t t0, int64_t row0, int W, int dil,
+                             int first, int s1) {
+    if (first >= s1) return;
+    float wt[K][8];
+    float ring[K][8];  // ring[K-1] = u of the current token, ring[K-1-m] = m*d back
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const float4 w0 = *reinterpret_cast<const float4*>(w_col + i * chunk);
+      const float4 w1 = *reinterpret_cast<const float4*>(w_col + i * chunk + 4);
+      wt[i][0] = w0.x; wt[i][1] = w0.y; wt[i][2] = w0.z; wt[i][3] = w0.w;
+      wt[i][4] = w1.x; wt[i][5] = w1.y; wt[i][6] = w1.z; wt[i][7] = w1.w;
+    }
+    int cur_start = -1 << 30;  // tile-relative start of the ring's request
+    for (int tt = first; tt < s1; tt += dil) {
+      const int4 sr = tok_s[tt];  // (start - t0, end - t0, request)
+      const int64_t t = t0 + tt;
+      const int64_t start = t0 + sr.x;
+      if (sr.x != cur_start) {  // first token of the walk or a new request: refill
+        cur_start = sr.x;
+#pragma unroll
+        for (int m = 1; m < K; ++m)
+          load_u(a, win, g_s, vecs, cv, c, t - static_cast<int64_t>(m) * dil, start, sr.z, row0, W,
+                 ring[K - 1 - m]);
+      } else {
+#pragma unroll
+        for (int i = 0; i + 1 < K; ++i)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ring[i][e] = ring[i + 1][e];
+      }
+      load_u(a, win, g_s, vecs, cv, c, t, start, sr.z, row0, W, ring[K - 1]);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < K; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wt[i][e], ring[i][e], acc[e]);
+      *reinterpret_cast<uint4*>(a.out + t * a.C + c) = pack8(acc);
+      // Carry-over: the walker holding a request's last token writes the
+      // request's new state (the last W inputs, any residue class).
+      if (a.state_out != nullptr && W > 0 && tt == sr.y - 1) {
+        for (int jj = 0; jj < W; ++jj) {
+          float u[8];
+          load_u(a, win, g_s, vecs, cv, c, t - W + 1 + jj, start, sr.z, row0, W, u);
+          *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(sr.z) * W + jj) * a.C + c) =
+              pack8(u);
+        }
+      }
+    }
+  }
+};
+
 constexpr int kStagedBounds = 1024;  // request boundaries staged per CTA
 constexpr int kMaxTileTokens = 64;   // tokens per CTA (bounds the staged window)
 
@@ -250,11 +327,10 @@ __host__ __device__ inline int conv_chunk(int C, int W, int tile_tokens, bool ga
   return 0;
 }
 
-template <bool GATED>
+template <bool GATED, int K>
 __global__ void __launch_bounds__(kConvThreads, 1)
 conv_kernel(const __grid_constant__ ConvArgs a, int tile_tokens, int chunk) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int K = a.K;
   const int dil = a.dil;
   const int W = (K - 1) * dil;
   const int C = a.C;
@@ -351,91 +427,53 @@ conv_kernel(const __grid_constant__ ConvArgs a, int tile_tokens, int chunk) {
   }
   __syncthreads();
 
-  // 2. per channel chunk: wait for the window, gate it in place, convolve
+  // 2. per channel chunk: wait for the window, then walkers convolve it.
+  //    A walker owns 8 channels, one residue class rho mod d and a segment of
+  //    the tile; the taps of y_t sit at t, t-d, ..., t-(K-1)d, all in its own
+  //    class, so a ring of K gated values (float32 registers) holds the
+  //    dilation window and each gated value is computed once.
+  const int per_seg = vecs * dil;
+  int segs = kConvThreads / per_seg;
+  if (segs < 1) segs = 1;
+  const int max_segs = (n_tok + dil - 1) / dil;
+  if (segs > max_segs) segs = max_segs > 0 ? max_segs : 1;
   bool ok = true;
-  for (int k = 0; k < n_chunks && ok; ++k) {
-    const int bsel = k & 1;
-    const uint32_t parity = static_cast<uint32_t>(k >> 1) & 1u;
-    ok = mbar_wait(bar0 + 8u * bsel, parity, nullptr);
-    if (!ok) {
-      if (tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
-      break;
-    }
-    uint4* win = buffer(bsel);
-    const int c0 = k * chunk;
-    if constexpr (GATED) {
-      for (int idx = i_lo * vecs + tid; idx < i_hi * vecs; idx += kConvThreads)
-        win[idx] = gate8(win[idx], g_s[idx / vecs]);
-    }
+  for (int kc = 0; kc < n_chunks && ok; ++kc) {
+    const int bsel = kc & 1;
+    const uint32_t parity = static_cast<uint32_t>(kc >> 1) & 1u;
+    const int c0 = kc * chunk;
     for (int idx = tid; idx < K * chunk; idx += kConvThreads) {
       const int i = idx / chunk;
       const int cc = idx - i * chunk;
       w_s[idx] = __uint_as_float(static_cast<uint32_t>(__ldg(
                      reinterpret_cast<const uint16_t*>(a.w) + static_cast<int64_t>(c0 + cc) * K + i)) << 16);
     }
-    __syncthreads();
-    for (int idx = tid; idx < n_tok * vecs; idx += kConvThreads) {
-      const int tt = idx / vecs;
-      const int cv = idx - tt * vecs;
-      const int c = c0 + cv * 8;
-      const int64_t t = t0 + tt;
-      const int4 sr = tok_s[tt];
-      const int64_t start = t0 + sr.x;
-      const int64_t end = t0 + sr.y;
-      const int r = sr.z;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int i = 0; i < K; ++i) {
-        const int64_t j = t - static_cast<int64_t>(K - 1 - i) * dil;
-        uint4 u;
-        if (j >= start) {
-          u = win[static_cast<int>(j - row0) * vecs + cv];
-        } else {
-          const int64_t hp = W + (j - start);  // history row, oldest first
-          u = (a.state != nullptr && hp >= 0)
-                  ? ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c)
-                  : make_uint4(0, 0, 0, 0);
-        }
-        float f[8];
-        unpack8(u, f);
-        const float4 w0 = *reinterpret_cast<const float4*>(w_s + i * chunk + cv * 8);
-        const float4 w1 = *reinterpret_cast<const float4*>(w_s + i * chunk + cv * 8 + 4);
-        acc[0] = fmaf(w0.x, f[0], acc[0]);
-        acc[1] = fmaf(w0.y, f[1], acc[1]);
-        acc[2] = fmaf(w0.z, f[2], acc[2]);
-        acc[3] = fmaf(w0.w, f[3], acc[3]);
-        acc[4] = fmaf(w1.x, f[4], acc[4]);
-        acc[5] = fmaf(w1.y, f[5], acc[5]);
-        acc[6] = fmaf(w1.z, f[6], acc[6]);
-        acc[7] = fmaf(w1.w, f[7], acc[7]);
-      }
-      *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
-      // Carry-over: the thread holding a request's last token writes its state.
-      if (a.state_out != nullptr && W > 0) {
-        if (t == end - 1) {
-          for (int jj = 0; jj < W; ++jj) {
-            const int64_t sj = t - W + 1 + jj;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (sj >= start) u = win[static_cast<int>(sj - row0) * vecs + cv];
-            else if (a.state != nullptr && W + (sj - start) >= 0)
-              u = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (sj - start)) * C + c);
-            *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
-          }
-        }
-      }
+    ok = mbar_wait(bar0 + 8u * bsel, parity, nullptr);
+    if (!ok) {
+      if (tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
+      break;
     }
-    // The buffer was written by generic stores (the gating) and is about to
-    // be refilled by async-proxy copies: every writer fences before the
-    // barrier that precedes the refill.
-    if (k + 2 < n_chunks) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();  // every access to this buffer is done
-    if (k + 2 < n_chunks) issue(k + 2);
+    __syncthreads();  // w_s complete (the window is complete per the barrier)
+    const uint4* win = buffer(bsel);
+    for (int item = tid; item < per_seg * segs; item += kConvThreads) {
+      const int cv = item % vecs;
+      const int rho = (item / vecs) % dil;
+      const int seg = item / per_seg;
+      const int c = c0 + cv * 8;
+      const int s0 = n_tok * seg / segs;
+      const int s1 = n_tok * (seg + 1) / segs;
+      ConvWalker<GATED, K>::run(a, win, g_s, w_s + cv * 8, chunk, vecs, cv, c, tok_s, t0, row0, W,
+                                dil, s0 + rho, s1);
+    }
+    __syncthreads();  // every read of this buffer is done
+    if (kc + 2 < n_chunks) issue(kc + 2);
   }
   if (!ok) {
     // never leave with copies in flight into this CTA's shared memory: wait
     // (bounded) for the last fill of each buffer
-    for (int bsel = 0; bsel < 2; ++bsel)
-      if (issued[bsel] > 0)
-        mbar_wait(bar0 + 8u * bsel, static_cast<uint32_t>(issued[bsel] - 1) & 1u, nullptr);
+    for (int b2 = 0; b2 < 2; ++b2)
+      if (issued[b2] > 0)
+        mbar_wait(bar0 + 8u * b2, static_cast<uint32_t>(issued[b2] - 1) & 1u, nullptr);
   }
 
   // Requests with no tokens keep their state (CTA 0 copies it through).
@@ -492,12 +530,23 @@ ple_status launch_conv(const ConvArgs& a, cudaStream_t stream, const char* name)
   const int chunk = conv_chunk(a.C, W, tile, GATED);
   if (chunk == 0) return fail(PLE_ERR_UNSUPPORTED, "%s: window does not fit in shared memory", name);
   const ConvLayout L = conv_layout(a.C, W, tile, GATED, chunk);
-  cudaError_t err = cudaFuncSetAttribute(conv_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kernel)(ConvArgs, int, int) = nullptr;
+  switch (a.K) {
+    case 1: kernel = conv_kernel<GATED, 1>; break;
+    case 2: kernel = conv_kernel<GATED, 2>; break;
+    case 3: kernel = conv_kernel<GATED, 3>; break;
+    case 4: kernel = conv_kernel<GATED, 4>; break;
+    case 5: kernel = conv_kernel<GATED, 5>; break;
+    case 6: kernel = conv_kernel<GATED, 6>; break;
+    case 7: kernel = conv_kernel<GATED, 7>; break;
+    default: kernel = conv_kernel<GATED, 8>; break;
+  }
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L.total));
   if (err != cudaSuccess) return check_cuda(err, name);
   const int64_t grid = (a.T + tile - 1) / tile;
   if (grid > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
-  conv_kernel<GATED><<<static_cast<unsigned>(grid), kConvThreads, L.total, stream>>>(a, tile, chunk);
+  kernel<<<static_cast<unsigned>(grid), kConvThreads, L.total, stream>>>(a, tile, chunk);
   return check_cuda(cudaGetLastError(), name);
 }
 

@@ -50,23 +50,43 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
                  int heads_per_ngram, int num_heads,
                  int64_t* __restrict__ out, int32_t* __restrict__ ctx_out,
                  int32_t* dev_err, const __grid_constant__ NgramConsts k) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // 32-bit indices: the host caps num_tokens * num_heads below 2^31.
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t work = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(num_heads);
 
-  // Request boundaries staged once per block (one coalesced load) so that
-  // every thread's binary search runs in shared memory, not through L1 misses.
+  // Request boundaries staged once per block (one coalesced load); the
+  // block's first token is searched once, every thread then steps forward
+  // from there (a block spans 256 / num_heads consecutive tokens).
   __shared__ int32_t qsl_s[kStagedBounds];
+  __shared__ int r_first_s;
   const bool staged = num_reqs < kStagedBounds;
-  if (staged) {
+  if (staged)
     for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
+  __syncthreads();
+  const uint32_t i_first = blockIdx.x * blockDim.x;
+  if (threadIdx.x == 0 && i_first < work) {
+    const int64_t t_first = i_first / static_cast<uint32_t>(num_heads);
+    int r;
+    if (staged) {
+      int lo = 0, hi = num_reqs + 1;  // count of boundaries <= t_first
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(qsl_s[mid]) <= t_first) lo = mid + 1; else hi = mid;
+      }
+      r = lo - 1 < 0 ? 0 : (lo - 1 >= num_reqs ? num_reqs - 1 : lo - 1);
+    } else {
+      r = find_request(qsl, num_reqs, t_first);
+    }
+    r_first_s = r;
   }
   __syncthreads();
 
   check_qsl(qsl, num_reqs, num_tokens, i, dev_err);
 
   // Carry-over: last ctx_len tokens of each request's virtual sequence.
-  if (ctx_out != nullptr && i < static_cast<int64_t>(num_reqs) * ctx_len) {
-    const int r = static_cast<int>(i / ctx_len);
-    const int j = static_cast<int>(i % ctx_len);
+  if (ctx_out != nullptr && i < static_cast<uint32_t>(num_reqs) * static_cast<uint32_t>(ctx_len)) {
+    const int r = static_cast<int>(i / static_cast<uint32_t>(ctx_len));
+    const int j = static_cast<int>(i - static_cast<uint32_t>(r) * ctx_len);
     int64_t start, end;
     request_span(qsl, num_reqs, num_tokens, r, &start, &end);
     const int64_t len = end - start;
@@ -77,23 +97,23 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
     ctx_out[i] = v;
   }
 
-  if (i >= num_tokens * num_heads) return;
-  const int64_t t = i / num_heads;
-  const int h = static_cast<int>(i - t * num_heads);
+  if (i >= work) return;
+  const uint32_t t32 = i / static_cast<uint32_t>(num_heads);
+  const int h = static_cast<int>(i - t32 * static_cast<uint32_t>(num_heads));
+  const int64_t t = t32;
   const int order_lags = h / heads_per_ngram + 1;  // n - 1 for this head
 
-  int r;
+  // Last request whose start is <= t (the right-sided search of the pages'
+  // CPU branch, clamped): step forward from the block's first request.
+  int r = r_first_s;
+  int64_t start;
   if (staged) {
-    int lo = 0, hi = num_reqs + 1;  // count of boundaries <= t lies in [lo, hi]
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (static_cast<int64_t>(qsl_s[mid]) <= t) lo = mid + 1; else hi = mid;
-    }
-    r = lo - 1 < 0 ? 0 : (lo - 1 >= num_reqs ? num_reqs - 1 : lo - 1);
+    while (r + 1 < num_reqs && static_cast<int64_t>(qsl_s[r + 1]) <= t) ++r;
+    start = qsl_s[r];
   } else {
     r = find_request(qsl, num_reqs, t);
+    start = __ldg(qsl + r);
   }
-  const int64_t start = staged ? qsl_s[r] : __ldg(qsl + r);
   const int64_t pos = t - start;  // position inside the request
 
   int64_t mixed = 0;
@@ -180,7 +200,8 @@ PLE_EXPORT ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens
   const int64_t carry = static_cast<int64_t>(num_reqs) * ctx_len;
   const int64_t threads = work > carry ? work : carry;
   const int64_t blocks = (threads + 255) / 256;
-  if (blocks > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "ple_ngram_ids: too many tokens");
+  if (threads >= (int64_t(1) << 31))
+    return fail(PLE_ERR_UNSUPPORTED, "ple_ngram_ids: num_tokens * heads must stay below 2^31");
   ngram_ids_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       input_ids, num_tokens, query_start_loc, num_reqs, ngram_context, ctx_len, eos_token_id,
       heads_per_ngram, num_heads, out, ngram_context_out, dev_err, k);
