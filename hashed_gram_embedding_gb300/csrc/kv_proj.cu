@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 namespace ple {
 namespace {
 
@@ -59,6 +61,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Multicast variant: the box lands at the same shared-memory offset in every
+// CTA of ctaMask and completes bytes on the mbarrier at the same offset there.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar, int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -98,6 +121,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Arrive (once the MMAs issued so far complete) on the mbarrier at the same
+// offset in every CTA of ctaMask.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -119,6 +151,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// CLUSTER = 2: the two CTAs of a cluster take vertically adjacent 128-row
+// tiles of the same 256 output columns, so they need the same W tile; each
+// loads half of it and multicasts that half to both, halving W's L2 reads.
+// A stage is then refilled only after both CTAs' MMAs released it.
+template <int CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                ple_bf16_t* __restrict__ out, int M, int N, int K, int32_t* dev_err) {
@@ -139,14 +176,22 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = CLUSTER > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const int cluster_id = blockIdx.x / CLUSTER;
+  const int num_clusters = gridDim.x / CLUSTER;
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = ((M + BM - 1) / BM) * n_tiles;
+  const int m_groups = ((M + BM - 1) / BM + CLUSTER - 1) / CLUSTER;
+  const int num_tiles = m_groups * n_tiles;  // tiles per CTA position in the cluster
   const int num_kb = (K + BK - 1) / BK;
+  constexpr uint16_t kAll = static_cast<uint16_t>((1u << CLUSTER) - 1);
+  // tile -> (m block, n block); the cluster's CTAs share the n block
+  auto m_block = [&](int tile) { return (tile / n_tiles) * CLUSTER + rank; };
+  auto n_block = [&](int tile) { return tile % n_tiles; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CLUSTER);  // released by every CTA's MMAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -165,6 +210,7 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   }
   tc_fence_before();
   __syncthreads();
+  if (CLUSTER > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -177,14 +223,20 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint32_t armed = 0;        // stages holding a copy this thread issued
     uint32_t armed_parity = 0; // parity of that copy's full-barrier phase
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * BM;
-      const int n0 = (tile % n_tiles) * BN;
+    for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      const int m0 = m_block(tile) * BM;
+      const int n0 = n_block(tile) * BN;
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
         tma_load_2d(smem_u32(a_smem + stage * A_STAGE), &map_a, full_bar(stage), kb * BK, m0);
-        tma_load_2d(smem_u32(b_smem + stage * B_STAGE), &map_b, full_bar(stage), kb * BK, n0);
+        if constexpr (CLUSTER == 1) {
+          tma_load_2d(smem_u32(b_smem + stage * B_STAGE), &map_b, full_bar(stage), kb * BK, n0);
+        } else {
+          constexpr int kPart = BN / CLUSTER;  // W rows this CTA loads for the cluster
+          tma_load_2d_multicast(smem_u32(b_smem + stage * B_STAGE + rank * kPart * BK * 2), &map_b,
+                                full_bar(stage), kb * BK, n0 + rank * kPart, kAll);
+        }
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -202,7 +254,7 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -217,7 +269,9 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
             umma_bf16(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          // frees the stage (in every CTA whose smem it fed) once these MMAs finish
+          if constexpr (CLUSTER == 1) umma_commit(empty_bar(stage));
+          else umma_commit_multicast(empty_bar(stage), kAll);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -236,15 +290,15 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int row_in_tile = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag));
       if (!ok) {
         if (lane == 0) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
         break;
       }
       tc_fence_after();
-      const int m = (tile / n_tiles) * BM + row_in_tile;
-      const int n_base = (tile % n_tiles) * BN;
+      const int m = m_block(tile) * BM + row_in_tile;
+      const int n_base = n_block(tile) * BN;
       ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
 #pragma unroll 1
       for (int chunk = 0; chunk < BN / 32; ++chunk) {
@@ -274,6 +328,9 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while a peer may still multicast into its shared memory or
+  // arrive on its barriers.
+  if (CLUSTER > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -335,13 +392,36 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
   CUtensorMap map_a, map_b;
   ple_status s = make_map(&map_a, emb, M, K, BM);
   if (s != PLE_OK) return s;
-  s = make_map(&map_b, w, N, K, BN);
+  const int cluster_rows = (M > BM) ? BN / 2 : BN;  // W rows one CTA loads per stage
+  int b_box = cluster_rows;
+  if (const char* e = getenv("PLE_KVPROJ_CLUSTER")) b_box = (atoi(e) == 1) ? BN : b_box;
+  s = make_map(&map_b, w, N, K, b_box);
   if (s != PLE_OK) return s;
-  cudaError_t err = cudaFuncSetAttribute(kv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // Clusters of two CTAs sharing W tiles when there are at least two row
+  // blocks; PLE_KVPROJ_CLUSTER=1 forces single CTAs (launch-shape sweeps).
+  int cluster = (M > BM) ? 2 : 1;
+  if (const char* e = getenv("PLE_KVPROJ_CLUSTER")) cluster = (atoi(e) == 1) ? 1 : cluster;
+  auto kernel = cluster == 2 ? kv_proj_kernel<2> : kv_proj_kernel<1>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj: smem attribute");
-  const int num_tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = num_tiles < num_sms() ? num_tiles : num_sms();
-  kv_proj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, kv, M, N, K, dev_err);
+  const int m_groups = ((M + BM - 1) / BM + cluster - 1) / cluster;
+  const int tiles = m_groups * ((N + BN - 1) / BN);
+  const int max_clusters = num_sms() / cluster;
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, kv, M, N, K, dev_err);
+  if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj launch");
   return check_cuda(cudaGetLastError(), "ple_kv_proj launch");
 }

@@ -59,9 +59,20 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   // from there (a block spans 256 / num_heads consecutive tokens).
   __shared__ int32_t qsl_s[kStagedBounds];
   __shared__ int r_first_s;
+  // Per-head constants: the lanes of a warp index different heads, so they
+  // are read from shared memory (a lane-varying index into the parameter
+  // block would serialise on the constant cache).
+  __shared__ uint64_t vocab_s[PLE_MAX_HEADS], offset_s[PLE_MAX_HEADS];
+  __shared__ uint64_t magic_s[PLE_MAX_HEADS], pow64_s[PLE_MAX_HEADS];
   const bool staged = num_reqs < kStagedBounds;
   if (staged)
     for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
+  for (int h = threadIdx.x; h < num_heads; h += blockDim.x) {
+    vocab_s[h] = static_cast<uint64_t>(k.vocab[h]);
+    offset_s[h] = static_cast<uint64_t>(k.offset[h]);
+    magic_s[h] = k.magic[h];
+    pow64_s[h] = k.pow64_mod[h];
+  }
   __syncthreads();
   const uint32_t i_first = blockIdx.x * blockDim.x;
   if (threadIdx.x == 0 && i_first < work) {
@@ -137,8 +148,8 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
     mixed = (s == 0) ? static_cast<int64_t>(term)
                      : static_cast<int64_t>(static_cast<uint64_t>(mixed) ^ term);
   }
-  out[i] = floor_mod(mixed, static_cast<uint64_t>(k.vocab[h]), k.magic[h],
-                     k.pow64_mod[h]) + k.offset[h];
+  out[i] = floor_mod(mixed, vocab_s[h], magic_s[h], pow64_s[h]) +
+           static_cast<int64_t>(offset_s[h]);
 }
 
 }  // namespace

@@ -67,3 +67,17 @@ def test_kv_proj_prefill_8k_shape():
     # all rows against cuBLAS (library cross-check, fp32 accumulate)
     lib_ref = (emb.float() @ w.float().T).to(torch.bfloat16)
     assert_close(bits(kv), bits(lib_ref), what="kv vs cuBLAS")
+
+
+@pytest.mark.parametrize("M,E,C", [(512, 512, 1024), (300, 2048, 4096), (129, 200, 48)])
+def test_kv_proj_single_cta_variant(M, E, C, monkeypatch):
+    """The launch without W multicast (one CTA per tile) gives the same result."""
+    monkeypatch.setenv("PLE_KVPROJ_CLUSTER", "1")
+    emb = rand_bf16((M, E), 0.5, M + E)
+    w = rand_bf16((2 * C, E), 0.05, C + 7)
+    kv = torch.empty((M, 2 * C), dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_kv_proj(emb.cuda(), w.cuda(), kv, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(bits(kv), oracle_kv_proj(bits(emb), bits(w)), what=f"kv single-CTA {M}x{E}x{2*C}")
