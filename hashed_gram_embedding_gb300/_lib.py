@@ -47,6 +47,8 @@ SIGNATURES = {
     "ple_gate": [_P, _P, _P, _P, _F32, _I64, _I32, _P, _P, _P],
     "ple_conv": [_P, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P],
     "ple_gate_conv": [_P, _P, _P, _P, _F32, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P],
+    "ple_host_table_alloc": [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)],
+    "ple_host_table_free": [ctypes.c_void_p, ctypes.c_size_t],
     "ple_last_error": [],
     "ple_version": [],
 }
@@ -191,3 +193,33 @@ def ple_gate_conv(hidden, kv, gamma_h, gamma_k, query_start_loc, w, dilation, ou
 
 def ple_version():
     return lib().ple_version().decode()
+
+
+class HostTable:
+    """A table buffer from ple_host_table_alloc, viewed as a torch tensor.
+
+    Keep this object alive as long as the tensor is used; the memory is
+    unregistered and unmapped when it is garbage-collected (or on close()).
+    """
+
+    def __init__(self, rows, row_dim, dtype):
+        import torch
+        elem = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(rows) * int(row_dim) * elem
+        ptr = ctypes.c_void_p()
+        _check("ple_host_table_alloc", lib().ple_host_table_alloc(self.nbytes, ctypes.byref(ptr)))
+        self.ptr = ptr.value
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        self.tensor = torch.frombuffer(buf, dtype=torch.uint8).view(dtype).view(int(rows), int(row_dim))
+
+    def close(self):
+        if getattr(self, "ptr", None):
+            self.tensor = None
+            lib().ple_host_table_free(ctypes.c_void_p(self.ptr), self.nbytes)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -22,8 +22,6 @@
 
 #include <cuda_fp8.h>
 
-#include <cstdlib>
-
 namespace ple {
 namespace {
 
@@ -39,42 +37,35 @@ __device__ __forceinline__ uint4 load_row_vec(const void* p) {
 
 // bf16 rows: VPR = 16-byte vectors per row (template for the common sizes,
 // 0 = runtime value).
-// Rows are copied only when their id lies in the window [row_lo, row_hi) of
-// the table; ids outside the whole table are zeroed and flagged by the launch
-// whose window starts at row 0. A single launch passes the whole table.
 template <int VPR>
 __global__ void __launch_bounds__(kThreads)
 gather_bf16_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_rt,
-                   const uint4* __restrict__ table, int64_t table_rows, int64_t row_lo,
-                   int64_t row_hi, uint4* __restrict__ out, int32_t* dev_err) {
+                   const uint4* __restrict__ table, int64_t table_rows,
+                   uint4* __restrict__ out, int32_t* dev_err) {
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
        base += stride * kUnroll) {
     uint4 v[kUnroll];
     uint32_t idx[kUnroll];
-    bool mine[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       idx[u] = base + u * stride;
       v[u] = make_uint4(0, 0, 0, 0);
-      mine[u] = false;
       if (idx[u] < total_vecs) {
         const uint32_t row_out = idx[u] / vpr;  // (token, head) pair
         const uint32_t k = idx[u] - row_out * vpr;
         const int64_t id = __ldg(ids + row_out);
-        if (id >= row_lo && id < row_hi) {
+        if (static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
           v[u] = load_row_vec(table + id * vpr + k);
-          mine[u] = true;
-        } else if (row_lo == 0 && static_cast<uint64_t>(id) >= static_cast<uint64_t>(table_rows)) {
-          set_dev_err(dev_err, PLE_DEVERR_BOUNDS);
-          mine[u] = true;  // written as zeros
+        } else {
+          set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // the row is written as zeros
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (mine[u]) out[idx[u]] = v[u];
+      if (idx[u] < total_vecs) out[idx[u]] = v[u];
   }
 }
 
@@ -102,8 +93,7 @@ template <int VPR>
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_rt,
                   const uint4* __restrict__ table, const float* __restrict__ row_scale,
-                  int64_t table_rows, int64_t row_lo, int64_t row_hi,
-                  uint4* __restrict__ out, int32_t* dev_err) {
+                  int64_t table_rows, uint4* __restrict__ out, int32_t* dev_err) {
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
@@ -111,30 +101,26 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_
     uint4 c[kUnroll];
     float s[kUnroll];
     uint32_t idx[kUnroll];
-    bool mine[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       idx[u] = base + u * stride;
       c[u] = make_uint4(0, 0, 0, 0);
       s[u] = 0.f;
-      mine[u] = false;
       if (idx[u] < total_vecs) {
         const uint32_t row_out = idx[u] / vpr;
         const uint32_t k = idx[u] - row_out * vpr;
         const int64_t id = __ldg(ids + row_out);
-        if (id >= row_lo && id < row_hi) {
+        if (static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
           c[u] = load_row_vec(table + id * vpr + k);
           s[u] = __ldg(row_scale + id);
-          mine[u] = true;
-        } else if (row_lo == 0 && static_cast<uint64_t>(id) >= static_cast<uint64_t>(table_rows)) {
-          set_dev_err(dev_err, PLE_DEVERR_BOUNDS);
-          mine[u] = true;  // written as zeros
+        } else {
+          set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // the row is written as zeros
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (mine[u]) {
+      if (idx[u] < total_vecs) {
         uint4 lo, hi;
         dequant16(c[u], s[u], &lo, &hi);
         out[2 * static_cast<size_t>(idx[u])] = lo;
@@ -195,39 +181,18 @@ ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_hea
   const void* dev_table = attr.devicePointer ? attr.devicePointer : table;
   const uint4* tab = static_cast<const uint4*>(dev_table);
   uint4* o = reinterpret_cast<uint4*>(out);
-  {
-    // A random gather over a host table much larger than the GPU's address
-    // translation reach runs at a few GB/s, while the same rows visited one
-    // window of a few GB at a time stream at the link rate. Host tables are
-    // therefore gathered window by window (one launch per window); HBM tables
-    // in one launch.
-    int64_t window = table_rows;
-    if (loc == PLE_HOST_UVA) {
-      int64_t window_bytes = int64_t(4) << 30;
-      if (const char* e = getenv("PLE_UVA_WINDOW_MB")) {
-        const long long mb = atoll(e);
-        if (mb > 0) window_bytes = static_cast<int64_t>(mb) << 20;
-      }
-      window = window_bytes / (static_cast<int64_t>(head_dim) * elem);
-      if (window < 1) window = 1;
-    }
-    for (int64_t lo = 0; lo < table_rows || lo == 0; lo += window) {
-      const int64_t hi = lo + window < table_rows ? lo + window : table_rows;
-      if (dtype == PLE_BF16) {
-        if (vpr == 16)
-          gather_bf16_kernel<16><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, lo, hi, o, dev_err);
-        else if (vpr == 8)
-          gather_bf16_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, lo, hi, o, dev_err);
-        else
-          gather_bf16_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, lo, hi, o, dev_err);
-      } else {
-        if (vpr == 8)
-          gather_fp8_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, lo, hi, o, dev_err);
-        else
-          gather_fp8_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, lo, hi, o, dev_err);
-      }
-      if (hi >= table_rows) break;
-    }
+  if (dtype == PLE_BF16) {
+    if (vpr == 16)
+      gather_bf16_kernel<16><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+    else if (vpr == 8)
+      gather_bf16_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+    else
+      gather_bf16_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+  } else {
+    if (vpr == 8)
+      gather_fp8_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, o, dev_err);
+    else
+      gather_fp8_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, o, dev_err);
   }
   return check_cuda(cudaGetLastError(), name);
 }

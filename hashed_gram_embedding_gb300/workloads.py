@@ -300,7 +300,12 @@ def make_table(torch, w, device, layer=0, rows=None):
             codes = host
         return codes, scale
     if w.table_loc == "host":
-        table = torch.empty((rows, D), dtype=torch.bfloat16, pin_memory=True)
+        # huge-page-backed registered host memory (see ple_host_table_alloc);
+        # the HostTable owner rides along on the tensor to keep it alive
+        from ._lib import HostTable
+        owner = HostTable(rows, D, torch.bfloat16)
+        table = owner.tensor
+        table.host_table_owner = owner
     else:
         table = torch.empty((rows, D), dtype=torch.bfloat16, device=device)
     fill_table_bf16(torch, table, w.seed, tag)

@@ -32,8 +32,9 @@
  *     host memory.
  *   - Calls are asynchronous on the given stream (0 = legacy default stream)
  *     and never synchronise it, except ple_wait with a host timeout.
- *   - The library allocates no device or host memory and keeps no state
- *     between calls other than the thread-local error text.
+ *   - The library allocates no device or host memory (except the explicit
+ *     ple_host_table_alloc) and keeps no state between calls other than the
+ *     thread-local error text.
  *   - bf16 data is passed as 16-bit containers (ple_bf16_t): IEEE binary32
  *     truncated to its high half, row-major.
  *   - A call returns PLE_OK when its work was enqueued. Argument errors found
@@ -53,6 +54,7 @@
 #ifndef PLE_H_
 #define PLE_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -261,6 +263,24 @@ ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* kv,
                          ple_bf16_t* conv_state_out, ple_bf16_t* out,
                          float* gate_out, int32_t* dev_err,
                          cudaStream_t stream);
+
+/*
+ * ple_host_table_alloc / ple_host_table_free -- host memory for a table read
+ * over UVA (PLE_HOST_UVA). (PR#54371 report: the pinned-host backend keeps the
+ * weight in pinned memory and the GPU reads the rows it needs in place;
+ * PR#56512 report: a mapped table registered with cudaHostRegister.)
+ * The memory is an anonymous mapping aligned to 1 GiB, advised for
+ * transparent huge pages and registered with cudaHostRegister, so the GPU
+ * translates it with huge pages: a random row gather over a multi-GB table
+ * then runs near the host-link rate, where cudaHostAlloc memory is bounded by
+ * address-translation misses. These are the only entry points that allocate;
+ * the caller owns the memory and frees it with the same byte count.
+ *   bytes      > 0.    host_ptr   receives the 1 GiB-aligned host address.
+ * Errors: mmap failure or cudaHostRegister failure -> PLE_ERR_CUDA
+ * (nothing stays allocated).
+ */
+ple_status ple_host_table_alloc(size_t bytes, void** host_ptr);
+ple_status ple_host_table_free(void* host_ptr, size_t bytes);
 
 /* Text of the last non-OK status on this host thread ("" if none). */
 const char* ple_last_error(void);

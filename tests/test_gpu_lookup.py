@@ -197,29 +197,30 @@ def test_prefill_8k_full_size_table():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_uva_gather_in_windows(dtype, monkeypatch):
-    """Host tables are gathered one address window at a time; with 1 MB
-    windows over a ~10 MB table every row must still land exactly once."""
-    monkeypatch.setenv("PLE_UVA_WINDOW_MB", "1")
+def test_uva_gather_from_huge_page_host_table(dtype):
+    """A table from ple_host_table_alloc (huge-page-backed registered host
+    memory) is read in place over UVA, bit-exact, with bad ids flagged."""
     rng = np.random.default_rng(12)
     D, T, H = 128, 700, 16
+    rows = 300000
     if dtype == "bf16":
-        rows = 40000
+        owner = _lib.HostTable(rows, D, torch.bfloat16)
         table = random_table_bits(rng, rows, D)
-        host = to_dev_bf16(table, pinned=True)
+        owner.tensor.view(torch.int16).copy_(torch.from_numpy(table.view(np.int16)))
         scale = None
     else:
-        rows = 80000
+        owner = _lib.HostTable(rows, D, torch.uint8)
         codes = rng.integers(0, 0x7E, size=(rows, D), dtype=np.uint8)
+        owner.tensor.copy_(torch.from_numpy(codes))
         sc = (np.abs(rng.standard_normal(rows)) * 1e-3 + 1e-6).astype(np.float32)
-        host = torch.from_numpy(codes).pin_memory()
         scale = torch.from_numpy(sc).cuda()
+    assert owner.ptr % (1 << 30) == 0
     ids = rng.integers(0, rows, size=(T, H))
     ids[3, 2] = rows + 5          # outside the table: zero row + flag
     ids[9, 0] = -7
     out = torch.full((T, H * D), 3.0, dtype=torch.bfloat16, device="cuda")
     err = dev_err_word()
-    _lib.ple_lookup(torch.from_numpy(ids).cuda(), host, out, row_scale=scale, dev_err=err)
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), owner.tensor, out, row_scale=scale, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & _lib.PLE_DEVERR_BOUNDS
     ok = ids.copy()
@@ -229,3 +230,4 @@ def test_uva_gather_in_windows(dtype, monkeypatch):
     ref[3, 2 * D:3 * D] = 0
     ref[9, 0:D] = 0
     assert np.array_equal(bits(out), ref)
+    owner.close()
