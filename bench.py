@@ -39,6 +39,9 @@ UNIT = "tokens/s/layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NUM_SETS = 4
 KERNELS = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
+# libple kernel launches per step: ids, gather, kv_proj, and gate_conv's two
+# passes (gate reduction, gated conv)
+LAUNCHES_PER_STEP = 5
 
 
 # ---------------------------------------------------------------------------
@@ -256,6 +259,7 @@ def run_ours(args):
     y = torch.empty((T, C), dtype=torch.bfloat16, device=device)
     ctx_out = torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device)
     st_out = (torch.empty_like(sets[0]["conv_state"]) if w.decode else None)
+    gate = torch.empty((T,), dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -276,7 +280,7 @@ def run_ours(args):
             ev[3].record(stream)
         _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"],
                            w.dilation, y, conv_state=p.get("conv_state"), conv_state_out=st_out,
-                           dev_err=err, stream=stream)
+                           gate_out=gate, dev_err=err, stream=stream)
         if ev is not None:
             ev[4].record(stream)
 
@@ -394,7 +398,7 @@ def run_ours(args):
         "gather": {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]},
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

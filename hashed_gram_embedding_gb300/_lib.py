@@ -184,7 +184,12 @@ def ple_conv(x, query_start_loc, w, dilation, out, conv_state=None, conv_state_o
 
 def ple_gate_conv(hidden, kv, gamma_h, gamma_k, query_start_loc, w, dilation, out, eps=1e-6,
                   conv_state=None, conv_state_out=None, gate_out=None, dev_err=None, stream=None):
+    """gate_out [T] float32 receives the gate scalars (a fresh buffer is made
+    when it is not given: pass one in to avoid the allocation)."""
     T, C = hidden.shape
+    if gate_out is None:
+        import torch
+        gate_out = torch.empty((T,), dtype=torch.float32, device=hidden.device)
     return _check("ple_gate_conv", lib().ple_gate_conv(
         _ptr(hidden), _ptr(kv), _ptr(gamma_h), _ptr(gamma_k), float(eps), _ptr(query_start_loc),
         query_start_loc.numel() - 1, T, C, _ptr(w), w.shape[1], int(dilation), _ptr(conv_state),

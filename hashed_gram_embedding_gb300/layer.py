@@ -56,6 +56,7 @@ class PLELayer:
                 "emb": torch.empty((num_tokens, E), dtype=torch.bfloat16, device=device),
                 "kv": torch.empty((num_tokens, 2 * self.hidden), dtype=torch.bfloat16, device=device),
                 "y": torch.empty((num_tokens, self.hidden), dtype=torch.bfloat16, device=device),
+                "gate": torch.empty((num_tokens,), dtype=torch.float32, device=device),
             }
             self._bufs = {key: b}
         return b
@@ -74,8 +75,9 @@ class PLELayer:
         _lib.ple_kv_proj(b["emb"], self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
         _lib.ple_gate_conv(hidden, b["kv"], self.gamma_h, self.gamma_k, query_start_loc,
                            self.conv_w, self.dilation, y, eps=self.eps, conv_state=conv_state,
-                           conv_state_out=conv_state_out, dev_err=dev_err, stream=stream)
+                           conv_state_out=conv_state_out, gate_out=b["gate"],
+                           dev_err=dev_err, stream=stream)
         return y
 
-    # launches of libple kernels per forward (ids, gather, kv_proj, gate+conv)
-    LAUNCHES_PER_FORWARD = 4
+    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv)
+    LAUNCHES_PER_FORWARD = 5

@@ -239,6 +239,7 @@ ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
  *                   each virtual sequence. Must not overlap conv_state.
  *   out             [num_tokens][C] bf16.
  * K in 1 .. 8, dilation >= 1, (K-1)*dilation <= 64, C a multiple of 8.
+ * The state buffers must be 16-byte aligned.
  */
 ple_status ple_conv(const ple_bf16_t* x, const int32_t* query_start_loc,
                     int32_t num_reqs, int64_t num_tokens, int32_t hidden_size,
@@ -247,11 +248,14 @@ ple_status ple_conv(const ple_bf16_t* x, const int32_t* query_start_loc,
                     ple_bf16_t* out, int32_t* dev_err, cudaStream_t stream);
 
 /*
- * ple_gate_conv -- ple_gate followed by ple_conv in one kernel: the gate
- * scalars of a token tile (and its dilation halo) are reduced on chip, the
- * gated values u = bf16_rn(g * v) are staged in shared memory and never
- * written to global memory. Same results as ple_gate then ple_conv.
- * Arguments as in those two calls; gate_out optional.
+ * ple_gate_conv -- ple_gate followed by ple_conv without materialising u:
+ * a reduction pass writes the gate scalars g_t to gate_out (4 bytes per
+ * token), then the conv pass stages the dilation window u = bf16_rn(g * v)
+ * in shared memory and convolves it; u never reaches global memory. Same
+ * results as ple_gate then ple_conv.
+ * Arguments as in those two calls; gate_out [num_tokens] float32 is
+ * REQUIRED here (it carries g between the two passes), else
+ * PLE_ERR_INVALID_ARG.
  */
 ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* kv,
                          const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k,

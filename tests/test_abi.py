@@ -109,3 +109,16 @@ def test_conv_and_gate_reject_bad_shapes(lib):
 
 def test_wait_rejects_null_event(lib):
     assert lib.ple_wait(None, None, 0) == 1
+
+
+def test_gate_conv_requires_gate_out(lib):
+    p = ctypes.c_void_p(256)  # never dereferenced: the call fails on the host first
+    assert lib.ple_gate_conv(p, p, p, p, 1e-6, p, 1, 4, 64, p, 4, 3, None, None, p, None, None,
+                             None) == 1
+    assert b"gate_out" in lib.ple_last_error()
+
+
+def test_host_table_rejects_zero_bytes(lib):
+    out = ctypes.c_void_p()
+    assert lib.ple_host_table_alloc(0, ctypes.byref(out)) == 1
+    assert lib.ple_host_table_free(None, 0) == 0
