@@ -163,16 +163,39 @@ struct ConvArgs {
   int32_t* dev_err;
 };
 
-// Pass 1 of ple_gate_conv: the gate scalars only.
-__global__ void __launch_bounds__(kGateThreads)
+// gamma_h[c] * gamma_k[c], precomputed once per CTA in shared memory (the
+// same float32 products GammaFromGlobal forms, so both kernels agree bit for
+// bit).
+struct GammaFromShared {
+  const float* gg;
+  __device__ __forceinline__ void operator()(int c, float out[8]) const {
+    const float4 x = *reinterpret_cast<const float4*>(gg + c);
+    const float4 y = *reinterpret_cast<const float4*>(gg + c + 4);
+    out[0] = x.x; out[1] = x.y; out[2] = x.z; out[3] = x.w;
+    out[4] = y.x; out[5] = y.y; out[6] = y.z; out[7] = y.w;
+  }
+};
+
+constexpr int kGateScalarThreads = 512;
+constexpr int kGateScalarWarps = kGateScalarThreads / 32;
+
+// Pass 1 of ple_gate_conv: the gate scalars only, one warp per token.
+__global__ void __launch_bounds__(kGateScalarThreads)
 gate_scalar_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
                    const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
                    float eps, int64_t T, int C, float* __restrict__ gate_out) {
+  extern __shared__ __align__(16) float gg_s[];  // [C]
+  for (int c = threadIdx.x * 8; c < C; c += kGateScalarThreads * 8) {
+    float f[8];
+    GammaFromGlobal{gamma_h, gamma_k}(c, f);
+    *reinterpret_cast<float4*>(gg_s + c) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(gg_s + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5);
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateScalarWarps + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float g = gate_scalar(hidden + t * C, kv + t * 2 * C, GammaFromGlobal{gamma_h, gamma_k},
-                              C, eps, lane);
+  const float g = gate_scalar(hidden + t * C, kv + t * 2 * C, GammaFromShared{gg_s}, C, eps, lane);
   if (lane == 0) gate_out[t] = g;
 }
 
@@ -234,16 +257,21 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   __syncthreads();
   if (!active) return;
 
-  // taps of this lane's 8 channels
+  // taps of this lane's 8 channels: w[c..c+7][0..K-1] is 8*K contiguous bf16
+  // (K 16-byte loads), transposed into wt[tap][channel]
   float wt[K][8];
   {
-    const uint16_t* w = reinterpret_cast<const uint16_t*>(a.w);
+    const uint4* wv = reinterpret_cast<const uint4*>(a.w + static_cast<int64_t>(c0 + lane * 8) * K);
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
+    for (int q = 0; q < K; ++q) {
+      float f[8];
+      unpack8(__ldg(wv + q), f);  // elements 8q .. 8q+7 of the [8][K] block
 #pragma unroll
-      for (int i = 0; i < K; ++i)
-        wt[i][e] = __uint_as_float(static_cast<uint32_t>(
-                       __ldg(w + static_cast<int64_t>(c0 + lane * 8 + e) * K + i)) << 16);
+      for (int e = 0; e < 8; ++e) {
+        const int flat = 8 * q + e;
+        wt[flat % K][flat / K] = f[e];
+      }
+    }
   }
   const int c = c0 + lane * 8;
   for (int tt = warp; tt < n_tok; tt += kConvThreads / 32) {
@@ -307,6 +335,7 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   if (num_reqs < 0 || (num_reqs == 0 && T > 0))
     return fail(PLE_ERR_INVALID_ARG, "%s: num_reqs must be >= 1 when there are tokens", name);
   if (!w || (T > 0 && !qsl)) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned16(w)) return fail(PLE_ERR_INVALID_ARG, "%s: conv taps must be 16-byte aligned", name);
   const size_t state_bytes = static_cast<size_t>(num_reqs) * (K - 1) * dil * C * 2;
   if (state && state_out && state_bytes > 0 && overlaps(state, state_bytes, state_out, state_bytes))
     return fail(PLE_ERR_INVALID_ARG, "%s: conv_state_out overlaps conv_state", name);
@@ -416,8 +445,14 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   a.gate_out = gate_out;
   a.dev_err = dev_err;
   if (!gated) return launch_conv<false>(a, nullptr, stream, name);
-  const int64_t blocks = (T + kGateWarps - 1) / kGateWarps;
-  gate_scalar_kernel<<<static_cast<unsigned>(blocks), kGateThreads, 0, stream>>>(
+  const int64_t blocks = (T + kGateScalarWarps - 1) / kGateScalarWarps;
+  const size_t gg_bytes = static_cast<size_t>(C) * sizeof(float);
+  if (gg_bytes > 200 * 1024) return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d too large", name, C);
+  cudaError_t ferr = cudaFuncSetAttribute(gate_scalar_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(gg_bytes));
+  if (ferr != cudaSuccess) return check_cuda(ferr, name);
+  gate_scalar_kernel<<<static_cast<unsigned>(blocks), kGateScalarThreads, gg_bytes, stream>>>(
       hidden, src, gamma_h, gamma_k, eps, T, C, gate_out);
   ple_status st = check_cuda(cudaGetLastError(), name);
   if (st != PLE_OK) return st;

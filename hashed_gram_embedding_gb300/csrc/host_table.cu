@@ -44,6 +44,11 @@ PLE_EXPORT ple_status ple_host_table_alloc(size_t bytes, void** host_ptr) {
   if (map_end > end) munmap(reinterpret_cast<void*>(end), map_end - end);
   void* p = reinterpret_cast<void*>(aligned);
   madvise(p, bytes, MADV_HUGEPAGE);  // advisory: failure only costs speed
+  // Fault the memory in from the CPU first, one byte per 2 MiB: with the
+  // advice in place each fault maps a whole huge page (pinning alone may
+  // populate small pages).
+  volatile uint8_t* bytes_p = static_cast<volatile uint8_t*>(p);
+  for (size_t off = 0; off < bytes; off += size_t(2) << 20) bytes_p[off] = 0;
   cudaError_t err = cudaHostRegister(p, bytes, cudaHostRegisterPortable | cudaHostRegisterMapped);
   if (err != cudaSuccess) {
     munmap(p, bytes);
