@@ -200,9 +200,11 @@ def algorithmic_work(w):
     T, H, D, C, E = w.num_tokens, w.num_heads, w.head_dim, w.hidden, w.emb_dim
     elem = 1 if w.table_dtype == "fp8" else 2
     row_read = H * D * elem + (H * 4 if w.table_dtype == "fp8" else 0)
+    lookup = (("link", T * row_read) if w.table_loc == "host"
+              else ("hbm", T * (H * 8 + row_read + H * D * 2)))
     return {
         "ngram_ids": ("hbm", T * 4 + T * H * 8 + (w.num_reqs + 1) * 4),
-        "lookup": ("hbm", T * (H * 8 + row_read + H * D * 2)),
+        "lookup": lookup,
         "kv_proj": ("tensor", 2.0 * T * E * 2 * C),
         "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2)),
     }
@@ -354,6 +356,7 @@ def run_ours(args):
     if rank != 0:
         return None
     peaks, peak_kind = load_peaks()
+    link_gbs = measure_link_gbs(torch, device) if w.table_loc == "host" else None
     work = algorithmic_work(w)
     kernels = {}
     for k in KERNELS:
@@ -363,6 +366,10 @@ def run_ours(args):
             achieved = amount / (avg_ms * 1e-3) / 1e12
             peak = peaks["bf16_tflops"]
             unit = "TFLOP/s"
+        elif bound == "link":  # rows read over the host link
+            achieved = amount / (avg_ms * 1e-3) / 1e9
+            peak = link_gbs
+            unit = "GB/s"
         else:
             achieved = amount / (avg_ms * 1e-3) / 1e9
             peak = peaks["hbm_gbs"]
@@ -375,9 +382,11 @@ def run_ours(args):
     dk = kernels[dominant]
     bound, amount = work[dominant]
     traffic = ncu_traffic(dominant) if args.workload == "prefill8k" else None
+    dpeak = {"tensor": peaks["bf16_tflops"], "link": link_gbs}.get(dk["bound"], peaks["hbm_gbs"])
     roofline = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
-                "peak": peaks["bf16_tflops"] if dk["bound"] == "tensor" else peaks["hbm_gbs"],
-                "unit": dk["unit"], "frac": dk["frac"], "peak_source": peak_kind,
+                "peak": dpeak, "unit": dk["unit"], "frac": dk["frac"],
+                "peak_source": ("pinned host-to-device copy measured in this run"
+                                if dk["bound"] == "link" else peak_kind),
                 "algorithmic_per_launch": amount, "traffic": traffic}
     value = world * args.steps * T / (total_ms * 1e-3)
     line = {
@@ -395,10 +404,12 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
         "kernels": kernels,
-        "gather": {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]},
+        "gather": ({"gbs": kernels["lookup"]["achieved"], "link_gbs": link_gbs,
+                    "frac_link": kernels["lookup"]["frac"]} if w.table_loc == "host" else
+                   {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]}),
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches_per_step(w, sets[0]["table"]) * args.steps,
         "clocks": clocks,
     }
     if w.table_loc == "host":
@@ -406,6 +417,30 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
+
+
+def launches_per_step(w, table):
+    """libple kernels one step launches: ids, gather, kv_proj, and the gate
+    and conv passes."""
+    return LAUNCHES_PER_STEP
+
+
+def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
+    """Host-to-device copy rate from pinned memory (the host link's usable
+    peak, the denominator of a gather from a host table)."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
 
 
 def uva_overlap(torch, _lib, p, ids, emb, w, device, reps=20):

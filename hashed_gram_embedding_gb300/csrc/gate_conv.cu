@@ -12,19 +12,24 @@
 // over each request's virtual sequence (conv state ++ segment, zeros before).
 //
 // Design (HBM-bound: read h, k, v once, write y once; u never reaches HBM):
-//   pass 1 (gate_scalar_kernel): one warp per token reduces sum h^2, sum k^2
-//     and sum h*k*gh*gk over the hidden row (16-byte loads, four blocks of
-//     loads in flight per lane, warp-shuffle reductions) and writes the gate
-//     scalar g_t (4 bytes per token) -- many warps per SM keep enough loads in
-//     flight to stream h and k near the HBM rate;
+//   pass 1 (gate_reduce_kernel): a group of G threads (one to eight warps)
+//     reduces sum h^2, sum k^2 and sum h*k*gh*gk over one token's hidden row:
+//     every thread owns the same channels for all tokens (their gamma
+//     products stay in registers), issues all its 16-byte loads of the row at
+//     once, and the group combines its warps' partial sums through shared
+//     memory in a fixed order. A persistent grid strides over tokens, so work
+//     is spread evenly over the SMs whatever T is. It writes the gate scalar
+//     g_t (4 bytes per token); ple_gate's variant also writes u = bf16(g*v).
 //   pass 2 (conv_kernel<GATED=true>): a CTA takes a tile of tokens and a
-//     256-channel slice, stages its dilation window -- the gated values
-//     u = bf16(g*v) of the tile and of the (K-1)*d tokens before it, inside
-//     the same request -- in shared memory with coalesced 16-byte loads, then
-//     each lane owns 8 channels (taps in registers) and each warp walks tokens:
-//     y_t = sum_i w_i * u_{t-(K-1-i)d} from shared memory (or from the
-//     carry-over state before a request's first token). The CTA holding a
-//     request's last token writes the request's new state for its channels.
+//     256-channel slice, stages its dilation window -- u of the tile and of
+//     the (K-1)*d tokens before it -- in shared memory as float32 (values
+//     already rounded to bf16), then each lane owns 8 channels (taps in
+//     registers as float pairs) and each warp walks tokens. A token whose
+//     taps all lie inside its own request (every token but the first (K-1)*d
+//     of a request) reads the K window rows and accumulates with packed
+//     two-wide FMAs; the others take the taps before their request's first
+//     token from the carry-over state. The CTA holding a request's last token
+//     writes the request's new state for its channels.
 // ple_conv is pass 2 on an ungated input; ple_gate is pass 1 plus u = g*v.
 #include "common.cuh"
 
@@ -34,40 +39,58 @@ namespace ple {
 namespace {
 
 constexpr int kGateThreads = 256;
-constexpr int kGateWarps = kGateThreads / 32;
 constexpr int kConvThreads = 256;
 constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
+constexpr int kMaxGateC = 16384;  // 8 vectors per thread at 256 threads per token
 
 __device__ __forceinline__ uint4 ldg16(const ple_bf16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// bf16 pair word -> its two float32 values (low half is the first element).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 __device__ __forceinline__ void unpack8(uint4 v, float f[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 x = __bfloat1622float2(b[e]);
-    f[2 * e] = x.x;
-    f[2 * e + 1] = x.y;
-  }
+  f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
+  f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+  f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
+  f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
 }
 
-__device__ __forceinline__ uint4 pack8(const float f[8]) {
-  uint4 v;
-  __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) b[e] = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-  return v;
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// u = bf16(g * v) for 8 packed bf16 values.
+// Packed float32 pairs (sm_100+ two-wide FMA/MUL; each lane is an IEEE
+// single-precision operation, identical to fmaf / __fmul_rn on that lane).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// u = bf16(g * v) for one bf16 pair word.
+__device__ __forceinline__ uint32_t gate2(uint32_t w, float g) {
+  return pack2(__fmul_rn(bf_lo(w), g), __fmul_rn(bf_hi(w), g));
+}
 __device__ __forceinline__ uint4 gate8(uint4 v, float g) {
-  float f[8];
-  unpack8(v, f);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) f[e] *= g;
-  return pack8(f);
+  return make_uint4(gate2(v.x, g), gate2(v.y, g), gate2(v.z, g), gate2(v.w, g));
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -83,72 +106,175 @@ __device__ __forceinline__ float gate_of(float sh, float sk, float sd, int C, fl
   return 1.0f / (1.0f + expf(-score));
 }
 
-// gamma_h[c] * gamma_k[c] for 8 channels, from the two bf16 vectors.
-struct GammaFromGlobal {
-  const ple_bf16_t* gh;
-  const ple_bf16_t* gk;
-  __device__ __forceinline__ void operator()(int c, float out[8]) const {
-    float a[8], b[8];
-    unpack8(ldg16(gh + c), a);
-    unpack8(ldg16(gk + c), b);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) out[e] = a[e] * b[e];
-  }
-};
+// ---------------------------------------------------------------------------
+// Pass 1: gate scalars (and, for ple_gate, u = bf16(g * v)).
+// G threads per token (a power of two, 32..256); thread j of a group owns the
+// 16-byte vectors j, j+G, ..., j+(VPT-1)G of the row. Sums are kept as float
+// pairs (even / odd channel of each bf16 pair) with two-wide FMAs. Reduction
+// order: the thread's vectors in order, the 4 pairs of each, then even +
+// odd; butterfly over the warp; the group's warps in order. ple_gate and
+// ple_gate_conv share it, so both produce the same g bit for bit.
+// ---------------------------------------------------------------------------
+template <int VPT, bool WRITE_U>
+__global__ void __launch_bounds__(kGateThreads)
+gate_reduce_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
+                   const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
+                   float eps, int64_t T, int C, int G, ple_bf16_t* __restrict__ u_out,
+                   float* __restrict__ gate_out) {
+  __shared__ float red[3][kGateThreads / 32];
+  __shared__ float g_s[kGateThreads / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int groups = kGateThreads / G;
+  const int grp = tid / G;
+  const int j = tid - grp * G;
+  const int nv = C >> 3;
 
-// Gate scalar of one token, computed by a whole warp; every lane gets it.
-// <rms(h)*gh, rms(k)*gk> = sum(h*k*gh*gk) / (rms_h * rms_k).
-template <class Gamma>
-__device__ __forceinline__ float gate_scalar(const ple_bf16_t* __restrict__ h_row,
-                                             const ple_bf16_t* __restrict__ k_row,
-                                             const Gamma& gamma, int C, float eps, int lane) {
-  float sh = 0.f, sk = 0.f, sd = 0.f;
-#pragma unroll 4
-  for (int c = lane * 8; c < C; c += 32 * 8) {
-    float h[8], k[8], g[8];
-    unpack8(ldg16(h_row + c), h);
-    unpack8(ldg16(k_row + c), k);
-    gamma(c, g);
+  uint64_t gg[VPT][4];  // gamma_h * gamma_k of this thread's channels, as pairs
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      sh = fmaf(h[e], h[e], sh);
-      sk = fmaf(k[e], k[e], sk);
-      sd = fmaf(h[e] * k[e], g[e], sd);
+  for (int i = 0; i < VPT; ++i) {
+    const int v = j + i * G;
+    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    if (v < nv) {
+      a = ldg16(gamma_h + v * 8);
+      b = ldg16(gamma_k + v * 8);
+    }
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+      gg[i][p] = f2_mul(f2(bf_lo(aw[p]), bf_hi(aw[p])), f2(bf_lo(bw[p]), bf_hi(bw[p])));
+  }
+
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * groups;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * groups; base < T; base += stride) {
+    const int64_t t = base + grp;
+    const bool valid = t < T;
+    uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // +0.0f pairs
+    uint4 vv[WRITE_U ? VPT : 1];
+    if (valid) {
+      const ple_bf16_t* h_row = hidden + t * C;
+      const ple_bf16_t* k_row = kv + t * 2 * C;
+      uint4 hv[VPT], kk[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = j + i * G;
+        hv[i] = make_uint4(0, 0, 0, 0);
+        kk[i] = make_uint4(0, 0, 0, 0);
+        if (v < nv) {
+          hv[i] = ldg16(h_row + v * 8);
+          kk[i] = ldg16(k_row + v * 8);
+          if constexpr (WRITE_U) vv[i] = ldg16(k_row + C + v * 8);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+        const uint32_t kw[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const uint64_t h2 = f2(bf_lo(hw[p]), bf_hi(hw[p]));
+          const uint64_t k2 = f2(bf_lo(kw[p]), bf_hi(kw[p]));
+          sh2 = f2_fma(h2, h2, sh2);
+          sk2 = f2_fma(k2, k2, sk2);
+          sd2 = f2_fma(f2_mul(h2, k2), gg[i][p], sd2);
+        }
+      }
+    }
+    float a0, a1, b0, b1, d0, d1;
+    f2_split(sh2, a0, a1);
+    f2_split(sk2, b0, b1);
+    f2_split(sd2, d0, d1);
+    const float sh = warp_sum(a0 + a1);
+    const float sk = warp_sum(b0 + b1);
+    const float sd = warp_sum(d0 + d1);
+    if (lane == 0) {
+      red[0][warp] = sh;
+      red[1][warp] = sk;
+      red[2][warp] = sd;
+    }
+    __syncthreads();
+    if (valid && j == 0) {
+      const int w0 = grp * (G >> 5);
+      float a = red[0][w0], b = red[1][w0], d = red[2][w0];
+      for (int w = 1; w < (G >> 5); ++w) {
+        a += red[0][w0 + w];
+        b += red[1][w0 + w];
+        d += red[2][w0 + w];
+      }
+      const float g = gate_of(a, b, d, C, eps);
+      if (gate_out != nullptr) gate_out[t] = g;
+      if constexpr (WRITE_U) g_s[grp] = g;
+    }
+    __syncthreads();
+    if constexpr (WRITE_U) {
+      if (valid) {
+        const float g = g_s[grp];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = j + i * G;
+          if (v < nv) *reinterpret_cast<uint4*>(u_out + t * C + v * 8) = gate8(vv[i], g);
+        }
+      }
     }
   }
-  return gate_of(warp_sum(sh), warp_sum(sk), warp_sum(sd), C, eps);
 }
 
-// ---------------------------------------------------------------------------
-// ple_gate: one warp per token.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kGateThreads)
-gate_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
-            const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
-            float eps, int64_t T, int C, ple_bf16_t* __restrict__ out,
-            float* __restrict__ gate_out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const ple_bf16_t* h_row = hidden + t * C;
-  const ple_bf16_t* k_row = kv + t * 2 * C;
-  const float g = gate_scalar(h_row, k_row, GammaFromGlobal{gamma_h, gamma_k}, C, eps, lane);
-  if (gate_out != nullptr && lane == 0) gate_out[t] = g;
-  const ple_bf16_t* v_row = k_row + C;
-#pragma unroll 4
-  for (int c = lane * 8; c < C; c += 32 * 8)
-    *reinterpret_cast<uint4*>(out + t * C + c) = gate8(ldg16(v_row + c), g);
+// Threads per token and vectors per thread for hidden size C: about four
+// vectors of each operand per thread.
+void gate_shape(int C, int* G, int* vpt) {
+  const int nv = C / 8;
+  int g = 32;
+  while (g < kGateThreads && 4 * g < nv) g *= 2;
+  int v = 1;
+  while (v * g < nv) v *= 2;
+  *G = g;
+  *vpt = v;
+}
+
+template <int VPT, bool WRITE_U>
+ple_status launch_gate_reduce(const ple_bf16_t* hidden, const ple_bf16_t* kv,
+                              const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k, float eps,
+                              int64_t T, int C, int G, ple_bf16_t* u_out, float* gate_out,
+                              cudaStream_t stream, const char* name) {
+  static int per_sm = 0;  // resident CTAs per SM of this instantiation
+  if (per_sm == 0) {
+    int n = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, gate_reduce_kernel<VPT, WRITE_U>, kGateThreads, 0);
+    if (err != cudaSuccess) return check_cuda(err, name);
+    per_sm = n > 0 ? n : 1;
+  }
+  const int groups = kGateThreads / G;
+  const int64_t need = (T + groups - 1) / groups;
+  const int64_t resident = static_cast<int64_t>(num_sms()) * per_sm;
+  const unsigned blocks = static_cast<unsigned>(need < resident ? need : resident);
+  gate_reduce_kernel<VPT, WRITE_U><<<blocks, kGateThreads, 0, stream>>>(
+      hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out);
+  return check_cuda(cudaGetLastError(), name);
+}
+
+template <bool WRITE_U>
+ple_status gate_pass(const ple_bf16_t* hidden, const ple_bf16_t* kv, const ple_bf16_t* gamma_h,
+                     const ple_bf16_t* gamma_k, float eps, int64_t T, int C, ple_bf16_t* u_out,
+                     float* gate_out, cudaStream_t stream, const char* name) {
+  int G, vpt;
+  gate_shape(C, &G, &vpt);
+  switch (vpt) {
+    case 1: return launch_gate_reduce<1, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
+    case 2: return launch_gate_reduce<2, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
+    case 4: return launch_gate_reduce<4, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
+    case 8: return launch_gate_reduce<8, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
+    default: return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d above %d", name, C, kMaxGateC);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // ple_conv (GATED = false, input x) and ple_gate_conv (GATED = true).
 // ---------------------------------------------------------------------------
 struct ConvArgs {
-  const ple_bf16_t* hidden;   // gated only
-  const ple_bf16_t* src;      // kv (gated) or x (plain)
-  const ple_bf16_t* gamma_h;
-  const ple_bf16_t* gamma_k;
-  float eps;
+  const ple_bf16_t* src;      // kv (gated: v is its second half) or x
   const int32_t* qsl;
   int num_reqs;
   int64_t T;
@@ -159,51 +285,96 @@ struct ConvArgs {
   const ple_bf16_t* state;
   ple_bf16_t* state_out;
   ple_bf16_t* out;
-  float* gate_out;
   int32_t* dev_err;
 };
 
-// gamma_h[c] * gamma_k[c], precomputed once per CTA in shared memory (the
-// same float32 products GammaFromGlobal forms, so both kernels agree bit for
-// bit).
-struct GammaFromShared {
-  const float* gg;
-  __device__ __forceinline__ void operator()(int c, float out[8]) const {
-    const float4 x = *reinterpret_cast<const float4*>(gg + c);
-    const float4 y = *reinterpret_cast<const float4*>(gg + c + 4);
-    out[0] = x.x; out[1] = x.y; out[2] = x.z; out[3] = x.w;
-    out[4] = y.x; out[5] = y.y; out[6] = y.z; out[7] = y.w;
-  }
+constexpr int kConvSlice = 256;  // channels per CTA (8 per lane)
+
+// Shared memory of one conv CTA: the float32 window (rows x 1 KB; a row is
+// two halves of 32 float4 so that a warp's 16-byte accesses are contiguous:
+// lane l holds channels 8l..8l+3 in half 0 and 8l+4..8l+7 in half 1), then
+// per-token and per-request integers.
+struct ConvSmem {
+  float4* win;
+  int* tok_start;  // [tile] start of the token's request, relative to t0
+  int* tok_req;    // [tile] the token's request
+  int* req_s;      // [tile] requests overlapping the tile: start, end (rel.), index
+  int* req_e;
+  int* req_r;
+  int* counts;     // [0] requests listed, [1] requests ending in the tile
+  int* end_k;      // [tile] list positions of the requests ending in the tile
 };
 
-constexpr int kGateScalarThreads = 512;
-constexpr int kGateScalarWarps = kGateScalarThreads / 32;
-
-// Pass 1 of ple_gate_conv: the gate scalars only, one warp per token.
-__global__ void __launch_bounds__(kGateScalarThreads)
-gate_scalar_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
-                   const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
-                   float eps, int64_t T, int C, float* __restrict__ gate_out) {
-  extern __shared__ __align__(16) float gg_s[];  // [C]
-  for (int c = threadIdx.x * 8; c < C; c += kGateScalarThreads * 8) {
-    float f[8];
-    GammaFromGlobal{gamma_h, gamma_k}(c, f);
-    *reinterpret_cast<float4*>(gg_s + c) = make_float4(f[0], f[1], f[2], f[3]);
-    *reinterpret_cast<float4*>(gg_s + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateScalarWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float g = gate_scalar(hidden + t * C, kv + t * 2 * C, GammaFromShared{gg_s}, C, eps, lane);
-  if (lane == 0) gate_out[t] = g;
+__host__ __device__ inline size_t conv_smem_bytes(int tile, int W) {
+  return static_cast<size_t>(tile + W) * kConvSlice * 4 + static_cast<size_t>(tile) * 6 * 4 + 16;
 }
 
-constexpr int kConvSlice = 256;            // channels per CTA (8 per lane)
-constexpr int kConvSliceVecs = kConvSlice / 8;
+__device__ __forceinline__ ConvSmem conv_smem(uint8_t* base, int tile, int W) {
+  ConvSmem s;
+  s.win = reinterpret_cast<float4*>(base);
+  int* p = reinterpret_cast<int*>(base + static_cast<size_t>(tile + W) * kConvSlice * 4);
+  s.tok_start = p;
+  s.tok_req = p + tile;
+  s.req_s = p + 2 * tile;
+  s.req_e = p + 3 * tile;
+  s.req_r = p + 4 * tile;
+  s.end_k = p + 5 * tile;
+  s.counts = p + 6 * tile;
+  return s;
+}
 
-// Pass 2: the dilated causal depthwise conv of one (token tile, channel
-// slice); GATED: its input is u = bf16(g * v) with g from pass 1.
+// Requests overlapping [t0, t0 + n_tok), found by warp 0: a 32-way search
+// for the request of t0, then the following qsl entries 32 at a time. Spans
+// follow request_span (clamped; the last request ends at T). With a valid
+// qsl there are at most n_tok non-empty overlapping requests; extra entries
+// (possible only for an invalid qsl) are dropped.
+__device__ void find_tile_requests(const int32_t* __restrict__ qsl, int R, int64_t T, int64_t t0,
+                                   int n_tok, int cap, ConvSmem s, int lane) {
+  // cnt = number of entries qsl[0..R] <= t0 for a non-decreasing qsl
+  int lo = 0, hi = R + 1;
+  while (lo < hi) {
+    const int step = (hi - lo + 31) >> 5;
+    const int p = lo + lane * step;
+    const bool le = p < hi && static_cast<int64_t>(__ldg(qsl + p)) <= t0;
+    const int k = __popc(__ballot_sync(0xffffffffu, le));
+    if (k == 0) break;
+    const int nlo = lo + (k - 1) * step + 1;
+    hi = min(lo + k * step, hi);
+    lo = nlo;
+  }
+  int r = lo - 1;
+  r = r < 0 ? 0 : (r >= R ? R - 1 : r);
+  int listed = 0, ending = 0;
+  const int64_t t1 = t0 + n_tok;
+  for (; r < R; r += 32) {
+    const int rr = r + lane;
+    bool take = false, beyond = false;
+    int64_t st = 0, en = 0;
+    if (rr < R) {
+      request_span(qsl, R, T, rr, &st, &en);
+      take = en > st && st < t1 && en > t0;
+      beyond = st >= t1;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    const int pos = listed + __popc(m & ((1u << lane) - 1));
+    if (take && pos < cap) {
+      s.req_s[pos] = static_cast<int>(st - t0);
+      s.req_e[pos] = static_cast<int>(en - t0);
+      s.req_r[pos] = rr;
+    }
+    const bool ends = take && pos < cap && en <= t1;
+    const unsigned me = __ballot_sync(0xffffffffu, ends);
+    if (ends) s.end_k[ending + __popc(me & ((1u << lane) - 1))] = pos;
+    listed = min(listed + __popc(m), cap);
+    ending = min(ending + __popc(me), cap);
+    if (__ballot_sync(0xffffffffu, beyond) != 0u) break;
+  }
+  if (lane == 0) {
+    s.counts[0] = listed;
+    s.counts[1] = ending;
+  }
+}
+
 template <bool GATED, int K>
 __global__ void __launch_bounds__(kConvThreads)
 conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int tile_tokens) {
@@ -211,57 +382,125 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   const int dil = a.dil;
   const int W = (K - 1) * dil;
   const int C = a.C;
+  const int R = a.num_reqs;
   const int64_t T = a.T;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tile_tokens;
-  const int64_t t1 = t0 + tile_tokens < T ? t0 + tile_tokens : T;
-  const int n_tok = static_cast<int>(t1 - t0);
+  const int n_tok = static_cast<int>((t0 + tile_tokens < T ? t0 + tile_tokens : T) - t0);
   const int c0 = blockIdx.y * kConvSlice;
-  const int64_t row0 = t0 - W;                 // window row i <-> token row0 + i
-  const int rows = n_tok + W;
-  uint4* win = reinterpret_cast<uint4*>(smem);  // [rows][kConvSliceVecs]
-  int4* tok_s = reinterpret_cast<int4*>(smem + static_cast<size_t>(tile_tokens + W) * kConvSlice * 2);
+  const int c = c0 + lane * 8;
+  const bool active = c < C;  // lanes past the last channel only help with bookkeeping
+  const ConvSmem s = conv_smem(smem, tile_tokens, W);
   const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
-  const int64_t src_off = GATED ? C : 0;       // v sits after k in kv
+  const ple_bf16_t* src = a.src + (GATED ? C : 0) + c;
 
   if (blockIdx.x == 0 && blockIdx.y == 0)
-    for (int i = tid; i < a.num_reqs + 1; i += kConvThreads)
-      check_qsl(a.qsl, a.num_reqs, T, i, a.dev_err);
+    for (int i = tid; i < R + 1; i += kConvThreads) check_qsl(a.qsl, R, T, i, a.dev_err);
 
-  // request (start, end, index) of every tile token
-  for (int i = tid; i < n_tok; i += kConvThreads) {
-    const int r = find_request(a.qsl, a.num_reqs, t0 + i);
-    int64_t st, en;
-    request_span(a.qsl, a.num_reqs, T, r, &st, &en);
-    tok_s[i] = make_int4(static_cast<int>(st - t0), static_cast<int>(en - t0), r, 0);
-  }
-  // window rows from the start of t0's request on (earlier rows belong to
-  // other requests and are never read)
-  int64_t lo, lo_end;
-  request_span(a.qsl, a.num_reqs, T, find_request(a.qsl, a.num_reqs, t0), &lo, &lo_end);
-  const int i_lo = static_cast<int>(lo > row0 ? lo - row0 : 0);
-  // lanes past the last channel (C not a multiple of the slice) stay idle
-  const bool active = c0 + lane * 8 < C;
-  // one warp per window row: 32 lanes x 16 bytes = the slice's 512 bytes
+  if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
+
+  // Window row i <-> token t0 - W + i (rows of tokens before 0 are not
+  // loaded; rows of an earlier request are loaded but never read). Each warp
+  // takes every 8th row, 8 rows' loads in flight per lane at a time.
   if (active) {
-#pragma unroll 4
-    for (int i = i_lo + warp; i < rows; i += kConvThreads / 32) {
-      const int64_t j = row0 + i;
-      uint4 v = ldg16(a.src + j * src_pitch + src_off + c0 + lane * 8);
-      if constexpr (GATED) v = gate8(v, __ldg(g + j));
-      win[i * kConvSliceVecs + lane] = v;
+    constexpr int kWarps = kConvThreads / 32;
+    constexpr int kBatch = 8;
+    const int i0 = t0 >= W ? 0 : static_cast<int>(W - t0);
+    const int rows = n_tok + W;
+    for (int first = i0 + warp; first < rows; first += kWarps * kBatch) {
+      uint4 v[kBatch];
+      float gv[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int i = first + q * kWarps;
+        v[q] = make_uint4(0, 0, 0, 0);
+        gv[q] = 0.f;
+        if (i < rows) {
+          const int64_t tok = t0 - W + i;
+          v[q] = ldg16(src + tok * src_pitch);
+          if constexpr (GATED) gv[q] = __ldg(g + tok);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int i = first + q * kWarps;
+        if (i < rows) {
+          float f[8];
+          if constexpr (GATED) {
+            const uint64_t gg = f2(gv[q], gv[q]);
+            const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              float lo, hi;
+              f2_split(f2_mul(f2(bf_lo(w4[p]), bf_hi(w4[p])), gg), lo, hi);
+              const uint32_t u = pack2(lo, hi);  // round to bf16
+              f[2 * p] = bf_lo(u);
+              f[2 * p + 1] = bf_hi(u);
+            }
+          } else {
+            unpack8(v[q], f);
+          }
+          s.win[(i * 2) * 32 + lane] = make_float4(f[0], f[1], f[2], f[3]);
+          s.win[(i * 2 + 1) * 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
     }
   }
   __syncthreads();
+
+  // request of every tile token (binary search over the listed starts)
+  const int listed = s.counts[0];
+  int all_fast = 1;  // every token's taps inside its own request
+  for (int tt = tid; tt < n_tok; tt += kConvThreads) {
+    int lo = 0, hi = listed;  // last k with req_s[k] <= tt
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s.req_s[mid] <= tt) lo = mid + 1; else hi = mid;
+    }
+    const int k = lo - 1;
+    if (k >= 0 && tt < s.req_e[k]) {
+      s.tok_start[tt] = s.req_s[k];
+      s.tok_req[tt] = s.req_r[k];
+    } else {  // only for an invalid qsl: no history
+      s.tok_start[tt] = tt;
+      s.tok_req[tt] = 0;
+    }
+    all_fast &= (tt - W >= s.tok_start[tt]) ? 1 : 0;
+  }
+  all_fast = __syncthreads_and(all_fast);
+
+  // requests with no tokens keep their state (copied by the first token
+  // tile; every lane of a warp takes part in the scan)
+  if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
+    for (int base = warp * 32; base < R; base += kConvThreads) {
+      bool empty = false;
+      if (base + lane < R) {
+        int64_t s0, e0;
+        request_span(a.qsl, R, T, base + lane, &s0, &e0);
+        empty = e0 == s0;
+      }
+      unsigned m = __ballot_sync(0xffffffffu, empty);
+      while (m != 0u && active) {
+        const int r = base + __ffs(m) - 1;
+        m &= m - 1;
+        for (int jj = 0; jj < W; ++jj) {
+          const int64_t off = (static_cast<int64_t>(r) * W + jj) * C + c;
+          const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(a.state_out + off) = v;
+        }
+      }
+    }
+  }
   if (!active) return;
 
   // taps of this lane's 8 channels: w[c..c+7][0..K-1] is 8*K contiguous bf16
-  // (K 16-byte loads), transposed into wt[tap][channel]
-  float wt[K][8];
+  // (K 16-byte loads), regrouped as float pairs wt[tap][pair]
+  uint64_t wt[K][4];
   {
-    const uint4* wv = reinterpret_cast<const uint4*>(a.w + static_cast<int64_t>(c0 + lane * 8) * K);
+    float wf[K][8];
+    const uint4* wv = reinterpret_cast<const uint4*>(a.w + static_cast<int64_t>(c) * K);
 #pragma unroll
     for (int q = 0; q < K; ++q) {
       float f[8];
@@ -269,59 +508,122 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int flat = 8 * q + e;
-        wt[flat % K][flat / K] = f[e];
+        wf[flat % K][flat / K] = f[e];
       }
     }
-  }
-  const int c = c0 + lane * 8;
-  for (int tt = warp; tt < n_tok; tt += kConvThreads / 32) {
-    const int4 sr = tok_s[tt];
-    const int64_t t = t0 + tt;
-    const int64_t start = t0 + sr.x;
-    const int r = sr.z;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < K; ++i) {
-      const int64_t j = t - static_cast<int64_t>(K - 1 - i) * dil;
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (j >= start) {
-        u = win[static_cast<int>(j - row0) * kConvSliceVecs + lane];
-      } else if (a.state != nullptr) {
-        const int64_t hp = W + (j - start);  // history row, oldest first
-        if (hp >= 0) u = ldg16(a.state + (static_cast<int64_t>(r) * W + hp) * C + c);
-      }
-      float f[8];
-      unpack8(u, f);
+    for (int i = 0; i < K; ++i)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(wt[i][e], f[e], acc[e]);
-    }
-    *reinterpret_cast<uint4*>(a.out + t * C + c) = pack8(acc);
-    // carry-over: the CTA holding a request's last token writes its state
-    if (a.state_out != nullptr && W > 0 && tt == sr.y - 1) {
-      for (int jj = 0; jj < W; ++jj) {
-        const int64_t sj = t - W + 1 + jj;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (sj >= start) u = win[static_cast<int>(sj - row0) * kConvSliceVecs + lane];
-        else if (a.state != nullptr && W + (sj - start) >= 0)
-          u = ldg16(a.state + (static_cast<int64_t>(r) * W + W + (sj - start)) * C + c);
-        *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
-      }
-    }
+      for (int p = 0; p < 4; ++p) wt[i][p] = f2(wf[i][2 * p], wf[i][2 * p + 1]);
   }
 
-  // Requests with no tokens keep their state (the first token tile copies it;
-  // only active lanes get here).
-  if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
-    for (int r = 0; r < a.num_reqs; ++r) {
-      int64_t s0, e0;
-      request_span(a.qsl, a.num_reqs, T, r, &s0, &e0);
-      if (e0 != s0) continue;
-      for (int jj = warp; jj < W; jj += kConvThreads / 32) {
-        const int64_t off = (static_cast<int64_t>(r) * W + jj) * C + c;
-        const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(a.state_out + off) = v;
+  const ulonglong2* win2 = reinterpret_cast<const ulonglong2*>(s.win);
+  if (all_fast) {
+    // no branches: two tokens per iteration so that one's shared-memory
+    // loads overlap the other's FMAs
+    constexpr int kWarps = kConvThreads / 32;
+    for (int tt = warp; tt < n_tok; tt += 2 * kWarps) {
+      const bool two = tt + kWarps < n_tok;
+      uint64_t acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const int row = (z == 0 || two ? tt + z * kWarps : tt) + i * dil;
+          const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
+          const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
+          acc[z][0] = f2_fma(wt[i][0], x0.x, acc[z][0]);
+          acc[z][1] = f2_fma(wt[i][1], x0.y, acc[z][1]);
+          acc[z][2] = f2_fma(wt[i][2], x1.x, acc[z][2]);
+          acc[z][3] = f2_fma(wt[i][3], x1.y, acc[z][3]);
+        }
+      }
+#pragma unroll
+      for (int z = 0; z < 2; ++z) {
+        if (z == 1 && !two) break;
+        uint4 y;
+        float lo, hi;
+        f2_split(acc[z][0], lo, hi); y.x = pack2(lo, hi);
+        f2_split(acc[z][1], lo, hi); y.y = pack2(lo, hi);
+        f2_split(acc[z][2], lo, hi); y.z = pack2(lo, hi);
+        f2_split(acc[z][3], lo, hi); y.w = pack2(lo, hi);
+        *reinterpret_cast<uint4*>(a.out + (t0 + tt + z * kWarps) * C + c) = y;
       }
     }
+  } else
+  for (int tt = warp; tt < n_tok; tt += kConvThreads / 32) {
+    const int st = s.tok_start[tt];
+    uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
+    if (tt - W >= st) {
+      // all taps inside the request: window rows tt, tt + d, ..., tt + W
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int row = tt + i * dil;
+        const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
+        const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
+        acc[0] = f2_fma(wt[i][0], x0.x, acc[0]);
+        acc[1] = f2_fma(wt[i][1], x0.y, acc[1]);
+        acc[2] = f2_fma(wt[i][2], x1.x, acc[2]);
+        acc[3] = f2_fma(wt[i][3], x1.y, acc[3]);
+      }
+    } else {
+      // a request's first W tokens: taps before its start come from the
+      // carry-over state (zeros without one); all state loads first
+      const int r = s.tok_req[tt];
+      uint4 hist[K];
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j = tt - (K - 1 - i) * dil;
+        hist[i] = make_uint4(0, 0, 0, 0);
+        if (j < st && a.state != nullptr)
+          hist[i] = ldg16(a.state + (static_cast<int64_t>(r) * W + (W + j - st)) * C + c);
+      }
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int j = tt - (K - 1 - i) * dil;
+        uint64_t x[4];
+        if (j >= st) {
+          const int row = tt + i * dil;
+          const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
+          const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
+          x[0] = x0.x; x[1] = x0.y; x[2] = x1.x; x[3] = x1.y;
+        } else {
+          x[0] = f2(bf_lo(hist[i].x), bf_hi(hist[i].x));
+          x[1] = f2(bf_lo(hist[i].y), bf_hi(hist[i].y));
+          x[2] = f2(bf_lo(hist[i].z), bf_hi(hist[i].z));
+          x[3] = f2(bf_lo(hist[i].w), bf_hi(hist[i].w));
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc[p] = f2_fma(wt[i][p], x[p], acc[p]);
+      }
+    }
+    uint4 y;
+    float lo, hi;
+    f2_split(acc[0], lo, hi); y.x = pack2(lo, hi);
+    f2_split(acc[1], lo, hi); y.y = pack2(lo, hi);
+    f2_split(acc[2], lo, hi); y.z = pack2(lo, hi);
+    f2_split(acc[3], lo, hi); y.w = pack2(lo, hi);
+    *reinterpret_cast<uint4*>(a.out + (t0 + tt) * C + c) = y;
+  }
+
+  if (a.state_out == nullptr || W == 0) return;
+  // new state of the requests ending in this tile: their last W virtual rows
+  const int ending = s.counts[1];
+  for (int q = warp; q < ending * W; q += kConvThreads / 32) {
+    const int kk = s.end_k[q / W];
+    const int jj = q % W;
+    const int st = s.req_s[kk];
+    const int r = s.req_r[kk];
+    const int sj = s.req_e[kk] - W + jj;  // token of state row jj, relative to t0
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (sj >= st) {
+      const float4 x0 = s.win[((sj + W) * 2) * 32 + lane];
+      const float4 x1 = s.win[((sj + W) * 2 + 1) * 32 + lane];
+      u = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(x1.x, x1.y), pack2(x1.z, x1.w));
+    } else if (a.state != nullptr) {
+      u = ldg16(a.state + (static_cast<int64_t>(r) * W + (W + sj - st)) * C + c);
+    }
+    *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
   }
 }
 
@@ -334,6 +636,8 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
     return fail(PLE_ERR_INVALID_ARG, "%s: kernel_size %d / dilation %d out of range", name, K, dil);
   if (num_reqs < 0 || (num_reqs == 0 && T > 0))
     return fail(PLE_ERR_INVALID_ARG, "%s: num_reqs must be >= 1 when there are tokens", name);
+  if (T > 0x7fffffff - 2 * kMaxHalo)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: %lld tokens is too many", name, static_cast<long long>(T));
   if (!w || (T > 0 && !qsl)) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(w)) return fail(PLE_ERR_INVALID_ARG, "%s: conv taps must be 16-byte aligned", name);
   const size_t state_bytes = static_cast<size_t>(num_reqs) * (K - 1) * dil * C * 2;
@@ -352,7 +656,7 @@ int conv_tile_tokens(int64_t T, int C) {
   while (tile > 8 && ((T + tile - 1) / tile) * slices < 4 * static_cast<int64_t>(num_sms())) tile >>= 1;
   if (const char* e = getenv("PLE_CONV_TILE")) {
     const int v = atoi(e);
-    if (v >= 1 && v <= 256) tile = v;
+    if (v >= 1 && v <= 128) tile = v;
   }
   return tile;
 }
@@ -361,7 +665,7 @@ template <bool GATED>
 ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, const char* name) {
   const int W = (a.K - 1) * a.dil;
   const int tile = conv_tile_tokens(a.T, a.C);
-  const size_t smem = static_cast<size_t>(tile + W) * kConvSlice * 2 + static_cast<size_t>(tile) * 16;
+  const size_t smem = conv_smem_bytes(tile, W);
   void (*kernel)(ConvArgs, const float*, int) = nullptr;
   switch (a.K) {
     case 1: kernel = conv_kernel<GATED, 1>; break;
@@ -377,7 +681,6 @@ ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, c
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, name);
   const int64_t tiles = (a.T + tile - 1) / tile;
-  if (tiles > 0x7fffffff) return fail(PLE_ERR_UNSUPPORTED, "%s: too many tokens", name);
   const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>((a.C + kConvSlice - 1) / kConvSlice));
   kernel<<<grid, kConvThreads, smem, stream>>>(a, g, tile);
   return check_cuda(cudaGetLastError(), name);
@@ -394,16 +697,16 @@ PLE_EXPORT ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
   if (num_tokens < 0 || hidden_size < 8 || hidden_size % 8 != 0)
     return fail(PLE_ERR_INVALID_ARG, "ple_gate: hidden_size %d must be a positive multiple of 8",
                 hidden_size);
+  if (hidden_size > kMaxGateC)
+    return fail(PLE_ERR_UNSUPPORTED, "ple_gate: hidden_size %d above %d", hidden_size, kMaxGateC);
   if (num_tokens == 0) return PLE_OK;
   if (!hidden || !kv || !gamma_h || !gamma_k || !out)
     return fail(PLE_ERR_INVALID_ARG, "ple_gate: null pointer");
   if (!aligned16(hidden) || !aligned16(kv) || !aligned16(gamma_h) || !aligned16(gamma_k) ||
       !aligned16(out))
     return fail(PLE_ERR_INVALID_ARG, "ple_gate: buffers must be 16-byte aligned");
-  const int64_t blocks = (num_tokens + kGateWarps - 1) / kGateWarps;
-  gate_kernel<<<static_cast<unsigned>(blocks), kGateThreads, 0, stream>>>(
-      hidden, kv, gamma_h, gamma_k, eps, num_tokens, hidden_size, out, gate_out);
-  return check_cuda(cudaGetLastError(), "ple_gate launch");
+  return gate_pass<true>(hidden, kv, gamma_h, gamma_k, eps, num_tokens, hidden_size, out,
+                         gate_out, stream, "ple_gate");
 }
 
 static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf16_t* src,
@@ -416,6 +719,8 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   using namespace ple;
   ple_status s = validate_conv(qsl, num_reqs, T, C, w, K, dil, state, state_out, name);
   if (s != PLE_OK) return s;
+  if (gated && C > kMaxGateC)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d above %d", name, C, kMaxGateC);
   const size_t state_bytes = static_cast<size_t>(num_reqs) * (K - 1) * dil * C * 2;
   if (T == 0) return copy_carry(state_out, state, state_bytes, stream);
   if (!src || !out || (gated && (!hidden || !gamma_h || !gamma_k)))
@@ -427,11 +732,7 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
     return fail(PLE_ERR_INVALID_ARG, "%s: gate_out is required (it carries the gate scalars "
                 "from the reduction pass to the conv pass)", name);
   ConvArgs a{};
-  a.hidden = hidden;
   a.src = src;
-  a.gamma_h = gamma_h;
-  a.gamma_k = gamma_k;
-  a.eps = eps;
   a.qsl = qsl;
   a.num_reqs = num_reqs;
   a.T = T;
@@ -442,20 +743,10 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   a.state = state;
   a.state_out = state_out;
   a.out = out;
-  a.gate_out = gate_out;
   a.dev_err = dev_err;
   if (!gated) return launch_conv<false>(a, nullptr, stream, name);
-  const int64_t blocks = (T + kGateScalarWarps - 1) / kGateScalarWarps;
-  const size_t gg_bytes = static_cast<size_t>(C) * sizeof(float);
-  if (gg_bytes > 200 * 1024) return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d too large", name, C);
-  cudaError_t ferr = cudaFuncSetAttribute(gate_scalar_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(gg_bytes));
-  if (ferr != cudaSuccess) return check_cuda(ferr, name);
-  gate_scalar_kernel<<<static_cast<unsigned>(blocks), kGateScalarThreads, gg_bytes, stream>>>(
-      hidden, src, gamma_h, gamma_k, eps, T, C, gate_out);
-  ple_status st = check_cuda(cudaGetLastError(), name);
-  if (st != PLE_OK) return st;
+  s = gate_pass<false>(hidden, src, gamma_h, gamma_k, eps, T, C, nullptr, gate_out, stream, name);
+  if (s != PLE_OK) return s;
   return launch_conv<true>(a, gate_out, stream, name);
 }
 

@@ -26,7 +26,7 @@ namespace ple {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 8;  // independent rows per thread (the grid gives most threads one pass)
+constexpr int kUnroll = 4;
 
 __device__ __forceinline__ uint4 load_row_vec(const void* p) {
   uint4 v;

@@ -216,7 +216,8 @@ ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w,
  *   hidden      [num_tokens][C] bf16.   kv [num_tokens][2C] bf16 (k | v).
  *   gamma_h/k   [C] bf16.                out (u) [num_tokens][C] bf16.
  *   gate_out    [num_tokens] float32 or NULL (the scalar gates).
- * C must be a multiple of 8.
+ * C must be a multiple of 8 (else PLE_ERR_INVALID_ARG) and at most 16384
+ * (else PLE_ERR_UNSUPPORTED); the same bound holds for ple_gate_conv.
  */
 ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
                     const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k,

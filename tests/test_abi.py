@@ -107,6 +107,11 @@ def test_conv_and_gate_reject_bad_shapes(lib):
                              None, None, None, None, None) == 1
 
 
+def test_gate_rejects_hidden_above_limit(lib):
+    assert lib.ple_gate(None, None, None, None, 1e-6, 4, 16392, None, None, None) == 2
+    assert b"16384" in lib.ple_last_error()
+
+
 def test_wait_rejects_null_event(lib):
     assert lib.ple_wait(None, None, 0) == 1
 

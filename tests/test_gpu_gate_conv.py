@@ -31,7 +31,8 @@ def dev_qsl(q):
     return torch.from_numpy(np.asarray(q, dtype=np.int32)).cuda()
 
 
-@pytest.mark.parametrize("T,C", [(1, 8), (37, 64), (512, 1024), (300, 4096)])
+@pytest.mark.parametrize("T,C", [(1, 8), (37, 64), (65, 520), (512, 1024), (300, 4096),
+                                 (40, 8192), (17, 16384)])
 def test_gate_matches_oracle(T, C):
     h = rand_bf16((T, C), 1.0, 1)
     kv = rand_bf16((T, 2 * C), 0.02, 2)
@@ -55,6 +56,13 @@ CONV_CASES = [
     ([70, 2, 33], 24, 8, 9),
     ([10, 20], 40, 2, 5),
     ([1] * 50, 8, 4, 3),
+    # decode-like: every token's taps reach into the carry-over state; C not a
+    # multiple of the 256-channel slice (idle lanes in the last slice)
+    ([1] * 300, 264, 4, 3),
+    # hundreds of empty requests around a few non-empty ones
+    ([0] * 40 + [5] + [0] * 300 + [7, 0, 0, 3], 48, 3, 2),
+    # one long request over many token tiles
+    ([2000], 72, 4, 3),
 ]
 
 
@@ -107,7 +115,8 @@ def _gate_conv_inputs(lengths, C, seed):
 
 
 @pytest.mark.parametrize("lengths,C", [([64, 100, 150, 198], 1024), ([7, 0, 30, 2, 0, 61], 256),
-                                       ([1] * 40, 64), ([300], 4096)])
+                                       ([1] * 40, 64), ([300], 4096),
+                                       ([1] * 70 + [3, 0, 9], 264)])
 def test_gate_conv_matches_oracle_and_separate_kernels(lengths, C):
     q, T, h, kv, gh, gk, w = _gate_conv_inputs(lengths, C, 20)
     R = len(lengths)
