@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
+#include <cstring>
 
 namespace ple {
 namespace {
@@ -339,6 +340,249 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel: tcgen05.mma.cta_group::2, M = 256 (128 rows per SM) x
+// N = 256. Each CTA of a cluster pair stages its own 128 rows of A and its own
+// half (128 rows) of the W tile; the pair's tensor cores read both halves of
+// W, so each SM reads 32 KB of operands from shared memory per K step of 64
+// instead of 48 KB, and a stage is 32 KB, leaving room for 6 stages in
+// flight. The even CTA (leader) issues the MMAs; TMA copies of both CTAs
+// complete on the leader's full barrier; the leader's commits release the
+// stages and hand the accumulators to the epilogues of both CTAs; both
+// epilogues report back to the leader's accumulator-empty barrier.
+// ---------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_STAGE = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of the W tile
+constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
+constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
+constexpr int kEpilogueWarps = kEpilogueThreads / 32;
+// kind::f16 instruction descriptor for M = 256 (two SMs) x N = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
+                                (uint32_t(BN >> 3) << 17) | (uint32_t((2 * BM) >> 4) << 24);
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdescPair), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` in both CTAs of the pair once the
+// pair MMAs issued so far complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b, ple_bf16_t* __restrict__ out,
+                    int M, int N, int K, int32_t* dev_err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* a_smem = smem;
+  uint8_t* b_smem = smem + P_STAGES * P_A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * P_STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();     // 0 = leader (issues the MMAs)
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int n_tiles = (N + BN - 1) / BN;
+  const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
+  const int num_tiles = m_tiles * n_tiles;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);    // the leader's expect_tx; bytes from both CTAs
+      mbar_init(empty_bar(s), 1);   // one commit of the leader per use
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 2 * kEpilogueWarps);  // every epilogue warp of the pair
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    // collective over the pair: the same columns in both SMs' tensor memory
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and tensor memory exist
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+      const int m0 = (tile / n_tiles) * 2 * BM + static_cast<int>(rank) * BM;
+      const int n0 = (tile % n_tiles) * BN + static_cast<int>(rank) * (BN / 2);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+        const uint32_t leader_full = map_to_rank(full_bar(stage), 0);
+        if (rank == 0) {
+          mbar_arrive_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        }
+        tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE), &map_a, leader_full, kb * BK, m0);
+        tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE), &map_b, leader_full, kb * BK, n0);
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+    // The leader does not leave with copies of an armed stage in flight.
+    for (int s = 0; s < P_STAGES; ++s)
+      if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u, nullptr);
+  } else if (warp == 1) {
+    if (rank == 0 && lane == 0) {
+      // ---------------- MMA issuer (leader only) ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_desc(smem_u32(a_smem + stage * P_A_STAGE));
+          const uint64_t b_desc = sw128_desc(smem_u32(b_smem + stage * P_B_STAGE));
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
+            umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(empty_bar(stage));   // frees the stage in both CTAs
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(accf_bar(acc));        // accumulator halves ready in both SMs
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+      umma_commit_pair_local(done_bar);
+      mbar_wait(done_bar, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs): this SM's 128 rows ----------------
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag));
+      if (!ok) {
+        if (lane == 0) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
+        break;
+      }
+      tc_fence_after();
+      const int m = (tile / n_tiles) * 2 * BM + static_cast<int>(rank) * BM + row_in_tile;
+      const int n_base = (tile % n_tiles) * BN;
+      ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
+#pragma unroll 1
+      for (int chunk = 0; chunk < BN / 32; ++chunk) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                      static_cast<uint32_t>(acc * ACC_COLS + chunk * 32),
+                  r);
+        const int n = n_base + chunk * 32;
+        if (m < M && n < N) {
+          uint4* dst = reinterpret_cast<uint4*>(row_out + n);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(r[8 * q + 0], r[8 * q + 1]);
+            v.y = pack_bf16x2(r[8 * q + 2], r[8 * q + 3]);
+            v.z = pack_bf16x2(r[8 * q + 4], r[8 * q + 5]);
+            v.w = pack_bf16x2(r[8 * q + 6], r[8 * q + 7]);
+            dst[q] = v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(acc), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // No CTA leaves while its peer may still read its shared memory (the pair
+  // MMAs), copy into it or arrive on its barriers.
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -389,30 +633,39 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
   const int M = static_cast<int>(num_tokens);
   const int N = 2 * hidden;
   const int K = emb_dim;
+  // Kernel: the CTA-pair kernel when there are at least two 128-row blocks,
+  // else one CTA per tile. PLE_KVPROJ_MODE = pair | cluster | single
+  // overrides (launch-shape sweeps and tests; cluster = 2-CTA clusters that
+  // share the W tile by TMA multicast, each CTA with its own 1-SM MMAs).
+  enum { kSingle, kCluster, kPair } mode = (M > BM) ? kPair : kSingle;
+  if (const char* e = getenv("PLE_KVPROJ_MODE")) {
+    if (strcmp(e, "single") == 0) mode = kSingle;
+    else if (strcmp(e, "cluster") == 0) mode = kCluster;
+    else if (strcmp(e, "pair") == 0) mode = kPair;
+  }
+  if (const char* e = getenv("PLE_KVPROJ_CLUSTER"))
+    if (atoi(e) == 1) mode = kSingle;
+  const int cluster = mode == kSingle ? 1 : 2;
   CUtensorMap map_a, map_b;
   ple_status s = make_map(&map_a, emb, M, K, BM);
   if (s != PLE_OK) return s;
-  const int cluster_rows = (M > BM) ? BN / 2 : BN;  // W rows one CTA loads per stage
-  int b_box = cluster_rows;
-  if (const char* e = getenv("PLE_KVPROJ_CLUSTER")) b_box = (atoi(e) == 1) ? BN : b_box;
-  s = make_map(&map_b, w, N, K, b_box);
+  s = make_map(&map_b, w, N, K, mode == kSingle ? BN : BN / 2);  // W rows one CTA loads per stage
   if (s != PLE_OK) return s;
-  // Clusters of two CTAs sharing W tiles when there are at least two row
-  // blocks; PLE_KVPROJ_CLUSTER=1 forces single CTAs (launch-shape sweeps).
-  int cluster = (M > BM) ? 2 : 1;
-  if (const char* e = getenv("PLE_KVPROJ_CLUSTER")) cluster = (atoi(e) == 1) ? 1 : cluster;
-  auto kernel = cluster == 2 ? kv_proj_kernel<2> : kv_proj_kernel<1>;
+  void (*kernel)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*) =
+      mode == kPair ? kv_proj_pair_kernel : (mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>);
+  const size_t smem = mode == kPair ? kPairSmemBytes : kSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+                                         static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj: smem attribute");
-  const int m_groups = ((M + BM - 1) / BM + cluster - 1) / cluster;
-  const int tiles = m_groups * ((N + BN - 1) / BN);
+  // work units: pair tiles (256 rows) or, per cluster position, 128-row tiles
+  const int rows_per_unit = mode == kPair ? 2 * BM : BM * cluster;
+  const int units = ((M + rows_per_unit - 1) / rows_per_unit) * ((N + BN - 1) / BN);
   const int max_clusters = num_sms() / cluster;
-  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  const int clusters = units < max_clusters ? units : max_clusters;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

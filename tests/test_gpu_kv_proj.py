@@ -3,7 +3,7 @@ matmul, on tile-aligned and ragged shapes (M tails, N not a multiple of the
 256-wide tile, K not a multiple of the 64-wide k-block), the tiny workload's
 512 -> 2 x 1024 shape, and the 8k-prefill shape 8192 x 2048 -> 2 x 4096 in the
 launch configuration the benchmark times (sampled rows through the oracle,
-every row against cuBLAS as a library cross-check)."""
+every row against cuBLAS as a library cross-check), for each kernel variant."""
 
 import numpy as np
 import pytest
@@ -69,15 +69,35 @@ def test_kv_proj_prefill_8k_shape():
     assert_close(bits(kv), bits(lib_ref), what="kv vs cuBLAS")
 
 
-@pytest.mark.parametrize("M,E,C", [(512, 512, 1024), (300, 2048, 4096), (129, 200, 48)])
-def test_kv_proj_single_cta_variant(M, E, C, monkeypatch):
-    """The launch without W multicast (one CTA per tile) gives the same result."""
-    monkeypatch.setenv("PLE_KVPROJ_CLUSTER", "1")
+@pytest.mark.parametrize("mode", ["single", "cluster", "pair"])
+@pytest.mark.parametrize("M,E,C", [(512, 512, 1024), (300, 2048, 4096), (129, 200, 48),
+                                   (257, 72, 112), (1000, 128, 128)])
+def test_kv_proj_kernel_variants(M, E, C, mode, monkeypatch):
+    """Each kernel variant -- one CTA per 128 x 256 tile, 2-CTA clusters
+    sharing the W tile by multicast, CTA pairs with cta_group::2 MMAs over
+    256 x 256 tiles -- gives the oracle's result, ragged edges included."""
+    monkeypatch.setenv("PLE_KVPROJ_MODE", mode)
     emb = rand_bf16((M, E), 0.5, M + E)
     w = rand_bf16((2 * C, E), 0.05, C + 7)
-    kv = torch.empty((M, 2 * C), dtype=torch.bfloat16, device="cuda")
+    kv = torch.full((M, 2 * C), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = dev_err_word()
     _lib.ple_kv_proj(emb.cuda(), w.cuda(), kv, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert_close(bits(kv), oracle_kv_proj(bits(emb), bits(w)), what=f"kv single-CTA {M}x{E}x{2*C}")
+    assert_close(bits(kv), oracle_kv_proj(bits(emb), bits(w)), what=f"kv {mode} {M}x{E}x{2*C}")
+
+
+@pytest.mark.parametrize("mode", ["single", "cluster", "pair"])
+def test_kv_proj_variants_prefill_8k_against_cublas(mode, monkeypatch):
+    monkeypatch.setenv("PLE_KVPROJ_MODE", mode)
+    M, E, C = 8192, 2048, 4096
+    g = torch.Generator(device="cuda").manual_seed(12)
+    emb = (torch.randn((M, E), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    w = (torch.randn((2 * C, E), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    kv = torch.empty((M, 2 * C), dtype=torch.bfloat16, device="cuda")
+    err = dev_err_word()
+    _lib.ple_kv_proj(emb, w, kv, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lib_ref = (emb.float() @ w.float().T).to(torch.bfloat16)
+    assert_close(bits(kv), bits(lib_ref), what=f"kv {mode} vs cuBLAS")
