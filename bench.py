@@ -264,6 +264,18 @@ def run_ours(args):
     gate = torch.empty((T,), dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
+    order_ws = None
+    if w.table_loc == "host":  # a host table is gathered in table order
+        order_ws = torch.empty((_lib.ple_lookup_ordered_workspace(
+            T, H, sets[0]["table"], sets[0]["row_scale"]),), dtype=torch.uint8, device=device)
+
+    def gather(p):
+        if order_ws is not None:
+            _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, row_scale=p["row_scale"],
+                                    dev_err=err, stream=stream)
+        else:
+            _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err,
+                            stream=stream)
 
     def step(s, ev=None):
         p = sets[s % num_sets]
@@ -274,7 +286,7 @@ def run_ours(args):
                            ctx_out if w.decode else None, err, stream)
         if ev is not None:
             ev[1].record(stream)
-        _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err, stream=stream)
+        gather(p)
         if ev is not None:
             ev[2].record(stream)
         _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=stream)
@@ -413,7 +425,7 @@ def run_ours(args):
         "clocks": clocks,
     }
     if w.table_loc == "host":
-        line["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device)
+        line["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
@@ -421,8 +433,9 @@ def run_ours(args):
 
 def launches_per_step(w, table):
     """libple kernels one step launches: ids, gather, kv_proj, and the gate
-    and conv passes."""
-    return LAUNCHES_PER_STEP
+    and conv passes; a host table's ordered gather adds its count, scan and
+    scatter kernels."""
+    return LAUNCHES_PER_STEP + (3 if w.table_loc == "host" else 0)
 
 
 def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
@@ -443,10 +456,11 @@ def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
     return round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
 
 
-def uva_overlap(torch, _lib, p, ids, emb, w, device, reps=20):
-    """The pinned-host gather prefetched on a side stream (half the SMs)
-    while a 4096^3 bf16 GEMM -- a stand-in for the previous layer, run by
-    cuBLAS through torch -- occupies the main stream: each alone, then both."""
+def uva_overlap(torch, _lib, p, ids, emb, w, device, order_ws, reps=20):
+    """The pinned-host gather (in table order) prefetched on a side stream
+    (half the SMs) while a 4096^3 bf16 GEMM -- a stand-in for the previous
+    layer, run by cuBLAS through torch -- occupies the main stream: each
+    alone, then both; plus the gather in (token, head) order alone."""
     main = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device)
     half = max(1, torch.cuda.get_device_properties(device).multi_processor_count // 2)
@@ -458,11 +472,20 @@ def uva_overlap(torch, _lib, p, ids, emb, w, device, reps=20):
     def gemm():
         torch.matmul(a, b, out=c)
 
+    def prefetch():
+        _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, max_ctas=half, stream=side)
+        done.record(side)
+
     def gather():
+        side.wait_stream(main)
+        prefetch()
+        _lib.ple_wait(done, main)
+
+    def gather_unordered():
         _lib.ple_lookup_prefetch(ids, p["table"], emb, side, done, max_ctas=half)
         _lib.ple_wait(done, main)
 
-    def timed(fn):
+    def timed(fn, reps=reps):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -478,15 +501,17 @@ def uva_overlap(torch, _lib, p, ids, emb, w, device, reps=20):
 
     def both():
         side.wait_stream(main)
-        _lib.ple_lookup_prefetch(ids, p["table"], emb, side, done, max_ctas=half)
+        prefetch()
         gemm()
         _lib.ple_wait(done, main)
 
     g_us, m_us, b_us = timed(gather), timed(gemm), timed(both)
+    u_us = timed(gather_unordered, reps=3)
     row_bytes = w.num_tokens * w.num_heads * w.head_dim * 2
     return {"gather_alone_us": round(g_us, 1), "gemm_alone_us": round(m_us, 1),
             "overlapped_us": round(b_us, 1), "hidden_fraction": round((g_us + m_us - b_us) / g_us, 3),
             "gather_link_gbs": round(row_bytes / (g_us * 1e-6) / 1e9, 1),
+            "gather_unordered_alone_us": round(u_us, 1),
             "gather_ctas": half, "gemm": "4096x4096x4096 bf16 (cuBLAS via torch.matmul)"}
 
 

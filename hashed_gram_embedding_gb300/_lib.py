@@ -42,6 +42,9 @@ SIGNATURES = {
     "ple_lookup": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32, _P, _P],
     "ple_lookup_prefetch": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32,
                             _P, _P, _P],
+    "ple_lookup_ordered_workspace": [_I64, _I32, _I64, _I32, ctypes.c_int],
+    "ple_lookup_ordered": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32,
+                           _P, ctypes.c_size_t, _P, _P],
     "ple_wait": [_P, _P, _I32],
     "ple_kv_proj": [_P, _P, _I64, _I32, _I32, _P, _P, _P],
     "ple_gate": [_P, _P, _P, _P, _F32, _I64, _I32, _P, _P, _P],
@@ -75,7 +78,8 @@ def lib():
         for name, args in SIGNATURES.items():
             fn = getattr(handle, name)
             fn.argtypes = args
-            fn.restype = ctypes.c_char_p if name in ("ple_last_error", "ple_version") else ctypes.c_int
+            fn.restype = (ctypes.c_char_p if name in ("ple_last_error", "ple_version") else
+                          ctypes.c_size_t if name.endswith("_workspace") else ctypes.c_int)
         _lib = handle
     return _lib
 
@@ -133,6 +137,23 @@ def ple_lookup(ids, table, out, row_scale=None, max_ctas=0, dev_err=None, loc=No
     [T, H*D]."""
     return _check("ple_lookup", lib().ple_lookup(
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
+
+
+def ple_lookup_ordered_workspace(num_tokens, num_heads, table, row_scale=None):
+    """Bytes of device workspace ple_lookup_ordered needs."""
+    dtype = PLE_FP8_E4M3 if row_scale is not None else PLE_BF16
+    return int(lib().ple_lookup_ordered_workspace(int(num_tokens), int(num_heads),
+                                                  table.shape[0], table.shape[1], dtype))
+
+
+def ple_lookup_ordered(ids, table, out, workspace, row_scale=None, max_ctas=0, dev_err=None,
+                       loc=None, stream=None):
+    """ple_lookup with the rows read in table order; workspace: a device
+    uint8 tensor of at least ple_lookup_ordered_workspace(...) bytes."""
+    a = _lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc)
+    return _check("ple_lookup_ordered", lib().ple_lookup_ordered(
+        *a[:-1], _ptr(workspace), workspace.numel() * workspace.element_size(), a[-1],
+        _stream(stream)))
 
 
 def _event_handle(event, stream):

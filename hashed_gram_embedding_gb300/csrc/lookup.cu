@@ -17,7 +17,8 @@
 // enough bytes in flight (HBM: ~64 KB per SM; host link: more, hence the
 // unroll). Table reads bypass L1 (ld.global.nc.L1::no_allocate) and ask L2 for
 // the whole 256-B row; output stores are ordinary write-back stores so that
-// the next kernel (kv_proj) finds the rows in L2.
+// the next kernel (kv_proj) finds the rows in L2. ple_lookup_ordered walks
+// the items in table order (see the page-ordered walk below).
 #include "common.cuh"
 
 #include <cuda_fp8.h>
@@ -39,22 +40,26 @@ __device__ __forceinline__ uint4 load_row_vec(const void* p) {
 // 0 = runtime value).
 template <int VPR>
 __global__ void __launch_bounds__(kThreads)
-gather_bf16_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_rt,
-                   const uint4* __restrict__ table, int64_t table_rows,
-                   uint4* __restrict__ out, int32_t* dev_err) {
+gather_bf16_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ perm,
+                   uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
+                   int64_t table_rows, uint4* __restrict__ out, int32_t* dev_err) {
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
        base += stride * kUnroll) {
     uint4 v[kUnroll];
-    uint32_t idx[kUnroll];
+    uint32_t o[kUnroll];  // output vector of each work item
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      idx[u] = base + u * stride;
+      const uint32_t idx = base + u * stride;
       v[u] = make_uint4(0, 0, 0, 0);
-      if (idx[u] < total_vecs) {
-        const uint32_t row_out = idx[u] / vpr;  // (token, head) pair
-        const uint32_t k = idx[u] - row_out * vpr;
+      o[u] = total_vecs;
+      if (idx < total_vecs) {
+        const uint32_t p = idx / vpr;  // position in the walk
+        const uint32_t k = idx - p * vpr;
+        const uint32_t row_out = perm != nullptr ? __ldg(perm + p) : p;  // (token, head) pair
+        if (row_out >= total_vecs / vpr) continue;  // (never, for a walk order from the sort)
+        o[u] = row_out * vpr + k;
         const int64_t id = __ldg(ids + row_out);
         if (static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
           v[u] = load_row_vec(table + id * vpr + k);
@@ -65,7 +70,7 @@ gather_bf16_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (idx[u] < total_vecs) out[idx[u]] = v[u];
+      if (o[u] < total_vecs) out[o[u]] = v[u];
   }
 }
 
@@ -91,24 +96,29 @@ __device__ __forceinline__ void dequant16(uint4 c, float s, uint4* lo, uint4* hi
 
 template <int VPR>
 __global__ void __launch_bounds__(kThreads)
-gather_fp8_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_rt,
-                  const uint4* __restrict__ table, const float* __restrict__ row_scale,
-                  int64_t table_rows, uint4* __restrict__ out, int32_t* dev_err) {
+gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ perm,
+                  uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
+                  const float* __restrict__ row_scale, int64_t table_rows,
+                  uint4* __restrict__ out, int32_t* dev_err) {
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
        base += stride * kUnroll) {
     uint4 c[kUnroll];
     float s[kUnroll];
-    uint32_t idx[kUnroll];
+    uint32_t o[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      idx[u] = base + u * stride;
+      const uint32_t idx = base + u * stride;
       c[u] = make_uint4(0, 0, 0, 0);
       s[u] = 0.f;
-      if (idx[u] < total_vecs) {
-        const uint32_t row_out = idx[u] / vpr;
-        const uint32_t k = idx[u] - row_out * vpr;
+      o[u] = total_vecs;
+      if (idx < total_vecs) {
+        const uint32_t p = idx / vpr;
+        const uint32_t k = idx - p * vpr;
+        const uint32_t row_out = perm != nullptr ? __ldg(perm + p) : p;
+        if (row_out >= total_vecs / vpr) continue;  // (never, for a walk order from the sort)
+        o[u] = row_out * vpr + k;
         const int64_t id = __ldg(ids + row_out);
         if (static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
           c[u] = load_row_vec(table + id * vpr + k);
@@ -120,21 +130,137 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, uint32_t total_vecs, int vpr_
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (idx[u] < total_vecs) {
+      if (o[u] < total_vecs) {
         uint4 lo, hi;
         dequant16(c[u], s[u], &lo, &hi);
-        out[2 * static_cast<size_t>(idx[u])] = lo;
-        out[2 * static_cast<size_t>(idx[u]) + 1] = hi;
+        out[2 * static_cast<size_t>(o[u])] = lo;
+        out[2 * static_cast<size_t>(o[u]) + 1] = hi;
       }
     }
   }
 }
 
-ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_heads,
-                         const void* table, int64_t table_rows, int32_t head_dim,
-                         ple_dtype dtype, const float* row_scale, ple_table_loc loc,
-                         ple_bf16_t* out, int32_t max_ctas, int32_t* dev_err,
-                         cudaStream_t stream, const char* name) {
+// ---------------------------------------------------------------------------
+// Page-ordered walk (for tables in host memory). The GPU translates host
+// addresses through a cache of limited reach: a random row gather over a
+// 32 GB host table misses it on almost every row and runs at a tenth of the
+// link rate, while the same rows read in table order run at the link rate
+// (measured on a GB300: 16 vs 197 GB/s). The ordered gather first sorts the
+// (token, head) items by the 2 MiB span of the table their row lies in
+// (counting sort: count, scan, scatter), then walks them in that order and
+// writes every row to its own output slot, so the result is identical.
+// ---------------------------------------------------------------------------
+constexpr int kOrderThreads = 256;
+constexpr int kScanThreads = 1024;
+constexpr uint32_t kMaxBuckets = 1u << 20;
+
+struct OrderPlan {
+  int shift;         // rows of one bucket = 2^shift (2 MiB of table, or more)
+  uint32_t buckets;  // spans of the table + one bucket for ids outside it
+  size_t counts_off, cursor_off, perm_off, bytes;
+};
+
+OrderPlan order_plan(int64_t items, int64_t table_rows, int row_bytes) {
+  OrderPlan p{};
+  int shift = 0;
+  while ((static_cast<int64_t>(row_bytes) << (shift + 1)) <= (int64_t(2) << 20)) ++shift;
+  while (((table_rows + (int64_t(1) << shift) - 1) >> shift) + 1 > kMaxBuckets) ++shift;
+  p.shift = shift;
+  p.buckets = static_cast<uint32_t>(((table_rows + (int64_t(1) << shift) - 1) >> shift) + 1);
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  p.counts_off = 0;
+  p.cursor_off = up(static_cast<size_t>(p.buckets) * 4);
+  p.perm_off = p.cursor_off + up(static_cast<size_t>(p.buckets) * 4);
+  p.bytes = p.perm_off + up(static_cast<size_t>(items) * 4);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t bucket_of(int64_t id, int64_t rows, int shift,
+                                              uint32_t buckets) {
+  return static_cast<uint64_t>(id) < static_cast<uint64_t>(rows)
+             ? static_cast<uint32_t>(id >> shift)
+             : buckets - 1;
+}
+
+__global__ void __launch_bounds__(kOrderThreads)
+order_count_kernel(const int64_t* __restrict__ ids, uint32_t items, int64_t rows, int shift,
+                   uint32_t buckets, uint32_t* __restrict__ counts) {
+  for (uint32_t i = blockIdx.x * kOrderThreads + threadIdx.x; i < items;
+       i += gridDim.x * kOrderThreads)
+    atomicAdd(counts + bucket_of(__ldg(ids + i), rows, shift, buckets), 1u);
+}
+
+// Exclusive prefix sum of counts[0, n) into cursor[0, n), one CTA.
+__global__ void __launch_bounds__(kScanThreads)
+order_scan_kernel(const uint32_t* __restrict__ counts, uint32_t n, uint32_t* __restrict__ cursor) {
+  __shared__ uint32_t warp_tot[kScanThreads / 32];
+  const uint32_t tid = threadIdx.x;
+  const uint32_t chunk = (n + kScanThreads - 1) / kScanThreads;
+  const uint32_t b0 = tid * chunk;
+  const uint32_t b1 = min(b0 + chunk, n);
+  uint32_t sum = 0;
+  for (uint32_t b = b0; b < b1; ++b) sum += counts[b];
+  // block-wide exclusive scan of the per-thread sums
+  uint32_t x = sum;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  uint32_t run = x - sum + (warp > 0 ? warp_tot[warp - 1] : 0u);
+  for (uint32_t b = b0; b < b1; ++b) {
+    const uint32_t c = counts[b];
+    cursor[b] = run;
+    run += c;
+  }
+}
+
+__global__ void __launch_bounds__(kOrderThreads)
+order_scatter_kernel(const int64_t* __restrict__ ids, uint32_t items, int64_t rows, int shift,
+                     uint32_t buckets, uint32_t* __restrict__ cursor,
+                     uint32_t* __restrict__ perm) {
+  for (uint32_t i = blockIdx.x * kOrderThreads + threadIdx.x; i < items;
+       i += gridDim.x * kOrderThreads) {
+    const uint32_t b = bucket_of(__ldg(ids + i), rows, shift, buckets);
+    perm[atomicAdd(cursor + b, 1u)] = i;
+  }
+}
+
+// A validated gather: everything the kernels need.
+struct Gather {
+  const int64_t* ids;
+  int64_t items;      // num_tokens * num_heads
+  int64_t table_rows;
+  int vpr;            // 16-byte vectors per table row
+  int row_bytes;
+  ple_dtype dtype;
+  const float* row_scale;
+  const uint4* table;  // device view
+  uint4* out;
+  uint32_t total_vecs;
+  unsigned grid;
+  int32_t* dev_err;
+};
+
+ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_heads,
+                          const void* table, int64_t table_rows, int32_t head_dim,
+                          ple_dtype dtype, const float* row_scale, ple_table_loc loc,
+                          ple_bf16_t* out, int32_t max_ctas, int32_t* dev_err,
+                          const char* name, Gather* g, bool* empty) {
+  *empty = false;
   if (num_tokens < 0 || num_heads < 1 || head_dim < 1 || table_rows < 0)
     return fail(PLE_ERR_INVALID_ARG, "%s: bad sizes (T=%lld H=%d D=%d rows=%lld)", name,
                 static_cast<long long>(num_tokens), num_heads, head_dim,
@@ -147,7 +273,10 @@ ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_hea
   if ((static_cast<int64_t>(head_dim) * elem) % 16 != 0)
     return fail(PLE_ERR_UNSUPPORTED, "%s: row of %d bytes is not a multiple of 16", name,
                 head_dim * elem);
-  if (num_tokens == 0) return PLE_OK;
+  if (num_tokens == 0) {
+    *empty = true;
+    return PLE_OK;
+  }
   if (!ids || !table || !out) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
   if (dtype == PLE_FP8_E4M3 && !row_scale)
     return fail(PLE_ERR_INVALID_ARG, "%s: fp8 table needs row_scale", name);
@@ -170,31 +299,79 @@ ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_hea
   if (total >= (int64_t(1) << 31))
     return fail(PLE_ERR_UNSUPPORTED, "%s: %lld row vectors exceed one launch", name,
                 static_cast<long long>(total));
-  const uint32_t total_vecs = static_cast<uint32_t>(total);
   int64_t blocks = (total + kThreads * kUnroll - 1) / (kThreads * kUnroll);
   const int64_t full_grid = static_cast<int64_t>(num_sms()) * (2048 / kThreads);
   if (blocks > full_grid) blocks = full_grid;
   if (max_ctas > 0 && blocks > max_ctas) blocks = max_ctas;
-  const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+  g->ids = ids;
+  g->items = num_tokens * num_heads;
+  g->table_rows = table_rows;
+  g->vpr = vpr;
+  g->row_bytes = vpr * 16;
+  g->dtype = dtype;
+  g->row_scale = row_scale;
   // Read the table through the device view of the allocation (identical to
   // the host address under unified addressing, but ask rather than assume).
-  const void* dev_table = attr.devicePointer ? attr.devicePointer : table;
-  const uint4* tab = static_cast<const uint4*>(dev_table);
-  uint4* o = reinterpret_cast<uint4*>(out);
-  if (dtype == PLE_BF16) {
+  g->table = static_cast<const uint4*>(attr.devicePointer ? attr.devicePointer : table);
+  g->out = reinterpret_cast<uint4*>(out);
+  g->total_vecs = static_cast<uint32_t>(total);
+  g->grid = static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+  g->dev_err = dev_err;
+  return PLE_OK;
+}
+
+ple_status launch_gather_kernel(const Gather& g, const uint32_t* perm, cudaStream_t stream,
+                                const char* name) {
+  const int vpr = g.vpr;
+  if (g.dtype == PLE_BF16) {
     if (vpr == 16)
-      gather_bf16_kernel<16><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+      gather_bf16_kernel<16><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else if (vpr == 8)
-      gather_bf16_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+      gather_bf16_kernel<8><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else
-      gather_bf16_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, table_rows, o, dev_err);
+      gather_bf16_kernel<0><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
   } else {
     if (vpr == 8)
-      gather_fp8_kernel<8><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, o, dev_err);
+      gather_fp8_kernel<8><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
     else
-      gather_fp8_kernel<0><<<grid, kThreads, 0, stream>>>(ids, total_vecs, vpr, tab, row_scale, table_rows, o, dev_err);
+      gather_fp8_kernel<0><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
   }
   return check_cuda(cudaGetLastError(), name);
+}
+
+ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_heads,
+                         const void* table, int64_t table_rows, int32_t head_dim,
+                         ple_dtype dtype, const float* row_scale, ple_table_loc loc,
+                         ple_bf16_t* out, int32_t max_ctas, int32_t* dev_err,
+                         cudaStream_t stream, const char* name) {
+  Gather g{};
+  bool empty = false;
+  ple_status s = prepare_gather(ids, num_tokens, num_heads, table, table_rows, head_dim, dtype,
+                                row_scale, loc, out, max_ctas, dev_err, name, &g, &empty);
+  if (s != PLE_OK || empty) return s;
+  return launch_gather_kernel(g, nullptr, stream, name);
+}
+
+// Sort the items by table span into the workspace, then gather in that order.
+ple_status launch_ordered(const Gather& g, uint8_t* ws, const OrderPlan& plan,
+                          cudaStream_t stream, const char* name) {
+  uint32_t* counts = reinterpret_cast<uint32_t*>(ws + plan.counts_off);
+  uint32_t* cursor = reinterpret_cast<uint32_t*>(ws + plan.cursor_off);
+  uint32_t* perm = reinterpret_cast<uint32_t*>(ws + plan.perm_off);
+  const uint32_t items = static_cast<uint32_t>(g.items);
+  cudaError_t err = cudaMemsetAsync(counts, 0, static_cast<size_t>(plan.buckets) * 4, stream);
+  if (err != cudaSuccess) return check_cuda(err, name);
+  int64_t blocks = (g.items + kOrderThreads - 1) / kOrderThreads;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 4;
+  const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
+  order_count_kernel<<<grid, kOrderThreads, 0, stream>>>(g.ids, items, g.table_rows, plan.shift,
+                                                          plan.buckets, counts);
+  order_scan_kernel<<<1, kScanThreads, 0, stream>>>(counts, plan.buckets, cursor);
+  order_scatter_kernel<<<grid, kOrderThreads, 0, stream>>>(g.ids, items, g.table_rows,
+                                                            plan.shift, plan.buckets, cursor, perm);
+  ple_status s = check_cuda(cudaGetLastError(), name);
+  if (s != PLE_OK) return s;
+  return launch_gather_kernel(g, perm, stream, name);
 }
 
 }  // namespace
@@ -223,4 +400,36 @@ PLE_EXPORT ple_status ple_lookup_prefetch(const int64_t* ids, int64_t num_tokens
                                     "ple_lookup_prefetch");
   if (s != PLE_OK) return s;
   return ple::check_cuda(cudaEventRecord(done, side_stream), "ple_lookup_prefetch: record");
+}
+
+PLE_EXPORT size_t ple_lookup_ordered_workspace(int64_t num_tokens, int32_t num_heads,
+                                               int64_t table_rows, int32_t head_dim,
+                                               ple_dtype dtype) {
+  if (num_tokens < 0 || num_heads < 1 || head_dim < 1 || table_rows < 0) return 0;
+  const int elem = (dtype == PLE_FP8_E4M3) ? 1 : 2;
+  const int row_bytes = static_cast<int>((static_cast<int64_t>(head_dim) * elem + 15) / 16 * 16);
+  return ple::order_plan(num_tokens * num_heads, table_rows, row_bytes).bytes;
+}
+
+PLE_EXPORT ple_status ple_lookup_ordered(const int64_t* ids, int64_t num_tokens,
+                                         int32_t num_heads, const void* table,
+                                         int64_t table_rows, int32_t head_dim, ple_dtype dtype,
+                                         const float* row_scale, ple_table_loc loc,
+                                         ple_bf16_t* out, int32_t max_ctas, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err,
+                                         cudaStream_t stream) {
+  using namespace ple;
+  const char* name = "ple_lookup_ordered";
+  Gather g{};
+  bool empty = false;
+  ple_status s = prepare_gather(ids, num_tokens, num_heads, table, table_rows, head_dim, dtype,
+                                row_scale, loc, out, max_ctas, dev_err, name, &g, &empty);
+  if (s != PLE_OK || empty) return s;
+  const OrderPlan plan = order_plan(g.items, table_rows, g.row_bytes);
+  if (workspace == nullptr || workspace_bytes < plan.bytes)
+    return fail(PLE_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name,
+                workspace_bytes, plan.bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PLE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", name);
+  return launch_ordered(g, static_cast<uint8_t*>(workspace), plan, stream, name);
 }

@@ -1,8 +1,8 @@
 """PLELayer: one per-layer n-gram embedding step through libple.
 
 The user-facing call of the path: n-gram ids -> row gather -> kv_proj ->
-gate + short conv, four libple launches on one stream with reusable
-intermediate buffers. Device memory comes from PyTorch; all arithmetic is in
+gate + short conv, four libple calls on one stream with reusable
+intermediate buffers (a table in host memory is gathered in table order). Device memory comes from PyTorch; all arithmetic is in
 libple's kernels.
 """
 
@@ -51,7 +51,12 @@ class PLELayer:
         b = self._bufs.get(key)
         if b is None:
             E = self.num_heads * self.head_dim
+            ws = 0
+            if not self.table.is_cuda:  # host table: gather in table order
+                ws = _lib.ple_lookup_ordered_workspace(num_tokens, self.num_heads, self.table,
+                                                       self.row_scale)
             b = {
+                "order_ws": torch.empty((ws,), dtype=torch.uint8, device=device) if ws else None,
                 "ids": torch.empty((num_tokens, self.num_heads), dtype=torch.int64, device=device),
                 "emb": torch.empty((num_tokens, E), dtype=torch.bfloat16, device=device),
                 "kv": torch.empty((num_tokens, 2 * self.hidden), dtype=torch.bfloat16, device=device),
@@ -70,8 +75,13 @@ class PLELayer:
         y = out if out is not None else b["y"]
         _lib.ple_ngram_ids(input_ids, query_start_loc, ngram_context, self.mult, self.V, self.O,
                            self.eos, self.hpn, b["ids"], ngram_context_out, dev_err, stream)
-        _lib.ple_lookup(b["ids"], self.table, b["emb"], row_scale=self.row_scale,
-                        max_ctas=self.max_ctas, dev_err=dev_err, stream=stream)
+        if b["order_ws"] is not None:
+            _lib.ple_lookup_ordered(b["ids"], self.table, b["emb"], b["order_ws"],
+                                    row_scale=self.row_scale, max_ctas=self.max_ctas,
+                                    dev_err=dev_err, stream=stream)
+        else:
+            _lib.ple_lookup(b["ids"], self.table, b["emb"], row_scale=self.row_scale,
+                            max_ctas=self.max_ctas, dev_err=dev_err, stream=stream)
         _lib.ple_kv_proj(b["emb"], self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
         _lib.ple_gate_conv(hidden, b["kv"], self.gamma_h, self.gamma_k, query_start_loc,
                            self.conv_w, self.dilation, y, eps=self.eps, conv_state=conv_state,
@@ -79,5 +89,10 @@ class PLELayer:
                            dev_err=dev_err, stream=stream)
         return y
 
-    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv)
+    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv);
+    # a host table's ordered gather adds three (count, scan, scatter)
     LAUNCHES_PER_FORWARD = 5
+    ORDERED_GATHER_EXTRA = 3
+
+    def launches_per_forward(self):
+        return self.LAUNCHES_PER_FORWARD + (0 if self.table.is_cuda else self.ORDERED_GATHER_EXTRA)

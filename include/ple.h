@@ -179,6 +179,36 @@ ple_status ple_lookup_prefetch(const int64_t* ids, int64_t num_tokens,
                                cudaStream_t side_stream, cudaEvent_t done);
 
 /*
+ * ple_lookup_ordered -- ple_lookup with the rows read in table order: the
+ * (token, head) items are first sorted by the 2 MiB span of the table their
+ * row lies in (a counting sort into `workspace`), then gathered in that order,
+ * each row written to its own output slot, so `out` is identical to
+ * ple_lookup's. For tables in host memory (PLE_HOST_UVA): the GPU's address
+ * translation for host memory has limited reach, and random rows over tens of
+ * GB miss it on almost every row (a tenth of the link rate on a GB300), while
+ * rows read in table order run at the link rate. Same ids/table/out rules and
+ * device error word as ple_lookup. (PR#54371 report: the pinned-host backend
+ * reads the rows it needs in place; the ordering is this library's.)
+ *   workspace        device memory, 256-byte aligned, at least
+ *                    ple_lookup_ordered_workspace(...) bytes (else
+ *                    PLE_ERR_INVALID_ARG); its contents on entry do not
+ *                    matter and are unspecified afterwards. Two calls in
+ *                    flight at once must not share one workspace.
+ * Four kernel launches and one memset on `stream`.
+ */
+size_t ple_lookup_ordered_workspace(int64_t num_tokens, int32_t num_heads,
+                                    int64_t table_rows, int32_t head_dim,
+                                    ple_dtype dtype);
+ple_status ple_lookup_ordered(const int64_t* ids, int64_t num_tokens,
+                              int32_t num_heads, const void* table,
+                              int64_t table_rows, int32_t head_dim,
+                              ple_dtype dtype, const float* row_scale,
+                              ple_table_loc loc, ple_bf16_t* out,
+                              int32_t max_ctas, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_err,
+                              cudaStream_t stream);
+
+/*
  * ple_wait -- make `consumer` wait for `done`.
  *   timeout_ms <= 0: enqueue a device-side wait only (cudaStreamWaitEvent);
  *                    the host does not block.

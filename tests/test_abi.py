@@ -112,6 +112,22 @@ def test_gate_rejects_hidden_above_limit(lib):
     assert b"16384" in lib.ple_last_error()
 
 
+def test_ordered_gather_workspace_size(lib):
+    # 32 GiB bf16 table, D = 128 (256-byte rows): one bucket per 2 MiB span =
+    # 8192 rows, ceil(134219512 / 8192) = 16385 spans + 1 bucket for ids outside
+    # the table; counts and cursors (4 bytes per bucket) and the walk order
+    # (4 bytes per item), each rounded up to 256 bytes.
+    up = lambda x: (x + 255) // 256 * 256
+    buckets = 16385 + 1
+    want = 2 * up(4 * buckets) + up(4 * 8192 * 16)
+    assert lib.ple_lookup_ordered_workspace(8192, 16, 134219512, 128, 0) == want
+    # fp8 rows of 128 bytes: 16384 rows per 2 MiB span
+    buckets = -(-67110742 // 16384) + 1
+    assert lib.ple_lookup_ordered_workspace(100, 16, 67110742, 128, 1) == \
+        2 * up(4 * buckets) + up(4 * 1600)
+    assert lib.ple_lookup_ordered_workspace(-1, 16, 10, 128, 0) == 0
+
+
 def test_wait_rejects_null_event(lib):
     assert lib.ple_wait(None, None, 0) == 1
 

@@ -231,3 +231,62 @@ def test_uva_gather_from_huge_page_host_table(dtype):
     ref[9, 0:D] = 0
     assert np.array_equal(bits(out), ref)
     owner.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("rows", [10, 5000, 300000])
+def test_ordered_gather_equals_plain_gather(dtype, rows):
+    """ple_lookup_ordered (items sorted by table span, then gathered) writes
+    exactly what ple_lookup writes, for device and host tables, with ids
+    outside the table zeroed and flagged."""
+    rng = np.random.default_rng(rows)
+    D, T, H = 128, 333, 16
+    if dtype == "bf16":
+        table = random_table_bits(rng, rows, D)
+        dev_table = to_dev_bf16(table)
+        host = _lib.HostTable(rows, D, torch.bfloat16)
+        host.tensor.view(torch.int16).copy_(torch.from_numpy(table.view(np.int16)))
+        scale = None
+    else:
+        codes = rng.integers(0, 0x7E, size=(rows, D), dtype=np.uint8)
+        dev_table = torch.from_numpy(codes).cuda()
+        host = _lib.HostTable(rows, D, torch.uint8)
+        host.tensor.copy_(torch.from_numpy(codes))
+        sc = (np.abs(rng.standard_normal(rows)) * 1e-3 + 1e-6).astype(np.float32)
+        scale = torch.from_numpy(sc).cuda()
+    ids = rng.integers(0, rows, size=(T, H))
+    ids[5, 3] = rows
+    ids[17, 0] = -2
+    d_ids = torch.from_numpy(ids).cuda()
+    ref = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    err0 = dev_err_word()
+    _lib.ple_lookup(d_ids, dev_table, ref, row_scale=scale, dev_err=err0)
+    for tab in (dev_table, host.tensor):
+        ws = torch.empty((_lib.ple_lookup_ordered_workspace(T, H, tab, scale),), dtype=torch.uint8,
+                         device="cuda")
+        ws.fill_(0xAB)  # contents on entry do not matter
+        out = torch.full((T, H * D), 5.0, dtype=torch.bfloat16, device="cuda")
+        err = dev_err_word()
+        _lib.ple_lookup_ordered(d_ids, tab, out, ws, row_scale=scale, dev_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) & _lib.PLE_DEVERR_BOUNDS
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))  # bits (tables hold NaNs)
+    ok = ids.copy()
+    ok[5, 3] = 0
+    ok[17, 0] = 0
+    want = lookup_bf16(ok, table) if dtype == "bf16" else lookup_fp8(ok, codes, sc)
+    want[5, 3 * D:4 * D] = 0
+    want[17, 0:D] = 0
+    assert np.array_equal(bits(ref), want)
+    host.close()
+
+
+def test_ordered_gather_rejects_small_workspace():
+    rows, D, T, H = 1000, 64, 8, 2
+    table = torch.zeros((rows, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((T, H), dtype=torch.int64, device="cuda")
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    need = _lib.ple_lookup_ordered_workspace(T, H, table)
+    ws = torch.empty((need - 256,), dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.PleError, match="workspace"):
+        _lib.ple_lookup_ordered(ids, table, out, ws)
