@@ -45,6 +45,8 @@ SIGNATURES = {
     "ple_lookup_ordered_workspace": [_I64, _I32, _I64, _I32, ctypes.c_int],
     "ple_lookup_ordered": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32,
                            _P, ctypes.c_size_t, _P, _P],
+    "ple_lookup_ordered_static": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P,
+                                  _I32, _P, _P],
     "ple_wait": [_P, _P, _I32],
     "ple_kv_proj": [_P, _P, _I64, _I32, _I32, _P, _P, _P],
     "ple_gate": [_P, _P, _P, _P, _F32, _I64, _I32, _P, _P, _P],
@@ -154,6 +156,14 @@ def ple_lookup_ordered(ids, table, out, workspace, row_scale=None, max_ctas=0, d
     return _check("ple_lookup_ordered", lib().ple_lookup_ordered(
         *a[:-1], _ptr(workspace), workspace.numel() * workspace.element_size(), a[-1],
         _stream(stream)))
+
+
+def ple_lookup_ordered_static(ids, table, out, row_scale=None, max_ctas=0, dev_err=None,
+                              loc=None, stream=None):
+    """ple_lookup_ordered with the library's fixed per-device scratch (no
+    workspace, no allocation); calls in flight at once must not overlap."""
+    return _check("ple_lookup_ordered_static", lib().ple_lookup_ordered_static(
+        *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
 
 
 def _event_handle(event, stream):

@@ -23,6 +23,8 @@
 
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 namespace ple {
 namespace {
 
@@ -432,4 +434,74 @@ PLE_EXPORT ple_status ple_lookup_ordered(const int64_t* ids, int64_t num_tokens,
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(PLE_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", name);
   return launch_ordered(g, static_cast<uint8_t*>(workspace), plan, stream, name);
+}
+
+// ---------------------------------------------------------------------------
+// ple_lookup_ordered_static: ple_lookup_ordered without a caller workspace.
+// For callers that may not allocate device memory on their serving path: an
+// engine that carves all device memory into its own pools at start-up and
+// forbids any later allocation, or a C caller with no device allocator of
+// its own. The sort's scratch (bucket counters, cursors, walk order) lives in
+// one file-scope device array of fixed size per device instead; the call
+// allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+// ---------------------------------------------------------------------------
+namespace ple {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB per device
+static __device__ __align__(256) uint8_t g_order_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint8_t*> g_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (cudaGetSymbolAddress) and cached.
+ple_status static_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return check_cuda(err, "ple_lookup_ordered_static: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(PLE_ERR_UNSUPPORTED, "ple_lookup_ordered_static: device %d beyond %d", dev,
+                kMaxDevices);
+  uint8_t* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void* sym = nullptr;
+    err = cudaGetSymbolAddress(&sym, g_order_scratch);
+    if (err != cudaSuccess)
+      return check_cuda(err, "ple_lookup_ordered_static: cudaGetSymbolAddress");
+    p = static_cast<uint8_t*>(sym);
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return PLE_OK;
+}
+
+}  // namespace
+}  // namespace ple
+
+PLE_EXPORT ple_status ple_lookup_ordered_static(const int64_t* ids, int64_t num_tokens,
+                                                int32_t num_heads, const void* table,
+                                                int64_t table_rows, int32_t head_dim,
+                                                ple_dtype dtype, const float* row_scale,
+                                                ple_table_loc loc, ple_bf16_t* out,
+                                                int32_t max_ctas, int32_t* dev_err,
+                                                cudaStream_t stream) {
+  using namespace ple;
+  const char* name = "ple_lookup_ordered_static";
+  Gather g{};
+  bool empty = false;
+  ple_status s = prepare_gather(ids, num_tokens, num_heads, table, table_rows, head_dim, dtype,
+                                row_scale, loc, out, max_ctas, dev_err, name, &g, &empty);
+  if (s != PLE_OK || empty) return s;
+  const OrderPlan plan = order_plan(g.items, table_rows, g.row_bytes);
+  if (plan.bytes > kStaticScratchBytes)
+    return fail(PLE_ERR_UNSUPPORTED,
+                "%s: %lld items over %lld table rows need %zu bytes of scratch, above the "
+                "%zu-byte static scratch (use ple_lookup_ordered with a workspace)",
+                name, static_cast<long long>(g.items), static_cast<long long>(table_rows),
+                plan.bytes, kStaticScratchBytes);
+  uint8_t* scratch = nullptr;
+  s = static_scratch(&scratch);
+  if (s != PLE_OK) return s;
+  return launch_ordered(g, scratch, plan, stream, name);
 }

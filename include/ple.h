@@ -209,6 +209,34 @@ ple_status ple_lookup_ordered(const int64_t* ids, int64_t num_tokens,
                               cudaStream_t stream);
 
 /*
+ * ple_lookup_ordered_static -- ple_lookup_ordered with its scratch in a
+ * fixed 8 MiB device array inside the library (one per device) instead of a
+ * caller workspace. The pages have no counterpart: it exists for callers
+ * that may not allocate device memory on their serving path (an engine that
+ * carves all device memory into its own pools at start-up, or a C caller
+ * without a device allocator); the call itself allocates nothing.
+ *   Same arguments, results and device error word as ple_lookup_ordered,
+ *   minus the workspace.
+ *   Limit: ple_lookup_ordered_workspace(...) of the call must be at most
+ *   8 MiB (for 256-byte rows over a 32 GiB table: up to about 1.9 million
+ *   (token, head) items), else PLE_ERR_UNSUPPORTED naming the sizes.
+ *   Set-up: the first call on a device looks the array's address up
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture. Nothing in the scratch has to start at zero: each call
+ *   clears the counters it uses on `stream` before the kernels.
+ *   Races: all calls on one device share the scratch, so two calls in
+ *   flight at once (other streams, other host threads) corrupt each other's
+ *   walk order; callers must keep such calls ordered.
+ */
+ple_status ple_lookup_ordered_static(const int64_t* ids, int64_t num_tokens,
+                                     int32_t num_heads, const void* table,
+                                     int64_t table_rows, int32_t head_dim,
+                                     ple_dtype dtype, const float* row_scale,
+                                     ple_table_loc loc, ple_bf16_t* out,
+                                     int32_t max_ctas, int32_t* dev_err,
+                                     cudaStream_t stream);
+
+/*
  * ple_wait -- make `consumer` wait for `done`.
  *   timeout_ms <= 0: enqueue a device-side wait only (cudaStreamWaitEvent);
  *                    the host does not block.
