@@ -1,6 +1,8 @@
 // Status text, device-property cache, event wait, version.
 #include "common.cuh"
 
+#include <cstdlib>
+
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -36,6 +38,14 @@ int num_sms() {
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (dev >= 0 && dev < kMaxDevices) g_sms[dev] = n;
   return n;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("PLE_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
 }
 
 ple_status copy_carry(void* dst, const void* src, size_t bytes,

@@ -28,6 +28,44 @@ inline bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// Programmatic dependent launch. Every libple kernel is launched with
+// programmatic stream serialization, so it may begin while the kernel before
+// it in the stream is finishing: it first does set-up that touches no global
+// memory (barriers, tensor memory, tensor-map prefetch), then pdl_wait()
+// (griddepcontrol.wait: the previous grid has completed and its writes are
+// visible) before its first global load or store, then pdl_trigger()
+// (griddepcontrol.launch_dependents) so the next kernel may start launching.
+// PLE_PDL=0 launches without the attribute (both instructions are then
+// no-ops).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Copy a carry-over buffer (context / conv state) through when a call has
 // no tokens, so ping-pong callers always find the next state in `dst`.
 ple_status copy_carry(void* dst, const void* src, size_t bytes,
@@ -36,6 +74,11 @@ ple_status copy_carry(void* dst, const void* src, size_t bytes,
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_dev_err(int32_t* dev_err, int32_t bit) {
   if (dev_err != nullptr) atomicOr(dev_err, bit);

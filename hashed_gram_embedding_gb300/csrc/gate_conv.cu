@@ -12,14 +12,11 @@
 // over each request's virtual sequence (conv state ++ segment, zeros before).
 //
 // Design (HBM-bound: read h, k, v once, write y once; u never reaches HBM):
-//   pass 1 (gate_reduce_kernel): a group of G threads (one to eight warps)
-//     reduces sum h^2, sum k^2 and sum h*k*gh*gk over one token's hidden row:
-//     every thread owns the same channels for all tokens (their gamma
-//     products stay in registers), issues all its 16-byte loads of the row at
-//     once, and the group combines its warps' partial sums through shared
-//     memory in a fixed order. A persistent grid strides over tokens, so work
-//     is spread evenly over the SMs whatever T is. It writes the gate scalar
-//     g_t (4 bytes per token); ple_gate's variant also writes u = bf16(g*v).
+//   pass 1 (gate_stream_kernel): one warp per token reduces sum h^2, sum k^2
+//     and sum h*k*gh*gk over the hidden row; the rows stream into shared
+//     memory by bulk async copies, several tokens in flight per warp, one CTA
+//     per SM over a contiguous token range. It writes the gate scalar g_t
+//     (4 bytes per token); ple_gate's variant also writes u = bf16(g*v).
 //   pass 2 (conv_kernel<GATED=true>): a CTA takes a tile of tokens and a
 //     256-channel slice, stages its dilation window -- u of the tile and of
 //     the (K-1)*d tokens before it -- in shared memory as float32 (values
@@ -34,11 +31,11 @@
 #include "common.cuh"
 
 #include <cstdlib>
+#include <cstring>
 
 namespace ple {
 namespace {
 
-constexpr int kGateThreads = 256;
 constexpr int kConvThreads = 256;
 constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
@@ -107,167 +104,191 @@ __device__ __forceinline__ float gate_of(float sh, float sk, float sd, int C, fl
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1: gate scalars (and, for ple_gate, u = bf16(g * v)).
-// G threads per token (a power of two, 32..256); thread j of a group owns the
-// 16-byte vectors j, j+G, ..., j+(VPT-1)G of the row. Sums are kept as float
-// pairs (even / odd channel of each bf16 pair) with two-wide FMAs. Reduction
-// order: the thread's vectors in order, the 4 pairs of each, then even +
-// odd; butterfly over the warp; the group's warps in order. ple_gate and
-// ple_gate_conv share it, so both produce the same g bit for bit.
+// Pass 1: gate scalars (and, for ple_gate, u = bf16(g * v)), streamed.
+// One CTA per SM takes a contiguous range of tokens; each warp takes every
+// W-th token of it and keeps S tokens in flight: lane 0 bulk-copies the
+// token's h row and k row (4C bytes) into one of the warp's S shared-memory
+// slots, completing on that slot's mbarrier, so HBM sees W*S*4C bytes of
+// requests per SM at once while the warp reduces an earlier slot. Lane l
+// owns the 16-byte vectors l, l+32, ... of a row; gamma_h * gamma_k sits in
+// shared memory laid out to match. Sums are float pairs (even / odd channel)
+// accumulated with two-wide FMAs over the lane's vectors in order, then
+// even + odd, then a butterfly over the warp: ple_gate and ple_gate_conv run
+// this same kernel, so both produce the same g bit for bit.
 // ---------------------------------------------------------------------------
-template <int VPT, bool WRITE_U>
-__global__ void __launch_bounds__(kGateThreads)
-gate_reduce_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
+constexpr int kGsMaxWarps = 8;
+constexpr size_t kGsSmemBudget = 220 * 1024;
+constexpr int kGsChunk = 2048;  // channels of a row per slot (rows stream in chunks)
+
+// Bytes of the gamma-product table: [ceil(nv / 32)][2][32] float4, nv = C / 8
+// (whole groups of 32 vectors, so a ragged last group still has its place).
+__host__ __device__ inline size_t gate_gg_bytes(int C) {
+  return static_cast<size_t>((C / 8 + 31) / 32) * 1024;
+}
+
+struct GateStream {
+  int warps;     // per CTA
+  int slots;     // per warp
+  size_t gg_bytes, slot_bytes, smem;
+};
+
+GateStream gate_stream_shape(int C) {
+  GateStream g{};
+  g.gg_bytes = gate_gg_bytes(C);
+  g.slot_bytes = static_cast<size_t>(C < kGsChunk ? C : kGsChunk) * 4;  // h and k chunk, bf16
+  for (int slots = 3; slots >= 2; --slots) {
+    const size_t per_warp = slots * (g.slot_bytes + 8);
+    if (g.gg_bytes + per_warp > kGsSmemBudget) continue;
+    size_t warps = (kGsSmemBudget - g.gg_bytes) / per_warp;
+    if (warps > kGsMaxWarps) warps = kGsMaxWarps;
+    g.warps = static_cast<int>(warps);
+    g.slots = slots;
+    g.smem = g.gg_bytes + warps * per_warp;
+    return g;
+  }
+  return g;  // warps == 0: too large
+}
+
+template <bool WRITE_U>
+__global__ void __launch_bounds__(kGsMaxWarps * 32)
+gate_stream_kernel(const ple_bf16_t* __restrict__ hidden, const ple_bf16_t* __restrict__ kv,
                    const ple_bf16_t* __restrict__ gamma_h, const ple_bf16_t* __restrict__ gamma_k,
-                   float eps, int64_t T, int C, int G, ple_bf16_t* __restrict__ u_out,
-                   float* __restrict__ gate_out) {
-  __shared__ float red[3][kGateThreads / 32];
-  __shared__ float g_s[kGateThreads / 32];
+                   float eps, int64_t T, int C, int slots, ple_bf16_t* __restrict__ u_out,
+                   float* __restrict__ gate_out, int32_t* dev_err) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int groups = kGateThreads / G;
-  const int grp = tid / G;
-  const int j = tid - grp * G;
+  const int warps = blockDim.x >> 5;
   const int nv = C >> 3;
+  const size_t gg_bytes = gate_gg_bytes(C);
+  const int CC = C < kGsChunk ? C : kGsChunk;  // channels per chunk
+  const int nch = (C + CC - 1) / CC;           // chunks per row
+  const size_t slot_bytes = static_cast<size_t>(CC) * 4;
+  float4* gg4 = reinterpret_cast<float4*>(smem);  // [nv/32][2][32]
+  uint8_t* slot0 = smem + gg_bytes + static_cast<size_t>(warp) * slots * slot_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + gg_bytes +
+                                               static_cast<size_t>(warps) * slots * slot_bytes);
+  const uint32_t bar0 = smem_u32(bars + warp * slots);
 
-  uint64_t gg[VPT][4];  // gamma_h * gamma_k of this thread's channels, as pairs
-#pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int v = j + i * G;
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-    if (v < nv) {
-      a = ldg16(gamma_h + v * 8);
-      b = ldg16(gamma_k + v * 8);
-    }
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-      gg[i][p] = f2_mul(f2(bf_lo(aw[p]), bf_hi(aw[p])), f2(bf_lo(bw[p]), bf_hi(bw[p])));
+  if (tid == 0) {
+    for (int i = 0; i < warps * slots; ++i) mbar_init(smem_u32(bars + i), 1);
+    mbar_fence_init();
   }
+  pdl_wait();  // k comes from the previous kernel
+  pdl_trigger();
+  for (int v = tid; v < nv; v += blockDim.x) {
+    const uint4 a = ldg16(gamma_h + v * 8);
+    const uint4 b = ldg16(gamma_k + v * 8);
+    float fa[8], fb[8];
+    unpack8(a, fa);
+    unpack8(b, fb);
+    gg4[((v >> 5) * 2) * 32 + (v & 31)] =
+        make_float4(fa[0] * fb[0], fa[1] * fb[1], fa[2] * fb[2], fa[3] * fb[3]);
+    gg4[((v >> 5) * 2 + 1) * 32 + (v & 31)] =
+        make_float4(fa[4] * fb[4], fa[5] * fb[5], fa[6] * fb[6], fa[7] * fb[7]);
+  }
+  __syncthreads();
 
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * groups;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * groups; base < T; base += stride) {
-    const int64_t t = base + grp;
-    const bool valid = t < T;
-    uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // +0.0f pairs
-    uint4 vv[WRITE_U ? VPT : 1];
-    if (valid) {
-      const ple_bf16_t* h_row = hidden + t * C;
-      const ple_bf16_t* k_row = kv + t * 2 * C;
-      uint4 hv[VPT], kk[VPT];
+  // items of this warp: (token k, chunk j), m = k * nch + j
+  const int64_t ta = T * blockIdx.x / gridDim.x;
+  const int64_t tb = T * (blockIdx.x + 1) / gridDim.x;
+  const int64_t n_tok = tb - ta > warp ? (tb - ta - warp + warps - 1) / warps : 0;
+  const int64_t n_items = n_tok * nch;
+  auto token = [&](int64_t k) { return ta + warp + k * warps; };
+  auto chunk_ch = [&](int j) { return C - j * CC < CC ? C - j * CC : CC; };
+  auto issue = [&](int64_t m) {  // lane 0 only
+    const int64_t t = token(m / nch);
+    const int j = static_cast<int>(m % nch);
+    const uint32_t bytes = static_cast<uint32_t>(chunk_ch(j)) * 2;
+    const int sl = static_cast<int>(m % slots);
+    const uint32_t bar = bar0 + 8u * sl;
+    const uint32_t dst = smem_u32(slot0 + sl * slot_bytes);
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_copy_g2s(dst, hidden + t * C + j * CC, bytes, bar);
+    bulk_copy_g2s(dst + static_cast<uint32_t>(CC) * 2, kv + t * 2 * C + j * CC, bytes, bar);
+  };
+  if (lane == 0)
+    for (int64_t m = 0; m < n_items && m < slots; ++m) issue(m);
+
+  uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // +0.0f pairs, over a token's chunks
+  int64_t m = 0;
+  for (; m < n_items; ++m) {
+    const int sl = static_cast<int>(m % slots);
+    const uint32_t parity = static_cast<uint32_t>((m / slots) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * sl, parity, nullptr))) {
+      if (lane == 0) set_dev_err(dev_err, PLE_DEVERR_TIMEOUT);
+      break;
+    }
+    const int j = static_cast<int>(m % nch);
+    const int nvc = chunk_ch(j) >> 3;
+    const int v0 = j * (CC >> 3);  // first vector of the chunk (a multiple of 32 or 0)
+    const uint4* h4 = reinterpret_cast<const uint4*>(slot0 + sl * slot_bytes);
+    const uint4* k4 = reinterpret_cast<const uint4*>(slot0 + sl * slot_bytes + static_cast<size_t>(CC) * 2);
+    for (int vl = lane; vl < nvc; vl += 32) {
+      const int i = (v0 + vl) >> 5;  // group of 32 vectors of the row
+      const uint4 hv = h4[vl];
+      const uint4 kk = k4[vl];
+      const float4 g0 = gg4[(i * 2) * 32 + lane];
+      const float4 g1 = gg4[(i * 2 + 1) * 32 + lane];
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w};
+      const uint64_t gp[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = j + i * G;
-        hv[i] = make_uint4(0, 0, 0, 0);
-        kk[i] = make_uint4(0, 0, 0, 0);
-        if (v < nv) {
-          hv[i] = ldg16(h_row + v * 8);
-          kk[i] = ldg16(k_row + v * 8);
-          if constexpr (WRITE_U) vv[i] = ldg16(k_row + C + v * 8);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
-        const uint32_t kw[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const uint64_t h2 = f2(bf_lo(hw[p]), bf_hi(hw[p]));
-          const uint64_t k2 = f2(bf_lo(kw[p]), bf_hi(kw[p]));
-          sh2 = f2_fma(h2, h2, sh2);
-          sk2 = f2_fma(k2, k2, sk2);
-          sd2 = f2_fma(f2_mul(h2, k2), gg[i][p], sd2);
-        }
+      for (int p = 0; p < 4; ++p) {
+        const uint64_t h2 = f2(bf_lo(hw[p]), bf_hi(hw[p]));
+        const uint64_t k2 = f2(bf_lo(kw[p]), bf_hi(kw[p]));
+        sh2 = f2_fma(h2, h2, sh2);
+        sk2 = f2_fma(k2, k2, sk2);
+        sd2 = f2_fma(f2_mul(h2, k2), gp[p], sd2);
       }
     }
+    __syncwarp();
+    if (lane == 0 && m + slots < n_items) {
+      // the slot was read through the generic proxy; order that before the
+      // bulk copy (async proxy) that refills it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(m + slots);
+    }
+    if (j != nch - 1) continue;
     float a0, a1, b0, b1, d0, d1;
     f2_split(sh2, a0, a1);
     f2_split(sk2, b0, b1);
     f2_split(sd2, d0, d1);
-    const float sh = warp_sum(a0 + a1);
-    const float sk = warp_sum(b0 + b1);
-    const float sd = warp_sum(d0 + d1);
-    if (lane == 0) {
-      red[0][warp] = sh;
-      red[1][warp] = sk;
-      red[2][warp] = sd;
-    }
-    __syncthreads();
-    if (valid && j == 0) {
-      const int w0 = grp * (G >> 5);
-      float a = red[0][w0], b = red[1][w0], d = red[2][w0];
-      for (int w = 1; w < (G >> 5); ++w) {
-        a += red[0][w0 + w];
-        b += red[1][w0 + w];
-        d += red[2][w0 + w];
-      }
-      const float g = gate_of(a, b, d, C, eps);
-      if (gate_out != nullptr) gate_out[t] = g;
-      if constexpr (WRITE_U) g_s[grp] = g;
-    }
-    __syncthreads();
+    sh2 = sk2 = sd2 = 0;
+    const float g = gate_of(warp_sum(a0 + a1), warp_sum(b0 + b1), warp_sum(d0 + d1), C, eps);
+    const int64_t t = token(m / nch);
+    if (lane == 0 && gate_out != nullptr) gate_out[t] = g;
     if constexpr (WRITE_U) {
-      if (valid) {
-        const float g = g_s[grp];
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v = j + i * G;
-          if (v < nv) *reinterpret_cast<uint4*>(u_out + t * C + v * 8) = gate8(vv[i], g);
-        }
-      }
+      const ple_bf16_t* v_row = kv + t * 2 * C + C;
+      for (int v = lane; v < nv; v += 32)
+        *reinterpret_cast<uint4*>(u_out + t * C + v * 8) = gate8(ldg16(v_row + v * 8), g);
     }
   }
-}
-
-// Threads per token and vectors per thread for hidden size C: about four
-// vectors of each operand per thread.
-void gate_shape(int C, int* G, int* vpt) {
-  const int nv = C / 8;
-  int g = 32;
-  while (g < kGateThreads && 4 * g < nv) g *= 2;
-  int v = 1;
-  while (v * g < nv) v *= 2;
-  *G = g;
-  *vpt = v;
-}
-
-template <int VPT, bool WRITE_U>
-ple_status launch_gate_reduce(const ple_bf16_t* hidden, const ple_bf16_t* kv,
-                              const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k, float eps,
-                              int64_t T, int C, int G, ple_bf16_t* u_out, float* gate_out,
-                              cudaStream_t stream, const char* name) {
-  static int per_sm = 0;  // resident CTAs per SM of this instantiation
-  if (per_sm == 0) {
-    int n = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, gate_reduce_kernel<VPT, WRITE_U>, kGateThreads, 0);
-    if (err != cudaSuccess) return check_cuda(err, name);
-    per_sm = n > 0 ? n : 1;
-  }
-  const int groups = kGateThreads / G;
-  const int64_t need = (T + groups - 1) / groups;
-  const int64_t resident = static_cast<int64_t>(num_sms()) * per_sm;
-  const unsigned blocks = static_cast<unsigned>(need < resident ? need : resident);
-  gate_reduce_kernel<VPT, WRITE_U><<<blocks, kGateThreads, 0, stream>>>(
-      hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out);
-  return check_cuda(cudaGetLastError(), name);
+  // after a timeout: never leave with a copy in flight into this warp's slots
+  if (lane == 0)
+    for (int64_t q = m; q < n_items && q < m + slots; ++q)
+      mbar_wait(bar0 + 8u * static_cast<uint32_t>(q % slots),
+                static_cast<uint32_t>((q / slots) & 1), nullptr);
 }
 
 template <bool WRITE_U>
 ple_status gate_pass(const ple_bf16_t* hidden, const ple_bf16_t* kv, const ple_bf16_t* gamma_h,
                      const ple_bf16_t* gamma_k, float eps, int64_t T, int C, ple_bf16_t* u_out,
-                     float* gate_out, cudaStream_t stream, const char* name) {
-  int G, vpt;
-  gate_shape(C, &G, &vpt);
-  switch (vpt) {
-    case 1: return launch_gate_reduce<1, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
-    case 2: return launch_gate_reduce<2, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
-    case 4: return launch_gate_reduce<4, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
-    case 8: return launch_gate_reduce<8, WRITE_U>(hidden, kv, gamma_h, gamma_k, eps, T, C, G, u_out, gate_out, stream, name);
-    default: return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d above %d", name, C, kMaxGateC);
-  }
+                     float* gate_out, int32_t* dev_err, cudaStream_t stream, const char* name) {
+  const GateStream gs = gate_stream_shape(C);
+  if (gs.warps == 0 || C > kMaxGateC)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d above %d", name, C, kMaxGateC);
+  cudaError_t err = cudaFuncSetAttribute(gate_stream_kernel<WRITE_U>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(gs.smem));
+  if (err != cudaSuccess) return check_cuda(err, name);
+  const int64_t grid = T < num_sms() ? T : num_sms();
+  err = launch_kernel(gate_stream_kernel<WRITE_U>, dim3(static_cast<unsigned>(grid)),
+                      dim3(gs.warps * 32), gs.smem, stream, 1, hidden, kv, gamma_h, gamma_k, eps,
+                      T, C, gs.slots, u_out, gate_out, dev_err);
+  if (err != cudaSuccess) return check_cuda(err, name);
+  return check_cuda(cudaGetLastError(), name);
 }
 
 // ---------------------------------------------------------------------------
@@ -395,6 +416,8 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   const ConvSmem s = conv_smem(smem, tile_tokens, W);
   const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
   const ple_bf16_t* src = a.src + (GATED ? C : 0) + c;
+  pdl_wait();  // v and g come from the previous kernels
+  pdl_trigger();
 
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = tid; i < R + 1; i += kConvThreads) check_qsl(a.qsl, R, T, i, a.dev_err);
@@ -627,6 +650,295 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming conv pass: one CTA per (token range, 256-channel slice), two per
+// SM. The CTA walks its range in chunks of CH >= (K-1)*d tokens. Thread 0
+// bulk-copies each chunk's rows of the slice (512 bytes each) into one of
+// three raw shared-memory slots, two chunks ahead of the one being computed;
+// all warps then convert the chunk into a float32 ring of CH + (K-1)*d rows
+// (gated: u = bf16(g * v)), which still holds the (K-1)*d rows before the
+// chunk, and compute the chunk's outputs from the ring exactly as the tiled
+// kernel does (same taps, same FMA order, same bits). Chunk 0 is the halo:
+// the (K-1)*d rows before the range.
+// ---------------------------------------------------------------------------
+constexpr int kCsSlots = 3;
+
+__host__ __device__ inline int conv_stream_chunk(int W) { return W > 32 ? W : 32; }
+
+__host__ __device__ inline size_t conv_stream_smem(int CH, int W) {
+  return static_cast<size_t>(CH + W) * kConvSlice * 4           // float32 ring
+         + static_cast<size_t>(kCsSlots) * CH * kConvSlice * 2  // raw slots
+         + 64                                                   // mbarriers
+         + static_cast<size_t>(CH) * 6 * 4 + 16;                // request lists
+}
+
+template <bool GATED, int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv_stream_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int CH) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int dil = a.dil;
+  const int W = (K - 1) * dil;
+  const int C = a.C;
+  const int R = a.num_reqs;
+  const int64_t T = a.T;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  constexpr int kWarps = kConvThreads / 32;
+  const int c0 = blockIdx.y * kConvSlice;
+  const int slice_ch = C - c0 < kConvSlice ? C - c0 : kConvSlice;
+  const uint32_t row_bytes = static_cast<uint32_t>(slice_ch) * 2;
+  const int c = c0 + lane * 8;
+  const bool active = c < C;
+  const int NW = CH + W;  // ring rows
+  const int64_t ta = T * blockIdx.x / gridDim.x;
+  const int64_t tb = T * (blockIdx.x + 1) / gridDim.x;
+  const int nq = static_cast<int>((tb - ta + CH - 1) / CH);  // token chunks; chunk 0 = halo
+
+  float4* ring = reinterpret_cast<float4*>(smem);  // [NW][2][32]
+  uint8_t* raw = smem + static_cast<size_t>(NW) * kConvSlice * 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + static_cast<size_t>(kCsSlots) * CH * kConvSlice * 2);
+  ConvSmem sm;
+  {
+    int* p = reinterpret_cast<int*>(bars + 8);
+    sm.win = nullptr;
+    sm.tok_start = nullptr;
+    sm.tok_req = nullptr;
+    sm.req_s = p;
+    sm.req_e = p + CH;
+    sm.req_r = p + 2 * CH;
+    sm.end_k = p + 3 * CH;
+    sm.counts = p + 4 * CH;
+  }
+  const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
+  const ple_bf16_t* src_slice = a.src + (GATED ? C : 0) + c0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kCsSlots; ++i) mbar_init(smem_u32(bars + i), 1);
+    mbar_fence_init();
+  }
+  pdl_wait();  // v and g come from the previous kernels
+  pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = tid; i < R + 1; i += kConvThreads) check_qsl(a.qsl, R, T, i, a.dev_err);
+  __syncthreads();
+
+  // rows of chunk q: [first, first + count); chunk 0 is the halo before ta
+  auto chunk_first = [&](int q) { return q == 0 ? ta - W : ta + static_cast<int64_t>(q - 1) * CH; };
+  auto chunk_count = [&](int q) -> int {
+    if (q == 0) return W;
+    const int64_t f = ta + static_cast<int64_t>(q - 1) * CH;
+    return static_cast<int>(tb - f < CH ? tb - f : CH);
+  };
+  auto issue = [&](int q) {  // thread 0
+    const int sl = q % kCsSlots;
+    const uint32_t bar = smem_u32(bars + sl);
+    const int64_t first = chunk_first(q);
+    const int count = chunk_count(q);
+    const int skip = first < 0 ? static_cast<int>(-first) : 0;  // rows before token 0
+    const int n = count > skip ? count - skip : 0;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * row_bytes);
+    const uint32_t dst = smem_u32(raw + static_cast<size_t>(sl) * CH * kConvSlice * 2);
+    for (int r = skip; r < count; ++r)
+      bulk_copy_g2s(dst + static_cast<uint32_t>(r) * kConvSlice * 2,
+                    src_slice + (first + r) * src_pitch, row_bytes, bar);
+  };
+  if (tid == 0)
+    for (int q = 0; q <= nq && q < kCsSlots; ++q) issue(q);
+
+  // requests with no tokens keep their state (copied by the first range)
+  if (a.state_out != nullptr && W > 0 && blockIdx.x == 0) {
+    for (int base = warp * 32; base < R; base += kConvThreads) {
+      bool empty = false;
+      if (base + lane < R) {
+        int64_t s0, e0;
+        request_span(a.qsl, R, T, base + lane, &s0, &e0);
+        empty = e0 == s0;
+      }
+      unsigned m = __ballot_sync(0xffffffffu, empty);
+      while (m != 0u && active) {
+        const int r = base + __ffs(m) - 1;
+        m &= m - 1;
+        for (int jj = 0; jj < W; ++jj) {
+          const int64_t off = (static_cast<int64_t>(r) * W + jj) * C + c;
+          const uint4 v = a.state ? ldg16(a.state + off) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(a.state_out + off) = v;
+        }
+      }
+    }
+  }
+
+  // taps of this lane's 8 channels as float pairs wt[tap][pair]
+  uint64_t wt[K][4];
+  {
+    float wf[K][8];
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (active)
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.w + static_cast<int64_t>(c) * K) + q), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int flat = 8 * q + e;
+        wf[flat % K][flat / K] = f[e];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) wt[i][p] = f2(wf[i][2 * p], wf[i][2 * p + 1]);
+  }
+  const ulonglong2* ring2 = reinterpret_cast<const ulonglong2*>(ring);
+  // The ring holds token ta - W + i at row i mod NW; row of chunk q's first
+  // token, and a row a few positions on (less than NW) with one wrap.
+  auto chunk_row0 = [&](int q) { return q == 0 ? 0 : static_cast<int>((W + static_cast<int64_t>(q - 1) * CH) % NW); };
+  auto wrap = [&](int row) { return row >= NW ? row - NW : row; };
+
+  int q = 0;
+  for (; q <= nq; ++q) {
+    const int sl = q % kCsSlots;
+    const uint32_t parity = static_cast<uint32_t>((q / kCsSlots) & 1);
+    const bool ok = mbar_wait(smem_u32(bars + sl), parity, nullptr);
+    // B1: every warp is done with chunk q-1 (its ring rows may be reused)
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
+      break;
+    }
+    const int64_t first = chunk_first(q);
+    const int count = chunk_count(q);
+    const int row0 = chunk_row0(q);
+    if (q > 0 && warp == 0) find_tile_requests(a.qsl, R, T, first, count, CH, sm, lane);
+    // convert the chunk's rows into the ring
+    if (active) {
+      const uint8_t* slot = raw + static_cast<size_t>(sl) * CH * kConvSlice * 2;
+      for (int r = warp; r < count; r += kWarps) {
+        const int64_t tok = first + r;
+        if (tok < 0) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(slot + static_cast<size_t>(r) * kConvSlice * 2 + lane * 16);
+        float f[8];
+        if constexpr (GATED) {
+          const float gx = __ldg(g + tok);
+          const uint64_t gg = f2(gx, gx);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            float lo, hi;
+            f2_split(f2_mul(f2(bf_lo(w4[p]), bf_hi(w4[p])), gg), lo, hi);
+            const uint32_t u = pack2(lo, hi);  // round to bf16
+            f[2 * p] = bf_lo(u);
+            f[2 * p + 1] = bf_hi(u);
+          }
+        } else {
+          unpack8(v, f);
+        }
+        const int rr = wrap(row0 + r);
+        ring[(rr * 2) * 32 + lane] = make_float4(f[0], f[1], f[2], f[3]);
+        ring[(rr * 2 + 1) * 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+    }
+    __syncthreads();  // B2: ring rows and request lists ready; raw slot free
+    if (tid == 0 && q + kCsSlots <= nq) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(q + kCsSlots);
+    }
+    if (q == 0 || !active) continue;
+
+    const int listed = sm.counts[0];
+    for (int tt = warp; tt < count; tt += kWarps) {
+      // the token's request: last listed start <= tt
+      int lo = 0, hi = listed;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.req_s[mid] <= tt) lo = mid + 1; else hi = mid;
+      }
+      const int k = lo - 1;
+      int st = tt, r = 0;  // (invalid qsl only: no history)
+      if (k >= 0 && tt < sm.req_e[k]) {
+        st = sm.req_s[k];
+        r = sm.req_r[k];
+      }
+      const int64_t t = first + tt;
+      const int p0 = wrap(row0 + tt);
+      uint64_t acc[4] = {0, 0, 0, 0};
+      if (tt - W >= st) {
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+          int row = p0 - (K - 1 - i) * dil;
+          if (row < 0) row += NW;
+          const ulonglong2 x0 = ring2[(row * 2) * 32 + lane];
+          const ulonglong2 x1 = ring2[(row * 2 + 1) * 32 + lane];
+          acc[0] = f2_fma(wt[i][0], x0.x, acc[0]);
+          acc[1] = f2_fma(wt[i][1], x0.y, acc[1]);
+          acc[2] = f2_fma(wt[i][2], x1.x, acc[2]);
+          acc[3] = f2_fma(wt[i][3], x1.y, acc[3]);
+        }
+      } else {
+        uint4 hist[K];
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+          const int j = tt - (K - 1 - i) * dil;
+          hist[i] = make_uint4(0, 0, 0, 0);
+          if (j < st && a.state != nullptr)
+            hist[i] = ldg16(a.state + (static_cast<int64_t>(r) * W + (W + j - st)) * C + c);
+        }
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+          const int j = tt - (K - 1 - i) * dil;
+          uint64_t x[4];
+          if (j >= st) {
+            int row = p0 - (K - 1 - i) * dil;
+            if (row < 0) row += NW;
+            const ulonglong2 x0 = ring2[(row * 2) * 32 + lane];
+            const ulonglong2 x1 = ring2[(row * 2 + 1) * 32 + lane];
+            x[0] = x0.x; x[1] = x0.y; x[2] = x1.x; x[3] = x1.y;
+          } else {
+            x[0] = f2(bf_lo(hist[i].x), bf_hi(hist[i].x));
+            x[1] = f2(bf_lo(hist[i].y), bf_hi(hist[i].y));
+            x[2] = f2(bf_lo(hist[i].z), bf_hi(hist[i].z));
+            x[3] = f2(bf_lo(hist[i].w), bf_hi(hist[i].w));
+          }
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) acc[pp] = f2_fma(wt[i][pp], x[pp], acc[pp]);
+        }
+      }
+      uint4 y;
+      float lo2, hi2;
+      f2_split(acc[0], lo2, hi2); y.x = pack2(lo2, hi2);
+      f2_split(acc[1], lo2, hi2); y.y = pack2(lo2, hi2);
+      f2_split(acc[2], lo2, hi2); y.z = pack2(lo2, hi2);
+      f2_split(acc[3], lo2, hi2); y.w = pack2(lo2, hi2);
+      *reinterpret_cast<uint4*>(a.out + t * C + c) = y;
+    }
+
+    if (a.state_out == nullptr || W == 0) continue;
+    // new state of the requests ending in this chunk: their last W virtual rows
+    const int ending = sm.counts[1];
+    for (int qq = warp; qq < ending * W; qq += kWarps) {
+      const int kk = sm.end_k[qq / W];
+      const int jj = qq % W;
+      const int st = sm.req_s[kk];
+      const int r = sm.req_r[kk];
+      const int sj = sm.req_e[kk] - W + jj;  // relative to the chunk start
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (sj >= st) {
+        int rr = row0 + sj;  // sj in [-W, CH): one wrap either way
+        rr = rr < 0 ? rr + NW : wrap(rr);
+        const float4 x0 = ring[(rr * 2) * 32 + lane];
+        const float4 x1 = ring[(rr * 2 + 1) * 32 + lane];
+        u = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(x1.x, x1.y), pack2(x1.z, x1.w));
+      } else if (a.state != nullptr) {
+        u = ldg16(a.state + (static_cast<int64_t>(r) * W + (W + sj - st)) * C + c);
+      }
+      *reinterpret_cast<uint4*>(a.state_out + (static_cast<int64_t>(r) * W + jj) * C + c) = u;
+    }
+  }
+  // never leave with a bulk copy in flight into this CTA's shared memory
+  // (chunks q .. q+2 may still be in flight only after a timeout above)
+  if (tid == 0)
+    for (int j = q; j <= nq && j < q + kCsSlots; ++j)
+      mbar_wait(smem_u32(bars + j % kCsSlots), static_cast<uint32_t>((j / kCsSlots) & 1), nullptr);
+}
+
 ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_t C,
                          const ple_bf16_t* w, int32_t K, int32_t dil,
                          const ple_bf16_t* state, ple_bf16_t* state_out, const char* name) {
@@ -664,25 +976,51 @@ int conv_tile_tokens(int64_t T, int C) {
 template <bool GATED>
 ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, const char* name) {
   const int W = (a.K - 1) * a.dil;
-  const int tile = conv_tile_tokens(a.T, a.C);
-  const size_t smem = conv_smem_bytes(tile, W);
+  const int slices = (a.C + kConvSlice - 1) / kConvSlice;
+  // Tiled kernel by default (measured faster at 8k prefill and 256 x 4
+  // decode); PLE_CONV_MODE=stream selects the streaming kernel (comparison
+  // sweeps and tests: both give the same bits).
+  const char* mode = getenv("PLE_CONV_MODE");
+  const bool tiled = !(mode != nullptr && strcmp(mode, "stream") == 0);
   void (*kernel)(ConvArgs, const float*, int) = nullptr;
   switch (a.K) {
-    case 1: kernel = conv_kernel<GATED, 1>; break;
-    case 2: kernel = conv_kernel<GATED, 2>; break;
-    case 3: kernel = conv_kernel<GATED, 3>; break;
-    case 4: kernel = conv_kernel<GATED, 4>; break;
-    case 5: kernel = conv_kernel<GATED, 5>; break;
-    case 6: kernel = conv_kernel<GATED, 6>; break;
-    case 7: kernel = conv_kernel<GATED, 7>; break;
-    default: kernel = conv_kernel<GATED, 8>; break;
+    case 1: kernel = tiled ? conv_kernel<GATED, 1> : conv_stream_kernel<GATED, 1>; break;
+    case 2: kernel = tiled ? conv_kernel<GATED, 2> : conv_stream_kernel<GATED, 2>; break;
+    case 3: kernel = tiled ? conv_kernel<GATED, 3> : conv_stream_kernel<GATED, 3>; break;
+    case 4: kernel = tiled ? conv_kernel<GATED, 4> : conv_stream_kernel<GATED, 4>; break;
+    case 5: kernel = tiled ? conv_kernel<GATED, 5> : conv_stream_kernel<GATED, 5>; break;
+    case 6: kernel = tiled ? conv_kernel<GATED, 6> : conv_stream_kernel<GATED, 6>; break;
+    case 7: kernel = tiled ? conv_kernel<GATED, 7> : conv_stream_kernel<GATED, 7>; break;
+    default: kernel = tiled ? conv_kernel<GATED, 8> : conv_stream_kernel<GATED, 8>; break;
+  }
+  int param = 0;
+  size_t smem = 0;
+  dim3 grid;
+  if (tiled) {
+    const int tile = conv_tile_tokens(a.T, a.C);
+    param = tile;
+    smem = conv_smem_bytes(tile, W);
+    grid = dim3(static_cast<unsigned>((a.T + tile - 1) / tile), static_cast<unsigned>(slices));
+  } else {
+    const int CH = conv_stream_chunk(W);
+    param = CH;
+    smem = conv_stream_smem(CH, W);
+    // about two CTAs per SM, each over a contiguous token range of one slice
+    int64_t ranges = (2 * static_cast<int64_t>(num_sms()) + slices - 1) / slices;
+    const int64_t max_ranges = (a.T + 15) / 16;
+    if (ranges > max_ranges) ranges = max_ranges;
+    if (ranges < 1) ranges = 1;
+    if (const char* e = getenv("PLE_CONV_RANGES")) {
+      const long v = atol(e);
+      if (v >= 1 && v <= 65535) ranges = v;
+    }
+    grid = dim3(static_cast<unsigned>(ranges), static_cast<unsigned>(slices));
   }
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, name);
-  const int64_t tiles = (a.T + tile - 1) / tile;
-  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>((a.C + kConvSlice - 1) / kConvSlice));
-  kernel<<<grid, kConvThreads, smem, stream>>>(a, g, tile);
+  err = launch_kernel(kernel, grid, dim3(kConvThreads), smem, stream, 1, a, g, param);
+  if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
 }
 
@@ -706,7 +1044,7 @@ PLE_EXPORT ple_status ple_gate(const ple_bf16_t* hidden, const ple_bf16_t* kv,
       !aligned16(out))
     return fail(PLE_ERR_INVALID_ARG, "ple_gate: buffers must be 16-byte aligned");
   return gate_pass<true>(hidden, kv, gamma_h, gamma_k, eps, num_tokens, hidden_size, out,
-                         gate_out, stream, "ple_gate");
+                         gate_out, nullptr, stream, "ple_gate");
 }
 
 static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf16_t* src,
@@ -745,7 +1083,8 @@ static ple_status conv_entry(bool gated, const ple_bf16_t* hidden, const ple_bf1
   a.out = out;
   a.dev_err = dev_err;
   if (!gated) return launch_conv<false>(a, nullptr, stream, name);
-  s = gate_pass<false>(hidden, src, gamma_h, gamma_k, eps, T, C, nullptr, gate_out, stream, name);
+  s = gate_pass<false>(hidden, src, gamma_h, gamma_k, eps, T, C, nullptr, gate_out, dev_err,
+                       stream, name);
   if (s != PLE_OK) return s;
   return launch_conv<true>(a, gate_out, stream, name);
 }

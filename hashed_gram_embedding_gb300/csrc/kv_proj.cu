@@ -214,6 +214,8 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   if (CLUSTER > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // emb (A) comes from the previous kernel
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -464,6 +466,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   cluster_sync();  // both CTAs' barriers and tensor memory exist
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // emb (A) comes from the previous kernel
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
@@ -662,19 +666,8 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
   const int units = ((M + rows_per_unit - 1) / rows_per_unit) * ((N + BN - 1) / BN);
   const int max_clusters = num_sms() / cluster;
   const int clusters = units < max_clusters ? units : max_clusters;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, kv, M, N, K, dev_err);
+  err = launch_kernel(kernel, dim3(static_cast<unsigned>(clusters * cluster)), dim3(kThreads), smem,
+                      stream, static_cast<unsigned>(cluster), map_a, map_b, kv, M, N, K, dev_err);
   if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj launch");
   return check_cuda(cudaGetLastError(), "ple_kv_proj launch");
 }

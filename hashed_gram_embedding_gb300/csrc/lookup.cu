@@ -24,6 +24,8 @@
 #include <cuda_fp8.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 
 namespace ple {
 namespace {
@@ -45,6 +47,8 @@ __global__ void __launch_bounds__(kThreads)
 gather_bf16_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ perm,
                    uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
                    int64_t table_rows, uint4* __restrict__ out, int32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
@@ -102,6 +106,8 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
                   uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
                   const float* __restrict__ row_scale, int64_t table_rows,
                   uint4* __restrict__ out, int32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
@@ -140,6 +146,109 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy gather (bf16 rows, table in HBM). The copy engine moves the rows:
+// a warp takes a token, each lane one of its heads, and every lane issues one
+// 1-D bulk copy of its row (table -> shared memory) completing on the token's
+// mbarrier; once all rows are in, lane 0 writes the token's H*D output values
+// (contiguous) back with one bulk store. Each warp keeps kBgSlots tokens in
+// flight, so a CTA holds 64 KB of row requests with a few registers per thread
+// (the register-fed kernel above is bounded by the registers its in-flight
+// loads occupy). Ids outside the table give zero rows written by the lane.
+// ---------------------------------------------------------------------------
+constexpr int kBgWarps = 4;
+constexpr int kBgSlots = 4;
+constexpr size_t kBgSmemBudget = 200 * 1024;
+
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kBgWarps * 32)
+gather_bulk_kernel(const int64_t* __restrict__ ids, int64_t T, int H, int row_bytes,
+                   const uint8_t* __restrict__ table, int64_t table_rows, uint8_t* __restrict__ out,
+                   int32_t* dev_err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t tok_bytes = static_cast<uint32_t>(H) * row_bytes;
+  uint8_t* slots = smem + static_cast<size_t>(warp) * kBgSlots * tok_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kBgWarps) * kBgSlots * tok_bytes) +
+                   warp * kBgSlots;
+  if (lane == 0) {
+    for (int i = 0; i < kBgSlots; ++i) mbar_init(smem_u32(bars + i), 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  pdl_wait();
+  pdl_trigger();
+
+  const int64_t ta = T * blockIdx.x / gridDim.x;
+  const int64_t tb = T * (blockIdx.x + 1) / gridDim.x;
+  const int64_t n_my = tb - ta > warp ? (tb - ta - warp + kBgWarps - 1) / kBgWarps : 0;
+  auto token = [&](int64_t k) { return ta + warp + k * kBgWarps; };
+
+  // all lanes: start the row copies of token k into its slot
+  auto issue = [&](int64_t k) {
+    const int64_t t = token(k);
+    const int sl = static_cast<int>(k % kBgSlots);
+    const uint32_t bar = smem_u32(bars + sl);
+    uint8_t* slot = slots + static_cast<size_t>(sl) * tok_bytes;
+    int valid = 0;
+    for (int h0 = 0; h0 < H; h0 += 32) {
+      const int h = h0 + lane;
+      bool ok = false;
+      int64_t id = 0;
+      if (h < H) {
+        id = __ldg(ids + t * H + h);
+        ok = static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows);
+      }
+      valid += __popc(__ballot_sync(0xffffffffu, ok));
+      if (h < H && !ok) {  // zero row + flag; ordered before the bulk store below
+        uint4* z = reinterpret_cast<uint4*>(slot + static_cast<size_t>(h) * row_bytes);
+        for (int q = 0; q < row_bytes / 16; ++q) z[q] = make_uint4(0, 0, 0, 0);
+        set_dev_err(dev_err, PLE_DEVERR_BOUNDS);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      if (ok)
+        bulk_copy_g2s(smem_u32(slot + static_cast<size_t>(h) * row_bytes),
+                      table + id * row_bytes, static_cast<uint32_t>(row_bytes), bar);
+    }
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(valid) * row_bytes);
+  };
+
+  for (int64_t k = 0; k < n_my && k < kBgSlots; ++k) issue(k);
+  int64_t k = 0;
+  for (; k < n_my; ++k) {
+    const int sl = static_cast<int>(k % kBgSlots);
+    const uint32_t parity = static_cast<uint32_t>((k / kBgSlots) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(bars + sl), parity, nullptr))) {
+      if (lane == 0) set_dev_err(dev_err, PLE_DEVERR_TIMEOUT);
+      break;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      bulk_store_s2g(out + token(k) * tok_bytes,
+                     smem_u32(slots + static_cast<size_t>(sl) * tok_bytes), tok_bytes);
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // all but the store just issued have read their slot
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    }
+    __syncwarp();
+    // refill the slot of token k-1 (its store has read it) with token k-1+S
+    if (k >= 1 && k - 1 + kBgSlots < n_my) issue(k - 1 + kBgSlots);
+  }
+  if (lane == 0) {
+    // after a timeout: copies of issued tokens k .. may still be landing
+    for (int64_t j = k; j < n_my && j < k + kBgSlots; ++j)
+      mbar_wait(smem_u32(bars + j % kBgSlots), static_cast<uint32_t>((j / kBgSlots) & 1), nullptr);
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -187,6 +296,8 @@ __device__ __forceinline__ uint32_t bucket_of(int64_t id, int64_t rows, int shif
 __global__ void __launch_bounds__(kOrderThreads)
 order_count_kernel(const int64_t* __restrict__ ids, uint32_t items, int64_t rows, int shift,
                    uint32_t buckets, uint32_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   for (uint32_t i = blockIdx.x * kOrderThreads + threadIdx.x; i < items;
        i += gridDim.x * kOrderThreads)
     atomicAdd(counts + bucket_of(__ldg(ids + i), rows, shift, buckets), 1u);
@@ -196,6 +307,8 @@ order_count_kernel(const int64_t* __restrict__ ids, uint32_t items, int64_t rows
 __global__ void __launch_bounds__(kScanThreads)
 order_scan_kernel(const uint32_t* __restrict__ counts, uint32_t n, uint32_t* __restrict__ cursor) {
   __shared__ uint32_t warp_tot[kScanThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tid = threadIdx.x;
   const uint32_t chunk = (n + kScanThreads - 1) / kScanThreads;
   const uint32_t b0 = tid * chunk;
@@ -234,6 +347,8 @@ __global__ void __launch_bounds__(kOrderThreads)
 order_scatter_kernel(const int64_t* __restrict__ ids, uint32_t items, int64_t rows, int shift,
                      uint32_t buckets, uint32_t* __restrict__ cursor,
                      uint32_t* __restrict__ perm) {
+  pdl_wait();
+  pdl_trigger();
   for (uint32_t i = blockIdx.x * kOrderThreads + threadIdx.x; i < items;
        i += gridDim.x * kOrderThreads) {
     const uint32_t b = bucket_of(__ldg(ids + i), rows, shift, buckets);
@@ -325,19 +440,21 @@ ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_he
 ple_status launch_gather_kernel(const Gather& g, const uint32_t* perm, cudaStream_t stream,
                                 const char* name) {
   const int vpr = g.vpr;
+  cudaError_t err = cudaSuccess;
   if (g.dtype == PLE_BF16) {
     if (vpr == 16)
-      gather_bf16_kernel<16><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel(gather_bf16_kernel<16>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else if (vpr == 8)
-      gather_bf16_kernel<8><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel(gather_bf16_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else
-      gather_bf16_kernel<0><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel(gather_bf16_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
   } else {
     if (vpr == 8)
-      gather_fp8_kernel<8><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel(gather_fp8_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
     else
-      gather_fp8_kernel<0><<<g.grid, kThreads, 0, stream>>>(g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel(gather_fp8_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
   }
+  if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
 }
 
@@ -351,6 +468,32 @@ ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_hea
   ple_status s = prepare_gather(ids, num_tokens, num_heads, table, table_rows, head_dim, dtype,
                                 row_scale, loc, out, max_ctas, dev_err, name, &g, &empty);
   if (s != PLE_OK || empty) return s;
+  // PLE_GATHER_MODE=bulk sends bf16 rows in HBM through the copy engine when a
+  // token's rows fit the slots (sweeps, tests); the register-fed kernel is the
+  // default: on a GB300 at 8k prefill both take the same time.
+  const size_t tok_bytes = static_cast<size_t>(num_heads) * g.row_bytes;
+  const size_t smem = static_cast<size_t>(kBgWarps) * kBgSlots * (tok_bytes + 8);
+  const char* mode = getenv("PLE_GATHER_MODE");
+  const bool bulk = mode != nullptr && strcmp(mode, "bulk") == 0;
+  if (bulk && dtype == PLE_BF16 && loc == PLE_HBM && smem <= kBgSmemBudget) {
+    cudaError_t err = cudaFuncSetAttribute(gather_bulk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return check_cuda(err, name);
+    // as many CTAs as fit (shared memory), at least one token per warp
+    const int64_t per_sm = static_cast<int64_t>(kBgSmemBudget) / static_cast<int64_t>(smem);
+    int64_t grid = static_cast<int64_t>(num_sms()) * (per_sm < 1 ? 1 : per_sm);
+    const int64_t by_tokens = (num_tokens + kBgWarps - 1) / kBgWarps;
+    if (grid > by_tokens) grid = by_tokens;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    if (grid < 1) grid = 1;
+    err = launch_kernel(gather_bulk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kBgWarps * 32),
+                        smem, stream, 1, ids, num_tokens, static_cast<int>(num_heads),
+                        g.row_bytes, reinterpret_cast<const uint8_t*>(g.table), table_rows,
+                        reinterpret_cast<uint8_t*>(g.out), dev_err);
+    if (err != cudaSuccess) return check_cuda(err, name);
+    return check_cuda(cudaGetLastError(), name);
+  }
   return launch_gather_kernel(g, nullptr, stream, name);
 }
 
@@ -366,11 +509,15 @@ ple_status launch_ordered(const Gather& g, uint8_t* ws, const OrderPlan& plan,
   int64_t blocks = (g.items + kOrderThreads - 1) / kOrderThreads;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 4;
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  order_count_kernel<<<grid, kOrderThreads, 0, stream>>>(g.ids, items, g.table_rows, plan.shift,
-                                                          plan.buckets, counts);
-  order_scan_kernel<<<1, kScanThreads, 0, stream>>>(counts, plan.buckets, cursor);
-  order_scatter_kernel<<<grid, kOrderThreads, 0, stream>>>(g.ids, items, g.table_rows,
-                                                            plan.shift, plan.buckets, cursor, perm);
+  err = launch_kernel(order_count_kernel, dim3(grid), dim3(kOrderThreads), 0, stream, 1, g.ids,
+                      items, g.table_rows, plan.shift, plan.buckets, counts);
+  if (err == cudaSuccess)
+    err = launch_kernel(order_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, 1,
+                        static_cast<const uint32_t*>(counts), plan.buckets, cursor);
+  if (err == cudaSuccess)
+    err = launch_kernel(order_scatter_kernel, dim3(grid), dim3(kOrderThreads), 0, stream, 1, g.ids,
+                        items, g.table_rows, plan.shift, plan.buckets, cursor, perm);
+  if (err != cudaSuccess) return check_cuda(err, name);
   ple_status s = check_cuda(cudaGetLastError(), name);
   if (s != PLE_OK) return s;
   return launch_gather_kernel(g, perm, stream, name);

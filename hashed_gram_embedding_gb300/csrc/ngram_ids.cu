@@ -65,14 +65,16 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   __shared__ uint64_t vocab_s[PLE_MAX_HEADS], offset_s[PLE_MAX_HEADS];
   __shared__ uint64_t magic_s[PLE_MAX_HEADS], pow64_s[PLE_MAX_HEADS];
   const bool staged = num_reqs < kStagedBounds;
-  if (staged)
-    for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
   for (int h = threadIdx.x; h < num_heads; h += blockDim.x) {
     vocab_s[h] = static_cast<uint64_t>(k.vocab[h]);
     offset_s[h] = static_cast<uint64_t>(k.offset[h]);
     magic_s[h] = k.magic[h];
     pow64_s[h] = k.pow64_mod[h];
   }
+  pdl_wait();
+  pdl_trigger();
+  if (staged)
+    for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
   __syncthreads();
   const uint32_t i_first = blockIdx.x * blockDim.x;
   if (threadIdx.x == 0 && i_first < work) {
@@ -213,8 +215,10 @@ PLE_EXPORT ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens
   const int64_t blocks = (threads + 255) / 256;
   if (threads >= (int64_t(1) << 31))
     return fail(PLE_ERR_UNSUPPORTED, "ple_ngram_ids: num_tokens * heads must stay below 2^31");
-  ngram_ids_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      input_ids, num_tokens, query_start_loc, num_reqs, ngram_context, ctx_len, eos_token_id,
-      heads_per_ngram, num_heads, out, ngram_context_out, dev_err, k);
+  cudaError_t lerr = launch_kernel(ngram_ids_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                   stream, 1, input_ids, num_tokens, query_start_loc, num_reqs,
+                                   ngram_context, ctx_len, eos_token_id, heads_per_ngram,
+                                   num_heads, out, ngram_context_out, dev_err, k);
+  if (lerr != cudaSuccess) return check_cuda(lerr, "ple_ngram_ids launch");
   return check_cuda(cudaGetLastError(), "ple_ngram_ids launch");
 }

@@ -66,9 +66,23 @@ CONV_CASES = [
 ]
 
 
+# conv pass variants: the one-shot tiled kernel (default) and the streaming
+# kernel (default launch shape, one token range per slice, seven ranges)
+CONV_MODES = {"tile": {}, "stream": {"PLE_CONV_MODE": "stream"},
+              "stream-1range": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "1"},
+              "stream-7ranges": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "7"}}
+
+
+@pytest.fixture(params=list(CONV_MODES))
+def conv_mode(request, monkeypatch):
+    for k, v in CONV_MODES[request.param].items():
+        monkeypatch.setenv(k, v)
+    return request.param
+
+
 @pytest.mark.parametrize("with_state", [False, True])
 @pytest.mark.parametrize("case", CONV_CASES, ids=lambda c: f"{len(c[0])}req-C{c[1]}-K{c[2]}-d{c[3]}")
-def test_conv_matches_oracle(case, with_state):
+def test_conv_matches_oracle(case, with_state, conv_mode):
     lengths, C, K, d = case
     q = qsl_of(lengths)
     T = int(q[-1])
@@ -117,7 +131,7 @@ def _gate_conv_inputs(lengths, C, seed):
 @pytest.mark.parametrize("lengths,C", [([64, 100, 150, 198], 1024), ([7, 0, 30, 2, 0, 61], 256),
                                        ([1] * 40, 64), ([300], 4096),
                                        ([1] * 70 + [3, 0, 9], 264)])
-def test_gate_conv_matches_oracle_and_separate_kernels(lengths, C):
+def test_gate_conv_matches_oracle_and_separate_kernels(lengths, C, conv_mode):
     q, T, h, kv, gh, gk, w = _gate_conv_inputs(lengths, C, 20)
     R = len(lengths)
     state = rand_bf16((R, 9, C), 0.01, 30)
@@ -145,7 +159,7 @@ def test_gate_conv_matches_oracle_and_separate_kernels(lengths, C):
     assert torch.equal(y, y2) and torch.equal(st_out, st2)
 
 
-def test_gate_conv_decode_two_steps_ping_pong():
+def test_gate_conv_decode_two_steps_ping_pong(conv_mode):
     w_ = wl.WORKLOADS["decode256x4"]
     R, C = w_.num_reqs, w_.hidden
     lengths = [4] * R
@@ -179,7 +193,7 @@ def test_zero_tokens_copy_state_through():
     assert torch.equal(state, out_state)
 
 
-def test_gate_conv_prefill_8k_sampled():
+def test_gate_conv_prefill_8k_sampled(conv_mode):
     w_ = wl.WORKLOADS["prefill8k"]
     host = wl.host_inputs(w_)
     q = host["query_start_loc"]

@@ -29,9 +29,18 @@ def to_dev_bf16(a, pinned=False):
     return t.cuda()
 
 
+@pytest.fixture(params=["lsu", "bulk"])
+def gather_mode(request, monkeypatch):
+    """bf16 HBM gathers: the register-fed kernel (default) and the copy-engine one."""
+    if request.param == "bulk":
+        monkeypatch.setenv("PLE_GATHER_MODE", "bulk")
+    return request.param
+
+
 @pytest.mark.parametrize("T,H,D,rows", [(1, 1, 64, 10), (37, 5, 64, 1000), (513, 16, 128, 4096),
-                                        (29, 3, 8, 77), (31, 2, 24, 50), (1000, 8, 256, 333)])
-def test_bf16_gather_bit_exact(T, H, D, rows):
+                                        (29, 3, 8, 77), (31, 2, 24, 50), (1000, 8, 256, 333),
+                                        (70, 40, 64, 900)])
+def test_bf16_gather_bit_exact(T, H, D, rows, gather_mode):
     rng = np.random.default_rng(T * 7 + D)
     table = random_table_bits(rng, rows, D)
     ids = rng.integers(0, rows, size=(T, H))
@@ -44,7 +53,7 @@ def test_bf16_gather_bit_exact(T, H, D, rows):
 
 
 @pytest.mark.parametrize("max_ctas", [1, 3, 152])
-def test_capped_grid_and_uva_table(max_ctas):
+def test_capped_grid_and_uva_table(max_ctas, gather_mode):
     rng = np.random.default_rng(max_ctas)
     rows, D, T, H = 5000, 128, 300, 16
     table = random_table_bits(rng, rows, D)
@@ -104,7 +113,7 @@ def test_fp8_workload_rows_bit_exact():
     assert np.array_equal(bits(out), lookup_fp8(ids, codes.cpu().numpy(), scale.cpu().numpy()))
 
 
-def test_out_of_range_ids_are_zeroed_and_flagged():
+def test_out_of_range_ids_are_zeroed_and_flagged(gather_mode):
     rng = np.random.default_rng(5)
     rows, D = 100, 64
     table = random_table_bits(rng, rows, D)
@@ -168,7 +177,7 @@ def test_wait_times_out_then_completes():
     torch.cuda.synchronize()
 
 
-def test_prefill_8k_full_size_table():
+def test_prefill_8k_full_size_table(gather_mode):
     w = wl.WORKLOADS["prefill8k"]
     h = wl.host_inputs(w)
     table, _ = wl.make_table(torch, w, "cuda")
