@@ -323,43 +323,38 @@ def run_ours(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the timed region")
 
-    # ---- end to end through PLELayer with host buffers ----
-    from hashed_gram_embedding_gb300 import PLELayer
+    # ---- end to end through PLEHostPipeline with pinned host buffers ----
+    # Every step uploads its inputs (token ids, query_start_loc, hidden) from
+    # pinned host memory and reads y back into pinned host memory; uploads,
+    # compute and read-backs of neighbouring steps overlap on three streams.
+    from hashed_gram_embedding_gb300 import PLELayer, PLEHostPipeline
     p0 = sets[0]
     layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
                      w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
                      p0["conv_w"], w.dilation)
+    depth = 2
+    pipe = PLEHostPipeline(layer, T, w.num_reqs, device, depth=depth)
     h_ids = torch.from_numpy(p0["host"]["input_ids"]).pin_memory()
     h_qsl = torch.from_numpy(p0["host"]["query_start_loc"]).pin_memory()
     h_hidden = p0["hidden"].cpu().pin_memory()
-    h_y = torch.empty((T, C), dtype=torch.bfloat16).pin_memory()
-    d_ids = torch.empty_like(p0["input_ids"])
-    d_qsl = torch.empty_like(p0["qsl"])
-    d_hidden = torch.empty_like(p0["hidden"])
+    h_ys = [torch.empty((T, C), dtype=torch.bfloat16).pin_memory() for _ in range(depth)]
     h2d = h_ids.numel() * 4 + h_qsl.numel() * 4 + h_hidden.numel() * 2
-    d2h = h_y.numel() * 2
+    d2h = h_ys[0].numel() * 2
+    fwd = dict(ngram_context=p0["ctx"], ngram_context_out=ctx_out if w.decode else None,
+               conv_state=p0.get("conv_state"), conv_state_out=st_out, dev_err=err)
 
-    def e2e_step():
-        d_ids.copy_(h_ids, non_blocking=True)
-        d_qsl.copy_(h_qsl, non_blocking=True)
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        out = layer.forward(d_ids, d_qsl, d_hidden, ngram_context=p0["ctx"],
-                            ngram_context_out=ctx_out if w.decode else None,
-                            conv_state=p0.get("conv_state"), conv_state_out=st_out,
-                            dev_err=err, stream=stream)
-        h_y.copy_(out, non_blocking=True)
-
-    for _ in range(min(args.warmup, 3) or 1):
-        e2e_step()
+    for i in range(min(args.warmup, 3) or 1):
+        pipe.submit(h_ids, h_qsl, h_hidden, h_ys[i % depth], **fwd)
+    pipe.synchronize()
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    e_start.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e_end.record(stream)
+    e_start.record(pipe.copy_in)
+    for i in range(args.steps):
+        pipe.submit(h_ids, h_qsl, h_hidden, h_ys[i % depth], **fwd)
+    e_end.record(pipe.copy_out)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device)
@@ -426,6 +421,8 @@ def run_ours(args):
     }
     if w.table_loc == "host":
         line["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
+    if w.num_layers > 1 and len(sets) >= w.num_layers:
+        line["chain"] = chain_timing(torch, w, sets, device, err)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
@@ -436,6 +433,41 @@ def launches_per_step(w, table):
     and conv passes; a host table's ordered gather adds its count, scan and
     scatter kernels."""
     return LAUNCHES_PER_STEP + (3 if w.table_loc == "host" else 0)
+
+
+def chain_timing(torch, w, sets, device, err, reps=10):
+    """All layers of a multi-layer workload through PLEChain: with the next
+    layers' ids and gathers prefetched on a side stream, and in line."""
+    from hashed_gram_embedding_gb300 import PLELayer, PLEChain
+    layers = [PLELayer(p["table"], p["row_scale"], p["mult"], p["host"]["V"], p["host"]["O"],
+                       w.eos_token_id, w.heads_per_ngram, p["w_kv"], p["gamma_h"], p["gamma_k"],
+                       p["conv_w"], w.dilation) for p in sets[:w.num_layers]]
+    p0 = sets[0]
+    T, C, L = w.num_tokens, w.hidden, w.num_layers
+    hiddens = [p["hidden"] for p in sets[:L]]
+    outs = [torch.empty((T, C), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    stream = torch.cuda.current_stream(device)
+    res = {"layers": L}
+    for name, prefetch in (("prefetch", True), ("inline", False)):
+        chain = PLEChain(layers, prefetch=prefetch)
+        for _ in range(2):
+            chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
+                          dev_err=err, stream=stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
+                          dev_err=err, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[f"{name}_ms"] = round(ms, 4)
+        res[f"{name}_tokens_per_s_per_layer"] = round(T * L / (ms * 1e-3), 1)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the chain timing")
+    return res
 
 
 def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
@@ -456,62 +488,56 @@ def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
     return round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
 
 
-def uva_overlap(torch, _lib, p, ids, emb, w, device, order_ws, reps=20):
+def uva_overlap(torch, _lib, p, ids, emb, w, device, order_ws, reps=10):
     """The pinned-host gather (in table order) prefetched on a side stream
     (half the SMs) while a 4096^3 bf16 GEMM -- a stand-in for the previous
     layer, run by cuBLAS through torch -- occupies the main stream: each
-    alone, then both; plus the gather in (token, head) order alone."""
+    alone, then both. Gather times come from events on the side stream,
+    totals from events on the main stream, which joins the side stream at
+    the end."""
     main = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device)
     half = max(1, torch.cuda.get_device_properties(device).multi_processor_count // 2)
     a = torch.randn((4096, 4096), device=device, dtype=torch.bfloat16)
     b = torch.randn((4096, 4096), device=device, dtype=torch.bfloat16)
     c = torch.empty((4096, 4096), device=device, dtype=torch.bfloat16)
-    done = torch.cuda.Event()
 
-    def gemm():
-        torch.matmul(a, b, out=c)
+    def run(with_gather, with_gemm, ordered=True):
+        g_us, t_us = [], []
+        for rep in range(reps + 2):
+            torch.cuda.synchronize()
+            s0, s1, m0, m1 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+            m0.record(main)
+            side.wait_stream(main)
+            s0.record(side)
+            if with_gather:
+                if ordered:
+                    _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, max_ctas=half,
+                                            stream=side)
+                else:
+                    _lib.ple_lookup(ids, p["table"], emb, max_ctas=half, stream=side)
+            s1.record(side)
+            if with_gemm:
+                torch.matmul(a, b, out=c)
+            main.wait_stream(side)
+            m1.record(main)
+            torch.cuda.synchronize()
+            if rep >= 2:
+                g_us.append(s0.elapsed_time(s1) * 1e3)
+                t_us.append(m0.elapsed_time(m1) * 1e3)
+        return float(np.mean(g_us)), float(np.mean(t_us))
 
-    def prefetch():
-        _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, max_ctas=half, stream=side)
-        done.record(side)
-
-    def gather():
-        side.wait_stream(main)
-        prefetch()
-        _lib.ple_wait(done, main)
-
-    def gather_unordered():
-        _lib.ple_lookup_prefetch(ids, p["table"], emb, side, done, max_ctas=half)
-        _lib.ple_wait(done, main)
-
-    def timed(fn, reps=reps):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        side.wait_stream(main)
-        e0.record(main)
-        for _ in range(reps):
-            fn()
-        e1.record(main)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps * 1e3  # us
-
-    def both():
-        side.wait_stream(main)
-        prefetch()
-        gemm()
-        _lib.ple_wait(done, main)
-
-    g_us, m_us, b_us = timed(gather), timed(gemm), timed(both)
-    u_us = timed(gather_unordered, reps=3)
+    g_alone, _ = run(True, False)
+    _, m_alone = run(False, True)
+    g_over, t_over = run(True, True)
+    u_alone, _ = run(True, False, ordered=False)
     row_bytes = w.num_tokens * w.num_heads * w.head_dim * 2
-    return {"gather_alone_us": round(g_us, 1), "gemm_alone_us": round(m_us, 1),
-            "overlapped_us": round(b_us, 1), "hidden_fraction": round((g_us + m_us - b_us) / g_us, 3),
-            "gather_link_gbs": round(row_bytes / (g_us * 1e-6) / 1e9, 1),
-            "gather_unordered_alone_us": round(u_us, 1),
+    return {"gather_alone_us": round(g_alone, 1), "gemm_alone_us": round(m_alone, 1),
+            "overlapped_total_us": round(t_over, 1), "overlapped_gather_us": round(g_over, 1),
+            "saved_us": round(g_alone + m_alone - t_over, 1),
+            "hidden_fraction": round((g_alone + m_alone - t_over) / min(g_alone, m_alone), 3),
+            "gather_link_gbs": round(row_bytes / (g_alone * 1e-6) / 1e9, 1),
+            "gather_unordered_alone_us": round(u_alone, 1),
             "gather_ctas": half, "gemm": "4096x4096x4096 bf16 (cuBLAS via torch.matmul)"}
 
 

@@ -2,7 +2,9 @@
 
 The compute path is libple.so (hand-written CUDA for sm_103a, C ABI in
 include/ple.h); this package holds its build script, a ctypes binding with
-the C names, the PLELayer convenience wrapper and the seeded synthetic
+the C names, the PLELayer convenience wrapper (and PLEHostPipeline, which
+runs it over pinned host buffers with transfers overlapping compute) and the
+seeded synthetic
 workloads used by the tests and the benchmark.
 """
 
@@ -11,6 +13,9 @@ from ._lib import (  # noqa: F401
     ple_ngram_ids,
     ple_lookup,
     ple_lookup_prefetch,
+    ple_lookup_ordered,
+    ple_lookup_ordered_workspace,
+    ple_lookup_ordered_static,
     ple_wait,
     ple_kv_proj,
     ple_gate,
@@ -23,4 +28,4 @@ from ._lib import (  # noqa: F401
     PLE_HBM,
     PLE_HOST_UVA,
 )
-from .layer import PLELayer  # noqa: F401
+from .layer import PLELayer, PLEHostPipeline, PLEChain  # noqa: F401

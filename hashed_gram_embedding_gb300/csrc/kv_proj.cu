@@ -347,13 +347,13 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // N = 256. Each CTA of a cluster pair stages its own 128 rows of A and its own
 // half (128 rows) of the W tile; the pair's tensor cores read both halves of
 // W, so each SM reads 32 KB of operands from shared memory per K step of 64
-// instead of 48 KB, and a stage is 32 KB, leaving room for 6 stages in
+// instead of 48 KB, and a stage is 32 KB, leaving room for 7 stages in
 // flight. The even CTA (leader) issues the MMAs; TMA copies of both CTAs
 // complete on the leader's full barrier; the leader's commits release the
 // stages and hand the accumulators to the epilogues of both CTAs; both
 // epilogues report back to the leader's accumulator-empty barrier.
 // ---------------------------------------------------------------------------
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = 7;
 constexpr int P_A_STAGE = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
 constexpr int P_B_STAGE = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of the W tile
 constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
@@ -381,6 +381,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Multicast variant: the box lands at the same shared-memory offset in every
+// CTA of ctaMask, and each landing completes on the mbarrier at offset `bar`
+// in that CTA's pair leader (bar: this CTA's own barrier address with the
+// pair bit, bit 24 of a shared::cluster address, cleared).
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
+                                                           uint32_t bar, int x, int y,
+                                                           uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t accumulate) {
   asm volatile(
@@ -391,12 +405,12 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
-// Arrive on the mbarrier at offset `bar` in both CTAs of the pair once the
+// Arrive on the mbarrier at offset `bar` in every CTA of ctaMask once the
 // pair MMAs issued so far complete.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(static_cast<uint16_t>(3))
+      " [%0], %1;" ::"r"(bar), "h"(mask)
       : "memory");
 }
 
@@ -411,6 +425,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// PAIRS = CTA pairs per cluster. PAIRS = 2: the two pairs of a 4-CTA cluster
+// take adjacent 256-column tiles of the same 256 rows; CTAs 0/2 (and 1/3)
+// need the same 128 rows of A, so each loads 64 of them and multicasts them
+// to both, cutting each SM's A traffic in half; a stage may then be refilled
+// only after both pairs' MMAs released it.
+template <int PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, ple_bf16_t* __restrict__ out,
@@ -432,18 +452,23 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();     // 0 = leader (issues the MMAs)
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
+  const uint32_t rank = cluster_rank();
+  const uint32_t leader = rank & ~1u;       // even CTA of the pair: issues the MMAs
+  const int pidx = static_cast<int>(rank >> 1);  // pair within the cluster
+  const int cl = blockIdx.x / (2 * PAIRS);
+  const int num_cl = gridDim.x / (2 * PAIRS);
   const int n_tiles = (N + BN - 1) / BN;
+  const int n_groups = (n_tiles + PAIRS - 1) / PAIRS;
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
-  const int num_tiles = m_tiles * n_tiles;
+  const int num_units = m_tiles * n_groups;  // (256 rows, PAIRS x 256 columns) per cluster
   const int num_kb = (K + BK - 1) / BK;
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << (2 * PAIRS)) - 1);
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pidx));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
-      mbar_init(full_bar(s), 1);    // the leader's expect_tx; bytes from both CTAs
-      mbar_init(empty_bar(s), 1);   // one commit of the leader per use
+      mbar_init(full_bar(s), 1);      // the leader's expect_tx; bytes from both CTAs
+      mbar_init(empty_bar(s), PAIRS); // one commit of each pair's leader per use
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -477,18 +502,26 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-      const int m0 = (tile / n_tiles) * 2 * BM + static_cast<int>(rank) * BM;
-      const int n0 = (tile % n_tiles) * BN + static_cast<int>(rank) * (BN / 2);
+    const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
+    for (int u = cl; ok && u < num_units; u += num_cl) {
+      const int m0 = (u / n_groups) * 2 * BM + q * BM;
+      const int n0 = ((u % n_groups) * PAIRS + pidx) * BN + q * (BN / 2);
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-        const uint32_t leader_full = map_to_rank(full_bar(stage), 0);
-        if (rank == 0) {
+        const uint32_t leader_full = map_to_rank(full_bar(stage), leader);
+        if (rank == leader) {
           mbar_arrive_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         }
-        tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE), &map_a, leader_full, kb * BK, m0);
+        if constexpr (PAIRS == 1) {
+          tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE), &map_a, leader_full, kb * BK, m0);
+        } else {
+          // 64 of the 128 A rows, to this CTA and its counterpart in the other pair
+          tma_load_2d_pair_multicast(smem_u32(a_smem + stage * P_A_STAGE + pidx * (P_A_STAGE / 2)),
+                                     &map_a, leader_full, kb * BK, m0 + pidx * (BM / 2),
+                                     static_cast<uint16_t>((1u << q) | (1u << (q + 2))));
+        }
         tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE), &map_b, leader_full, kb * BK, n0);
         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -498,14 +531,14 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     for (int s = 0; s < P_STAGES; ++s)
       if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u, nullptr);
   } else if (warp == 1) {
-    if (rank == 0 && lane == 0) {
-      // ---------------- MMA issuer (leader only) ----------------
+    if (rank == leader && lane == 0) {
+      // ---------------- MMA issuer (pair leaders only) ----------------
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+      for (int u = cl; ok && u < num_units; u += num_cl) {
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -519,11 +552,11 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
             const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
             umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit_pair(empty_bar(stage));   // frees the stage in both CTAs
+          umma_commit_pair(empty_bar(stage), kClusterMask);  // frees the stage everywhere it fed
           if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit_pair(accf_bar(acc));        // accumulator halves ready in both SMs
+        umma_commit_pair(accf_bar(acc), pair_mask);  // accumulator halves ready in both SMs
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
@@ -537,15 +570,15 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     const int row_in_tile = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+    for (int u = cl; u < num_units; u += num_cl) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag));
       if (!ok) {
         if (lane == 0) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
         break;
       }
       tc_fence_after();
-      const int m = (tile / n_tiles) * 2 * BM + static_cast<int>(rank) * BM + row_in_tile;
-      const int n_base = (tile % n_tiles) * BN;
+      const int m = (u / n_groups) * 2 * BM + static_cast<int>(rank & 1u) * BM + row_in_tile;
+      const int n_base = ((u % n_groups) * PAIRS + pidx) * BN;
       ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
 #pragma unroll 1
       for (int chunk = 0; chunk < BN / 32; ++chunk) {
@@ -569,7 +602,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(acc), 0));
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(acc), leader));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -638,33 +671,64 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
   const int N = 2 * hidden;
   const int K = emb_dim;
   // Kernel: the CTA-pair kernel when there are at least two 128-row blocks,
-  // else one CTA per tile. PLE_KVPROJ_MODE = pair | cluster | single
-  // overrides (launch-shape sweeps and tests; cluster = 2-CTA clusters that
-  // share the W tile by TMA multicast, each CTA with its own 1-SM MMAs).
-  enum { kSingle, kCluster, kPair } mode = (M > BM) ? kPair : kSingle;
+  // else one CTA per tile. PLE_KVPROJ_MODE = quad | pair | cluster | single
+  // overrides (launch-shape sweeps and tests): quad = two CTA pairs per
+  // cluster sharing A by multicast; cluster = 2-CTA clusters that share the
+  // W tile by TMA multicast, each CTA with its own 1-SM MMAs.
+  enum { kSingle, kCluster, kPair, kQuad } mode = (M > BM) ? kPair : kSingle;
   if (const char* e = getenv("PLE_KVPROJ_MODE")) {
     if (strcmp(e, "single") == 0) mode = kSingle;
     else if (strcmp(e, "cluster") == 0) mode = kCluster;
     else if (strcmp(e, "pair") == 0) mode = kPair;
+    else if (strcmp(e, "quad") == 0) mode = kQuad;
   }
   if (const char* e = getenv("PLE_KVPROJ_CLUSTER"))
     if (atoi(e) == 1) mode = kSingle;
-  const int cluster = mode == kSingle ? 1 : 2;
+  const int cluster = mode == kSingle ? 1 : (mode == kQuad ? 4 : 2);
   CUtensorMap map_a, map_b;
-  ple_status s = make_map(&map_a, emb, M, K, BM);
+  ple_status s = make_map(&map_a, emb, M, K, mode == kQuad ? BM / 2 : BM);  // A rows a CTA loads
   if (s != PLE_OK) return s;
   s = make_map(&map_b, w, N, K, mode == kSingle ? BN : BN / 2);  // W rows one CTA loads per stage
   if (s != PLE_OK) return s;
   void (*kernel)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*) =
-      mode == kPair ? kv_proj_pair_kernel : (mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>);
-  const size_t smem = mode == kPair ? kPairSmemBytes : kSmemBytes;
+      mode == kQuad ? kv_proj_pair_kernel<2>
+                    : mode == kPair ? kv_proj_pair_kernel<1>
+                                    : (mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>);
+  const size_t smem = (mode == kPair || mode == kQuad) ? kPairSmemBytes : kSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj: smem attribute");
-  // work units: pair tiles (256 rows) or, per cluster position, 128-row tiles
-  const int rows_per_unit = mode == kPair ? 2 * BM : BM * cluster;
-  const int units = ((M + rows_per_unit - 1) / rows_per_unit) * ((N + BN - 1) / BN);
-  const int max_clusters = num_sms() / cluster;
+  // work units per cluster: 256 rows x (pairs x 256 columns) for the pair
+  // kernels, else 128-row tiles per cluster position
+  int units;
+  if (mode == kPair || mode == kQuad) {
+    const int pairs = cluster / 2;
+    units = ((M + 2 * BM - 1) / (2 * BM)) * (((N + BN - 1) / BN + pairs - 1) / pairs);
+  } else {
+    units = ((M + BM * cluster - 1) / (BM * cluster)) * ((N + BN - 1) / BN);
+  }
+  // persistent grid: as many clusters as can be resident at once (a GPC may
+  // not hold a whole number of clusters), no more than there are units
+  int max_clusters = num_sms() / cluster;
+  if (cluster > 1) {
+    cudaLaunchConfig_t qcfg{};
+    qcfg.gridDim = dim3(static_cast<unsigned>(max_clusters * cluster));
+    qcfg.blockDim = dim3(kThreads);
+    qcfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute qattr[1];
+    qattr[0].id = cudaLaunchAttributeClusterDimension;
+    qattr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    qattr[0].val.clusterDim.y = 1;
+    qattr[0].val.clusterDim.z = 1;
+    qcfg.attrs = qattr;
+    qcfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, reinterpret_cast<const void*>(kernel), &qcfg) ==
+            cudaSuccess &&
+        active > 0 && active < max_clusters)
+      max_clusters = active;
+    cudaGetLastError();  // a failed query only leaves the SM-count bound
+  }
   const int clusters = units < max_clusters ? units : max_clusters;
   err = launch_kernel(kernel, dim3(static_cast<unsigned>(clusters * cluster)), dim3(kThreads), smem,
                       stream, static_cast<unsigned>(cluster), map_a, map_b, kv, M, N, K, dev_err);

@@ -50,14 +50,20 @@ gather_bf16_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__
   pdl_wait();
   pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
-  const uint32_t stride = gridDim.x * kThreads;
-  for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
-       base += stride * kUnroll) {
+  // Unsorted walk: a thread's items are a grid apart (all CTAs sweep the
+  // whole output together). Sorted walk (perm): a CTA takes kUnroll * 256
+  // consecutive items at a time, so the rows in flight at any moment are a
+  // narrow slice of the table.
+  const uint32_t item_step = perm != nullptr ? kThreads : gridDim.x * kThreads;
+  const uint32_t first = perm != nullptr ? blockIdx.x * kThreads * kUnroll + threadIdx.x
+                                         : blockIdx.x * kThreads + threadIdx.x;
+  const uint32_t iter_step = gridDim.x * kThreads * kUnroll;
+  for (uint32_t base = first; base < total_vecs; base += iter_step) {
     uint4 v[kUnroll];
     uint32_t o[kUnroll];  // output vector of each work item
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t idx = base + u * stride;
+      const uint32_t idx = base + u * item_step;
       v[u] = make_uint4(0, 0, 0, 0);
       o[u] = total_vecs;
       if (idx < total_vecs) {
@@ -109,15 +115,17 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
   pdl_wait();
   pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
-  const uint32_t stride = gridDim.x * kThreads;
-  for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total_vecs;
-       base += stride * kUnroll) {
+  const uint32_t item_step = perm != nullptr ? kThreads : gridDim.x * kThreads;
+  const uint32_t first = perm != nullptr ? blockIdx.x * kThreads * kUnroll + threadIdx.x
+                                         : blockIdx.x * kThreads + threadIdx.x;
+  const uint32_t iter_step = gridDim.x * kThreads * kUnroll;
+  for (uint32_t base = first; base < total_vecs; base += iter_step) {
     uint4 c[kUnroll];
     float s[kUnroll];
     uint32_t o[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t idx = base + u * stride;
+      const uint32_t idx = base + u * item_step;
       c[u] = make_uint4(0, 0, 0, 0);
       s[u] = 0.f;
       o[u] = total_vecs;
@@ -520,7 +528,13 @@ ple_status launch_ordered(const Gather& g, uint8_t* ws, const OrderPlan& plan,
   if (err != cudaSuccess) return check_cuda(err, name);
   ple_status s = check_cuda(cudaGetLastError(), name);
   if (s != PLE_OK) return s;
-  return launch_gather_kernel(g, perm, stream, name);
+  // Two CTAs per SM walk the sorted items: a slice of ~2.5 MB of rows in
+  // flight, enough for the host link, narrow enough to stay within the
+  // GPU's translation reach (a full grid spreads its rows over half the table).
+  Gather gw = g;
+  const unsigned walk_ctas = static_cast<unsigned>(2 * num_sms());
+  if (gw.grid > walk_ctas) gw.grid = walk_ctas;
+  return launch_gather_kernel(gw, perm, stream, name);
 }
 
 }  // namespace

@@ -73,21 +73,36 @@ class PLELayer:
         T = input_ids.numel()
         b = self.buffers(T, hidden.device)
         y = out if out is not None else b["y"]
+        self.embed(input_ids, query_start_loc, b["ids"], b["emb"], b["order_ws"],
+                   ngram_context=ngram_context, ngram_context_out=ngram_context_out,
+                   dev_err=dev_err, stream=stream)
+        self.mix(b["emb"], hidden, query_start_loc, y, conv_state=conv_state,
+                 conv_state_out=conv_state_out, dev_err=dev_err, stream=stream)
+        return y
+
+    def embed(self, input_ids, query_start_loc, ids, emb, order_ws=None, ngram_context=None,
+              ngram_context_out=None, dev_err=None, stream=None, max_ctas=None):
+        """n-gram ids -> row gather into ``emb`` [T, H*D] (``order_ws``: the
+        ordered gather's workspace, required for a host table)."""
+        ctas = self.max_ctas if max_ctas is None else int(max_ctas)
         _lib.ple_ngram_ids(input_ids, query_start_loc, ngram_context, self.mult, self.V, self.O,
-                           self.eos, self.hpn, b["ids"], ngram_context_out, dev_err, stream)
-        if b["order_ws"] is not None:
-            _lib.ple_lookup_ordered(b["ids"], self.table, b["emb"], b["order_ws"],
-                                    row_scale=self.row_scale, max_ctas=self.max_ctas,
-                                    dev_err=dev_err, stream=stream)
+                           self.eos, self.hpn, ids, ngram_context_out, dev_err, stream)
+        if not self.table.is_cuda:
+            _lib.ple_lookup_ordered(ids, self.table, emb, order_ws, row_scale=self.row_scale,
+                                    max_ctas=ctas, dev_err=dev_err, stream=stream)
         else:
-            _lib.ple_lookup(b["ids"], self.table, b["emb"], row_scale=self.row_scale,
-                            max_ctas=self.max_ctas, dev_err=dev_err, stream=stream)
-        _lib.ple_kv_proj(b["emb"], self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
+            _lib.ple_lookup(ids, self.table, emb, row_scale=self.row_scale, max_ctas=ctas,
+                            dev_err=dev_err, stream=stream)
+
+    def mix(self, emb, hidden, query_start_loc, out, conv_state=None, conv_state_out=None,
+            dev_err=None, stream=None):
+        """kv_proj of ``emb`` -> gate with ``hidden`` -> short conv into ``out``."""
+        b = self.buffers(hidden.shape[0], hidden.device)
+        _lib.ple_kv_proj(emb, self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
         _lib.ple_gate_conv(hidden, b["kv"], self.gamma_h, self.gamma_k, query_start_loc,
-                           self.conv_w, self.dilation, y, eps=self.eps, conv_state=conv_state,
+                           self.conv_w, self.dilation, out, eps=self.eps, conv_state=conv_state,
                            conv_state_out=conv_state_out, gate_out=b["gate"],
                            dev_err=dev_err, stream=stream)
-        return y
 
     # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv);
     # a host table's ordered gather adds three (count, scan, scatter)
@@ -96,3 +111,162 @@ class PLELayer:
 
     def launches_per_forward(self):
         return self.LAUNCHES_PER_FORWARD + (0 if self.table.is_cuda else self.ORDERED_GATHER_EXTRA)
+
+
+class PLEHostPipeline:
+    """PLELayer over pinned host buffers, with each step's transfers
+    overlapping its neighbours' compute.
+
+    ``submit`` enqueues one step: the inputs (token ids, query_start_loc,
+    hidden) go to the device on a copy-in stream, the layer runs on the
+    compute stream, and the output comes back on a copy-out stream into the
+    caller's pinned buffer. ``depth`` device buffer sets rotate, so step k's
+    upload and step k-1's download run while step k-1 / k computes; a buffer
+    set is reused only after the step that last used it has been read back.
+    The host output buffer of a step must not be read (or reused) before
+    ``synchronize`` (or the step's ``done`` event). All arithmetic is in
+    libple; the streams and events are PyTorch's.
+    """
+
+    def __init__(self, layer, num_tokens, num_reqs, device, depth=2):
+        self.layer = layer
+        self.device = torch.device(device)
+        self.copy_in = torch.cuda.Stream(self.device)
+        self.compute = torch.cuda.Stream(self.device)
+        self.copy_out = torch.cuda.Stream(self.device)
+        C = layer.hidden
+        self.slots = []
+        for _ in range(depth):
+            self.slots.append({
+                "ids": torch.empty((num_tokens,), dtype=torch.int32, device=self.device),
+                "qsl": torch.empty((num_reqs + 1,), dtype=torch.int32, device=self.device),
+                "hidden": torch.empty((num_tokens, C), dtype=torch.bfloat16, device=self.device),
+                "y": torch.empty((num_tokens, C), dtype=torch.bfloat16, device=self.device),
+                "loaded": torch.cuda.Event(),    # inputs on the device
+                "computed": torch.cuda.Event(),  # the layer has read the inputs, written y
+                "returned": torch.cuda.Event(),  # y is back on the host
+            })
+        self.k = 0
+
+    def submit(self, h_input_ids, h_query_start_loc, h_hidden, h_out, **forward_kwargs):
+        """Enqueue one step; ``forward_kwargs`` go to PLELayer.forward (device
+        carry-over buffers, dev_err). Returns the step's completion event."""
+        s = self.slots[self.k % len(self.slots)]
+        self.k += 1
+        # inputs may be overwritten once the previous user of the slot computed
+        self.copy_in.wait_event(s["computed"])
+        with torch.cuda.stream(self.copy_in):
+            s["ids"].copy_(h_input_ids, non_blocking=True)
+            s["qsl"].copy_(h_query_start_loc, non_blocking=True)
+            s["hidden"].copy_(h_hidden, non_blocking=True)
+        s["loaded"].record(self.copy_in)
+        # y may be overwritten once the previous user of the slot was read back
+        self.compute.wait_event(s["loaded"])
+        self.compute.wait_event(s["returned"])
+        self.layer.forward(s["ids"], s["qsl"], s["hidden"], stream=self.compute, out=s["y"],
+                           **forward_kwargs)
+        s["computed"].record(self.compute)
+        self.copy_out.wait_event(s["computed"])
+        with torch.cuda.stream(self.copy_out):
+            h_out.copy_(s["y"], non_blocking=True)
+        s["returned"].record(self.copy_out)
+        return s["returned"]
+
+    def synchronize(self):
+        self.copy_out.synchronize()
+
+
+class PLEChain:
+    """Several PLE layers over the same tokens, with the next layers' n-gram
+    ids and row gathers prefetched on a side stream.
+
+    Layer i+1's ids and gather (its embed stage) only need the tokens, so
+    they run on a side stream into one of two staging buffers while layer i's
+    kv_proj, gate and conv (its mix stage) run on the main stream; a staging
+    buffer is refilled once the kv_proj that read it has finished. With
+    ``prefetch=False`` the layers run one after the other on the main
+    stream. Results are the same either way.
+    """
+
+    def __init__(self, layers, prefetch=True, prefetch_ctas=0):
+        self.layers = list(layers)
+        self.prefetch = bool(prefetch)
+        self.prefetch_ctas = int(prefetch_ctas)
+        self._bufs = {}
+        self._side = {}
+
+    def _staging(self, num_tokens, device):
+        key = (num_tokens, str(device))
+        st = self._bufs.get(key)
+        if st is None:
+            l0 = self.layers[0]
+            E = l0.num_heads * l0.head_dim
+            st = []
+            for _ in range(2):
+                ws = None
+                host = [l for l in self.layers if not l.table.is_cuda]
+                if host:
+                    n = max(_lib.ple_lookup_ordered_workspace(num_tokens, l.num_heads, l.table,
+                                                              l.row_scale) for l in host)
+                    ws = torch.empty((n,), dtype=torch.uint8, device=device)
+                st.append({
+                    "ids": torch.empty((num_tokens, l0.num_heads), dtype=torch.int64, device=device),
+                    "emb": torch.empty((num_tokens, E), dtype=torch.bfloat16, device=device),
+                    "ws": ws, "ready": torch.cuda.Event(), "free": torch.cuda.Event(),
+                })
+            self._bufs = {key: st}
+        return st
+
+    def forward(self, input_ids, query_start_loc, hiddens, outs, ngram_context=None,
+                ngram_context_out=None, conv_states=None, conv_states_out=None, dev_err=None,
+                stream=None):
+        """Run every layer: layer i reads hiddens[i] and writes outs[i];
+        conv_states / conv_states_out are per-layer lists (or None);
+        ngram_context_out is written once (the tokens are the same for all
+        layers)."""
+        L = len(self.layers)
+        device = input_ids.device
+        main = stream if stream is not None else torch.cuda.current_stream(device)
+        st = self._staging(input_ids.numel(), device)
+        cs = conv_states or [None] * L
+        cso = conv_states_out or [None] * L
+
+        def embed(i, s):
+            slot = st[i % 2]
+            self.layers[i].embed(input_ids, query_start_loc, slot["ids"], slot["emb"], slot["ws"],
+                                 ngram_context=ngram_context,
+                                 ngram_context_out=ngram_context_out if i == 0 else None,
+                                 dev_err=dev_err, stream=s,
+                                 max_ctas=self.prefetch_ctas if s is not main else None)
+
+        if not self.prefetch:
+            for i in range(L):
+                embed(i, main)
+                self.layers[i].mix(st[i % 2]["emb"], hiddens[i], query_start_loc, outs[i],
+                                   conv_state=cs[i], conv_state_out=cso[i], dev_err=dev_err,
+                                   stream=main)
+            return outs
+        side = self._side.get(str(device))
+        if side is None:
+            side = self._side[str(device)] = torch.cuda.Stream(device)
+        side.wait_stream(main)  # inputs written on the main stream
+        for i in range(min(2, L)):
+            embed(i, side)
+            st[i % 2]["ready"].record(side)
+        for i in range(L):
+            slot = st[i % 2]
+            main.wait_event(slot["ready"])
+            layer = self.layers[i]
+            b = layer.buffers(input_ids.numel(), device)
+            _lib.ple_kv_proj(slot["emb"], layer.w_kv, b["kv"], dev_err=dev_err, stream=main)
+            slot["free"].record(main)
+            if i + 2 < L:  # refill this staging buffer with layer i+2's rows
+                side.wait_event(slot["free"])
+                embed(i + 2, side)
+                slot["ready"].record(side)
+            _lib.ple_gate_conv(hiddens[i], b["kv"], layer.gamma_h, layer.gamma_k,
+                               query_start_loc, layer.conv_w, layer.dilation, outs[i],
+                               eps=layer.eps, conv_state=cs[i], conv_state_out=cso[i],
+                               gate_out=b["gate"], dev_err=dev_err, stream=main)
+        main.wait_stream(side)
+        return outs

@@ -115,3 +115,90 @@ def test_prefill_8k_chain_sampled():
         assert_close(yb[t:t + 1], ref_y[-1:], atol_frac=CHAIN_ATOL_FRAC, what=f"token {t}")
     del table
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_host_pipeline_matches_layer(depth):
+    """PLEHostPipeline over pinned host buffers (transfers overlapping
+    compute) gives, step by step, exactly what PLELayer.forward gives on the
+    same inputs; every step has its own tokens and hidden states."""
+    from hashed_gram_embedding_gb300 import PLEHostPipeline
+    w, host, dense, table, row_scale = tiny_case(wl.WORKLOADS["tiny"])
+    d_dense = {k: v.cuda() for k, v in dense.items()}
+    layer = build_layer(w, host, d_dense, table.cuda(), None)
+    T, C = w.num_tokens, w.hidden
+    steps = 5
+    rng = np.random.default_rng(3)
+    g = torch.Generator().manual_seed(4)
+    h_ids = [torch.from_numpy(rng.integers(0, w.token_vocab, T).astype(np.int32)).pin_memory()
+             for _ in range(steps)]
+    h_qsl = torch.from_numpy(host["query_start_loc"]).pin_memory()
+    h_hidden = [torch.randn((T, C), generator=g).to(torch.bfloat16).pin_memory()
+                for _ in range(steps)]
+    h_out = [torch.empty((T, C), dtype=torch.bfloat16).pin_memory() for _ in range(steps)]
+    pipe = PLEHostPipeline(layer, T, len(host["query_start_loc"]) - 1, "cuda", depth=depth)
+    err = dev_err_word()
+    for k in range(steps):
+        pipe.submit(h_ids[k], h_qsl, h_hidden[k], h_out[k], dev_err=err)
+    pipe.synchronize()
+    assert int(err.item()) == 0
+    d_qsl = h_qsl.cuda()
+    for k in range(steps):
+        want = layer.forward(h_ids[k].cuda(), d_qsl, h_hidden[k].cuda()).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(h_out[k].view(torch.int16), want.cpu().view(torch.int16)), f"step {k}"
+
+
+@pytest.mark.parametrize("prefetch", [True, False])
+@pytest.mark.parametrize("on_host", [False, True])
+def test_chain_matches_layers(prefetch, on_host):
+    """PLEChain over four layers (own multipliers, tables, weights, hidden
+    states, conv states) gives each layer's PLELayer.forward output bit for
+    bit, with the next layers' ids and gathers prefetched on a side stream or
+    run in line; tables in HBM, or in host memory (ordered gather)."""
+    from hashed_gram_embedding_gb300 import PLEChain, _lib
+    L = 4
+    w = wl.scaled(wl.WORKLOADS["tiny"], num_layers=L, decode=True)
+    layers, hiddens, states, owners = [], [], [], []
+    host = None
+    for i in range(L):
+        w_i, host_i, dense, table, _ = tiny_case(w, seed_step=i)
+        host = host or host_i
+        d = {k: v.cuda() for k, v in dense.items()}
+        if on_host:
+            owner = _lib.HostTable(table.shape[0], table.shape[1], torch.bfloat16)
+            owner.tensor.copy_(table)
+            owners.append(owner)
+            tab = owner.tensor
+        else:
+            tab = table.cuda()
+        layers.append(PLELayer(tab, None, host["multipliers"][i], host["V"], host["O"],
+                               w.eos_token_id, w.heads_per_ngram, d["w_kv"], d["gamma_h"],
+                               d["gamma_k"], d["conv_w"], w.dilation))
+        hiddens.append(d["hidden"])
+        states.append(d["conv_state"])
+    T, C = w.num_tokens, w.hidden
+    ids = torch.from_numpy(host["input_ids"]).cuda()
+    qsl = torch.from_numpy(host["query_start_loc"]).cuda()
+    ctx = torch.from_numpy(host["ngram_context"]).cuda()
+    outs = [torch.empty((T, C), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    st_out = [torch.empty_like(s) for s in states]
+    ctx_out = torch.empty_like(ctx)
+    err = dev_err_word()
+    PLEChain(layers, prefetch=prefetch, prefetch_ctas=76).forward(
+        ids, qsl, hiddens, outs, ngram_context=ctx, ngram_context_out=ctx_out,
+        conv_states=states, conv_states_out=st_out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i in range(L):
+        so = torch.empty_like(states[i])
+        co = torch.empty_like(ctx)
+        want = layers[i].forward(ids, qsl, hiddens[i], ngram_context=ctx, ngram_context_out=co,
+                                 conv_state=states[i], conv_state_out=so).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i].view(torch.int16), want.view(torch.int16)), f"layer {i}"
+        assert torch.equal(st_out[i].view(torch.int16), so.view(torch.int16)), f"state {i}"
+        if i == 0:
+            assert torch.equal(ctx_out, co)
+    for o in owners:
+        o.close()
