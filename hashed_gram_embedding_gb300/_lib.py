@@ -30,6 +30,7 @@ PLE_BF16 = 0
 PLE_FP8_E4M3 = 1
 PLE_HBM = 0
 PLE_HOST_UVA = 1
+PLE_HOST_TABLE_REGISTER = 1
 
 # Every entry point of include/ple.h with its ctypes signature.
 _P = ctypes.c_void_p
@@ -54,6 +55,14 @@ SIGNATURES = {
     "ple_gate_conv": [_P, _P, _P, _P, _F32, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P],
     "ple_host_table_alloc": [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)],
     "ple_host_table_free": [ctypes.c_void_p, ctypes.c_size_t],
+    "ple_host_table_create_shared": [ctypes.c_char_p, ctypes.c_size_t, _I32,
+                                     ctypes.POINTER(ctypes.c_void_p)],
+    "ple_host_table_attach_shared": [ctypes.c_char_p, ctypes.c_size_t, _I32,
+                                     ctypes.POINTER(ctypes.c_void_p)],
+    "ple_host_table_unlink_shared": [ctypes.c_char_p],
+    "ple_host_table_map_file": [ctypes.c_char_p, ctypes.c_size_t, _I32,
+                                ctypes.POINTER(ctypes.c_void_p)],
+    "ple_host_table_unmap": [ctypes.c_void_p, ctypes.c_size_t, _I32],
     "ple_last_error": [],
     "ple_version": [],
 }
@@ -259,3 +268,42 @@ class HostTable:
             self.close()
         except Exception:
             pass
+
+
+class MappedHostTable:
+    """A table in a named shared-memory object or a file, mapped by
+    ple_host_table_create_shared / _attach_shared / _map_file and viewed as a
+    torch tensor [rows, row_dim]; ``register`` makes it readable by the GPU
+    over UVA. Unmapped on close() (the shared object itself stays until
+    unlink)."""
+
+    def __init__(self, kind, target, rows, row_dim, dtype, register=True):
+        import torch
+        elem = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(rows) * int(row_dim) * elem
+        self.flags = PLE_HOST_TABLE_REGISTER if register else 0
+        fn = {"create": "ple_host_table_create_shared", "attach": "ple_host_table_attach_shared",
+              "file": "ple_host_table_map_file"}[kind]
+        ptr = ctypes.c_void_p()
+        _check(fn, getattr(lib(), fn)(str(target).encode(), self.nbytes, self.flags,
+                                      ctypes.byref(ptr)))
+        self.ptr = ptr.value
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        view = torch.frombuffer(buf, dtype=torch.uint8)
+        self.tensor = view.view(dtype).view(int(rows), int(row_dim))
+
+    def close(self):
+        if getattr(self, "ptr", None):
+            self.tensor = None
+            lib().ple_host_table_unmap(ctypes.c_void_p(self.ptr), self.nbytes, self.flags)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def ple_host_table_unlink_shared(name):
+    return _check("ple_host_table_unlink_shared", lib().ple_host_table_unlink_shared(name.encode()))

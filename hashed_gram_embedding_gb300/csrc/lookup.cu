@@ -48,7 +48,10 @@ gather_bf16_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__
                    uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
                    int64_t table_rows, uint4* __restrict__ out, int32_t* dev_err) {
   pdl_wait();
-  pdl_trigger();
+  // The sorted walk over a host table does not let the next kernel launch
+  // early: kernels resident alongside it slow the walk's host reads (measured
+  // 3x on a GB300).
+  if (perm == nullptr) pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
   // Unsorted walk: a thread's items are a grid apart (all CTAs sweep the
   // whole output together). Sorted walk (perm): a CTA takes kUnroll * 256
@@ -113,7 +116,10 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
                   const float* __restrict__ row_scale, int64_t table_rows,
                   uint4* __restrict__ out, int32_t* dev_err) {
   pdl_wait();
-  pdl_trigger();
+  // The sorted walk over a host table does not let the next kernel launch
+  // early: kernels resident alongside it slow the walk's host reads (measured
+  // 3x on a GB300).
+  if (perm == nullptr) pdl_trigger();
   const int vpr = VPR ? VPR : vpr_rt;
   const uint32_t item_step = perm != nullptr ? kThreads : gridDim.x * kThreads;
   const uint32_t first = perm != nullptr ? blockIdx.x * kThreads * kUnroll + threadIdx.x
@@ -451,16 +457,16 @@ ple_status launch_gather_kernel(const Gather& g, const uint32_t* perm, cudaStrea
   cudaError_t err = cudaSuccess;
   if (g.dtype == PLE_BF16) {
     if (vpr == 16)
-      err = launch_kernel(gather_bf16_kernel<16>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_bf16_kernel<16>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else if (vpr == 8)
-      err = launch_kernel(gather_bf16_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_bf16_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
     else
-      err = launch_kernel(gather_bf16_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_bf16_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
   } else {
     if (vpr == 8)
-      err = launch_kernel(gather_fp8_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
     else
-      err = launch_kernel(gather_fp8_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
   }
   if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
@@ -517,14 +523,16 @@ ple_status launch_ordered(const Gather& g, uint8_t* ws, const OrderPlan& plan,
   int64_t blocks = (g.items + kOrderThreads - 1) / kOrderThreads;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 4;
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  err = launch_kernel(order_count_kernel, dim3(grid), dim3(kOrderThreads), 0, stream, 1, g.ids,
-                      items, g.table_rows, plan.shift, plan.buckets, counts);
+  // plain stream order for the sort (see the walk's note on early launches)
+  err = launch_kernel_pdl(false, order_count_kernel, dim3(grid), dim3(kOrderThreads), 0, stream,
+                          1, g.ids, items, g.table_rows, plan.shift, plan.buckets, counts);
   if (err == cudaSuccess)
-    err = launch_kernel(order_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, 1,
-                        static_cast<const uint32_t*>(counts), plan.buckets, cursor);
+    err = launch_kernel_pdl(false, order_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, 1,
+                            static_cast<const uint32_t*>(counts), plan.buckets, cursor);
   if (err == cudaSuccess)
-    err = launch_kernel(order_scatter_kernel, dim3(grid), dim3(kOrderThreads), 0, stream, 1, g.ids,
-                        items, g.table_rows, plan.shift, plan.buckets, cursor, perm);
+    err = launch_kernel_pdl(false, order_scatter_kernel, dim3(grid), dim3(kOrderThreads), 0,
+                            stream, 1, g.ids, items, g.table_rows, plan.shift, plan.buckets,
+                            cursor, perm);
   if (err != cudaSuccess) return check_cuda(err, name);
   ple_status s = check_cuda(cudaGetLastError(), name);
   if (s != PLE_OK) return s;

@@ -345,6 +345,51 @@ ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* kv,
 ple_status ple_host_table_alloc(size_t bytes, void** host_ptr);
 ple_status ple_host_table_free(void* host_ptr, size_t bytes);
 
+/* Flags of the shared and file-backed host tables below. */
+typedef enum {
+  PLE_HOST_TABLE_REGISTER = 1 /* cudaHostRegister the mapping (needed for UVA reads) */
+} ple_host_table_flags;
+
+/*
+ * ple_host_table_create_shared / ple_host_table_attach_shared /
+ * ple_host_table_unlink_shared -- a table in a named POSIX shared-memory
+ * object (/dev/shm), mapped MAP_SHARED by several processes and registered
+ * with cudaHostRegister so each one's GPU reads it in place over UVA.
+ * (PR#56512 report, 关键源码片段: a /dev/shm backing file mapped MAP_SHARED and
+ * registered with cudaHostRegister, created by one leader that alone writes
+ * the weights, with every step rolled back on failure.)
+ *   name        "/" then 1..254 characters without "/", else PLE_ERR_INVALID_ARG.
+ *   bytes       > 0; create sizes the object to `bytes` (it must not exist);
+ *               attach requires an existing object of at least `bytes`.
+ *   flags       PLE_HOST_TABLE_REGISTER to register for GPU reads (0: map only).
+ *   host_ptr    receives the mapping (advised for huge pages, NUMA policy set).
+ * On any failure everything the call did is undone (mapping, descriptor and,
+ * for create, the object itself) and *host_ptr is NULL. The object outlives
+ * its mappings until ple_host_table_unlink_shared.
+ */
+ple_status ple_host_table_create_shared(const char* name, size_t bytes, int32_t flags,
+                                        void** host_ptr);
+ple_status ple_host_table_attach_shared(const char* name, size_t bytes, int32_t flags,
+                                        void** host_ptr);
+ple_status ple_host_table_unlink_shared(const char* name);
+
+/*
+ * ple_host_table_map_file -- a table stored in a file, mapped read-only
+ * (MAP_SHARED, madvise MADV_RANDOM) and, with PLE_HOST_TABLE_REGISTER,
+ * registered read-only for GPU reads over UVA (registration pins the pages,
+ * reading the file into the page cache). Where read-only registration is
+ * not supported the file is mapped privately and registered (each page then
+ * gets its own copy in memory; the file is never written). (PR#53899 page:
+ * the disk-backed mmap table storage read with MADV_RANDOM.) The file must
+ * hold at least `bytes`; on failure nothing stays mapped.
+ */
+ple_status ple_host_table_map_file(const char* path, size_t bytes, int32_t flags,
+                                   void** host_ptr);
+
+/* Undo ple_host_table_create_shared / _attach_shared / _map_file (the same
+ * bytes and flags): unregister if registered, then unmap. */
+ple_status ple_host_table_unmap(void* host_ptr, size_t bytes, int32_t flags);
+
 /* Text of the last non-OK status on this host thread ("" if none). */
 const char* ple_last_error(void);
 

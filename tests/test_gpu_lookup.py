@@ -299,3 +299,61 @@ def test_ordered_gather_rejects_small_workspace():
     ws = torch.empty((need - 256,), dtype=torch.uint8, device="cuda")
     with pytest.raises(_lib.PleError, match="workspace"):
         _lib.ple_lookup_ordered(ids, table, out, ws)
+
+
+def test_fp8_global_scale():
+    """The pages' fp8 table carries one weight_scale for the whole table: a
+    row_scale holding that one value everywhere gives exactly the global-
+    scale dequantisation, e4m3 code times the scale, rounded to bf16."""
+    rng = np.random.default_rng(21)
+    rows, D, T, H = 3000, 128, 64, 16
+    codes = rng.integers(0, 0x7E, size=(rows, D), dtype=np.uint8)  # finite codes
+    weight_scale = np.float32(0.0123)
+    scale = np.full((rows,), weight_scale, dtype=np.float32)
+    ids = rng.integers(0, rows, size=(T, H))
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    _lib.ple_lookup(torch.from_numpy(ids).cuda(), torch.from_numpy(codes).cuda(), out,
+                    row_scale=torch.from_numpy(scale).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), lookup_fp8(ids, codes, scale))
+    # the same numbers from torch's own e4m3 decode times the one scale
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float() * float(weight_scale)
+    want = dec[torch.from_numpy(ids.reshape(-1))].reshape(T, H * D).to(torch.bfloat16)
+    assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind", ["shared", "file"])
+def test_gather_from_shared_and_file_backed_tables(kind, tmp_path):
+    """Tables in a named shared-memory object and in a file, registered for
+    GPU reads (the file read-only), give bit-exact rows through the plain and
+    the ordered gather."""
+    import uuid
+    rng = np.random.default_rng(31)
+    rows, D, T, H = 20000, 128, 257, 16
+    table = random_table_bits(rng, rows, D)
+    name = "/ple_gpu_" + uuid.uuid4().hex[:12]
+    if kind == "shared":
+        t = _lib.MappedHostTable("create", name, rows, D, torch.bfloat16, register=True)
+        t.tensor.view(torch.int16).copy_(torch.from_numpy(table.view(np.int16)))
+    else:
+        path = tmp_path / "rows.bin"
+        table.tofile(path)
+        t = _lib.MappedHostTable("file", path, rows, D, torch.bfloat16, register=True)
+    try:
+        ids = rng.integers(0, rows, size=(T, H))
+        d_ids = torch.from_numpy(ids).cuda()
+        want = lookup_bf16(ids, table)
+        out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+        _lib.ple_lookup(d_ids, t.tensor, out)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), want)
+        ws = torch.empty((_lib.ple_lookup_ordered_workspace(T, H, t.tensor),), dtype=torch.uint8,
+                         device="cuda")
+        out.zero_()
+        _lib.ple_lookup_ordered(d_ids, t.tensor, out, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), want)
+    finally:
+        t.close()
+        if kind == "shared":
+            _lib.ple_host_table_unlink_shared(name)
