@@ -269,34 +269,35 @@ def run_ours(args):
         order_ws = torch.empty((_lib.ple_lookup_ordered_workspace(
             T, H, sets[0]["table"], sets[0]["row_scale"]),), dtype=torch.uint8, device=device)
 
-    def gather(p):
+    def gather(p, st):
         if order_ws is not None:
             _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, row_scale=p["row_scale"],
-                                    dev_err=err, stream=stream)
+                                    dev_err=err, stream=st)
         else:
             _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err,
-                            stream=stream)
+                            stream=st)
 
-    def step(s, ev=None):
+    def step(s, ev=None, st=None):
+        st = stream if st is None else st
         p = sets[s % num_sets]
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         _lib.ple_ngram_ids(p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"],
                            p["host"]["O"], w.eos_token_id, w.heads_per_ngram, ids,
-                           ctx_out if w.decode else None, err, stream)
+                           ctx_out if w.decode else None, err, st)
         if ev is not None:
-            ev[1].record(stream)
-        gather(p)
+            ev[1].record(st)
+        gather(p, st)
         if ev is not None:
-            ev[2].record(stream)
-        _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=stream)
+            ev[2].record(st)
+        _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=st)
         if ev is not None:
-            ev[3].record(stream)
+            ev[3].record(st)
         _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"],
                            w.dilation, y, conv_state=p.get("conv_state"), conv_state_out=st_out,
-                           gate_out=gate, dev_err=err, stream=stream)
+                           gate_out=gate, dev_err=err, stream=st)
         if ev is not None:
-            ev[4].record(stream)
+            ev[4].record(st)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -306,7 +307,7 @@ def run_ours(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} during warm-up")
 
-    # ---- timed region: K steps, device events on the launching stream ----
+    # ---- eager steps with events between the kernels (per-kernel times) ----
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
@@ -314,14 +315,39 @@ def run_ours(args):
         step(i, events[i])
     torch.cuda.synchronize()
     barrier()
-    total_ms = events[0][0].elapsed_time(events[-1][4])
+    eager_ms = events[0][0].elapsed_time(events[-1][4])
     per_kernel = {k: [] for k in KERNELS}
     for ev in events:
         for j, k in enumerate(KERNELS):
             per_kernel[k].append(ev[j].elapsed_time(ev[j + 1]))
-    total_ms = max_over_ranks(total_ms, device)
+    eager_ms = max_over_ranks(eager_ms, device)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+
+    # ---- timed region: K steps replayed from CUDA graphs (one per layer
+    # set, captured once), device events on the replay stream ----
+    graphs, graph_error = capture_graphs(torch, step, num_sets, device)
+    if graphs is not None:
+        for i in range(min(args.warmup, len(graphs))):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        replay = torch.cuda.current_stream(device)
+        barrier()
+        torch.cuda.synchronize()
+        g0.record(replay)
+        for i in range(args.steps):
+            graphs[i % num_sets].replay()
+        g1.record(replay)
+        torch.cuda.synchronize()
+        barrier()
+        total_ms = max_over_ranks(g0.elapsed_time(g1), device)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error word {int(err.item())} in the graph replays")
+        mode = "cuda_graph"
+    else:
+        total_ms, mode = eager_ms, "eager"
 
     # ---- end to end through PLEHostPipeline with pinned host buffers ----
     # Every step uploads its inputs (token ids, query_start_loc, hidden) from
@@ -402,7 +428,8 @@ def run_ours(args):
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.table_dtype == "bf16" else "fp8->bf16",
         "data": "synthetic (seeded workload recipe; no dataset)",
-        "config": {"workload": w.name, "num_tokens": T, "num_reqs": w.num_reqs, "heads": H,
+        "config": {"workload": w.name, "mode": mode, "num_tokens": T, "num_reqs": w.num_reqs,
+                   "heads": H,
                    "head_dim": w.head_dim, "table_rows": int(sets[0]["table"].shape[0]),
                    "table_loc": w.table_loc, "table_dtype": w.table_dtype, "hidden": C,
                    "conv_kernel": w.conv_k, "dilation": w.dilation,
@@ -421,6 +448,11 @@ def run_ours(args):
     }
     if w.table_loc == "host":
         line["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
+    line["eager"] = {"ms_per_step": round(eager_ms / args.steps, 4),
+                     "value": round(world * args.steps * T / (eager_ms * 1e-3), 1),
+                     "note": "same steps launched one by one, events between kernels"}
+    if graph_error:
+        line["eager"]["graph_capture_error"] = graph_error
     if w.num_layers > 1 and len(sets) >= w.num_layers:
         line["chain"] = chain_timing(torch, w, sets, device, err)
     if not args.no_cpu_baseline:
@@ -433,6 +465,25 @@ def launches_per_step(w, table):
     and conv passes; a host table's ordered gather adds its count, scan and
     scatter kernels."""
     return LAUNCHES_PER_STEP + (3 if w.table_loc == "host" else 0)
+
+
+def capture_graphs(torch, step, num_sets, device):
+    """Each layer set's step captured once into a CUDA graph (the libple calls
+    on a capture stream); (graphs, None), or (None, reason) if capture fails."""
+    try:
+        capture = torch.cuda.Stream(device)
+        capture.wait_stream(torch.cuda.current_stream(device))
+        graphs = []
+        for s in range(num_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=capture):
+                step(s, st=capture)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs, None
+    except Exception as e:  # report it; the eager timing then stands
+        torch.cuda.synchronize()
+        return None, str(e)[:300]
 
 
 def chain_timing(torch, w, sets, device, err, reps=10):

@@ -422,34 +422,36 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = tid; i < R + 1; i += kConvThreads) check_qsl(a.qsl, R, T, i, a.dev_err);
 
-  if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
-
   // Window row i <-> token t0 - W + i (rows of tokens before 0 are not
   // loaded; rows of an earlier request are loaded but never read). Each warp
-  // takes every 8th row, 8 rows' loads in flight per lane at a time.
-  if (active) {
+  // takes every 8th row, kBatch rows' loads in flight per lane at a time (one
+  // batch covers a 64-token tile and its halo); warp 0 searches the tile's
+  // requests while its first batch is in flight.
+  {
     constexpr int kWarps = kConvThreads / 32;
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 10;
     const int i0 = t0 >= W ? 0 : static_cast<int>(W - t0);
     const int rows = n_tok + W;
-    for (int first = i0 + warp; first < rows; first += kWarps * kBatch) {
-      uint4 v[kBatch];
-      float gv[kBatch];
+    uint4 v[kBatch];
+    float gv[kBatch];
+    auto load = [&](int first) {
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int i = first + q * kWarps;
         v[q] = make_uint4(0, 0, 0, 0);
         gv[q] = 0.f;
-        if (i < rows) {
+        if (active && i < rows) {
           const int64_t tok = t0 - W + i;
           v[q] = ldg16(src + tok * src_pitch);
           if constexpr (GATED) gv[q] = __ldg(g + tok);
         }
       }
+    };
+    auto stage = [&](int first) {
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int i = first + q * kWarps;
-        if (i < rows) {
+        if (active && i < rows) {
           float f[8];
           if constexpr (GATED) {
             const uint64_t gg = f2(gv[q], gv[q]);
@@ -469,6 +471,14 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
           s.win[(i * 2 + 1) * 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
         }
       }
+    };
+    int first = i0 + warp;
+    load(first);
+    if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
+    stage(first);
+    for (first += kWarps * kBatch; first < rows; first += kWarps * kBatch) {
+      load(first);
+      stage(first);
     }
   }
   __syncthreads();

@@ -202,3 +202,46 @@ def test_chain_matches_layers(prefetch, on_host):
             assert torch.equal(ctx_out, co)
     for o in owners:
         o.close()
+
+
+@pytest.mark.parametrize("on_host", [False, True])
+def test_layer_in_cuda_graph_matches_eager(on_host):
+    """PLELayer.forward captured once into a CUDA graph and replayed gives the
+    eager result bit for bit; replays pick up new inputs written into the
+    captured buffers."""
+    from hashed_gram_embedding_gb300 import _lib
+    w, host, dense, table, _ = tiny_case(wl.WORKLOADS["tiny"])
+    d = {k: v.cuda() for k, v in dense.items()}
+    owner = None
+    if on_host:
+        owner = _lib.HostTable(table.shape[0], table.shape[1], torch.bfloat16)
+        owner.tensor.copy_(table)
+        tab = owner.tensor
+    else:
+        tab = table.cuda()
+    layer = build_layer(w, host, d, tab, None)
+    ids = torch.from_numpy(host["input_ids"]).cuda()
+    qsl = torch.from_numpy(host["query_start_loc"]).cuda()
+    hidden = d["hidden"].clone()
+    out = torch.empty_like(hidden)
+    err = dev_err_word()
+    layer.forward(ids, qsl, hidden, out=out, dev_err=err)  # buffers exist before capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(ids, qsl, hidden, out=out, dev_err=err, stream=s)
+    for k in range(2):
+        ids.copy_(torch.from_numpy(np.random.default_rng(k).integers(
+            0, w.token_vocab, w.num_tokens).astype(np.int32)))
+        hidden.copy_(torch.randn(hidden.shape, generator=torch.Generator().manual_seed(k))
+                     .to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        want = layer.forward(ids, qsl, hidden).clone()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(out.view(torch.int16), want.view(torch.int16)), f"replay {k}"
+    if owner is not None:
+        owner.close()
