@@ -38,10 +38,13 @@ METRIC = "PLE tokens/sec/layer"
 UNIT = "tokens/s/layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NUM_SETS = 4
-KERNELS = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
-# libple kernel launches per step: ids, gather, kv_proj, and gate_conv's two
-# passes (gate reduction, gated conv)
-LAUNCHES_PER_STEP = 5
+# the oracle's stages (cpu_baseline and the reference arm)
+ORACLE_STAGES = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
+# timed kernels per step: the projection with the gate reductions fused, then
+# the gated conv (hidden sizes that are multiples of 256), else the
+# projection, then gate_conv's two passes (gate reduction, gated conv)
+KERNELS_FUSED = ("ngram_ids", "lookup", "kv_proj_gate", "conv")
+KERNELS_UNFUSED = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
 
 
 # ---------------------------------------------------------------------------
@@ -172,8 +175,9 @@ def ncu_traffic(kernel):
     or None when the summary is missing or the kernel source changed since."""
     summary = os.path.join(ROOT, "profiles", f"{kernel}_prefill8k.md")
     src = os.path.join(ROOT, "hashed_gram_embedding_gb300", "csrc",
-                       {"kv_proj": "kv_proj.cu", "lookup": "lookup.cu",
-                        "gate_conv": "gate_conv.cu", "ngram_ids": "ngram_ids.cu"}[kernel])
+                       {"kv_proj": "kv_proj.cu", "kv_proj_gate": "kv_proj.cu",
+                        "lookup": "lookup.cu", "gate_conv": "gate_conv.cu",
+                        "conv": "gate_conv.cu", "ngram_ids": "ngram_ids.cu"}[kernel])
     try:
         text = open(summary).read()
     except OSError:
@@ -207,6 +211,10 @@ def algorithmic_work(w):
         "lookup": lookup,
         "kv_proj": ("tensor", 2.0 * T * E * 2 * C),
         "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2)),
+        # the gate reductions ride in the projection's epilogue: tensor-bound
+        "kv_proj_gate": ("tensor", 2.0 * T * E * 2 * C),
+        # v and g in, y out
+        "conv": ("hbm", T * (C * 2 + 4 + C * 2)),
     }
 
 
@@ -255,6 +263,10 @@ def run_ours(args):
         num_sets = args.layer_sets
     sets = make_sets(torch, w, device, num_sets)
     T, H, C = w.num_tokens, w.num_heads, w.hidden
+    fuse = C % 256 == 0 and not args.no_fuse_gate
+    KERNELS = KERNELS_FUSED if fuse else KERNELS_UNFUSED
+    gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
+                           device=device) if fuse else None)
     ids = torch.empty((T, H), dtype=torch.int64, device=device)
     emb = torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device)
     kv = torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device)
@@ -290,12 +302,21 @@ def run_ours(args):
         gather(p, st)
         if ev is not None:
             ev[2].record(st)
-        _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=st)
+        if fuse:
+            _lib.ple_kv_proj_gate(emb, p["w_kv"], p["hidden"], p["gamma_h"], p["gamma_k"], kv,
+                                  gate, gate_ws, dev_err=err, stream=st)
+        else:
+            _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=st)
         if ev is not None:
             ev[3].record(st)
-        _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"],
-                           w.dilation, y, conv_state=p.get("conv_state"), conv_state_out=st_out,
-                           gate_out=gate, dev_err=err, stream=st)
+        if fuse:
+            _lib.ple_gated_conv(kv, gate, p["qsl"], p["conv_w"], w.dilation, y,
+                                conv_state=p.get("conv_state"), conv_state_out=st_out,
+                                dev_err=err, stream=st)
+        else:
+            _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"],
+                               p["conv_w"], w.dilation, y, conv_state=p.get("conv_state"),
+                               conv_state_out=st_out, gate_out=gate, dev_err=err, stream=st)
         if ev is not None:
             ev[4].record(st)
 
@@ -357,7 +378,7 @@ def run_ours(args):
     p0 = sets[0]
     layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
                      w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
-                     p0["conv_w"], w.dilation)
+                     p0["conv_w"], w.dilation, fuse_gate=fuse)
     depth = 2
     pipe = PLEHostPipeline(layer, T, w.num_reqs, device, depth=depth)
     h_ids = torch.from_numpy(p0["host"]["input_ids"]).pin_memory()
@@ -433,7 +454,7 @@ def run_ours(args):
                    "head_dim": w.head_dim, "table_rows": int(sets[0]["table"].shape[0]),
                    "table_loc": w.table_loc, "table_dtype": w.table_dtype, "hidden": C,
                    "conv_kernel": w.conv_k, "dilation": w.dilation,
-                   "layer_sets": num_sets,
+                   "fuse_gate": fuse, "layer_sets": num_sets,
                    "l2": f"inputs rotate over {num_sets} layer sets (> 129 MB L2 per rotation); no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
@@ -443,7 +464,7 @@ def run_ours(args):
                    {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]}),
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": launches_per_step(w, sets[0]["table"]) * args.steps,
+        "gpu_launches": launches_per_step(w, fuse) * args.steps,
         "clocks": clocks,
     }
     if w.table_loc == "host":
@@ -454,17 +475,19 @@ def run_ours(args):
     if graph_error:
         line["eager"]["graph_capture_error"] = graph_error
     if w.num_layers > 1 and len(sets) >= w.num_layers:
-        line["chain"] = chain_timing(torch, w, sets, device, err)
+        line["chain"] = chain_timing(torch, w, sets, device, err, fuse)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
 
 
-def launches_per_step(w, table):
-    """libple kernels one step launches: ids, gather, kv_proj, and the gate
-    and conv passes; a host table's ordered gather adds its count, scan and
-    scatter kernels."""
-    return LAUNCHES_PER_STEP + (3 if w.table_loc == "host" else 0)
+def launches_per_step(w, fuse):
+    """libple kernels one step launches: ids, gather, then the fused
+    projection and the gated conv (4), or the projection and the gate and
+    conv passes (5); a host table's ordered gather adds its count, scan and
+    scatter kernels. (The fused projection's counter clear is a memset, not
+    a kernel.)"""
+    return (4 if fuse else 5) + (3 if w.table_loc == "host" else 0)
 
 
 def capture_graphs(torch, step, num_sets, device):
@@ -486,13 +509,13 @@ def capture_graphs(torch, step, num_sets, device):
         return None, str(e)[:300]
 
 
-def chain_timing(torch, w, sets, device, err, reps=10):
+def chain_timing(torch, w, sets, device, err, fuse, reps=10):
     """All layers of a multi-layer workload through PLEChain: with the next
     layers' ids and gathers prefetched on a side stream, and in line."""
     from hashed_gram_embedding_gb300 import PLELayer, PLEChain
     layers = [PLELayer(p["table"], p["row_scale"], p["mult"], p["host"]["V"], p["host"]["O"],
                        w.eos_token_id, w.heads_per_ngram, p["w_kv"], p["gamma_h"], p["gamma_k"],
-                       p["conv_w"], w.dilation) for p in sets[:w.num_layers]]
+                       p["conv_w"], w.dilation, fuse_gate=fuse) for p in sets[:w.num_layers]]
     p0 = sets[0]
     T, C, L = w.num_tokens, w.hidden, w.num_layers
     hiddens = [p["hidden"] for p in sets[:L]]
@@ -654,12 +677,12 @@ def cpu_baseline(w, p, budget_s=15.0):
     time budget is spent (at least one request)."""
     qsl = p["host"]["query_start_loc"]
     tokens = 0
-    stages = {k: 0.0 for k in KERNELS}
+    stages = {k: 0.0 for k in ORACLE_STAGES}
     r = 0
     while r < len(qsl) - 1:
         n, t = oracle_sample(w, p, (r, r + 1), 1 << 30, _bits)
         tokens += n
-        for k in KERNELS:
+        for k in ORACLE_STAGES:
             stages[k] += t[k]
         r += 1
         if sum(stages.values()) > budget_s:
@@ -719,6 +742,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fuse-gate", action="store_true",
+                    help="time ple_kv_proj + ple_gate_conv instead of the fused projection")
     ap.add_argument("--layer-sets", type=int, default=0,
                     help="layer parameter sets to rotate over (0 = workload default)")
     ap.add_argument("--vocab-start", type=int, default=0,

@@ -50,9 +50,13 @@ SIGNATURES = {
                                   _I32, _P, _P],
     "ple_wait": [_P, _P, _I32],
     "ple_kv_proj": [_P, _P, _I64, _I32, _I32, _P, _P, _P],
+    "ple_kv_proj_gate_workspace": [_I64, _I32],
+    "ple_kv_proj_gate": [_P, _P, _I64, _I32, _I32, _P, _P, _P, _F32, _P, _P, _P, ctypes.c_size_t,
+                         _P, _P],
     "ple_gate": [_P, _P, _P, _P, _F32, _I64, _I32, _P, _P, _P],
     "ple_conv": [_P, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P],
     "ple_gate_conv": [_P, _P, _P, _P, _F32, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P],
+    "ple_gated_conv": [_P, _P, _P, _I32, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P],
     "ple_host_table_alloc": [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)],
     "ple_host_table_free": [ctypes.c_void_p, ctypes.c_size_t],
     "ple_host_table_create_shared": [ctypes.c_char_p, ctypes.c_size_t, _I32,
@@ -206,6 +210,24 @@ def ple_kv_proj(emb, w, kv, dev_err=None, stream=None):
         _ptr(emb), _ptr(w), T, E, w.shape[0] // 2, _ptr(kv), _ptr(dev_err), _stream(stream)))
 
 
+def ple_kv_proj_gate_workspace(num_tokens, hidden):
+    """Bytes of device workspace ple_kv_proj_gate needs (0: sizes it rejects)."""
+    return int(lib().ple_kv_proj_gate_workspace(int(num_tokens), int(hidden)))
+
+
+def ple_kv_proj_gate(emb, w, hidden, gamma_h, gamma_k, kv, gate_out, workspace, eps=1e-6,
+                     dev_err=None, stream=None):
+    """Projection with the gate reductions fused: writes kv[:, C:] (v) and
+    gate_out [T] float32; kv[:, :C] is left untouched. workspace: a device
+    uint8 tensor of at least ple_kv_proj_gate_workspace(T, C) bytes,
+    zero-filled before its first use (the call leaves it zeroed)."""
+    T, E = emb.shape
+    return _check("ple_kv_proj_gate", lib().ple_kv_proj_gate(
+        _ptr(emb), _ptr(w), T, E, w.shape[0] // 2, _ptr(hidden), _ptr(gamma_h), _ptr(gamma_k),
+        float(eps), _ptr(kv), _ptr(gate_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+
+
 def ple_gate(hidden, kv, gamma_h, gamma_k, out, eps=1e-6, gate_out=None, stream=None):
     T, C = hidden.shape
     return _check("ple_gate", lib().ple_gate(
@@ -234,6 +256,16 @@ def ple_gate_conv(hidden, kv, gamma_h, gamma_k, query_start_loc, w, dilation, ou
         _ptr(hidden), _ptr(kv), _ptr(gamma_h), _ptr(gamma_k), float(eps), _ptr(query_start_loc),
         query_start_loc.numel() - 1, T, C, _ptr(w), w.shape[1], int(dilation), _ptr(conv_state),
         _ptr(conv_state_out), _ptr(out), _ptr(gate_out), _ptr(dev_err), _stream(stream)))
+
+
+def ple_gated_conv(kv, gate, query_start_loc, w, dilation, out, conv_state=None,
+                   conv_state_out=None, dev_err=None, stream=None):
+    """Conv of u = bf16(gate * v), v = kv[:, C:]; kv [T, 2C] bf16, gate [T] float32."""
+    T, C2 = kv.shape
+    return _check("ple_gated_conv", lib().ple_gated_conv(
+        _ptr(kv), _ptr(gate), _ptr(query_start_loc), query_start_loc.numel() - 1, T, C2 // 2,
+        _ptr(w), w.shape[1], int(dilation), _ptr(conv_state), _ptr(conv_state_out), _ptr(out),
+        _ptr(dev_err), _stream(stream)))
 
 
 def ple_version():

@@ -41,47 +41,6 @@ constexpr int kMaxK = 8;
 constexpr int kMaxHalo = 64;
 constexpr int kMaxGateC = 16384;  // 8 vectors per thread at 256 threads per token
 
-__device__ __forceinline__ uint4 ldg16(const ple_bf16_t* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-// bf16 pair word -> its two float32 values (low half is the first element).
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack8(uint4 v, float f[8]) {
-  f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
-  f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
-  f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
-  f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
-// Packed float32 pairs (sm_100+ two-wide FMA/MUL; each lane is an IEEE
-// single-precision operation, identical to fmaf / __fmul_rn on that lane).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t r, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 // u = bf16(g * v) for one bf16 pair word.
 __device__ __forceinline__ uint32_t gate2(uint32_t w, float g) {
   return pack2(__fmul_rn(bf_lo(w), g), __fmul_rn(bf_hi(w), g));
@@ -90,18 +49,6 @@ __device__ __forceinline__ uint4 gate8(uint4 v, float g) {
   return make_uint4(gate2(v.x, g), gate2(v.y, g), gate2(v.z, g), gate2(v.w, g));
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-__device__ __forceinline__ float gate_of(float sh, float sk, float sd, int C, float eps) {
-  const float inv_c = 1.0f / static_cast<float>(C);
-  const float score = sd / (sqrtf(fmaf(sh, inv_c, eps)) * sqrtf(fmaf(sk, inv_c, eps))) /
-                      sqrtf(static_cast<float>(C));
-  return 1.0f / (1.0f + expf(-score));
-}
 
 // ---------------------------------------------------------------------------
 // Pass 1: gate scalars (and, for ple_gate, u = bf16(g * v)), streamed.
@@ -1122,4 +1069,37 @@ PLE_EXPORT ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* 
   return conv_entry(true, hidden, kv, gamma_h, gamma_k, eps, query_start_loc, num_reqs,
                     num_tokens, hidden_size, w, kernel_size, dilation, conv_state,
                     conv_state_out, out, gate_out, dev_err, stream, "ple_gate_conv");
+}
+
+PLE_EXPORT ple_status ple_gated_conv(const ple_bf16_t* kv, const float* gate,
+                                     const int32_t* query_start_loc, int32_t num_reqs,
+                                     int64_t num_tokens, int32_t hidden_size,
+                                     const ple_bf16_t* w, int32_t kernel_size, int32_t dilation,
+                                     const ple_bf16_t* conv_state, ple_bf16_t* conv_state_out,
+                                     ple_bf16_t* out, int32_t* dev_err, cudaStream_t stream) {
+  using namespace ple;
+  const char* name = "ple_gated_conv";
+  ple_status s = validate_conv(query_start_loc, num_reqs, num_tokens, hidden_size, w, kernel_size,
+                               dilation, conv_state, conv_state_out, name);
+  if (s != PLE_OK) return s;
+  const size_t state_bytes =
+      static_cast<size_t>(num_reqs) * (kernel_size - 1) * dilation * hidden_size * 2;
+  if (num_tokens == 0) return copy_carry(conv_state_out, conv_state, state_bytes, stream);
+  if (!kv || !gate || !out) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned16(kv) || !aligned16(out))
+    return fail(PLE_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", name);
+  ConvArgs a{};
+  a.src = kv;
+  a.qsl = query_start_loc;
+  a.num_reqs = num_reqs;
+  a.T = num_tokens;
+  a.C = hidden_size;
+  a.w = w;
+  a.K = kernel_size;
+  a.dil = dilation;
+  a.state = conv_state;
+  a.state_out = conv_state_out;
+  a.out = out;
+  a.dev_err = dev_err;
+  return launch_conv<true>(a, gate, stream, name);
 }

@@ -430,11 +430,115 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 // need the same 128 rows of A, so each loads 64 of them and multicasts them
 // to both, cutting each SM's A traffic in half; a stage may then be refilled
 // only after both pairs' MMAs released it.
-template <int PAIRS>
+// Fused gate reductions (ple_kv_proj_gate). The key half of kv is never
+// stored: the epilogue of a key tile (columns [n, n+256) of [0, C)) rounds
+// each accumulator to bf16 -- the value ple_kv_proj would store -- reads the
+// same 256 channels of the token's hidden row and adds, per row,
+// sum h^2, sum k^2 and sum h*k*gamma_h*gamma_k (the three sums of the gate's
+// RMSNorm-and-dot, which split over channel blocks). Each sum triple goes to
+// partial[key tile][row]; the epilogue warp that delivers the last key tile
+// of its 32 rows (a per-32-row arrival counter) adds the C/256 triples in
+// key-tile order, writes g = sigmoid(...) for those rows and sets the
+// counter back to zero, so a launch that completes leaves every counter as
+// it found it (zero) and the next launch needs no clearing pass. Value
+// tiles are stored as in ple_kv_proj.
+struct GateEpi {
+  const ple_bf16_t* hidden;   // [M][C]
+  const ple_bf16_t* gamma_h;  // [C]
+  const ple_bf16_t* gamma_k;  // [C]
+  float4* partial;            // [C/256][M]: (sum h^2, sum k^2, sum h*k*gh*gk, 0)
+  unsigned* count_top;        // one past the arrival counters: group j (rows 32j..32j+31)
+                              // counts at count_top[-1 - j]; zero between launches
+  float* gate_out;            // [M]
+  float eps;
+  int C;
+};
+
+// One key tile of the fused gate epilogue for this thread's row m (one warp
+// = 32 consecutive rows). taddr: the warp's lane quadrant of the accumulator.
+// Releases the accumulator to the MMA issuer (acce_bar of the pair leader) as
+// soon as it is read, then publishes the row sums and, in the warp that
+// completes its 32 rows, the gate scalars.
+__device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int m, int M,
+                                          int n_base, int lane, uint32_t leader,
+                                          uint32_t acce_bar) {
+  const bool row_ok = m < M;
+  const ple_bf16_t* hrow = ge.hidden + static_cast<int64_t>(row_ok ? m : 0) * ge.C + n_base;
+  uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // (+0.0f, +0.0f) pairs
+  // h of the next chunk is in flight while this chunk is reduced
+  uint4 hn[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) hn[q] = row_ok ? ldg16(hrow + q * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+  for (int chunk = 0; chunk < BN / 32; ++chunk) {
+    const int c0 = chunk * 32;
+    uint4 hv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hv[q] = hn[q];
+      hn[q] = row_ok && chunk + 1 < BN / 32 ? ldg16(hrow + c0 + 32 + q * 8) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t r[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(c0), r);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 ga = ldg16(ge.gamma_h + n_base + c0 + q * 8);  // warp-uniform
+      const uint4 gb = ldg16(ge.gamma_k + n_base + c0 + q * 8);
+      const uint32_t hw[4] = {hv[q].x, hv[q].y, hv[q].z, hv[q].w};
+      const uint32_t aw[4] = {ga.x, ga.y, ga.z, ga.w};
+      const uint32_t bw[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t kb = pack_bf16x2(r[8 * q + 2 * p], r[8 * q + 2 * p + 1]);
+        const uint64_t k2 = f2(bf_lo(kb), bf_hi(kb));
+        const uint64_t h2 = f2(bf_lo(hw[p]), bf_hi(hw[p]));
+        const uint64_t gg = f2_mul(f2(bf_lo(aw[p]), bf_hi(aw[p])), f2(bf_lo(bw[p]), bf_hi(bw[p])));
+        sh2 = f2_fma(h2, h2, sh2);
+        sk2 = f2_fma(k2, k2, sk2);
+        sd2 = f2_fma(f2_mul(h2, k2), gg, sd2);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar, leader));
+
+  const int kt = n_base / BN;
+  const int n_kt = ge.C / BN;
+  if (row_ok) {
+    float a0, a1, b0, b1, d0, d1;
+    f2_split(sh2, a0, a1);
+    f2_split(sk2, b0, b1);
+    f2_split(sd2, d0, d1);
+    ge.partial[static_cast<int64_t>(kt) * M + m] = make_float4(a0 + a1, b0 + b1, d0 + d1, 0.f);
+  }
+  const int m0 = m - lane;  // first row of the warp
+  if (m0 >= M) return;      // no row of this warp exists: nothing to count
+  __threadfence();          // this lane's partial is visible GPU-wide ...
+  __syncwarp();             // ... before lane 0 counts the warp's delivery
+  unsigned last = 0;
+  unsigned* counter = ge.count_top - 1 - (m0 >> 5);
+  if (lane == 0) last = atomicAdd(counter, 1u) == static_cast<unsigned>(n_kt - 1);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  if (lane == 0) *counter = 0;  // every arrival of this launch is in: ready for the next
+  __threadfence();  // every other warp's partials of these rows are visible
+  if (!row_ok) return;
+  float sh = 0.f, sk = 0.f, sd = 0.f;
+  for (int j = 0; j < n_kt; ++j) {
+    const float4 p = __ldcg(ge.partial + static_cast<int64_t>(j) * M + m);
+    sh += p.x;
+    sk += p.y;
+    sd += p.z;
+  }
+  ge.gate_out[m] = gate_of(sh, sk, sd, ge.C, ge.eps);
+}
+
+template <int PAIRS, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, ple_bf16_t* __restrict__ out,
-                    int M, int N, int K, int32_t* dev_err) {
+                    int M, int N, int K, int32_t* dev_err, const __grid_constant__ GateEpi ge) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -579,6 +683,15 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_after();
       const int m = (u / n_groups) * 2 * BM + static_cast<int>(rank & 1u) * BM + row_in_tile;
       const int n_base = ((u % n_groups) * PAIRS + pidx) * BN;
+      if constexpr (GATE) {
+        if (n_base < ge.C) {
+          gate_tile(ge, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                            static_cast<uint32_t>(acc * ACC_COLS),
+                    m, M, n_base, lane, leader, acce_bar(acc));
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+          continue;
+        }
+      }
       ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
 #pragma unroll 1
       for (int chunk = 0; chunk < BN / 32; ++chunk) {
@@ -653,29 +766,37 @@ ple_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
 }  // namespace
 }  // namespace ple
 
-PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, int64_t num_tokens,
-                                  int32_t emb_dim, int32_t hidden, ple_bf16_t* kv,
-                                  int32_t* dev_err, cudaStream_t stream) {
-  using namespace ple;
+namespace ple {
+namespace {
+
+ple_status check_kv_args(const ple_bf16_t* emb, const ple_bf16_t* w, int64_t num_tokens,
+                         int32_t emb_dim, int32_t hidden, ple_bf16_t* kv, const char* name) {
   if (num_tokens < 0 || emb_dim < 1 || hidden < 1)
-    return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: bad sizes");
+    return fail(PLE_ERR_INVALID_ARG, "%s: bad sizes", name);
   if (emb_dim % 8 != 0 || hidden % 16 != 0)
-    return fail(PLE_ERR_UNSUPPORTED, "ple_kv_proj: emb_dim %% 8 and hidden %% 16 must be 0");
+    return fail(PLE_ERR_UNSUPPORTED, "%s: emb_dim %% 8 and hidden %% 16 must be 0", name);
   if (num_tokens > 0x7fffffffLL - BM || 2LL * hidden > 0x7fffffffLL)
-    return fail(PLE_ERR_UNSUPPORTED, "ple_kv_proj: sizes exceed 32-bit tile indexing");
+    return fail(PLE_ERR_UNSUPPORTED, "%s: sizes exceed 32-bit tile indexing", name);
   if (num_tokens == 0) return PLE_OK;
-  if (!emb || !w || !kv) return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: null pointer");
+  if (!emb || !w || !kv) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(emb) || !aligned16(w) || !aligned16(kv))
-    return fail(PLE_ERR_INVALID_ARG, "ple_kv_proj: buffers must be 16-byte aligned");
-  const int M = static_cast<int>(num_tokens);
-  const int N = 2 * hidden;
-  const int K = emb_dim;
-  // Kernel: the CTA-pair kernel when there are at least two 128-row blocks,
-  // else one CTA per tile. PLE_KVPROJ_MODE = quad | pair | cluster | single
-  // overrides (launch-shape sweeps and tests): quad = two CTA pairs per
-  // cluster sharing A by multicast; cluster = 2-CTA clusters that share the
-  // W tile by TMA multicast, each CTA with its own 1-SM MMAs.
-  enum { kSingle, kCluster, kPair, kQuad } mode = (M > BM) ? kPair : kSingle;
+    return fail(PLE_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", name);
+  return PLE_OK;
+}
+
+// Launch the projection; ge != nullptr selects the fused gate epilogue
+// (CTA-pair kernels only).
+ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, int N,
+                     ple_bf16_t* kv, int32_t* dev_err, cudaStream_t stream, const GateEpi* ge,
+                     const char* name) {
+  // Kernel: the CTA-pair kernel when there are at least two 128-row blocks
+  // (always, with the fused gate), else one CTA per tile.
+  // PLE_KVPROJ_MODE = quad | pair | cluster | single overrides (launch-shape
+  // sweeps and tests): quad = two CTA pairs per cluster sharing A by
+  // multicast; cluster = 2-CTA clusters that share the W tile by TMA
+  // multicast, each CTA with its own 1-SM MMAs. The fused gate takes pair or
+  // quad only.
+  enum { kSingle, kCluster, kPair, kQuad } mode = (M > BM || ge != nullptr) ? kPair : kSingle;
   if (const char* e = getenv("PLE_KVPROJ_MODE")) {
     if (strcmp(e, "single") == 0) mode = kSingle;
     else if (strcmp(e, "cluster") == 0) mode = kCluster;
@@ -684,24 +805,33 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
   }
   if (const char* e = getenv("PLE_KVPROJ_CLUSTER"))
     if (atoi(e) == 1) mode = kSingle;
+  if (ge != nullptr && mode != kQuad) mode = kPair;
+  const bool paired = mode == kPair || mode == kQuad;
   const int cluster = mode == kSingle ? 1 : (mode == kQuad ? 4 : 2);
   CUtensorMap map_a, map_b;
   ple_status s = make_map(&map_a, emb, M, K, mode == kQuad ? BM / 2 : BM);  // A rows a CTA loads
   if (s != PLE_OK) return s;
   s = make_map(&map_b, w, N, K, mode == kSingle ? BN : BN / 2);  // W rows one CTA loads per stage
   if (s != PLE_OK) return s;
-  void (*kernel)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*) =
-      mode == kQuad ? kv_proj_pair_kernel<2>
-                    : mode == kPair ? kv_proj_pair_kernel<1>
-                                    : (mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>);
-  const size_t smem = (mode == kPair || mode == kQuad) ? kPairSmemBytes : kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using PairFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*, GateEpi);
+  using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
+  PairFn pair_fn = nullptr;
+  TileFn tile_fn = nullptr;
+  if (paired) {
+    if (ge != nullptr) pair_fn = mode == kQuad ? kv_proj_pair_kernel<2, true> : kv_proj_pair_kernel<1, true>;
+    else pair_fn = mode == kQuad ? kv_proj_pair_kernel<2, false> : kv_proj_pair_kernel<1, false>;
+  } else {
+    tile_fn = mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>;
+  }
+  const void* fn = paired ? reinterpret_cast<const void*>(pair_fn) : reinterpret_cast<const void*>(tile_fn);
+  const size_t smem = paired ? kPairSmemBytes : kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
-  if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj: smem attribute");
+  if (err != cudaSuccess) return check_cuda(err, "kv projection: smem attribute");
   // work units per cluster: 256 rows x (pairs x 256 columns) for the pair
   // kernels, else 128-row tiles per cluster position
   int units;
-  if (mode == kPair || mode == kQuad) {
+  if (paired) {
     const int pairs = cluster / 2;
     units = ((M + 2 * BM - 1) / (2 * BM)) * (((N + BN - 1) / BN + pairs - 1) / pairs);
   } else {
@@ -723,15 +853,99 @@ PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, in
     qcfg.attrs = qattr;
     qcfg.numAttrs = 1;
     int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, reinterpret_cast<const void*>(kernel), &qcfg) ==
-            cudaSuccess &&
-        active > 0 && active < max_clusters)
+    if (cudaOccupancyMaxActiveClusters(&active, fn, &qcfg) == cudaSuccess && active > 0 &&
+        active < max_clusters)
       max_clusters = active;
     cudaGetLastError();  // a failed query only leaves the SM-count bound
   }
   const int clusters = units < max_clusters ? units : max_clusters;
-  err = launch_kernel(kernel, dim3(static_cast<unsigned>(clusters * cluster)), dim3(kThreads), smem,
-                      stream, static_cast<unsigned>(cluster), map_a, map_b, kv, M, N, K, dev_err);
-  if (err != cudaSuccess) return check_cuda(err, "ple_kv_proj launch");
-  return check_cuda(cudaGetLastError(), "ple_kv_proj launch");
+  const dim3 grid(static_cast<unsigned>(clusters * cluster));
+  if (paired)
+    err = launch_kernel(pair_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
+                        map_a, map_b, kv, M, N, K, dev_err, ge != nullptr ? *ge : GateEpi{});
+  else
+    err = launch_kernel(tile_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
+                        map_a, map_b, kv, M, N, K, dev_err);
+  if (err != cudaSuccess) return check_cuda(err, name);
+  return check_cuda(cudaGetLastError(), name);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of ple_kv_proj_gate, B bytes: the partial sums from the start
+// (16 bytes per token and key tile), the arrival counters at the end,
+// counter j at 4(j+1) bytes below the end. The counters' region is sized by B
+// alone -- room for one counter per 32 of the most tokens any hidden size
+// could fit in B (16 bytes each) -- so every call on the same buffer and
+// byte count finds its counters at the same addresses whatever its token
+// count or hidden size, and no call's partial sums overlap them.
+size_t gate_counter_bytes(size_t B) { return ((B / 16 + 31) / 32) * 4; }
+size_t gate_partial_bytes(int64_t M, int32_t C) {
+  return static_cast<size_t>(C / BN) * static_cast<size_t>(M) * 16;
+}
+size_t gate_ws_bytes(int64_t M, int32_t C) {
+  // the smallest multiple of 256 with room for both parts (a fixed point:
+  // the counters' share grows with B by 1/128 of it)
+  const size_t part = gate_partial_bytes(M, C);
+  size_t B = align256(part);
+  for (;;) {
+    const size_t need = align256(part + gate_counter_bytes(B));
+    if (need <= B) return B;
+    B = need;
+  }
+}
+
+}  // namespace
+}  // namespace ple
+
+PLE_EXPORT ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w, int64_t num_tokens,
+                                  int32_t emb_dim, int32_t hidden, ple_bf16_t* kv,
+                                  int32_t* dev_err, cudaStream_t stream) {
+  using namespace ple;
+  ple_status s = check_kv_args(emb, w, num_tokens, emb_dim, hidden, kv, "ple_kv_proj");
+  if (s != PLE_OK || num_tokens == 0) return s;
+  return launch_kv(emb, w, static_cast<int>(num_tokens), emb_dim, 2 * hidden, kv, dev_err, stream,
+                   nullptr, "ple_kv_proj launch");
+}
+
+PLE_EXPORT size_t ple_kv_proj_gate_workspace(int64_t num_tokens, int32_t hidden) {
+  using namespace ple;
+  if (num_tokens <= 0 || hidden < BN || hidden % BN != 0) return 0;
+  return gate_ws_bytes(num_tokens, hidden);
+}
+
+PLE_EXPORT ple_status ple_kv_proj_gate(const ple_bf16_t* emb, const ple_bf16_t* w,
+                                       int64_t num_tokens, int32_t emb_dim, int32_t hidden,
+                                       const ple_bf16_t* hidden_states, const ple_bf16_t* gamma_h,
+                                       const ple_bf16_t* gamma_k, float eps, ple_bf16_t* kv,
+                                       float* gate_out, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_err, cudaStream_t stream) {
+  using namespace ple;
+  const char* name = "ple_kv_proj_gate";
+  ple_status s = check_kv_args(emb, w, num_tokens, emb_dim, hidden, kv, name);
+  if (s != PLE_OK) return s;
+  if (hidden % BN != 0)
+    return fail(PLE_ERR_UNSUPPORTED, "%s: hidden_size %d must be a multiple of %d", name, hidden, BN);
+  if (num_tokens == 0) return PLE_OK;
+  if (!hidden_states || !gamma_h || !gamma_k || !gate_out || !workspace)
+    return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned16(hidden_states) || !aligned16(gamma_h) || !aligned16(gamma_k) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PLE_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned (workspace 256)", name);
+  if (gate_partial_bytes(num_tokens, hidden) + gate_counter_bytes(workspace_bytes) >
+      workspace_bytes)
+    return fail(PLE_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", name,
+                workspace_bytes, gate_ws_bytes(num_tokens, hidden));
+  GateEpi ge{};
+  ge.hidden = hidden_states;
+  ge.gamma_h = gamma_h;
+  ge.gamma_k = gamma_k;
+  ge.partial = static_cast<float4*>(workspace);
+  ge.count_top = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) +
+                                             (workspace_bytes & ~static_cast<size_t>(3)));
+  ge.gate_out = gate_out;
+  ge.eps = eps;
+  ge.C = hidden;
+  return launch_kv(emb, w, static_cast<int>(num_tokens), emb_dim, 2 * hidden, kv, dev_err, stream,
+                   &ge, "ple_kv_proj_gate launch");
 }

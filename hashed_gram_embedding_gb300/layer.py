@@ -25,7 +25,7 @@ class PLELayer:
 
     def __init__(self, table, row_scale, layer_multipliers, vocab_sizes, offsets,
                  eos_token_id, heads_per_ngram, w_kv, gamma_h, gamma_k, conv_w,
-                 dilation, eps=1e-6, max_ctas=0):
+                 dilation, eps=1e-6, max_ctas=0, fuse_gate=None):
         self.table = table
         self.row_scale = row_scale
         self.mult = [int(m) for m in layer_multipliers]
@@ -44,6 +44,14 @@ class PLELayer:
         self.eps = float(eps)
         self.max_ctas = int(max_ctas)
         self.hidden = w_kv.shape[0] // 2
+        # gate reductions inside the projection (ple_kv_proj_gate +
+        # ple_gated_conv) where the hidden size allows it (a multiple of 256),
+        # else ple_kv_proj + ple_gate_conv
+        can_fuse = self.hidden % 256 == 0
+        self.fuse_gate = can_fuse if fuse_gate is None else bool(fuse_gate)
+        if self.fuse_gate and not can_fuse:
+            raise ValueError(f"fuse_gate needs a hidden size that is a multiple of 256, "
+                             f"not {self.hidden}")
         self._bufs = {}
 
     def buffers(self, num_tokens, device):
@@ -62,6 +70,10 @@ class PLELayer:
                 "kv": torch.empty((num_tokens, 2 * self.hidden), dtype=torch.bfloat16, device=device),
                 "y": torch.empty((num_tokens, self.hidden), dtype=torch.bfloat16, device=device),
                 "gate": torch.empty((num_tokens,), dtype=torch.float32, device=device),
+                # zero-filled once: each completed call leaves it zeroed
+                "gate_ws": (torch.zeros((_lib.ple_kv_proj_gate_workspace(num_tokens, self.hidden),),
+                                        dtype=torch.uint8, device=device)
+                            if self.fuse_gate and num_tokens > 0 else None),
             }
             self._bufs = {key: b}
         return b
@@ -97,20 +109,45 @@ class PLELayer:
     def mix(self, emb, hidden, query_start_loc, out, conv_state=None, conv_state_out=None,
             dev_err=None, stream=None):
         """kv_proj of ``emb`` -> gate with ``hidden`` -> short conv into ``out``."""
-        b = self.buffers(hidden.shape[0], hidden.device)
-        _lib.ple_kv_proj(emb, self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
-        _lib.ple_gate_conv(hidden, b["kv"], self.gamma_h, self.gamma_k, query_start_loc,
-                           self.conv_w, self.dilation, out, eps=self.eps, conv_state=conv_state,
-                           conv_state_out=conv_state_out, gate_out=b["gate"],
-                           dev_err=dev_err, stream=stream)
+        self.project(emb, hidden, dev_err=dev_err, stream=stream)
+        self.convolve(hidden, query_start_loc, out, conv_state=conv_state,
+                      conv_state_out=conv_state_out, dev_err=dev_err, stream=stream)
 
-    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv);
-    # a host table's ordered gather adds three (count, scan, scatter)
+    def project(self, emb, hidden, dev_err=None, stream=None):
+        """The projection of ``emb`` into the layer's kv buffer; fused, it
+        writes v and the gate scalars (k stays on chip)."""
+        b = self.buffers(hidden.shape[0], hidden.device)
+        if self.fuse_gate:
+            _lib.ple_kv_proj_gate(emb, self.w_kv, hidden, self.gamma_h, self.gamma_k, b["kv"],
+                                  b["gate"], b["gate_ws"], eps=self.eps, dev_err=dev_err,
+                                  stream=stream)
+        else:
+            _lib.ple_kv_proj(emb, self.w_kv, b["kv"], dev_err=dev_err, stream=stream)
+
+    def convolve(self, hidden, query_start_loc, out, conv_state=None, conv_state_out=None,
+                 dev_err=None, stream=None):
+        """Gate (unless the projection did its reductions) and short conv of
+        the layer's kv buffer into ``out``."""
+        b = self.buffers(hidden.shape[0], hidden.device)
+        if self.fuse_gate:
+            _lib.ple_gated_conv(b["kv"], b["gate"], query_start_loc, self.conv_w, self.dilation,
+                                out, conv_state=conv_state, conv_state_out=conv_state_out,
+                                dev_err=dev_err, stream=stream)
+        else:
+            _lib.ple_gate_conv(hidden, b["kv"], self.gamma_h, self.gamma_k, query_start_loc,
+                               self.conv_w, self.dilation, out, eps=self.eps,
+                               conv_state=conv_state, conv_state_out=conv_state_out,
+                               gate_out=b["gate"], dev_err=dev_err, stream=stream)
+
+    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv;
+    # fused: ids, gather, kv_proj_gate, conv -- plus a counter memset, not a
+    # kernel); a host table's ordered gather adds three (count, scan, scatter)
     LAUNCHES_PER_FORWARD = 5
     ORDERED_GATHER_EXTRA = 3
 
     def launches_per_forward(self):
-        return self.LAUNCHES_PER_FORWARD + (0 if self.table.is_cuda else self.ORDERED_GATHER_EXTRA)
+        return (self.LAUNCHES_PER_FORWARD - (1 if self.fuse_gate else 0) +
+                (0 if self.table.is_cuda else self.ORDERED_GATHER_EXTRA))
 
 
 class PLEHostPipeline:
@@ -257,16 +294,13 @@ class PLEChain:
             slot = st[i % 2]
             main.wait_event(slot["ready"])
             layer = self.layers[i]
-            b = layer.buffers(input_ids.numel(), device)
-            _lib.ple_kv_proj(slot["emb"], layer.w_kv, b["kv"], dev_err=dev_err, stream=main)
+            layer.project(slot["emb"], hiddens[i], dev_err=dev_err, stream=main)
             slot["free"].record(main)
             if i + 2 < L:  # refill this staging buffer with layer i+2's rows
                 side.wait_event(slot["free"])
                 embed(i + 2, side)
                 slot["ready"].record(side)
-            _lib.ple_gate_conv(hiddens[i], b["kv"], layer.gamma_h, layer.gamma_k,
-                               query_start_loc, layer.conv_w, layer.dilation, outs[i],
-                               eps=layer.eps, conv_state=cs[i], conv_state_out=cso[i],
-                               gate_out=b["gate"], dev_err=dev_err, stream=main)
+            layer.convolve(hiddens[i], query_start_loc, outs[i], conv_state=cs[i],
+                           conv_state_out=cso[i], dev_err=dev_err, stream=main)
         main.wait_stream(side)
         return outs

@@ -10,7 +10,10 @@
  *                  short conv                    -> y   [T][C] bf16
  * with ple_gate / ple_conv as the two halves of ple_gate_conv, and
  * ple_lookup_prefetch / ple_wait for a gather on a side stream (a table in
- * pinned host memory read over UVA, overlapped with other work).
+ * pinned host memory read over UVA, overlapped with other work). The same
+ * layer with the gate's reductions moved into the projection:
+ *   ple_kv_proj_gate  projection + gate scalars -> v half of kv, g [T] f32
+ *   ple_gated_conv    short conv of u = g * v   -> y   [T][C] bf16
  *
  * Sources (page titles abbreviated):
  *   PR#54517 report "[Qwen3.8-Flash-Next] Fuse Qwen4Exp PLE kernels":
@@ -265,6 +268,51 @@ ple_status ple_kv_proj(const ple_bf16_t* emb, const ple_bf16_t* w,
                        ple_bf16_t* kv, int32_t* dev_err, cudaStream_t stream);
 
 /*
+ * ple_kv_proj_gate -- ple_kv_proj and the reduction half of ple_gate in one
+ * kernel: k is never written to memory. Every 256-column key tile of the
+ * projection is rounded to bf16 (the values ple_kv_proj would store) and
+ * reduced with the same 256 channels of hidden into per-token partial sums
+ * of h^2, k^2 and h*k*gamma_h*gamma_k; the tile that completes a token's
+ * sums writes the gate scalar (same formula as ple_gate):
+ *   gate_out[t] = sigmoid( <rms(h_t) * gamma_h, rms(k_t) * gamma_k> / sqrt(C) ).
+ * The value half kv[:, C:2C) is written exactly as ple_kv_proj writes it;
+ * the key half kv[:, 0:C) is left untouched. (The pages fuse the PLE kernels,
+ * PR#54517 report 实现拆解 items 1 and 2, without giving this split; it is
+ * this library's design.)
+ *
+ *   emb, w, kv       as in ple_kv_proj.
+ *   hidden_states    [num_tokens][hidden] bf16, 16-byte aligned.
+ *   gamma_h/gamma_k  [hidden] bf16, 16-byte aligned.
+ *   gate_out         [num_tokens] float32.
+ *   workspace        device scratch of at least
+ *                    ple_kv_proj_gate_workspace(num_tokens, hidden) bytes,
+ *                    256-byte aligned, ZERO-FILLED by the caller before its
+ *                    first use (e.g. one cudaMemset after allocation). Its
+ *                    last bytes hold arrival counters (one per 32 tokens, at
+ *                    places fixed by workspace_bytes alone); a call that
+ *                    completes leaves them zero again, so the workspace is
+ *                    reused with no clearing between calls (and no extra
+ *                    node in a CUDA graph), for any num_tokens and hidden it
+ *                    has room for -- pass the same workspace_bytes every
+ *                    time. After a call that raised a PLE_DEVERR_* bit the
+ *                    counters may be left non-zero: clear the workspace
+ *                    before reusing it. Stale counters never cause an
+ *                    out-of-range access, only wrong gate scalars. Calls in
+ *                    flight at once must not share a workspace.
+ * hidden must be a multiple of 256 (else PLE_ERR_UNSUPPORTED); a smaller
+ * workspace -> PLE_ERR_INVALID_ARG. ple_kv_proj_gate_workspace returns 0 for
+ * sizes the call rejects.
+ */
+size_t ple_kv_proj_gate_workspace(int64_t num_tokens, int32_t hidden);
+ple_status ple_kv_proj_gate(const ple_bf16_t* emb, const ple_bf16_t* w,
+                            int64_t num_tokens, int32_t emb_dim, int32_t hidden,
+                            const ple_bf16_t* hidden_states,
+                            const ple_bf16_t* gamma_h, const ple_bf16_t* gamma_k,
+                            float eps, ple_bf16_t* kv, float* gate_out,
+                            void* workspace, size_t workspace_bytes,
+                            int32_t* dev_err, cudaStream_t stream);
+
+/*
  * ple_gate -- RMSNorm + sigmoid gate ("PLE gating and normalisation",
  * PR#54517 report 实现拆解 item 2; the pages give no formula, this is the
  * reading the library implements):
@@ -326,6 +374,23 @@ ple_status ple_gate_conv(const ple_bf16_t* hidden, const ple_bf16_t* kv,
                          ple_bf16_t* conv_state_out, ple_bf16_t* out,
                          float* gate_out, int32_t* dev_err,
                          cudaStream_t stream);
+
+/*
+ * ple_gated_conv -- the conv pass of ple_gate_conv with the gate scalars
+ * given (from ple_kv_proj_gate or ple_gate): convolves
+ * u_t = bf16_rn(gate[t] * v_t), v_t = kv[t][C:2C), staged in shared memory
+ * only. Same results as ple_conv on u.
+ *   kv    [num_tokens][2 * hidden_size] bf16 (only the v half is read).
+ *   gate  [num_tokens] float32.
+ * Other arguments and limits as in ple_conv.
+ */
+ple_status ple_gated_conv(const ple_bf16_t* kv, const float* gate,
+                          const int32_t* query_start_loc, int32_t num_reqs,
+                          int64_t num_tokens, int32_t hidden_size,
+                          const ple_bf16_t* w, int32_t kernel_size,
+                          int32_t dilation, const ple_bf16_t* conv_state,
+                          ple_bf16_t* conv_state_out, ple_bf16_t* out,
+                          int32_t* dev_err, cudaStream_t stream);
 
 /*
  * ple_host_table_alloc / ple_host_table_free -- host memory for a table read

@@ -143,3 +143,45 @@ def test_host_table_rejects_zero_bytes(lib):
     out = ctypes.c_void_p()
     assert lib.ple_host_table_alloc(0, ctypes.byref(out)) == 1
     assert lib.ple_host_table_free(None, 0) == 0
+
+
+def test_kv_proj_gate_workspace_size(lib):
+    # partial sums: 16 bytes per token and 256-channel key tile; counters at
+    # the end: 4 bytes per 32 of the B/16 tokens a B-byte buffer could ever
+    # hold; B the smallest multiple of 256 with room for both. 8192 x 4096:
+    # 2 MiB of partials; B = 2113792 holds 4129 counters (16516 bytes) and
+    # 2097152 + 16516 <= 2113792 < 2097152 + 16516 + 256.
+    assert lib.ple_kv_proj_gate_workspace(8192, 4096) == 2113792
+    assert lib.ple_kv_proj_gate_workspace(1, 256) == 256      # 16 + 4 bytes
+    assert lib.ple_kv_proj_gate_workspace(33, 768) == 1792    # 1584 + 4 * 4
+    counters = lambda B: (B // 16 + 31) // 32 * 4
+    prev = 0
+    for M in (1, 2, 31, 32, 33, 100, 1000, 4097, 65536):
+        for C in (256, 1024, 4096):
+            B = lib.ple_kv_proj_gate_workspace(M, C)
+            part = C // 256 * M * 16
+            assert B % 256 == 0 and part + counters(B) <= B < part + counters(B) + 256
+        assert B >= prev
+        prev = B
+    for bad in ((100, 264), (100, 0), (0, 256), (-5, 256)):
+        assert lib.ple_kv_proj_gate_workspace(*bad) == 0
+
+
+def test_kv_proj_gate_host_checks(lib):
+    p = ctypes.c_void_p(256)  # never dereferenced: every call fails on the host first
+    ws = lib.ple_kv_proj_gate_workspace(64, 512)
+    # hidden not a multiple of 256
+    assert lib.ple_kv_proj_gate(p, p, 64, 64, 264, p, p, p, 1e-6, p, p, p, 1 << 20, None,
+                                None) == 2
+    # room for the partial sums but not the counters, then misaligned
+    assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, p, p, 2 * 64 * 16, None,
+                                None) == 1
+    assert b"workspace" in lib.ple_last_error()
+    assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, p, ctypes.c_void_p(272),
+                                ws, None, None) == 1
+    # gate_out missing
+    assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, None, p, ws, None,
+                                None) == 1
+    # no tokens: nothing to do
+    assert lib.ple_kv_proj_gate(None, None, 0, 64, 512, None, None, None, 1e-6, None, None,
+                                None, 0, None, None) == 0

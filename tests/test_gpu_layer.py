@@ -1,8 +1,10 @@
 """GPU parity of the whole per-layer chain (PLELayer.forward: ids -> gather ->
-kv_proj -> gate + conv, four libple launches) against the oracle's
-layer_forward: the tiny workload with a bf16 and with an fp8 table (every
-token), the decode workload's carry-over outputs, and the 8k prefill at full
-size (sampled tokens with their conv windows)."""
+kv_proj -> gate + conv; by default the projection does the gate's reductions,
+ple_kv_proj_gate + ple_gated_conv, and fuse_gate=False runs ple_kv_proj +
+ple_gate_conv) against the oracle's layer_forward: the tiny workload with a
+bf16 and with an fp8 table (every token, both projections), the decode
+workload's carry-over outputs, and the 8k prefill at full size (sampled
+tokens with their conv windows)."""
 
 import numpy as np
 import pytest
@@ -17,19 +19,21 @@ from _helpers import CHAIN_ATOL_FRAC, assert_close, bits, dev_err_word, tiny_cas
 pytestmark = pytest.mark.gpu
 
 
-def build_layer(w, host, dense, table, row_scale, layer=0):
+def build_layer(w, host, dense, table, row_scale, layer=0, fuse_gate=None):
     return PLELayer(table, row_scale, host["multipliers"][layer], host["V"], host["O"],
                     w.eos_token_id, w.heads_per_ngram, dense["w_kv"], dense["gamma_h"],
-                    dense["gamma_k"], dense["conv_w"], w.dilation)
+                    dense["gamma_k"], dense["conv_w"], w.dilation, fuse_gate=fuse_gate)
 
 
+@pytest.mark.parametrize("fuse_gate", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_tiny_chain_every_token(dtype):
+def test_tiny_chain_every_token(dtype, fuse_gate):
     w = wl.scaled(wl.WORKLOADS["tiny"], table_dtype=dtype)
     w, host, dense, table, row_scale = tiny_case(w)
     d_dense = {k: v.cuda() for k, v in dense.items()}
     layer = build_layer(w, host, d_dense, table.cuda(),
-                        None if row_scale is None else row_scale.cuda())
+                        None if row_scale is None else row_scale.cuda(), fuse_gate=fuse_gate)
+    assert layer.fuse_gate == fuse_gate
     err = dev_err_word()
     qsl = torch.from_numpy(host["query_start_loc"]).cuda()
     y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), qsl, d_dense["hidden"],
@@ -47,7 +51,9 @@ def test_tiny_chain_every_token(dtype):
     assert np.array_equal(b["ids"].cpu().numpy(), ref["ids"])
     assert np.array_equal(bits(b["emb"]), ref["emb"])
     tol = 1e-2 if dtype == "bf16" else 3e-2
-    assert_close(bits(b["kv"]), ref["kv"], rtol=tol, atol_frac=tol, what="kv")
+    C = w.hidden
+    cols = slice(C, 2 * C) if fuse_gate else slice(0, 2 * C)  # fused: k is never stored
+    assert_close(bits(b["kv"])[:, cols], ref["kv"][:, cols], rtol=tol, atol_frac=tol, what="kv")
     assert_close(bits(y), ref["y"], rtol=tol, atol_frac=max(tol, CHAIN_ATOL_FRAC), what="y")
 
 
