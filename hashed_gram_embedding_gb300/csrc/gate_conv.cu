@@ -19,8 +19,8 @@
 //     (4 bytes per token); ple_gate's variant also writes u = bf16(g*v).
 //   pass 2 (conv_kernel<GATED=true>): a CTA takes a tile of tokens and a
 //     256-channel slice, stages its dilation window -- u of the tile and of
-//     the (K-1)*d tokens before it -- in shared memory as float32 (values
-//     already rounded to bf16), then each lane owns 8 channels (taps in
+//     the (K-1)*d tokens before it -- in shared memory as bf16 (u is a bf16
+//     value; 512 bytes per row), then each lane owns 8 channels (taps in
 //     registers as float pairs) and each warp walks tokens. A token whose
 //     taps all lie inside its own request (every token but the first (K-1)*d
 //     of a request) reads the K window rows and accumulates with packed
@@ -258,12 +258,11 @@ struct ConvArgs {
 
 constexpr int kConvSlice = 256;  // channels per CTA (8 per lane)
 
-// Shared memory of one conv CTA: the float32 window (rows x 1 KB; a row is
-// two halves of 32 float4 so that a warp's 16-byte accesses are contiguous:
-// lane l holds channels 8l..8l+3 in half 0 and 8l+4..8l+7 in half 1), then
-// per-token and per-request integers.
+// Shared memory of one conv CTA: the bf16 window (rows x 512 bytes: lane l
+// holds channels 8l..8l+7 as one 16-byte vector, so a warp's accesses to a
+// row are contiguous), then per-token and per-request integers.
 struct ConvSmem {
-  float4* win;
+  uint4* win;
   int* tok_start;  // [tile] start of the token's request, relative to t0
   int* tok_req;    // [tile] the token's request
   int* req_s;      // [tile] requests overlapping the tile: start, end (rel.), index
@@ -274,13 +273,13 @@ struct ConvSmem {
 };
 
 __host__ __device__ inline size_t conv_smem_bytes(int tile, int W) {
-  return static_cast<size_t>(tile + W) * kConvSlice * 4 + static_cast<size_t>(tile) * 6 * 4 + 16;
+  return static_cast<size_t>(tile + W) * kConvSlice * 2 + static_cast<size_t>(tile) * 6 * 4 + 16;
 }
 
 __device__ __forceinline__ ConvSmem conv_smem(uint8_t* base, int tile, int W) {
   ConvSmem s;
-  s.win = reinterpret_cast<float4*>(base);
-  int* p = reinterpret_cast<int*>(base + static_cast<size_t>(tile + W) * kConvSlice * 4);
+  s.win = reinterpret_cast<uint4*>(base);
+  int* p = reinterpret_cast<int*>(base + static_cast<size_t>(tile + W) * kConvSlice * 2);
   s.tok_start = p;
   s.tok_req = p + tile;
   s.req_s = p + 2 * tile;
@@ -399,23 +398,19 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
       for (int q = 0; q < kBatch; ++q) {
         const int i = first + q * kWarps;
         if (active && i < rows) {
-          float f[8];
           if constexpr (GATED) {
             const uint64_t gg = f2(gv[q], gv[q]);
-            const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            uint32_t u4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
               float lo, hi;
-              f2_split(f2_mul(f2(bf_lo(w4[p]), bf_hi(w4[p])), gg), lo, hi);
-              const uint32_t u = pack2(lo, hi);  // round to bf16
-              f[2 * p] = bf_lo(u);
-              f[2 * p + 1] = bf_hi(u);
+              f2_split(f2_mul(f2(bf_lo(u4[p]), bf_hi(u4[p])), gg), lo, hi);
+              u4[p] = pack2(lo, hi);  // u = bf16(g * v)
             }
+            s.win[i * 32 + lane] = make_uint4(u4[0], u4[1], u4[2], u4[3]);
           } else {
-            unpack8(v[q], f);
+            s.win[i * 32 + lane] = v[q];
           }
-          s.win[(i * 2) * 32 + lane] = make_float4(f[0], f[1], f[2], f[3]);
-          s.win[(i * 2 + 1) * 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
         }
       }
     };
@@ -497,7 +492,14 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
       for (int p = 0; p < 4; ++p) wt[i][p] = f2(wf[i][2 * p], wf[i][2 * p + 1]);
   }
 
-  const ulonglong2* win2 = reinterpret_cast<const ulonglong2*>(s.win);
+  // window row -> its 8 channels as four float pairs
+  auto row_pairs = [&](int row, uint64_t (&x)[4]) {
+    const uint4 b = s.win[row * 32 + lane];
+    x[0] = f2(bf_lo(b.x), bf_hi(b.x));
+    x[1] = f2(bf_lo(b.y), bf_hi(b.y));
+    x[2] = f2(bf_lo(b.z), bf_hi(b.z));
+    x[3] = f2(bf_lo(b.w), bf_hi(b.w));
+  };
   if (all_fast) {
     // no branches: two tokens per iteration so that one's shared-memory
     // loads overlap the other's FMAs
@@ -510,12 +512,10 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
 #pragma unroll
         for (int z = 0; z < 2; ++z) {
           const int row = (z == 0 || two ? tt + z * kWarps : tt) + i * dil;
-          const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
-          const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
-          acc[z][0] = f2_fma(wt[i][0], x0.x, acc[z][0]);
-          acc[z][1] = f2_fma(wt[i][1], x0.y, acc[z][1]);
-          acc[z][2] = f2_fma(wt[i][2], x1.x, acc[z][2]);
-          acc[z][3] = f2_fma(wt[i][3], x1.y, acc[z][3]);
+          uint64_t x[4];
+          row_pairs(row, x);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) acc[z][p] = f2_fma(wt[i][p], x[p], acc[z][p]);
         }
       }
 #pragma unroll
@@ -538,13 +538,10 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
       // all taps inside the request: window rows tt, tt + d, ..., tt + W
 #pragma unroll
       for (int i = 0; i < K; ++i) {
-        const int row = tt + i * dil;
-        const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
-        const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
-        acc[0] = f2_fma(wt[i][0], x0.x, acc[0]);
-        acc[1] = f2_fma(wt[i][1], x0.y, acc[1]);
-        acc[2] = f2_fma(wt[i][2], x1.x, acc[2]);
-        acc[3] = f2_fma(wt[i][3], x1.y, acc[3]);
+        uint64_t x[4];
+        row_pairs(tt + i * dil, x);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc[p] = f2_fma(wt[i][p], x[p], acc[p]);
       }
     } else {
       // a request's first W tokens: taps before its start come from the
@@ -563,10 +560,7 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
         const int j = tt - (K - 1 - i) * dil;
         uint64_t x[4];
         if (j >= st) {
-          const int row = tt + i * dil;
-          const ulonglong2 x0 = win2[(row * 2) * 32 + lane];
-          const ulonglong2 x1 = win2[(row * 2 + 1) * 32 + lane];
-          x[0] = x0.x; x[1] = x0.y; x[2] = x1.x; x[3] = x1.y;
+          row_pairs(tt + i * dil, x);
         } else {
           x[0] = f2(bf_lo(hist[i].x), bf_hi(hist[i].x));
           x[1] = f2(bf_lo(hist[i].y), bf_hi(hist[i].y));
@@ -597,9 +591,7 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
     const int sj = s.req_e[kk] - W + jj;  // token of state row jj, relative to t0
     uint4 u = make_uint4(0, 0, 0, 0);
     if (sj >= st) {
-      const float4 x0 = s.win[((sj + W) * 2) * 32 + lane];
-      const float4 x1 = s.win[((sj + W) * 2 + 1) * 32 + lane];
-      u = make_uint4(pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(x1.x, x1.y), pack2(x1.z, x1.w));
+      u = s.win[(sj + W) * 32 + lane];
     } else if (a.state != nullptr) {
       u = ldg16(a.state + (static_cast<int64_t>(r) * W + (W + sj - st)) * C + c);
     }
