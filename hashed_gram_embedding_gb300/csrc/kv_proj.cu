@@ -360,9 +360,13 @@ constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
 constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
 constexpr int kEpilogueWarps = kEpilogueThreads / 32;
-// kind::f16 instruction descriptor for M = 256 (two SMs) x N = 256.
+// kind::f16 instruction descriptors for M = 256 (two SMs) x N = 256, and
+// x N = 128 (the half tiles of the last round).
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
                                 (uint32_t(BN >> 3) << 17) | (uint32_t((2 * BM) >> 4) << 24);
+constexpr uint32_t kIdescPairHalf = (1u << 4) | (1u << 7) | (1u << 10) |
+                                    (uint32_t((BN / 2) >> 3) << 17) |
+                                    (uint32_t((2 * BM) >> 4) << 24);
 
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -396,12 +400,12 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const C
 }
 
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                               uint32_t accumulate) {
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdescPair), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -425,28 +429,27 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
-// PAIRS = CTA pairs per cluster. PAIRS = 2: the two pairs of a 4-CTA cluster
-// take adjacent 256-column tiles of the same 256 rows; CTAs 0/2 (and 1/3)
-// need the same 128 rows of A, so each loads 64 of them and multicasts them
-// to both, cutting each SM's A traffic in half; a stage may then be refilled
-// only after both pairs' MMAs released it.
 // Fused gate reductions (ple_kv_proj_gate). The key half of kv is never
-// stored: the epilogue of a key tile (columns [n, n+256) of [0, C)) rounds
-// each accumulator to bf16 -- the value ple_kv_proj would store -- reads the
-// same 256 channels of the token's hidden row and adds, per row,
-// sum h^2, sum k^2 and sum h*k*gamma_h*gamma_k (the three sums of the gate's
-// RMSNorm-and-dot, which split over channel blocks). Each sum triple goes to
-// partial[key tile][row]; the epilogue warp that delivers the last key tile
-// of its 32 rows (a per-32-row arrival counter) adds the C/256 triples in
-// key-tile order, writes g = sigmoid(...) for those rows and sets the
+// stored: the epilogue of a key tile (columns [n, n+256) or, for a half
+// tile, [n, n+128) of [0, C)) rounds each accumulator to bf16 -- the value
+// ple_kv_proj would store -- reads the same channels of the token's hidden
+// row and adds, per row and 128-channel block, sum h^2, sum k^2 and
+// sum h*k*gamma_h*gamma_k (the three sums of the gate's RMSNorm-and-dot,
+// which split over channel blocks). Each block's triple goes to
+// partial[block][row] -- the same sums in the same order whether the block
+// came from a full or a half tile; the epilogue warp that delivers the last
+// blocks of its 32 rows (a per-32-row arrival counter) adds the C/128 triples
+// in block order, writes g = sigmoid(...) for those rows and sets the
 // counter back to zero, so a launch that completes leaves every counter as
-// it found it (zero) and the next launch needs no clearing pass. Value
-// tiles are stored as in ple_kv_proj.
+// it found it (zero) and the next launch needs no clearing pass. Value tiles
+// are stored as in ple_kv_proj.
+constexpr int kGateBlock = 128;  // channels per partial-sum block
+
 struct GateEpi {
   const ple_bf16_t* hidden;   // [M][C]
   const ple_bf16_t* gamma_h;  // [C]
   const ple_bf16_t* gamma_k;  // [C]
-  float4* partial;            // [C/256][M]: (sum h^2, sum k^2, sum h*k*gh*gk, 0)
+  float4* partial;            // [C/128][M]: (sum h^2, sum k^2, sum h*k*gh*gk, 0)
   unsigned* count_top;        // one past the arrival counters: group j (rows 32j..32j+31)
                               // counts at count_top[-1 - j]; zero between launches
   float* gate_out;            // [M]
@@ -454,29 +457,33 @@ struct GateEpi {
   int C;
 };
 
-// One key tile of the fused gate epilogue for this thread's row m (one warp
-// = 32 consecutive rows). taddr: the warp's lane quadrant of the accumulator.
-// Releases the accumulator to the MMA issuer (acce_bar of the pair leader) as
-// soon as it is read, then publishes the row sums and, in the warp that
-// completes its 32 rows, the gate scalars.
+// One key tile (cols = 256 or 128 channels from n_base) of the fused gate
+// epilogue for this thread's row m (one warp = 32 consecutive rows). taddr:
+// the warp's lane quadrant of the accumulator. Releases the accumulator to
+// the MMA issuer (acce_bar of the pair leader) as soon as it is read, then
+// publishes the row sums and, in the warp that completes its 32 rows, the
+// gate scalars.
 __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int m, int M,
-                                          int n_base, int lane, uint32_t leader,
+                                          int n_base, int cols, int lane, uint32_t leader,
                                           uint32_t acce_bar) {
   const bool row_ok = m < M;
   const ple_bf16_t* hrow = ge.hidden + static_cast<int64_t>(row_ok ? m : 0) * ge.C + n_base;
+  const int n_chunks = cols / 32;
   uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // (+0.0f, +0.0f) pairs
+  float4 part0 = make_float4(0.f, 0.f, 0.f, 0.f), part1 = part0;
   // h of the next chunk is in flight while this chunk is reduced
   uint4 hn[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) hn[q] = row_ok ? ldg16(hrow + q * 8) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-  for (int chunk = 0; chunk < BN / 32; ++chunk) {
+  for (int chunk = 0; chunk < n_chunks; ++chunk) {
     const int c0 = chunk * 32;
     uint4 hv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       hv[q] = hn[q];
-      hn[q] = row_ok && chunk + 1 < BN / 32 ? ldg16(hrow + c0 + 32 + q * 8) : make_uint4(0, 0, 0, 0);
+      hn[q] = row_ok && chunk + 1 < n_chunks ? ldg16(hrow + c0 + 32 + q * 8)
+                                             : make_uint4(0, 0, 0, 0);
     }
     uint32_t r[32];
     tmem_ld32(taddr + static_cast<uint32_t>(c0), r);
@@ -498,34 +505,43 @@ __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int
         sd2 = f2_fma(f2_mul(h2, k2), gg, sd2);
       }
     }
+    if ((chunk & 3) == 3) {  // a 128-channel block is complete
+      float a0, a1, b0, b1, d0, d1;
+      f2_split(sh2, a0, a1);
+      f2_split(sk2, b0, b1);
+      f2_split(sd2, d0, d1);
+      const float4 pb = make_float4(a0 + a1, b0 + b1, d0 + d1, 0.f);
+      if (chunk == 3) part0 = pb; else part1 = pb;
+      sh2 = sk2 = sd2 = 0;
+    }
   }
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar, leader));
 
-  const int kt = n_base / BN;
-  const int n_kt = ge.C / BN;
+  const int blk0 = n_base / kGateBlock;
+  const int nb = cols / kGateBlock;
+  const int n_blk = ge.C / kGateBlock;
   if (row_ok) {
-    float a0, a1, b0, b1, d0, d1;
-    f2_split(sh2, a0, a1);
-    f2_split(sk2, b0, b1);
-    f2_split(sd2, d0, d1);
-    ge.partial[static_cast<int64_t>(kt) * M + m] = make_float4(a0 + a1, b0 + b1, d0 + d1, 0.f);
+    ge.partial[static_cast<int64_t>(blk0) * M + m] = part0;
+    if (nb == 2) ge.partial[static_cast<int64_t>(blk0 + 1) * M + m] = part1;
   }
   const int m0 = m - lane;  // first row of the warp
   if (m0 >= M) return;      // no row of this warp exists: nothing to count
-  __threadfence();          // this lane's partial is visible GPU-wide ...
+  __threadfence();          // this lane's partials are visible GPU-wide ...
   __syncwarp();             // ... before lane 0 counts the warp's delivery
-  unsigned last = 0;
   unsigned* counter = ge.count_top - 1 - (m0 >> 5);
-  if (lane == 0) last = atomicAdd(counter, 1u) == static_cast<unsigned>(n_kt - 1);
+  unsigned last = 0;
+  if (lane == 0)
+    last = atomicAdd(counter, static_cast<unsigned>(nb)) + static_cast<unsigned>(nb) ==
+           static_cast<unsigned>(n_blk);
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   if (lane == 0) *counter = 0;  // every arrival of this launch is in: ready for the next
   __threadfence();  // every other warp's partials of these rows are visible
   if (!row_ok) return;
   float sh = 0.f, sk = 0.f, sd = 0.f;
-  for (int j = 0; j < n_kt; ++j) {
+  for (int j = 0; j < n_blk; ++j) {
     const float4 p = __ldcg(ge.partial + static_cast<int64_t>(j) * M + m);
     sh += p.x;
     sk += p.y;
@@ -534,11 +550,48 @@ __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int
   ge.gate_out[m] = gate_of(sh, sk, sd, ge.C, ge.eps);
 }
 
+// A work unit of the pair kernel: 256 rows from m_base, PAIRS x 256 columns
+// (this pair's from n_base), or -- units >= full_units, PAIRS == 1 only --
+// one 128-column half of a 256 x 256 tile. Splitting the last round's tiles
+// in halves lets twice as many CTA pairs share it when it would otherwise
+// leave more than half of them idle.
+struct PairUnit {
+  int m_base;
+  int n_base;
+  int cols;  // 256 or 128
+};
+
+template <int PAIRS>
+__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups, int pidx) {
+  PairUnit t;
+  if (PAIRS == 1 && u >= full_units) {
+    const int h = u - full_units;
+    const int v = full_units + (h >> 1);
+    t.m_base = (v / n_groups) * 2 * BM;
+    t.n_base = (v % n_groups) * BN + (h & 1) * (BN / 2);
+    t.cols = BN / 2;
+  } else {
+    t.m_base = (u / n_groups) * 2 * BM;
+    t.n_base = ((u % n_groups) * PAIRS + pidx) * BN;
+    t.cols = BN;
+  }
+  return t;
+}
+
+// PAIRS = CTA pairs per cluster. PAIRS = 2: the two pairs of a 4-CTA cluster
+// take adjacent 256-column tiles of the same 256 rows; CTAs 0/2 (and 1/3)
+// need the same 128 rows of A, so each loads 64 of them and multicasts them
+// to both, cutting each SM's A traffic in half; a stage may then be refilled
+// only after both pairs' MMAs released it.
+// Units [0, full_units) are full tiles; with PAIRS == 1 the units past them
+// are half tiles (2 per remaining tile; map_b_half loads 64 W rows per CTA).
 template <int PAIRS, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_b, ple_bf16_t* __restrict__ out,
-                    int M, int N, int K, int32_t* dev_err, const __grid_constant__ GateEpi ge) {
+                    const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_b_half, ple_bf16_t* __restrict__ out,
+                    int M, int N, int K, int full_units, int32_t* dev_err,
+                    const __grid_constant__ GateEpi ge) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -564,7 +617,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   const int n_tiles = (N + BN - 1) / BN;
   const int n_groups = (n_tiles + PAIRS - 1) / PAIRS;
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
-  const int num_units = m_tiles * n_groups;  // (256 rows, PAIRS x 256 columns) per cluster
+  const int base_units = m_tiles * n_groups;  // (256 rows, PAIRS x 256 columns) per cluster
+  const int num_units = PAIRS == 1 ? full_units + 2 * (base_units - full_units) : base_units;
   const int num_kb = (K + BK - 1) / BK;
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << (2 * PAIRS)) - 1);
   const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pidx));
@@ -602,19 +656,26 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     // ---------------- TMA producer (both CTAs) ----------------
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    if (num_units > base_units)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_half))
+                   : "memory");
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
     const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
     for (int u = cl; ok && u < num_units; u += num_cl) {
-      const int m0 = (u / n_groups) * 2 * BM + q * BM;
-      const int n0 = ((u % n_groups) * PAIRS + pidx) * BN + q * (BN / 2);
+      const PairUnit t = pair_unit<PAIRS>(u, full_units, n_groups, pidx);
+      const bool half = t.cols != BN;
+      const int m0 = t.m_base + q * BM;
+      const int n0 = t.n_base + q * (t.cols / 2);
+      // both CTAs' A rows and W rows of one stage
+      const uint32_t stage_tx = 2u * (P_A_STAGE + (half ? P_B_STAGE / 2 : P_B_STAGE));
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t leader_full = map_to_rank(full_bar(stage), leader);
         if (rank == leader) {
-          mbar_arrive_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+          mbar_arrive_expect_tx(full_bar(stage), stage_tx);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         }
@@ -626,7 +687,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                                      &map_a, leader_full, kb * BK, m0 + pidx * (BM / 2),
                                      static_cast<uint16_t>((1u << q) | (1u << (q + 2))));
         }
-        tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE), &map_b, leader_full, kb * BK, n0);
+        tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE), half ? &map_b_half : &map_b,
+                         leader_full, kb * BK, n0);
         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -643,6 +705,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = cl; ok && u < num_units; u += num_cl) {
+        const uint32_t idesc =
+            pair_unit<PAIRS>(u, full_units, n_groups, pidx).cols == BN ? kIdescPair : kIdescPairHalf;
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -654,7 +718,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
-            umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(empty_bar(stage), kClusterMask);  // frees the stage everywhere it fed
           if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
@@ -681,24 +745,23 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
         break;
       }
       tc_fence_after();
-      const int m = (u / n_groups) * 2 * BM + static_cast<int>(rank & 1u) * BM + row_in_tile;
-      const int n_base = ((u % n_groups) * PAIRS + pidx) * BN;
+      const PairUnit t = pair_unit<PAIRS>(u, full_units, n_groups, pidx);
+      const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
+      const int n_base = t.n_base;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc * ACC_COLS);
       if constexpr (GATE) {
         if (n_base < ge.C) {
-          gate_tile(ge, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                            static_cast<uint32_t>(acc * ACC_COLS),
-                    m, M, n_base, lane, leader, acce_bar(acc));
+          gate_tile(ge, taddr, m, M, n_base, t.cols, lane, leader, acce_bar(acc));
           if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
           continue;
         }
       }
       ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
 #pragma unroll 1
-      for (int chunk = 0; chunk < BN / 32; ++chunk) {
+      for (int chunk = 0; chunk < t.cols / 32; ++chunk) {
         uint32_t r[32];
-        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                      static_cast<uint32_t>(acc * ACC_COLS + chunk * 32),
-                  r);
+        tmem_ld32(taddr + static_cast<uint32_t>(chunk * 32), r);
         const int n = n_base + chunk * 32;
         if (m < M && n < N) {
           uint4* dst = reinterpret_cast<uint4*>(row_out + n);
@@ -808,12 +871,19 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   if (ge != nullptr && mode != kQuad) mode = kPair;
   const bool paired = mode == kPair || mode == kQuad;
   const int cluster = mode == kSingle ? 1 : (mode == kQuad ? 4 : 2);
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_b, map_b_half;
   ple_status s = make_map(&map_a, emb, M, K, mode == kQuad ? BM / 2 : BM);  // A rows a CTA loads
   if (s != PLE_OK) return s;
   s = make_map(&map_b, w, N, K, mode == kSingle ? BN : BN / 2);  // W rows one CTA loads per stage
   if (s != PLE_OK) return s;
-  using PairFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*, GateEpi);
+  if (mode == kPair) {
+    s = make_map(&map_b_half, w, N, K, BN / 4);  // a half tile's W rows per CTA
+    if (s != PLE_OK) return s;
+  } else {
+    map_b_half = map_b;  // not read
+  }
+  using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int,
+                          int32_t*, GateEpi);
   using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
   PairFn pair_fn = nullptr;
   TileFn tile_fn = nullptr;
@@ -858,11 +928,27 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
       max_clusters = active;
     cudaGetLastError();  // a failed query only leaves the SM-count bound
   }
+  // Last-round split (CTA pairs, one pair per cluster): when the tiles of
+  // the last round would keep at most half of the clusters busy, each of
+  // them becomes two 128-column halves, so the round ends in about half the
+  // time. PLE_KVPROJ_SPLIT=0 turns it off (launch-shape sweeps and tests).
+  int full_units = units;
+  if (mode == kPair) {
+    const int rem = units % max_clusters;
+    bool split = rem > 0 && 2 * rem <= max_clusters;
+    if (const char* e = getenv("PLE_KVPROJ_SPLIT"))
+      if (atoi(e) == 0) split = false;
+    if (split) {
+      full_units = units - rem;
+      units = full_units + 2 * rem;
+    }
+  }
   const int clusters = units < max_clusters ? units : max_clusters;
   const dim3 grid(static_cast<unsigned>(clusters * cluster));
   if (paired)
     err = launch_kernel(pair_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
-                        map_a, map_b, kv, M, N, K, dev_err, ge != nullptr ? *ge : GateEpi{});
+                        map_a, map_b, map_b_half, kv, M, N, K, full_units, dev_err,
+                        ge != nullptr ? *ge : GateEpi{});
   else
     err = launch_kernel(tile_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
                         map_a, map_b, kv, M, N, K, dev_err);
@@ -873,7 +959,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace of ple_kv_proj_gate, B bytes: the partial sums from the start
-// (16 bytes per token and key tile), the arrival counters at the end,
+// (16 bytes per token and 128-channel key block), the arrival counters at the end,
 // counter j at 4(j+1) bytes below the end. The counters' region is sized by B
 // alone -- room for one counter per 32 of the most tokens any hidden size
 // could fit in B (16 bytes each) -- so every call on the same buffer and
@@ -881,7 +967,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // count or hidden size, and no call's partial sums overlap them.
 size_t gate_counter_bytes(size_t B) { return ((B / 16 + 31) / 32) * 4; }
 size_t gate_partial_bytes(int64_t M, int32_t C) {
-  return static_cast<size_t>(C / BN) * static_cast<size_t>(M) * 16;
+  return static_cast<size_t>(C / kGateBlock) * static_cast<size_t>(M) * 16;
 }
 size_t gate_ws_bytes(int64_t M, int32_t C) {
   // the smallest multiple of 256 with room for both parts (a fixed point:

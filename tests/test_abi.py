@@ -146,20 +146,20 @@ def test_host_table_rejects_zero_bytes(lib):
 
 
 def test_kv_proj_gate_workspace_size(lib):
-    # partial sums: 16 bytes per token and 256-channel key tile; counters at
+    # partial sums: 16 bytes per token and 128-channel key block; counters at
     # the end: 4 bytes per 32 of the B/16 tokens a B-byte buffer could ever
     # hold; B the smallest multiple of 256 with room for both. 8192 x 4096:
-    # 2 MiB of partials; B = 2113792 holds 4129 counters (16516 bytes) and
-    # 2097152 + 16516 <= 2113792 < 2097152 + 16516 + 256.
-    assert lib.ple_kv_proj_gate_workspace(8192, 4096) == 2113792
-    assert lib.ple_kv_proj_gate_workspace(1, 256) == 256      # 16 + 4 bytes
-    assert lib.ple_kv_proj_gate_workspace(33, 768) == 1792    # 1584 + 4 * 4
+    # 4 MiB of partials; B = 4227584 holds 8257 counters (33028 bytes) and
+    # 4194304 + 33028 <= 4227584 < 4194304 + 33028 + 256.
+    assert lib.ple_kv_proj_gate_workspace(8192, 4096) == 4227584
+    assert lib.ple_kv_proj_gate_workspace(1, 256) == 256      # 32 + 4 bytes
+    assert lib.ple_kv_proj_gate_workspace(33, 768) == 3328    # 3168 + 7 * 4
     counters = lambda B: (B // 16 + 31) // 32 * 4
     prev = 0
     for M in (1, 2, 31, 32, 33, 100, 1000, 4097, 65536):
         for C in (256, 1024, 4096):
             B = lib.ple_kv_proj_gate_workspace(M, C)
-            part = C // 256 * M * 16
+            part = C // 128 * M * 16
             assert B % 256 == 0 and part + counters(B) <= B < part + counters(B) + 256
         assert B >= prev
         prev = B
@@ -174,7 +174,7 @@ def test_kv_proj_gate_host_checks(lib):
     assert lib.ple_kv_proj_gate(p, p, 64, 64, 264, p, p, p, 1e-6, p, p, p, 1 << 20, None,
                                 None) == 2
     # room for the partial sums but not the counters, then misaligned
-    assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, p, p, 2 * 64 * 16, None,
+    assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, p, p, 4 * 64 * 16, None,
                                 None) == 1
     assert b"workspace" in lib.ple_last_error()
     assert lib.ple_kv_proj_gate(p, p, 64, 64, 512, p, p, p, 1e-6, p, p, ctypes.c_void_p(272),

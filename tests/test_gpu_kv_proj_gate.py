@@ -69,10 +69,14 @@ CASES = [(512, 512, 1024), (1, 64, 256), (129, 200, 256), (300, 2048, 4096), (10
          (257, 72, 768), (33, 64, 512)]
 
 
-@pytest.mark.parametrize("mode", ["pair", "quad"])
+@pytest.mark.parametrize("mode", ["pair", "pair-nosplit", "quad"])
 @pytest.mark.parametrize("M,E,C", CASES)
 def test_kv_proj_gate_matches_oracle_and_unfused(M, E, C, mode, monkeypatch):
-    monkeypatch.setenv("PLE_KVPROJ_MODE", mode)
+    """Both CTA-pair kernels; "pair" splits the last round's tiles into
+    128-column halves where that shortens it (every case here but 300 x 4096
+    and 1000 x 512), "pair-nosplit" never does."""
+    monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
+    monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
     emb, w, h, gh, gk = (t.cuda() for t in inputs(M, E, C, M + C))
     kv, g = run_fused(emb, w, h, gh, gk)
     # value half: the unfused projection's bits; key half: never written
@@ -85,6 +89,10 @@ def test_kv_proj_gate_matches_oracle_and_unfused(M, E, C, mode, monkeypatch):
     assert torch.equal(kv[:, C:].view(torch.int16), kv_ref[:, C:].view(torch.int16))
     assert torch.isnan(kv[:, :C].float()).all()
     assert float((g - g_ref).abs().max()) < 1e-5
+    # the gate scalars do not depend on how the tiles were split
+    monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0")
+    _, g_nosplit = run_fused(emb, w, h, gh, gk)
+    assert torch.equal(g.view(torch.int32), g_nosplit.view(torch.int32))
     # against the oracle: kv in float64, the gate on the oracle's kv
     ref_kv = oracle_kv_proj(bits(emb), bits(w))
     assert_close(bits(kv[:, C:]), ref_kv[:, C:], what=f"v {M}x{E}x{2 * C}")
