@@ -28,6 +28,7 @@ PLE_DEVERR_TIMEOUT = 4
 
 PLE_BF16 = 0
 PLE_FP8_E4M3 = 1
+PLE_FP8_E4M3_TENSOR = 2
 PLE_HBM = 0
 PLE_HOST_UVA = 1
 PLE_HOST_TABLE_REGISTER = 1
@@ -137,8 +138,16 @@ def ple_ngram_ids(input_ids, query_start_loc, ngram_context, layer_multipliers,
         int(heads_per_ngram), _ptr(out), _ptr(ngram_context_out), _ptr(dev_err), _stream(stream)))
 
 
+def _fp8_dtype(row_scale):
+    """bf16 without a scale; one scale value -> the whole-table-scale fp8
+    type (a one-row table means the same either way); else per-row fp8."""
+    if row_scale is None:
+        return PLE_BF16
+    return PLE_FP8_E4M3_TENSOR if row_scale.numel() == 1 else PLE_FP8_E4M3
+
+
 def _lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc):
-    dtype = PLE_FP8_E4M3 if row_scale is not None else PLE_BF16
+    dtype = _fp8_dtype(row_scale)
     if loc is None:
         loc = PLE_HBM if table.is_cuda else PLE_HOST_UVA
     T, H = ids.shape
@@ -148,15 +157,15 @@ def _lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc):
 
 def ple_lookup(ids, table, out, row_scale=None, max_ctas=0, dev_err=None, loc=None, stream=None):
     """ids int64 [T, H]; table [rows, D] bf16 (or uint8 e4m3 codes with
-    row_scale float32 [rows]), on the device or pinned on the host; out bf16
-    [T, H*D]."""
+    row_scale float32 [rows], or [1] for one scale for the whole table), on
+    the device or pinned on the host; out bf16 [T, H*D]."""
     return _check("ple_lookup", lib().ple_lookup(
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
 
 
 def ple_lookup_ordered_workspace(num_tokens, num_heads, table, row_scale=None):
     """Bytes of device workspace ple_lookup_ordered needs."""
-    dtype = PLE_FP8_E4M3 if row_scale is not None else PLE_BF16
+    dtype = _fp8_dtype(row_scale)
     return int(lib().ple_lookup_ordered_workspace(int(num_tokens), int(num_heads),
                                                   table.shape[0], table.shape[1], dtype))
 

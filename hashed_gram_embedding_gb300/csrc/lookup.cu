@@ -113,7 +113,7 @@ template <int VPR>
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ perm,
                   uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
-                  const float* __restrict__ row_scale, int64_t table_rows,
+                  const float* __restrict__ row_scale, int scale_stride, int64_t table_rows,
                   uint4* __restrict__ out, int32_t* dev_err) {
   pdl_wait();
   // The sorted walk over a host table does not let the next kernel launch
@@ -144,7 +144,7 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
         const int64_t id = __ldg(ids + row_out);
         if (static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
           c[u] = load_row_vec(table + id * vpr + k);
-          s[u] = __ldg(row_scale + id);
+          s[u] = __ldg(row_scale + id * scale_stride);  // stride 0: one scale for the table
         } else {
           set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // the row is written as zeros
         }
@@ -396,7 +396,7 @@ ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_he
     return fail(PLE_ERR_INVALID_ARG, "%s: bad sizes (T=%lld H=%d D=%d rows=%lld)", name,
                 static_cast<long long>(num_tokens), num_heads, head_dim,
                 static_cast<long long>(table_rows));
-  if (dtype != PLE_BF16 && dtype != PLE_FP8_E4M3)
+  if (dtype != PLE_BF16 && dtype != PLE_FP8_E4M3 && dtype != PLE_FP8_E4M3_TENSOR)
     return fail(PLE_ERR_INVALID_ARG, "%s: unknown dtype %d", name, static_cast<int>(dtype));
   if (loc != PLE_HBM && loc != PLE_HOST_UVA)
     return fail(PLE_ERR_INVALID_ARG, "%s: unknown table location %d", name, static_cast<int>(loc));
@@ -409,7 +409,7 @@ ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_he
     return PLE_OK;
   }
   if (!ids || !table || !out) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
-  if (dtype == PLE_FP8_E4M3 && !row_scale)
+  if (dtype != PLE_BF16 && !row_scale)
     return fail(PLE_ERR_INVALID_ARG, "%s: fp8 table needs row_scale", name);
   if (!aligned16(table) || !aligned16(out))
     return fail(PLE_ERR_INVALID_ARG, "%s: table and out must be 16-byte aligned", name);
@@ -464,9 +464,9 @@ ple_status launch_gather_kernel(const Gather& g, const uint32_t* perm, cudaStrea
       err = launch_kernel_pdl(perm == nullptr, gather_bf16_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.table_rows, g.out, g.dev_err);
   } else {
     if (vpr == 8)
-      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<8>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.dtype == PLE_FP8_E4M3 ? 1 : 0, g.table_rows, g.out, g.dev_err);
     else
-      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.table_rows, g.out, g.dev_err);
+      err = launch_kernel_pdl(perm == nullptr, gather_fp8_kernel<0>, dim3(g.grid), dim3(kThreads), 0, stream, 1, g.ids, perm, g.total_vecs, vpr, g.table, g.row_scale, g.dtype == PLE_FP8_E4M3 ? 1 : 0, g.table_rows, g.out, g.dev_err);
   }
   if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
@@ -577,7 +577,8 @@ PLE_EXPORT size_t ple_lookup_ordered_workspace(int64_t num_tokens, int32_t num_h
                                                int64_t table_rows, int32_t head_dim,
                                                ple_dtype dtype) {
   if (num_tokens < 0 || num_heads < 1 || head_dim < 1 || table_rows < 0) return 0;
-  const int elem = (dtype == PLE_FP8_E4M3) ? 1 : 2;
+  if (dtype != PLE_BF16 && dtype != PLE_FP8_E4M3 && dtype != PLE_FP8_E4M3_TENSOR) return 0;
+  const int elem = (dtype == PLE_BF16) ? 2 : 1;
   const int row_bytes = static_cast<int>((static_cast<int64_t>(head_dim) * elem + 15) / 16 * 16);
   return ple::order_plan(num_tokens * num_heads, table_rows, row_bytes).bytes;
 }

@@ -81,7 +81,10 @@ typedef enum {
 #define PLE_DEVERR_QSL 2      /* query_start_loc not 0-based / non-decreasing / <= T */
 #define PLE_DEVERR_TIMEOUT 4  /* a kernel pipeline wait exceeded its limit */
 
-typedef enum { PLE_BF16 = 0, PLE_FP8_E4M3 = 1 } ple_dtype;
+/* Table element types: bf16 rows; fp8 e4m3 rows with a float32 scale per row;
+ * fp8 e4m3 rows with one float32 scale for the whole table (the pages'
+ * single weight_scale). */
+typedef enum { PLE_BF16 = 0, PLE_FP8_E4M3 = 1, PLE_FP8_E4M3_TENSOR = 2 } ple_dtype;
 typedef enum { PLE_HBM = 0, PLE_HOST_UVA = 1 } ple_table_loc;
 
 /* Limits of ple_ngram_ids (constants travel in the kernel's parameter block). */
@@ -135,13 +138,14 @@ ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens,
                          int32_t* dev_err, cudaStream_t stream);
 
 /*
- * ple_lookup -- multi-head row gather, bf16 or fp8 e4m3 with a per-row scale.
- * (PR#54371 report: device / pinned-host embedding backends, F.embedding;
- * BF16 / FP8 weight methods. PR#53899 page: FP8 table with weight_scale.)
+ * ple_lookup -- multi-head row gather, bf16 or fp8 e4m3 with a per-row or a
+ * whole-table scale. (PR#54371 report: device / pinned-host embedding
+ * backends, F.embedding; BF16 / FP8 weight methods. PR#53899 page: FP8 table
+ * with one weight_scale.)
  *
- *   out[t][h*D + c] = table[ids[t][h]][c]                         (bf16)
- *   out[t][h*D + c] = bf16_rn(float(e4m3(table[id][c])) * row_scale[id])  (fp8)
- * A global scale is row_scale filled with one value.
+ *   out[t][h*D + c] = table[ids[t][h]][c]                                 (bf16)
+ *   out[t][h*D + c] = bf16_rn(float(e4m3(table[id][c])) * row_scale[id])  (PLE_FP8_E4M3)
+ *   out[t][h*D + c] = bf16_rn(float(e4m3(table[id][c])) * row_scale[0])   (PLE_FP8_E4M3_TENSOR)
  *
  *   ids          [num_tokens][num_heads] int64 device (offsets already added).
  *   table        [table_rows][head_dim] (bf16 or uint8 e4m3 codes). In
@@ -149,7 +153,8 @@ ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens,
  *                registered host memory (checked with cudaPointerGetAttributes,
  *                else PLE_ERR_INVALID_ARG), read in place over the host link.
  *                16-byte aligned.
- *   row_scale    [table_rows] float32 device, fp8 only (NULL for bf16).
+ *   row_scale    float32 device: [table_rows] for PLE_FP8_E4M3, [1] for
+ *                PLE_FP8_E4M3_TENSOR; NULL for bf16.
  *   out          [num_tokens][num_heads * head_dim] bf16 device, 16-byte aligned.
  *   max_ctas     0 = a full-GPU grid; > 0 caps the grid (e.g. half the SMs
  *                for a side-stream prefetch that overlaps other kernels).

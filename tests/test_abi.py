@@ -126,6 +126,10 @@ def test_ordered_gather_workspace_size(lib):
     assert lib.ple_lookup_ordered_workspace(100, 16, 67110742, 128, 1) == \
         2 * up(4 * buckets) + up(4 * 1600)
     assert lib.ple_lookup_ordered_workspace(-1, 16, 10, 128, 0) == 0
+    # one scale for the whole fp8 table: the same 128-byte rows as per-row fp8
+    assert lib.ple_lookup_ordered_workspace(100, 16, 67110742, 128, 2) == \
+        lib.ple_lookup_ordered_workspace(100, 16, 67110742, 128, 1)
+    assert lib.ple_lookup_ordered_workspace(100, 16, 67110742, 128, 3) == 0  # no such dtype
 
 
 def test_wait_rejects_null_event(lib):

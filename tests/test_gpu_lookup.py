@@ -301,25 +301,43 @@ def test_ordered_gather_rejects_small_workspace():
         _lib.ple_lookup_ordered(ids, table, out, ws)
 
 
-def test_fp8_global_scale():
-    """The pages' fp8 table carries one weight_scale for the whole table: a
-    row_scale holding that one value everywhere gives exactly the global-
-    scale dequantisation, e4m3 code times the scale, rounded to bf16."""
+@pytest.mark.parametrize("ordered", [False, True])
+def test_fp8_global_scale(ordered):
+    """The pages' fp8 table carries one weight_scale for the whole table
+    (PLE_FP8_E4M3_TENSOR: a one-value row_scale): e4m3 code times that scale,
+    rounded to bf16 -- the oracle's per-row formula with every row's scale
+    equal, bit for bit, and the same bits as a per-row scale array holding
+    the value everywhere. Plain gather and table-order gather (host table)."""
     rng = np.random.default_rng(21)
     rows, D, T, H = 3000, 128, 64, 16
     codes = rng.integers(0, 0x7E, size=(rows, D), dtype=np.uint8)  # finite codes
     weight_scale = np.float32(0.0123)
     scale = np.full((rows,), weight_scale, dtype=np.float32)
     ids = rng.integers(0, rows, size=(T, H))
-    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
-    _lib.ple_lookup(torch.from_numpy(ids).cuda(), torch.from_numpy(codes).cuda(), out,
-                    row_scale=torch.from_numpy(scale).cuda())
+    d_ids = torch.from_numpy(ids).cuda()
+    if ordered:
+        table = torch.from_numpy(codes).pin_memory()
+    else:
+        table = torch.from_numpy(codes).cuda()
+    one = torch.tensor([weight_scale], dtype=torch.float32, device="cuda")
+    full = torch.from_numpy(scale).cuda()
+    outs = []
+    for row_scale in (one, full):
+        out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+        if ordered:
+            ws = torch.empty((_lib.ple_lookup_ordered_workspace(T, H, table, row_scale),),
+                             dtype=torch.uint8, device="cuda")
+            _lib.ple_lookup_ordered(d_ids, table, out, ws, row_scale=row_scale)
+        else:
+            _lib.ple_lookup(d_ids, table, out, row_scale=row_scale)
+        outs.append(out)
     torch.cuda.synchronize()
-    assert np.array_equal(bits(out), lookup_fp8(ids, codes, scale))
+    assert np.array_equal(bits(outs[0]), lookup_fp8(ids, codes, scale))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     # the same numbers from torch's own e4m3 decode times the one scale
     dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float() * float(weight_scale)
     want = dec[torch.from_numpy(ids.reshape(-1))].reshape(T, H * D).to(torch.bfloat16)
-    assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+    assert torch.equal(outs[0].cpu().view(torch.int16), want.view(torch.int16))
 
 
 @pytest.mark.parametrize("kind", ["shared", "file"])
