@@ -40,11 +40,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NUM_SETS = 4
 # the oracle's stages (cpu_baseline and the reference arm)
 ORACLE_STAGES = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
-# timed kernels per step: the projection with the gate reductions fused, then
-# the gated conv (hidden sizes that are multiples of 256), else the
-# projection, then gate_conv's two passes (gate reduction, gated conv)
-KERNELS_FUSED = ("ngram_ids", "lookup", "kv_proj_gate", "conv")
-KERNELS_UNFUSED = ("ngram_ids", "lookup", "kv_proj", "gate_conv")
+# Timed kernels per step. The ids and the gather: one kernel (ngram_lookup)
+# for a table in HBM, else the ids, then the table-order gather. The dense
+# part: the projection with the gate's reductions, then the gated conv (hidden
+# sizes that are multiples of 256), else the projection, then gate_conv's two
+# passes (gate reduction, gated conv).
 
 
 # ---------------------------------------------------------------------------
@@ -176,6 +176,7 @@ def ncu_traffic(kernel):
     summary = os.path.join(ROOT, "profiles", f"{kernel}_prefill8k.md")
     src = os.path.join(ROOT, "hashed_gram_embedding_gb300", "csrc",
                        {"kv_proj": "kv_proj.cu", "kv_proj_gate": "kv_proj.cu",
+                        "ngram_lookup": "lookup.cu",
                         "lookup": "lookup.cu", "gate_conv": "gate_conv.cu",
                         "conv": "gate_conv.cu", "ngram_ids": "ngram_ids.cu"}[kernel])
     try:
@@ -208,6 +209,8 @@ def algorithmic_work(w):
               else ("hbm", T * (H * 8 + row_read + H * D * 2)))
     return {
         "ngram_ids": ("hbm", T * 4 + T * H * 8 + (w.num_reqs + 1) * 4),
+        # token ids in, rows read, rows and ids written
+        "ngram_lookup": ("hbm", T * (4 + row_read + H * D * 2 + H * 8)),
         "lookup": lookup,
         "kv_proj": ("tensor", 2.0 * T * E * 2 * C),
         "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2)),
@@ -264,7 +267,9 @@ def run_ours(args):
     sets = make_sets(torch, w, device, num_sets)
     T, H, C = w.num_tokens, w.num_heads, w.hidden
     fuse = C % 256 == 0 and not args.no_fuse_gate
-    KERNELS = KERNELS_FUSED if fuse else KERNELS_UNFUSED
+    fuse_ids = w.table_loc == "hbm" and not args.no_fuse_ids
+    KERNELS = ((("ngram_lookup",) if fuse_ids else ("ngram_ids", "lookup")) +
+               (("kv_proj_gate", "conv") if fuse else ("kv_proj", "gate_conv")))
     gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
                            device=device) if fuse else None)
     ids = torch.empty((T, H), dtype=torch.int64, device=device)
@@ -292,33 +297,37 @@ def run_ours(args):
     def step(s, ev=None, st=None):
         st = stream if st is None else st
         p = sets[s % num_sets]
+        ctx_o = ctx_out if w.decode else None
+        stages = []
+        if fuse_ids:
+            stages.append(lambda: _lib.ple_ngram_lookup(
+                p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"], p["host"]["O"],
+                w.eos_token_id, w.heads_per_ngram, p["table"], emb, row_scale=p["row_scale"],
+                ids_out=ids, ngram_context_out=ctx_o, dev_err=err, stream=st))
+        else:
+            stages.append(lambda: _lib.ple_ngram_ids(
+                p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"], p["host"]["O"],
+                w.eos_token_id, w.heads_per_ngram, ids, ctx_o, err, st))
+            stages.append(lambda: gather(p, st))
+        if fuse:
+            stages.append(lambda: _lib.ple_kv_proj_gate(
+                emb, p["w_kv"], p["hidden"], p["gamma_h"], p["gamma_k"], kv, gate, gate_ws,
+                dev_err=err, stream=st))
+            stages.append(lambda: _lib.ple_gated_conv(
+                kv, gate, p["qsl"], p["conv_w"], w.dilation, y, conv_state=p.get("conv_state"),
+                conv_state_out=st_out, dev_err=err, stream=st))
+        else:
+            stages.append(lambda: _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=st))
+            stages.append(lambda: _lib.ple_gate_conv(
+                p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"], w.dilation, y,
+                conv_state=p.get("conv_state"), conv_state_out=st_out, gate_out=gate, dev_err=err,
+                stream=st))
         if ev is not None:
             ev[0].record(st)
-        _lib.ple_ngram_ids(p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"],
-                           p["host"]["O"], w.eos_token_id, w.heads_per_ngram, ids,
-                           ctx_out if w.decode else None, err, st)
-        if ev is not None:
-            ev[1].record(st)
-        gather(p, st)
-        if ev is not None:
-            ev[2].record(st)
-        if fuse:
-            _lib.ple_kv_proj_gate(emb, p["w_kv"], p["hidden"], p["gamma_h"], p["gamma_k"], kv,
-                                  gate, gate_ws, dev_err=err, stream=st)
-        else:
-            _lib.ple_kv_proj(emb, p["w_kv"], kv, dev_err=err, stream=st)
-        if ev is not None:
-            ev[3].record(st)
-        if fuse:
-            _lib.ple_gated_conv(kv, gate, p["qsl"], p["conv_w"], w.dilation, y,
-                                conv_state=p.get("conv_state"), conv_state_out=st_out,
-                                dev_err=err, stream=st)
-        else:
-            _lib.ple_gate_conv(p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"],
-                               p["conv_w"], w.dilation, y, conv_state=p.get("conv_state"),
-                               conv_state_out=st_out, gate_out=gate, dev_err=err, stream=st)
-        if ev is not None:
-            ev[4].record(st)
+        for j, run in enumerate(stages):
+            run()
+            if ev is not None:
+                ev[j + 1].record(st)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -329,14 +338,15 @@ def run_ours(args):
         raise RuntimeError(f"device error word {int(err.item())} during warm-up")
 
     # ---- eager steps with events between the kernels (per-kernel times) ----
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
+              for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
         step(i, events[i])
     torch.cuda.synchronize()
     barrier()
-    eager_ms = events[0][0].elapsed_time(events[-1][4])
+    eager_ms = events[0][0].elapsed_time(events[-1][-1])
     per_kernel = {k: [] for k in KERNELS}
     for ev in events:
         for j, k in enumerate(KERNELS):
@@ -378,7 +388,7 @@ def run_ours(args):
     p0 = sets[0]
     layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
                      w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
-                     p0["conv_w"], w.dilation, fuse_gate=fuse)
+                     p0["conv_w"], w.dilation, fuse_gate=fuse, fuse_ids=fuse_ids)
     depth = 2
     pipe = PLEHostPipeline(layer, T, w.num_reqs, device, depth=depth)
     h_ids = torch.from_numpy(p0["host"]["input_ids"]).pin_memory()
@@ -454,17 +464,18 @@ def run_ours(args):
                    "head_dim": w.head_dim, "table_rows": int(sets[0]["table"].shape[0]),
                    "table_loc": w.table_loc, "table_dtype": w.table_dtype, "hidden": C,
                    "conv_kernel": w.conv_k, "dilation": w.dilation,
-                   "fuse_gate": fuse, "layer_sets": num_sets,
+                   "fuse_gate": fuse, "fuse_ids": fuse_ids, "layer_sets": num_sets,
                    "l2": f"inputs rotate over {num_sets} layer sets (> 129 MB L2 per rotation); no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
         "kernels": kernels,
         "gather": ({"gbs": kernels["lookup"]["achieved"], "link_gbs": link_gbs,
                     "frac_link": kernels["lookup"]["frac"]} if w.table_loc == "host" else
-                   {"gbs": kernels["lookup"]["achieved"], "frac_hbm": kernels["lookup"]["frac"]}),
+                   {"gbs": kernels[KERNELS[0 if fuse_ids else 1]]["achieved"],
+                    "frac_hbm": kernels[KERNELS[0 if fuse_ids else 1]]["frac"]}),
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": launches_per_step(w, fuse) * args.steps,
+        "gpu_launches": launches_per_step(w, fuse, fuse_ids) * args.steps,
         "clocks": clocks,
     }
     if w.table_loc == "host":
@@ -481,13 +492,13 @@ def run_ours(args):
     return line
 
 
-def launches_per_step(w, fuse):
-    """libple kernels one step launches: ids, gather, then the fused
-    projection and the gated conv (4), or the projection and the gate and
-    conv passes (5); a host table's ordered gather adds its count, scan and
-    scatter kernels. (The fused projection's counter clear is a memset, not
-    a kernel.)"""
-    return (4 if fuse else 5) + (3 if w.table_loc == "host" else 0)
+def launches_per_step(w, fuse, fuse_ids):
+    """libple kernels one step launches: the n-gram lookup (1; or ids and
+    gather, 2; a host table's ordered gather adds its count, scan and scatter
+    kernels), then the fused projection and the gated conv (2), or the
+    projection and the gate and conv passes (3)."""
+    embed = 1 if fuse_ids else 2 + (3 if w.table_loc == "host" else 0)
+    return embed + (2 if fuse else 3)
 
 
 def capture_graphs(torch, step, num_sets, device):
@@ -742,6 +753,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fuse-ids", action="store_true",
+                    help="time ple_ngram_ids + ple_lookup instead of ple_ngram_lookup (HBM tables)")
     ap.add_argument("--no-fuse-gate", action="store_true",
                     help="time ple_kv_proj + ple_gate_conv instead of the fused projection")
     ap.add_argument("--layer-sets", type=int, default=0,

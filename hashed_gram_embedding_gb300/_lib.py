@@ -42,6 +42,8 @@ _I64P = ctypes.POINTER(ctypes.c_int64)
 SIGNATURES = {
     "ple_ngram_ids": [_P, _I64, _P, _I32, _P, _I32, _I64P, _I64P, _I64P, _I32, _I32, _P, _P, _P, _P],
     "ple_lookup": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32, _P, _P],
+    "ple_ngram_lookup": [_P, _I64, _P, _I32, _P, _I32, _I64P, _I64P, _I64P, _I32, _I32, _P, _I64,
+                         _I32, ctypes.c_int, _P, ctypes.c_int, _P, _P, _P, _I32, _P, _P],
     "ple_lookup_prefetch": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32,
                             _P, _P, _P],
     "ple_lookup_ordered_workspace": [_I64, _I32, _I64, _I32, ctypes.c_int],
@@ -161,6 +163,26 @@ def ple_lookup(ids, table, out, row_scale=None, max_ctas=0, dev_err=None, loc=No
     the device or pinned on the host; out bf16 [T, H*D]."""
     return _check("ple_lookup", lib().ple_lookup(
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
+
+
+def ple_ngram_lookup(input_ids, query_start_loc, ngram_context, layer_multipliers, vocab_sizes,
+                     offsets, eos_token_id, heads_per_ngram, table, out, row_scale=None,
+                     ids_out=None, ngram_context_out=None, max_ctas=0, dev_err=None, loc=None,
+                     stream=None):
+    """ple_ngram_ids + ple_lookup in one kernel: out bf16 [T, H*D] gets the
+    rows of the hashed ids (ids_out int64 [T, H] also gets the ids when
+    given). Other arguments as in ple_ngram_ids and ple_lookup."""
+    mult, mult_p = _i64_array(layer_multipliers)
+    V, V_p = _i64_array(vocab_sizes)
+    O, O_p = _i64_array(offsets)
+    if loc is None:
+        loc = PLE_HBM if table.is_cuda else PLE_HOST_UVA
+    return _check("ple_ngram_lookup", lib().ple_ngram_lookup(
+        _ptr(input_ids), input_ids.numel(), _ptr(query_start_loc), query_start_loc.numel() - 1,
+        _ptr(ngram_context), len(mult) - 1, mult_p, V_p, O_p, int(eos_token_id),
+        int(heads_per_ngram), _ptr(table), table.shape[0], table.shape[1], _fp8_dtype(row_scale),
+        _ptr(row_scale), loc, _ptr(out), _ptr(ids_out), _ptr(ngram_context_out), int(max_ctas),
+        _ptr(dev_err), _stream(stream)))
 
 
 def ple_lookup_ordered_workspace(num_tokens, num_heads, table, row_scale=None):

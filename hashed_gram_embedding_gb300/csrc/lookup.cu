@@ -20,6 +20,7 @@
 // the next kernel (kv_proj) finds the rows in L2. ple_lookup_ordered walks
 // the items in table order (see the page-ordered walk below).
 #include "common.cuh"
+#include "ngram_hash.cuh"
 
 #include <cuda_fp8.h>
 
@@ -157,6 +158,144 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
         dequant16(c[u], s[u], &lo, &hi);
         out[2 * static_cast<size_t>(o[u])] = lo;
         out[2 * static_cast<size_t>(o[u]) + 1] = hi;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// ple_ngram_lookup: the n-gram ids and the row gather in one kernel. Each work
+// item (one 16-byte table vector of one (token, head) row) hashes its row's
+// id itself (ngram_id, request boundaries staged in shared memory, the few
+// token loads hitting L1) where the plain gather would load it, so the ids
+// never make a round trip through memory; the first vector of each row also
+// stores the id when ids_out is given. The walk is the unsorted gather's.
+// ---------------------------------------------------------------------------
+struct NgramArgs {
+  const int32_t* input_ids;
+  int64_t num_tokens;
+  const int32_t* qsl;
+  int num_reqs;
+  const int32_t* ctx;
+  int ctx_len;
+  int eos;
+  int heads_per_ngram;
+  int num_heads;
+  int32_t* ctx_out;
+  int64_t* ids_out;
+};
+
+template <int VPR, bool FP8>
+__global__ void __launch_bounds__(kThreads, 2048 / kThreads)  // the plain gather's full grid
+ngram_gather_kernel(const __grid_constant__ NgramArgs na, const __grid_constant__ NgramConsts k,
+                    uint32_t total_vecs, int vpr_rt, const uint4* __restrict__ table,
+                    const float* __restrict__ row_scale, int scale_stride, int64_t table_rows,
+                    uint4* __restrict__ out, int32_t* dev_err) {
+  __shared__ int32_t qsl_s[kStagedBounds];
+  __shared__ NgramHeadsSmem hs;
+  const int R = na.num_reqs;
+  const bool staged = R < kStagedBounds;
+  stage_ngram_heads(k, na.num_heads, hs);
+  pdl_wait();
+  pdl_trigger();
+  if (staged)
+    for (int r = threadIdx.x; r <= R; r += kThreads) qsl_s[r] = __ldg(na.qsl + r);
+  __syncthreads();
+  const uint32_t gid = blockIdx.x * kThreads + threadIdx.x;
+  const uint32_t gsize = gridDim.x * kThreads;
+  for (uint32_t i = gid; i <= static_cast<uint32_t>(R); i += gsize)
+    check_qsl(na.qsl, R, na.num_tokens, i, dev_err);
+  if (na.ctx_out != nullptr)
+    for (uint32_t i = gid; i < static_cast<uint32_t>(R) * static_cast<uint32_t>(na.ctx_len);
+         i += gsize)
+      ngram_carry(na.input_ids, na.num_tokens, na.qsl, R, na.ctx, na.ctx_len, na.eos, i,
+                  na.ctx_out);
+
+  const int vpr = VPR ? VPR : vpr_rt;
+  const uint32_t H = static_cast<uint32_t>(na.num_heads);
+  const int lane = threadIdx.x & 31;
+  // The vpr lanes that read one row share its id: with at least kUnroll of
+  // them (and rows aligned to the warp), lane j of a row's group hashes the
+  // group's row of unrolled step j and passes it on by shuffle; else every
+  // lane hashes its own rows.
+  const bool shared_ids = vpr >= kUnroll && 32 % vpr == 0;
+  auto hash_row = [&](uint32_t p) -> int64_t {  // id of (token, head) row p
+    const uint32_t t32 = p / H;
+    const int h = static_cast<int>(p - t32 * H);
+    const int64_t t = t32;
+    // last request whose start is <= t, clamped (as ple_ngram_ids)
+    int r;
+    int64_t start;
+    if (staged) {
+      int lo = 0, hi = R + 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(qsl_s[mid]) <= t) lo = mid + 1; else hi = mid;
+      }
+      r = lo - 1 < 0 ? 0 : (lo - 1 >= R ? R - 1 : lo - 1);
+      start = qsl_s[r];
+    } else {
+      r = find_request(na.qsl, R, t);
+      start = __ldg(na.qsl + r);
+    }
+    return ngram_id(na.input_ids, na.ctx, na.ctx_len, na.eos, t, t - start, r, h,
+                    na.heads_per_ngram, k, hs);
+  };
+  // warp-uniform loop (the shuffles need every lane)
+  for (uint32_t wbase = gid - lane; wbase < total_vecs; wbase += gsize * kUnroll) {
+    const uint32_t base = wbase + lane;
+    int64_t id[kUnroll];
+    if (shared_ids) {
+      const int g = lane % vpr;  // my place in my row group
+      int64_t mine = -1;
+      if (g < kUnroll) {
+        const uint32_t idx = base - g + g * gsize;  // first vector of step g's row
+        if (idx < total_vecs) mine = hash_row(idx / vpr);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) id[u] = __shfl_sync(0xffffffffu, mine, lane - g + u);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t idx = base + u * gsize;
+        id[u] = idx < total_vecs ? hash_row(idx / vpr) : -1;
+      }
+    }
+    if (na.ids_out != nullptr) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t idx = base + u * gsize;
+        if (idx < total_vecs && idx % vpr == 0) na.ids_out[idx / vpr] = id[u];
+      }
+    }
+    uint4 c[kUnroll];
+    float sc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {  // their table vectors, all in flight
+      const uint32_t idx = base + u * gsize;
+      c[u] = make_uint4(0, 0, 0, 0);
+      sc[u] = 0.f;
+      if (idx < total_vecs) {
+        const uint32_t p = idx / vpr;
+        if (static_cast<uint64_t>(id[u]) < static_cast<uint64_t>(table_rows)) {
+          c[u] = load_row_vec(table + id[u] * vpr + (idx - p * vpr));
+          if constexpr (FP8) sc[u] = __ldg(row_scale + id[u] * scale_stride);
+        } else {
+          set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // the row is written as zeros
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t idx = base + u * gsize;
+      if (idx >= total_vecs) continue;
+      if constexpr (FP8) {
+        uint4 lo, hi;
+        dequant16(c[u], sc[u], &lo, &hi);
+        out[2 * static_cast<size_t>(idx)] = lo;
+        out[2 * static_cast<size_t>(idx) + 1] = hi;
+      } else {
+        out[idx] = c[u];
       }
     }
   }
@@ -390,7 +529,7 @@ ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_he
                           const void* table, int64_t table_rows, int32_t head_dim,
                           ple_dtype dtype, const float* row_scale, ple_table_loc loc,
                           ple_bf16_t* out, int32_t max_ctas, int32_t* dev_err,
-                          const char* name, Gather* g, bool* empty) {
+                          const char* name, Gather* g, bool* empty, bool ids_in = true) {
   *empty = false;
   if (num_tokens < 0 || num_heads < 1 || head_dim < 1 || table_rows < 0)
     return fail(PLE_ERR_INVALID_ARG, "%s: bad sizes (T=%lld H=%d D=%d rows=%lld)", name,
@@ -408,7 +547,8 @@ ple_status prepare_gather(const int64_t* ids, int64_t num_tokens, int32_t num_he
     *empty = true;
     return PLE_OK;
   }
-  if (!ids || !table || !out) return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
+  if ((ids_in && !ids) || !table || !out)
+    return fail(PLE_ERR_INVALID_ARG, "%s: null pointer", name);
   if (dtype != PLE_BF16 && !row_scale)
     return fail(PLE_ERR_INVALID_ARG, "%s: fp8 table needs row_scale", name);
   if (!aligned16(table) || !aligned16(out))
@@ -674,4 +814,88 @@ PLE_EXPORT ple_status ple_lookup_ordered_static(const int64_t* ids, int64_t num_
   s = static_scratch(&scratch);
   if (s != PLE_OK) return s;
   return launch_ordered(g, scratch, plan, stream, name);
+}
+
+PLE_EXPORT ple_status ple_ngram_lookup(const int32_t* input_ids, int64_t num_tokens,
+                                       const int32_t* query_start_loc, int32_t num_reqs,
+                                       const int32_t* ngram_context, int32_t ctx_len,
+                                       const int64_t* layer_multipliers,
+                                       const int64_t* vocab_sizes, const int64_t* offsets,
+                                       int32_t eos_token_id, int32_t heads_per_ngram,
+                                       const void* table, int64_t table_rows, int32_t head_dim,
+                                       ple_dtype dtype, const float* row_scale, ple_table_loc loc,
+                                       ple_bf16_t* out, int64_t* ids_out,
+                                       int32_t* ngram_context_out, int32_t max_ctas,
+                                       int32_t* dev_err, cudaStream_t stream) {
+  using namespace ple;
+  const char* name = "ple_ngram_lookup";
+  if (num_tokens < 0) return fail(PLE_ERR_INVALID_ARG, "%s: num_tokens < 0", name);
+  NgramConsts k{};
+  int num_heads = 0;
+  ple_status s = make_ngram_consts(ctx_len, heads_per_ngram, layer_multipliers, vocab_sizes,
+                                   offsets, &k, &num_heads, name);
+  if (s != PLE_OK) return s;
+  if (num_reqs < 0 || (num_reqs == 0 && num_tokens > 0))
+    return fail(PLE_ERR_INVALID_ARG, "%s: num_reqs must be >= 1 when there are tokens", name);
+  for (int h = 0; h < num_heads; ++h)
+    if (offsets[h] < 0 || offsets[h] > table_rows - vocab_sizes[h])
+      return fail(PLE_ERR_INVALID_ARG, "%s: head %d's partition [%lld, %lld + %lld) is outside "
+                  "the table's %lld rows", name, h, static_cast<long long>(offsets[h]),
+                  static_cast<long long>(offsets[h]), static_cast<long long>(vocab_sizes[h]),
+                  static_cast<long long>(table_rows));
+  if (ngram_context_out && ngram_context &&
+      overlaps(ngram_context, sizeof(int32_t) * num_reqs * ctx_len, ngram_context_out,
+               sizeof(int32_t) * num_reqs * ctx_len))
+    return fail(PLE_ERR_INVALID_ARG, "%s: ngram_context_out overlaps ngram_context", name);
+  Gather g;
+  bool empty = false;
+  s = prepare_gather(ids_out, num_tokens, num_heads, table, table_rows, head_dim, dtype,
+                     row_scale, loc, out, max_ctas, dev_err, name, &g, &empty,
+                     /*ids_in=*/false);
+  if (s != PLE_OK) return s;
+  if (empty) {
+    // no tokens: the carry-over is the history itself (EOS without one)
+    if (ngram_context_out == nullptr || num_reqs == 0) return PLE_OK;
+    if (ngram_context != nullptr)
+      return copy_carry(ngram_context_out, ngram_context, sizeof(int32_t) * num_reqs * ctx_len,
+                        stream);
+    return ple_ngram_ids(input_ids, 0, query_start_loc, num_reqs, nullptr, ctx_len,
+                         layer_multipliers, vocab_sizes, offsets, eos_token_id, heads_per_ngram,
+                         nullptr, ngram_context_out, dev_err, stream);
+  }
+  if (!input_ids || !query_start_loc)
+    return fail(PLE_ERR_INVALID_ARG, "%s: null device pointer", name);
+  NgramArgs na{};
+  na.input_ids = input_ids;
+  na.num_tokens = num_tokens;
+  na.qsl = query_start_loc;
+  na.num_reqs = num_reqs;
+  na.ctx = ngram_context;
+  na.ctx_len = ctx_len;
+  na.eos = eos_token_id;
+  na.heads_per_ngram = heads_per_ngram;
+  na.num_heads = num_heads;
+  na.ctx_out = ngram_context_out;
+  na.ids_out = ids_out;
+  const int scale_stride = dtype == PLE_FP8_E4M3 ? 1 : 0;
+  cudaError_t err;
+  if (dtype == PLE_BF16) {
+    err = g.vpr == 16
+              ? launch_kernel(ngram_gather_kernel<16, false>, dim3(g.grid), dim3(kThreads), 0,
+                              stream, 1, na, k, g.total_vecs, g.vpr, g.table, g.row_scale, 0,
+                              g.table_rows, g.out, dev_err)
+              : launch_kernel(ngram_gather_kernel<0, false>, dim3(g.grid), dim3(kThreads), 0,
+                              stream, 1, na, k, g.total_vecs, g.vpr, g.table, g.row_scale, 0,
+                              g.table_rows, g.out, dev_err);
+  } else {
+    err = g.vpr == 8
+              ? launch_kernel(ngram_gather_kernel<8, true>, dim3(g.grid), dim3(kThreads), 0,
+                              stream, 1, na, k, g.total_vecs, g.vpr, g.table, g.row_scale,
+                              scale_stride, g.table_rows, g.out, dev_err)
+              : launch_kernel(ngram_gather_kernel<0, true>, dim3(g.grid), dim3(kThreads), 0,
+                              stream, 1, na, k, g.total_vecs, g.vpr, g.table, g.row_scale,
+                              scale_stride, g.table_rows, g.out, dev_err);
+  }
+  if (err != cudaSuccess) return check_cuda(err, name);
+  return check_cuda(cudaGetLastError(), name);
 }

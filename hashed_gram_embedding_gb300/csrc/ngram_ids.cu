@@ -9,39 +9,13 @@
 // semantics).
 //
 // Design: one thread per (token, head) output, so the int64 stores of a warp
-// are contiguous. Each thread binary-searches its request in query_start_loc
-// (L1-resident), reads at most NGRAM_CONTEXT_LEN + 1 tokens, and reduces with
-// a multiply-high floor-mod instead of a 64-bit division:
-//   magic = floor(2^64 / V)  =>  q = umulhi(u, magic) is floor(u / V) or one
-//   less, so r = u - q*V lies in [0, 2V) and one conditional subtraction gives
-//   u mod V. A negative int64 m is u - 2^64, so floor_mod(m, V) is
-//   (u mod V - 2^64 mod V) mod V.
-// The constants (multipliers, V, O, magic numbers) travel by value in the
-// kernel's parameter block: no device allocation, graph-capture friendly.
-#include "common.cuh"
+// are contiguous. Request boundaries are staged in shared memory once per
+// block, the block's first token is searched once and every thread steps
+// forward from there; the hash itself is ngram_id (ngram_hash.cuh).
+#include "ngram_hash.cuh"
 
 namespace ple {
 namespace {
-
-constexpr int kStagedBounds = 4096;  // query_start_loc entries staged in shared memory
-
-struct NgramConsts {
-  int64_t mult[PLE_MAX_CTX_LEN + 1];
-  int64_t vocab[PLE_MAX_HEADS];
-  int64_t offset[PLE_MAX_HEADS];
-  uint64_t magic[PLE_MAX_HEADS];     // floor(2^64 / V), 0 when V == 1
-  uint64_t pow64_mod[PLE_MAX_HEADS]; // 2^64 mod V
-};
-
-__device__ __forceinline__ int64_t floor_mod(int64_t m, uint64_t V,
-                                             uint64_t magic, uint64_t pow64_mod) {
-  if (V == 1) return 0;
-  const uint64_t u = static_cast<uint64_t>(m);
-  uint64_t r = u - __umul64hi(u, magic) * V;
-  if (r >= V) r -= V;
-  if (m < 0) r = (r >= pow64_mod) ? r - pow64_mod : r + V - pow64_mod;
-  return static_cast<int64_t>(r);
-}
 
 __global__ void __launch_bounds__(256)
 ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
@@ -59,18 +33,9 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   // from there (a block spans 256 / num_heads consecutive tokens).
   __shared__ int32_t qsl_s[kStagedBounds];
   __shared__ int r_first_s;
-  // Per-head constants: the lanes of a warp index different heads, so they
-  // are read from shared memory (a lane-varying index into the parameter
-  // block would serialise on the constant cache).
-  __shared__ uint64_t vocab_s[PLE_MAX_HEADS], offset_s[PLE_MAX_HEADS];
-  __shared__ uint64_t magic_s[PLE_MAX_HEADS], pow64_s[PLE_MAX_HEADS];
+  __shared__ NgramHeadsSmem hs;
   const bool staged = num_reqs < kStagedBounds;
-  for (int h = threadIdx.x; h < num_heads; h += blockDim.x) {
-    vocab_s[h] = static_cast<uint64_t>(k.vocab[h]);
-    offset_s[h] = static_cast<uint64_t>(k.offset[h]);
-    magic_s[h] = k.magic[h];
-    pow64_s[h] = k.pow64_mod[h];
-  }
+  stage_ngram_heads(k, num_heads, hs);
   pdl_wait();
   pdl_trigger();
   if (staged)
@@ -97,24 +62,13 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   check_qsl(qsl, num_reqs, num_tokens, i, dev_err);
 
   // Carry-over: last ctx_len tokens of each request's virtual sequence.
-  if (ctx_out != nullptr && i < static_cast<uint32_t>(num_reqs) * static_cast<uint32_t>(ctx_len)) {
-    const int r = static_cast<int>(i / static_cast<uint32_t>(ctx_len));
-    const int j = static_cast<int>(i - static_cast<uint32_t>(r) * ctx_len);
-    int64_t start, end;
-    request_span(qsl, num_reqs, num_tokens, r, &start, &end);
-    const int64_t len = end - start;
-    const int64_t p = len + j;  // index into history ++ segment
-    int32_t v;
-    if (p < ctx_len) v = ctx ? __ldg(ctx + static_cast<int64_t>(r) * ctx_len + p) : eos;
-    else v = __ldg(input_ids + start + (p - ctx_len));
-    ctx_out[i] = v;
-  }
+  if (ctx_out != nullptr && i < static_cast<uint32_t>(num_reqs) * static_cast<uint32_t>(ctx_len))
+    ngram_carry(input_ids, num_tokens, qsl, num_reqs, ctx, ctx_len, eos, i, ctx_out);
 
   if (i >= work) return;
   const uint32_t t32 = i / static_cast<uint32_t>(num_heads);
   const int h = static_cast<int>(i - t32 * static_cast<uint32_t>(num_heads));
   const int64_t t = t32;
-  const int order_lags = h / heads_per_ngram + 1;  // n - 1 for this head
 
   // Last request whose start is <= t (the right-sided search of the pages'
   // CPU branch, clamped): step forward from the block's first request.
@@ -129,32 +83,43 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   }
   const int64_t pos = t - start;  // position inside the request
 
-  int64_t mixed = 0;
-  bool crossed = false;
-  for (int s = 0; s <= order_lags; ++s) {
-    int32_t x;
-    const int64_t q = pos - s;
-    if (q >= 0) {
-      x = (t - s >= 0) ? __ldg(input_ids + (t - s)) : eos;
-    } else {
-      const int64_t hist = ctx_len + q;  // history slot, oldest first
-      x = (ctx != nullptr && hist >= 0)
-              ? __ldg(ctx + static_cast<int64_t>(r) * ctx_len + hist) : eos;
-    }
-    if (s >= 1) {
-      if (crossed) x = eos;
-      else if (x == eos) crossed = true;
-    }
-    const uint64_t term = static_cast<uint64_t>(static_cast<int64_t>(x)) *
-                          static_cast<uint64_t>(k.mult[s]);
-    mixed = (s == 0) ? static_cast<int64_t>(term)
-                     : static_cast<int64_t>(static_cast<uint64_t>(mixed) ^ term);
-  }
-  out[i] = floor_mod(mixed, vocab_s[h], magic_s[h], pow64_s[h]) +
-           static_cast<int64_t>(offset_s[h]);
+  out[i] = ngram_id(input_ids, ctx, ctx_len, eos, t, pos, r, h, heads_per_ngram, k, hs);
 }
 
 }  // namespace
+
+ple_status make_ngram_consts(int32_t ctx_len, int32_t heads_per_ngram,
+                             const int64_t* layer_multipliers, const int64_t* vocab_sizes,
+                             const int64_t* offsets, NgramConsts* k, int* num_heads,
+                             const char* name) {
+  if (ctx_len < 1 || ctx_len > PLE_MAX_CTX_LEN)
+    return fail(PLE_ERR_INVALID_ARG, "%s: ctx_len %d not in [1, %d]", name, ctx_len,
+                PLE_MAX_CTX_LEN);
+  if (heads_per_ngram < 1)
+    return fail(PLE_ERR_INVALID_ARG, "%s: heads_per_ngram must be >= 1 "
+                "(empty head shards are rejected)", name);
+  const int H = ctx_len * heads_per_ngram;
+  if (H > PLE_MAX_HEADS)
+    return fail(PLE_ERR_INVALID_ARG, "%s: %d heads > %d", name, H, PLE_MAX_HEADS);
+  if (!layer_multipliers || !vocab_sizes || !offsets)
+    return fail(PLE_ERR_INVALID_ARG, "%s: null host constant array", name);
+  *k = NgramConsts{};
+  for (int s = 0; s <= ctx_len; ++s) k->mult[s] = layer_multipliers[s];
+  for (int h = 0; h < H; ++h) {
+    const int64_t V = vocab_sizes[h];
+    if (V < 1)
+      return fail(PLE_ERR_INVALID_ARG, "%s: vocab_sizes[%d] = %lld < 1", name, h,
+                  static_cast<long long>(V));
+    k->vocab[h] = V;
+    k->offset[h] = offsets[h];
+    const unsigned __int128 two64 = static_cast<unsigned __int128>(1) << 64;
+    k->magic[h] = (V == 1) ? 0 : static_cast<uint64_t>(two64 / static_cast<uint64_t>(V));
+    k->pow64_mod[h] = static_cast<uint64_t>(two64 % static_cast<uint64_t>(V));
+  }
+  *num_heads = H;
+  return PLE_OK;
+}
+
 }  // namespace ple
 
 PLE_EXPORT ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens,
@@ -167,36 +132,17 @@ PLE_EXPORT ple_status ple_ngram_ids(const int32_t* input_ids, int64_t num_tokens
                                     int32_t* dev_err, cudaStream_t stream) {
   using namespace ple;
   if (num_tokens < 0) return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: num_tokens < 0");
-  if (ctx_len < 1 || ctx_len > PLE_MAX_CTX_LEN)
-    return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: ctx_len %d not in [1, %d]", ctx_len,
-                PLE_MAX_CTX_LEN);
-  if (heads_per_ngram < 1)
-    return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: heads_per_ngram must be >= 1 "
-                "(empty head shards are rejected)");
-  const int num_heads = ctx_len * heads_per_ngram;
-  if (num_heads > PLE_MAX_HEADS)
-    return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: %d heads > %d", num_heads, PLE_MAX_HEADS);
+  NgramConsts k{};
+  int num_heads = 0;
+  ple_status cs = make_ngram_consts(ctx_len, heads_per_ngram, layer_multipliers, vocab_sizes,
+                                    offsets, &k, &num_heads, "ple_ngram_ids");
+  if (cs != PLE_OK) return cs;
   if (num_reqs < 0 || (num_reqs == 0 && num_tokens > 0))
     return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: num_reqs must be >= 1 when there are tokens");
-  if (!layer_multipliers || !vocab_sizes || !offsets)
-    return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: null host constant array");
   if (ngram_context_out && ngram_context &&
       overlaps(ngram_context, sizeof(int32_t) * num_reqs * ctx_len, ngram_context_out,
                sizeof(int32_t) * num_reqs * ctx_len))
     return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: ngram_context_out overlaps ngram_context");
-
-  NgramConsts k{};
-  for (int s = 0; s <= ctx_len; ++s) k.mult[s] = layer_multipliers[s];
-  for (int h = 0; h < num_heads; ++h) {
-    const int64_t V = vocab_sizes[h];
-    if (V < 1) return fail(PLE_ERR_INVALID_ARG, "ple_ngram_ids: vocab_sizes[%d] = %lld < 1",
-                           h, static_cast<long long>(V));
-    k.vocab[h] = V;
-    k.offset[h] = offsets[h];
-    const unsigned __int128 two64 = static_cast<unsigned __int128>(1) << 64;
-    k.magic[h] = (V == 1) ? 0 : static_cast<uint64_t>(two64 / static_cast<uint64_t>(V));
-    k.pow64_mod[h] = static_cast<uint64_t>(two64 % static_cast<uint64_t>(V));
-  }
 
   if (num_tokens == 0) {
     // Zero tokens: nothing to hash; the carry-over is the history itself.

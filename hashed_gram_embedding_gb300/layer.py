@@ -25,7 +25,7 @@ class PLELayer:
 
     def __init__(self, table, row_scale, layer_multipliers, vocab_sizes, offsets,
                  eos_token_id, heads_per_ngram, w_kv, gamma_h, gamma_k, conv_w,
-                 dilation, eps=1e-6, max_ctas=0, fuse_gate=None):
+                 dilation, eps=1e-6, max_ctas=0, fuse_gate=None, fuse_ids=None):
         self.table = table
         self.row_scale = row_scale
         self.mult = [int(m) for m in layer_multipliers]
@@ -52,6 +52,9 @@ class PLELayer:
         if self.fuse_gate and not can_fuse:
             raise ValueError(f"fuse_gate needs a hidden size that is a multiple of 256, "
                              f"not {self.hidden}")
+        # ids hashed inside the gather (ple_ngram_lookup) for a table in HBM;
+        # a host table is gathered in table order, after the ids
+        self.fuse_ids = table.is_cuda if fuse_ids is None else bool(fuse_ids) and table.is_cuda
         self._bufs = {}
 
     def buffers(self, num_tokens, device):
@@ -97,14 +100,21 @@ class PLELayer:
         """n-gram ids -> row gather into ``emb`` [T, H*D] (``order_ws``: the
         ordered gather's workspace, required for a host table)."""
         ctas = self.max_ctas if max_ctas is None else int(max_ctas)
-        _lib.ple_ngram_ids(input_ids, query_start_loc, ngram_context, self.mult, self.V, self.O,
-                           self.eos, self.hpn, ids, ngram_context_out, dev_err, stream)
-        if not self.table.is_cuda:
-            _lib.ple_lookup_ordered(ids, self.table, emb, order_ws, row_scale=self.row_scale,
-                                    max_ctas=ctas, dev_err=dev_err, stream=stream)
-        else:
-            _lib.ple_lookup(ids, self.table, emb, row_scale=self.row_scale, max_ctas=ctas,
-                            dev_err=dev_err, stream=stream)
+        if not self.fuse_ids:  # ids first, then the gather (table order for a host table)
+            _lib.ple_ngram_ids(input_ids, query_start_loc, ngram_context, self.mult, self.V,
+                               self.O, self.eos, self.hpn, ids, ngram_context_out, dev_err, stream)
+            if not self.table.is_cuda:
+                _lib.ple_lookup_ordered(ids, self.table, emb, order_ws, row_scale=self.row_scale,
+                                        max_ctas=ctas, dev_err=dev_err, stream=stream)
+            else:
+                _lib.ple_lookup(ids, self.table, emb, row_scale=self.row_scale, max_ctas=ctas,
+                                dev_err=dev_err, stream=stream)
+        else:  # HBM table: ids hashed inside the gather (ids still written to ``ids``)
+            _lib.ple_ngram_lookup(input_ids, query_start_loc, ngram_context, self.mult, self.V,
+                                  self.O, self.eos, self.hpn, self.table, emb,
+                                  row_scale=self.row_scale, ids_out=ids,
+                                  ngram_context_out=ngram_context_out, max_ctas=ctas,
+                                  dev_err=dev_err, stream=stream)
 
     def mix(self, emb, hidden, query_start_loc, out, conv_state=None, conv_state_out=None,
             dev_err=None, stream=None):
@@ -139,15 +149,13 @@ class PLELayer:
                                conv_state=conv_state, conv_state_out=conv_state_out,
                                gate_out=b["gate"], dev_err=dev_err, stream=stream)
 
-    # launches of libple kernels per forward (ids, gather, kv_proj, gate, conv;
-    # fused: ids, gather, kv_proj_gate, conv -- plus a counter memset, not a
-    # kernel); a host table's ordered gather adds three (count, scan, scatter)
-    LAUNCHES_PER_FORWARD = 5
-    ORDERED_GATHER_EXTRA = 3
-
     def launches_per_forward(self):
-        return (self.LAUNCHES_PER_FORWARD - (1 if self.fuse_gate else 0) +
-                (0 if self.table.is_cuda else self.ORDERED_GATHER_EXTRA))
+        """libple kernels per forward: the n-gram lookup (ids hashed inside the
+        gather; a host table: ids, then count, scan, scatter and the ordered
+        gather), then kv_proj_gate and the gated conv (unfused: kv_proj, the
+        gate pass and the conv pass)."""
+        embed = 1 if self.fuse_ids else (2 if self.table.is_cuda else 5)
+        return embed + (2 if self.fuse_gate else 3)
 
 
 class PLEHostPipeline:

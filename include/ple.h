@@ -5,6 +5,7 @@
  * The path (one transformer layer):
  *   ple_ngram_ids  ragged n-gram hash ids        -> ids [T][H] int64
  *   ple_lookup     multi-head row gather         -> emb [T][H*D] bf16
+ *                  (ple_ngram_lookup: both in one kernel)
  *   ple_kv_proj    merged key/value projection   -> kv  [T][2C] bf16
  *   ple_gate_conv  RMSNorm + sigmoid gate, then the dilated causal depthwise
  *                  short conv                    -> y   [T][C] bf16
@@ -254,6 +255,32 @@ ple_status ple_lookup_ordered_static(const int64_t* ids, int64_t num_tokens,
  *                    enqueue the device-side wait and return PLE_OK.
  */
 ple_status ple_wait(cudaEvent_t done, cudaStream_t consumer, int32_t timeout_ms);
+
+/*
+ * ple_ngram_lookup -- ple_ngram_ids and ple_lookup in one kernel: every
+ * gathered row's id is hashed where the gather needs it, so the ids make no
+ * round trip through memory (the page's two kernels, PR#54517 report
+ * 实现拆解 2 and PR#54371 report 实现拆解 1, fused; this split is the
+ * library's own). Arguments as in those two calls, with
+ *   ids_out   [num_tokens][H] int64 device or NULL: the ids, when wanted.
+ *   ngram_context_out, dev_err, max_ctas: as in ple_ngram_ids / ple_lookup.
+ * Results are bit for bit those of ple_ngram_ids followed by ple_lookup.
+ * Every head's partition [offsets[h], offsets[h] + vocab_sizes[h]) must lie
+ * inside the table's rows (checked on the host: PLE_ERR_INVALID_ARG). The
+ * rows are read in token order: for a table in host memory beyond ~16 GB use
+ * ple_ngram_ids + ple_lookup_ordered instead.
+ */
+ple_status ple_ngram_lookup(const int32_t* input_ids, int64_t num_tokens,
+                            const int32_t* query_start_loc, int32_t num_reqs,
+                            const int32_t* ngram_context, int32_t ctx_len,
+                            const int64_t* layer_multipliers,
+                            const int64_t* vocab_sizes, const int64_t* offsets,
+                            int32_t eos_token_id, int32_t heads_per_ngram,
+                            const void* table, int64_t table_rows, int32_t head_dim,
+                            ple_dtype dtype, const float* row_scale,
+                            ple_table_loc loc, ple_bf16_t* out, int64_t* ids_out,
+                            int32_t* ngram_context_out, int32_t max_ctas,
+                            int32_t* dev_err, cudaStream_t stream);
 
 /*
  * ple_kv_proj -- merged key/value projection, kv = emb @ W^T.

@@ -1,7 +1,8 @@
 """GPU parity of the whole per-layer chain (PLELayer.forward: ids -> gather ->
-kv_proj -> gate + conv; by default the projection does the gate's reductions,
-ple_kv_proj_gate + ple_gated_conv, and fuse_gate=False runs ple_kv_proj +
-ple_gate_conv) against the oracle's layer_forward: the tiny workload with a
+kv_proj -> gate + conv; by default the ids are hashed inside the gather
+(ple_ngram_lookup; fuse_ids=False runs ple_ngram_ids + ple_lookup) and the
+projection does the gate's reductions, ple_kv_proj_gate + ple_gated_conv
+(fuse_gate=False runs ple_kv_proj + ple_gate_conv)) against the oracle's layer_forward: the tiny workload with a
 bf16 and with an fp8 table (every token, both projections), the decode
 workload's carry-over outputs, and the 8k prefill at full size (sampled
 tokens with their conv windows)."""
@@ -19,21 +20,24 @@ from _helpers import CHAIN_ATOL_FRAC, assert_close, bits, dev_err_word, tiny_cas
 pytestmark = pytest.mark.gpu
 
 
-def build_layer(w, host, dense, table, row_scale, layer=0, fuse_gate=None):
+def build_layer(w, host, dense, table, row_scale, layer=0, fuse_gate=None, fuse_ids=None):
     return PLELayer(table, row_scale, host["multipliers"][layer], host["V"], host["O"],
                     w.eos_token_id, w.heads_per_ngram, dense["w_kv"], dense["gamma_h"],
-                    dense["gamma_k"], dense["conv_w"], w.dilation, fuse_gate=fuse_gate)
+                    dense["gamma_k"], dense["conv_w"], w.dilation, fuse_gate=fuse_gate,
+                    fuse_ids=fuse_ids)
 
 
+@pytest.mark.parametrize("fuse_ids", [True, False])
 @pytest.mark.parametrize("fuse_gate", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_tiny_chain_every_token(dtype, fuse_gate):
+def test_tiny_chain_every_token(dtype, fuse_gate, fuse_ids):
     w = wl.scaled(wl.WORKLOADS["tiny"], table_dtype=dtype)
     w, host, dense, table, row_scale = tiny_case(w)
     d_dense = {k: v.cuda() for k, v in dense.items()}
     layer = build_layer(w, host, d_dense, table.cuda(),
-                        None if row_scale is None else row_scale.cuda(), fuse_gate=fuse_gate)
-    assert layer.fuse_gate == fuse_gate
+                        None if row_scale is None else row_scale.cuda(), fuse_gate=fuse_gate,
+                        fuse_ids=fuse_ids)
+    assert layer.fuse_gate == fuse_gate and layer.fuse_ids == fuse_ids
     err = dev_err_word()
     qsl = torch.from_numpy(host["query_start_loc"]).cuda()
     y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), qsl, d_dense["hidden"],
