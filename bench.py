@@ -248,6 +248,7 @@ def run_ours(args):
     from hashed_gram_embedding_gb300 import build as build_mod
     from hashed_gram_embedding_gb300 import _lib
     from hashed_gram_embedding_gb300 import workloads as wl
+    from hashed_gram_embedding_gb300 import PLELayer
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
@@ -267,7 +268,8 @@ def run_ours(args):
     sets = make_sets(torch, w, device, num_sets)
     T, H, C = w.num_tokens, w.num_heads, w.hidden
     fuse = C % 256 == 0 and not args.no_fuse_gate
-    fuse_ids = w.table_loc == "hbm" and not args.no_fuse_ids
+    fuse_ids = w.table_loc == "hbm" and (
+        args.fuse_ids == "on" or (args.fuse_ids == "auto" and T <= PLELayer.FUSED_IDS_MAX_TOKENS))
     KERNELS = ((("ngram_lookup",) if fuse_ids else ("ngram_ids", "lookup")) +
                (("kv_proj_gate", "conv") if fuse else ("kv_proj", "gate_conv")))
     gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
@@ -384,7 +386,7 @@ def run_ours(args):
     # Every step uploads its inputs (token ids, query_start_loc, hidden) from
     # pinned host memory and reads y back into pinned host memory; uploads,
     # compute and read-backs of neighbouring steps overlap on three streams.
-    from hashed_gram_embedding_gb300 import PLELayer, PLEHostPipeline
+    from hashed_gram_embedding_gb300 import PLEHostPipeline
     p0 = sets[0]
     layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
                      w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
@@ -753,8 +755,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fuse-ids", action="store_true",
-                    help="time ple_ngram_ids + ple_lookup instead of ple_ngram_lookup (HBM tables)")
+    ap.add_argument("--fuse-ids", choices=["auto", "on", "off"], default="auto",
+                    help="ple_ngram_lookup (ids hashed in the gather) for HBM tables: auto = as "
+                         "PLELayer chooses (steps of up to 4096 tokens)")
     ap.add_argument("--no-fuse-gate", action="store_true",
                     help="time ple_kv_proj + ple_gate_conv instead of the fused projection")
     ap.add_argument("--layer-sets", type=int, default=0,
