@@ -347,15 +347,21 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 // N = 256. Each CTA of a cluster pair stages its own 128 rows of A and its own
 // half (128 rows) of the W tile; the pair's tensor cores read both halves of
 // W, so each SM reads 32 KB of operands from shared memory per K step of 64
-// instead of 48 KB, and a stage is 32 KB, leaving room for 7 stages in
-// flight. The even CTA (leader) issues the MMAs; TMA copies of both CTAs
+// instead of 48 KB. The even CTA (leader) issues the MMAs; TMA copies of both CTAs
 // complete on the leader's full barrier; the leader's commits release the
 // stages and hand the accumulators to the epilogues of both CTAs; both
 // epilogues report back to the leader's accumulator-empty barrier.
 // ---------------------------------------------------------------------------
-constexpr int P_STAGES = 7;
-constexpr int P_A_STAGE = BM * BK * 2;          // 16 KB: this CTA's 128 rows of A
-constexpr int P_B_STAGE = (BN / 2) * BK * 2;    // 16 KB: this CTA's half of the W tile
+// A stage holds two 64-wide K atoms (128 of K) of both operands: 3 stages of
+// 64 KB per CTA. Measured on a GB300 at 8192 x 2048 -> 8192: 153 us against
+// 169 us for 7 stages of one atom (half the full/empty handshakes per MMA)
+// and 172 us for 2 stages of three.
+constexpr int P_STAGES = 3;
+constexpr int P_ATOMS = 2;                      // 64-wide K atoms per stage
+constexpr int P_A_ATOM = BM * BK * 2;           // 16 KB
+constexpr int P_B_ATOM = (BN / 2) * BK * 2;     // 16 KB
+constexpr int P_A_STAGE = P_ATOMS * P_A_ATOM;
+constexpr int P_B_STAGE = P_ATOMS * P_B_ATOM;
 constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
 constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
@@ -619,7 +625,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
   const int base_units = m_tiles * n_groups;  // (256 rows, PAIRS x 256 columns) per cluster
   const int num_units = PAIRS == 1 ? full_units + 2 * (base_units - full_units) : base_units;
-  const int num_kb = (K + BK - 1) / BK;
+  const int num_kb = (K + BK * P_ATOMS - 1) / (BK * P_ATOMS);
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << (2 * PAIRS)) - 1);
   const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pidx));
 
@@ -679,16 +685,20 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         }
-        if constexpr (PAIRS == 1) {
-          tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE), &map_a, leader_full, kb * BK, m0);
-        } else {
-          // 64 of the 128 A rows, to this CTA and its counterpart in the other pair
-          tma_load_2d_pair_multicast(smem_u32(a_smem + stage * P_A_STAGE + pidx * (P_A_STAGE / 2)),
-                                     &map_a, leader_full, kb * BK, m0 + pidx * (BM / 2),
-                                     static_cast<uint16_t>((1u << q) | (1u << (q + 2))));
+        for (int at = 0; at < P_ATOMS; ++at) {
+          const int kx = (kb * P_ATOMS + at) * BK;
+          if constexpr (PAIRS == 1) {
+            tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM), &map_a,
+                             leader_full, kx, m0);
+          } else {
+            tma_load_2d_pair_multicast(
+                smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM + pidx * (P_A_ATOM / 2)),
+                &map_a, leader_full, kx, m0 + pidx * (BM / 2),
+                static_cast<uint16_t>((1u << q) | (1u << (q + 2))));
+          }
+          tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE + at * P_B_ATOM),
+                           half ? &map_b_half : &map_b, leader_full, kx, n0);
         }
-        tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE), half ? &map_b_half : &map_b,
-                         leader_full, kb * BK, n0);
         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -713,12 +723,16 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t a_desc = sw128_desc(smem_u32(a_smem + stage * P_A_STAGE));
-          const uint64_t b_desc = sw128_desc(smem_u32(b_smem + stage * P_B_STAGE));
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
-            umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int at = 0; at < P_ATOMS; ++at) {
+            const uint64_t a_desc = sw128_desc(smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM));
+            const uint64_t b_desc = sw128_desc(smem_u32(b_smem + stage * P_B_STAGE + at * P_B_ATOM));
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
+              umma_bf16_pair(d_tmem, a_desc + koff, b_desc + koff, idesc,
+                             (kb | at | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair(empty_bar(stage), kClusterMask);  // frees the stage everywhere it fed
           if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
