@@ -90,7 +90,60 @@ def test_decode_chain_carry_over():
                  what="decode state")
 
 
+def sampled_blocks(qsl, T, W, rng, n_blocks=30, block=64, first=10):
+    """Token ranges checked at full size: every request's first `first`
+    tokens, and `n_blocks` random blocks of `block` tokens inside requests,
+    each with the W tokens of history before it (its window starts at the
+    request start or W tokens earlier, so every checked token sees all its
+    taps). Returns [(lo, a, b)]: window [lo, b), checked tokens [a, b)."""
+    out = []
+    for r in range(len(qsl) - 1):
+        s, e = int(qsl[r]), int(qsl[r + 1]) if r + 1 < len(qsl) - 1 else T
+        if e > s:
+            out.append((s, s, min(e, s + first)))
+    spans = [(int(qsl[r]), int(qsl[r + 1]) if r + 1 < len(qsl) - 1 else T)
+             for r in range(len(qsl) - 1)]
+    long_spans = [(s, e) for s, e in spans if e - s >= block + W + first]
+    taken = []
+    while len(taken) < n_blocks:  # blocks that do not overlap one another
+        s, e = long_spans[rng.integers(len(long_spans))]
+        a = int(rng.integers(s + first + W, e - block + 1))
+        if all(a + block <= x or a >= x + block for x in taken):
+            taken.append(a)
+            out.append((a - W, a, a + block))
+    return out
+
+
+def check_chain_sampled(w, host, dense, table_bits_of, row_scale_of, y, ids, blocks):
+    """The oracle's layer on the sampled windows (kv computed once for all
+    their rows) against y, chain tolerance."""
+    qsl = host["query_start_loc"]
+    rows = np.unique(np.concatenate([np.arange(lo, b) for lo, _, b in blocks]))
+    pos = {int(t): i for i, t in enumerate(rows)}
+    win_ids = ids[rows]
+    uniq, inv = np.unique(win_ids, return_inverse=True)
+    if row_scale_of is None:
+        emb = oracle.lookup_bf16(inv.reshape(win_ids.shape), table_bits_of(uniq))
+    else:
+        emb = oracle.lookup_fp8(inv.reshape(win_ids.shape), table_bits_of(uniq), row_scale_of(uniq))
+    kv = oracle.kv_proj(emb, bits(dense["w_kv"]))
+    gh, gk, cw = (bits(dense[k]) for k in ("gamma_h", "gamma_k", "conv_w"))
+    hid = bits(dense["hidden"])
+    yb = bits(y)
+    checked = 0
+    for lo, a, b in blocks:
+        idx = [pos[t] for t in range(lo, b)]
+        ref_y, _, _ = oracle.gate_conv(hid[lo:b], kv[idx], gh, gk, 1e-6, [0, b - lo], cw,
+                                       w.dilation)
+        assert_close(yb[a:b], ref_y[a - lo:], atol_frac=CHAIN_ATOL_FRAC, what=f"tokens {a}..{b}")
+        checked += b - a
+    return checked  # distinct tokens: the blocks do not overlap each other or the first ones
+
+
 def test_prefill_8k_chain_sampled():
+    """The 8k prefill at full size (8.2 GB table) through PLELayer: every id
+    bit for bit, and y against the oracle on >= 2048 sampled tokens (every
+    request's first 10 and 30 blocks of 64 with their conv history)."""
     w = wl.WORKLOADS["prefill8k"]
     host = wl.host_inputs(w)
     table, _ = wl.make_table(torch, w, "cuda")
@@ -104,26 +157,44 @@ def test_prefill_8k_chain_sampled():
     assert int(err.item()) == 0
     ids, _ = oracle.ngram_ids(host["input_ids"], qsl, None, host["multipliers"][0], host["V"],
                               host["O"], w.eos_token_id, w.heads_per_ngram)
-    ids = np.asarray(ids, dtype=np.int64)
+    ids = np.asarray(ids, dtype=np.int64).reshape(w.num_tokens, -1)
     assert np.array_equal(layer.buffers(w.num_tokens, y.device)["ids"].cpu().numpy(), ids)
-    rng = np.random.default_rng(2)
-    sample = np.unique(np.concatenate([s + np.arange(4) for s in qsl[:-1]] +
-                                      [rng.integers(0, w.num_tokens, 56), [w.num_tokens - 1]]))
-    req_of = np.searchsorted(qsl, sample, side="right") - 1
-    wkv, gh, gk, cw = (bits(dense[k]) for k in ("w_kv", "gamma_h", "gamma_k", "conv_w"))
-    hid = dense["hidden"]
-    yb = bits(y)
-    for t, r in zip(sample, req_of):
-        lo = max(int(qsl[r]), int(t) - 9)
-        win_ids = ids[lo:t + 1]
-        uniq, inv = np.unique(win_ids, return_inverse=True)
-        compact = bits(table[torch.from_numpy(uniq).cuda()])
-        emb = oracle.lookup_bf16(inv.reshape(win_ids.shape), compact)
-        kv = oracle.kv_proj(emb, wkv)
-        ref_y, _, _ = oracle.gate_conv(bits(hid[lo:t + 1]), kv, gh, gk, 1e-6,
-                                       [0, int(t) + 1 - lo], cw, w.dilation)
-        assert_close(yb[t:t + 1], ref_y[-1:], atol_frac=CHAIN_ATOL_FRAC, what=f"token {t}")
+    blocks = sampled_blocks(qsl, w.num_tokens, (w.conv_k - 1) * w.dilation,
+                            np.random.default_rng(2))
+    n = check_chain_sampled(w, host, dense,
+                            lambda u: bits(table[torch.from_numpy(u).cuda()]), None, y, ids,
+                            blocks)
+    assert n >= 2048
     del table
+    torch.cuda.empty_cache()
+
+
+def test_fp8_32k_layer_sampled():
+    """One layer of the 32k-token fp8 workload at full size (8 GiB e4m3 table
+    with per-row scales, Zipf tokens): every id bit for bit, y against the
+    oracle on >= 2048 sampled tokens."""
+    w = wl.WORKLOADS["fp8x8"]
+    host = wl.host_inputs(w)
+    codes, scale = wl.make_table(torch, w, "cuda", layer=3)
+    dense = wl.dense_inputs(torch, w, "cuda", layer=3, random_gamma=True)
+    layer = build_layer(w, host, dense, codes, scale, layer=3)
+    qsl = host["query_start_loc"]
+    err = dev_err_word()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), torch.from_numpy(qsl).cuda(),
+                      dense["hidden"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ids, _ = oracle.ngram_ids(host["input_ids"], qsl, None, host["multipliers"][3], host["V"],
+                              host["O"], w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64).reshape(w.num_tokens, -1)
+    assert np.array_equal(layer.buffers(w.num_tokens, y.device)["ids"].cpu().numpy(), ids)
+    blocks = sampled_blocks(qsl, w.num_tokens, (w.conv_k - 1) * w.dilation,
+                            np.random.default_rng(3), n_blocks=24)
+    sel = lambda u: torch.from_numpy(u).cuda()
+    n = check_chain_sampled(w, host, dense, lambda u: codes[sel(u)].cpu().numpy(),
+                            lambda u: scale[sel(u)].cpu().numpy(), y, ids, blocks)
+    assert n >= 2048
+    del codes, scale
     torch.cuda.empty_cache()
 
 
