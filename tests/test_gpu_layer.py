@@ -90,6 +90,44 @@ def test_decode_chain_carry_over():
                  what="decode state")
 
 
+def test_decode_256x4_full_size():
+    """The decode workload at full size (256 requests x 4 tokens, n-gram
+    context and conv state carried over, hidden 4096, the 8.2 GB table)
+    through PLELayer (ids hashed inside the gather): ids, carry-over of both
+    kinds and y of every token against the oracle."""
+    w = wl.WORKLOADS["decode256x4"]
+    host = wl.host_inputs(w)
+    table, _ = wl.make_table(torch, w, "cuda")
+    dense = wl.dense_inputs(torch, w, "cuda", random_gamma=True)
+    layer = build_layer(w, host, dense, table, None)
+    qsl = host["query_start_loc"]
+    ctx_in = torch.from_numpy(host["ngram_context"]).cuda()
+    ctx_out = torch.empty_like(ctx_in)
+    st_out = torch.empty_like(dense["conv_state"])
+    err = dev_err_word()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), torch.from_numpy(qsl).cuda(),
+                      dense["hidden"], ngram_context=ctx_in, ngram_context_out=ctx_out,
+                      conv_state=dense["conv_state"], conv_state_out=st_out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and layer.fused_ids_for(w.num_tokens)
+    ids, ref_ctx = oracle.ngram_ids(host["input_ids"], qsl, host["ngram_context"],
+                                    host["multipliers"][0], host["V"], host["O"],
+                                    w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64).reshape(w.num_tokens, -1)
+    assert np.array_equal(layer.buffers(w.num_tokens, y.device)["ids"].cpu().numpy(), ids)
+    assert np.array_equal(ctx_out.cpu().numpy(), np.asarray(ref_ctx).reshape(ctx_out.shape))
+    uniq, inv = np.unique(ids, return_inverse=True)
+    emb = oracle.lookup_bf16(inv.reshape(ids.shape), bits(table[torch.from_numpy(uniq).cuda()]))
+    kv = oracle.kv_proj(emb, bits(dense["w_kv"]))
+    ref_y, ref_st, _ = oracle.gate_conv(bits(dense["hidden"]), kv, bits(dense["gamma_h"]),
+                                        bits(dense["gamma_k"]), 1e-6, qsl, bits(dense["conv_w"]),
+                                        w.dilation, bits(dense["conv_state"]))
+    assert_close(bits(y), ref_y, atol_frac=CHAIN_ATOL_FRAC, what="decode y")
+    assert_close(bits(st_out), ref_st, atol_frac=CHAIN_ATOL_FRAC, what="decode conv state")
+    del table
+    torch.cuda.empty_cache()
+
+
 def sampled_blocks(qsl, T, W, rng, n_blocks=30, block=64, first=10):
     """Token ranges checked at full size: every request's first `first`
     tokens, and `n_blocks` random blocks of `block` tokens inside requests,

@@ -242,6 +242,41 @@ def test_uva_gather_from_huge_page_host_table(dtype):
     owner.close()
 
 
+def test_uva32g_full_size_ordered_gather():
+    """The host-table workload at full size: 8192 tokens x 16 heads gathered
+    in table order from the 32 GiB huge-page-backed registered host table
+    (PLELayer.embed: ids, then the ordered gather), ids against the oracle
+    and every row bit for bit against the table read on the host."""
+    from hashed_gram_embedding_gb300 import PLELayer
+    w = wl.WORKLOADS["uva32g"]
+    host = wl.host_inputs(w)
+    table, _ = wl.make_table(torch, w, "cuda")
+    assert not table.is_cuda and wl.table_rows(w) == table.shape[0]
+    C = w.hidden
+    wkv = torch.zeros((2 * C, w.emb_dim), dtype=torch.bfloat16, device="cuda")
+    g1 = torch.ones((C,), dtype=torch.bfloat16, device="cuda")
+    cw = torch.zeros((C, w.conv_k), dtype=torch.bfloat16, device="cuda")
+    layer = PLELayer(table, None, host["multipliers"][0], host["V"], host["O"], w.eos_token_id,
+                     w.heads_per_ngram, wkv, g1, g1, cw, w.dilation)
+    T = w.num_tokens
+    b = layer.buffers(T, torch.device("cuda"))
+    err = dev_err_word()
+    layer.embed(torch.from_numpy(host["input_ids"]).cuda(),
+                torch.from_numpy(host["query_start_loc"]).cuda(), b["ids"], b["emb"],
+                b["order_ws"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ids, _ = oracle_ids(host["input_ids"], host["query_start_loc"], None, host["multipliers"][0],
+                        host["V"], host["O"], w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64).reshape(T, -1)
+    assert np.array_equal(b["ids"].cpu().numpy(), ids)
+    rows = table[torch.from_numpy(ids.reshape(-1))]  # read on the host
+    assert torch.equal(b["emb"].cpu().view(torch.int16),
+                       rows.reshape(T, -1).view(torch.int16))
+    del layer, table
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("rows", [10, 5000, 300000])
 def test_ordered_gather_equals_plain_gather(dtype, rows):
