@@ -487,8 +487,9 @@ def run_ours(args):
                      "note": "same steps launched one by one, events between kernels"}
     if graph_error:
         line["eager"]["graph_capture_error"] = graph_error
-    if w.num_layers > 1 and len(sets) >= w.num_layers:
-        line["chain"] = chain_timing(torch, w, sets, device, err, fuse)
+    chain_layers = args.chain_layers or (w.num_layers if w.num_layers > 1 else 0)
+    if chain_layers > 1:
+        line["chain"] = chain_timing(torch, w, sets, device, err, fuse, chain_layers)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
@@ -522,21 +523,33 @@ def capture_graphs(torch, step, num_sets, device):
         return None, str(e)[:300]
 
 
-def chain_timing(torch, w, sets, device, err, fuse, reps=10):
-    """All layers of a multi-layer workload through PLEChain: with the next
-    layers' ids and gathers prefetched on a side stream, and in line."""
+def chain_timing(torch, w, sets, device, err, fuse, L, reps=10):
+    """L layers over the same tokens through PLEChain: with the next layers'
+    ids and gathers prefetched on a side stream, and in line. Layer i uses
+    layer set i; past the resident sets (one 32 GiB table for the host-table
+    workload) layer i reuses set i mod sets' table and weights with its own
+    layer multipliers, so each layer gathers its own rows."""
     from hashed_gram_embedding_gb300 import PLELayer, PLEChain
-    layers = [PLELayer(p["table"], p["row_scale"], p["mult"], p["host"]["V"], p["host"]["O"],
-                       w.eos_token_id, w.heads_per_ngram, p["w_kv"], p["gamma_h"], p["gamma_k"],
-                       p["conv_w"], w.dilation, fuse_gate=fuse) for p in sets[:w.num_layers]]
+    from hashed_gram_embedding_gb300 import workloads as wl
+    layers = []
+    for i in range(L):
+        p = sets[i % len(sets)]
+        mult = p["mult"] if i < len(sets) else wl.layer_multipliers(w, i)
+        layers.append(PLELayer(p["table"], p["row_scale"], mult, p["host"]["V"], p["host"]["O"],
+                               w.eos_token_id, w.heads_per_ngram, p["w_kv"], p["gamma_h"],
+                               p["gamma_k"], p["conv_w"], w.dilation, fuse_gate=fuse))
     p0 = sets[0]
-    T, C, L = w.num_tokens, w.hidden, w.num_layers
-    hiddens = [p["hidden"] for p in sets[:L]]
+    T, C = w.num_tokens, w.hidden
+    hiddens = [sets[i % len(sets)]["hidden"] for i in range(L)]
     outs = [torch.empty((T, C), dtype=torch.bfloat16, device=device) for _ in range(L)]
     stream = torch.cuda.current_stream(device)
     res = {"layers": L}
-    for name, prefetch in (("prefetch", True), ("inline", False)):
-        chain = PLEChain(layers, prefetch=prefetch)
+    variants = [("prefetch", True, 0), ("inline", False, 0)]
+    if w.table_loc == "host":  # the pages cap the side-stream gather at half the SMs
+        half = torch.cuda.get_device_properties(device).multi_processor_count // 2
+        variants.insert(1, ("prefetch_half_grid", True, half))
+    for name, prefetch, ctas in variants:
+        chain = PLEChain(layers, prefetch=prefetch, prefetch_ctas=ctas)
         for _ in range(2):
             chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
                           dev_err=err, stream=stream)
@@ -755,6 +768,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chain-layers", type=int, default=0,
+                    help="also time a chain of this many layers through PLEChain (prefetch vs "
+                         "in line; 0 = the workload's layer count when it has several)")
     ap.add_argument("--fuse-ids", choices=["auto", "on", "off"], default="auto",
                     help="ple_ngram_lookup (ids hashed in the gather) for HBM tables: auto = as "
                          "PLELayer chooses (steps of up to 4096 tokens)")
