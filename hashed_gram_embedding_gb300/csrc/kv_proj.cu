@@ -880,8 +880,6 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
     else if (strcmp(e, "pair") == 0) mode = kPair;
     else if (strcmp(e, "quad") == 0) mode = kQuad;
   }
-  if (const char* e = getenv("PLE_KVPROJ_CLUSTER"))
-    if (atoi(e) == 1) mode = kSingle;
   if (ge != nullptr && mode != kQuad) mode = kPair;
   const bool paired = mode == kPair || mode == kQuad;
   const int cluster = mode == kSingle ? 1 : (mode == kQuad ? 4 : 2);
