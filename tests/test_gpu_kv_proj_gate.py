@@ -227,3 +227,20 @@ def test_kv_proj_gate_prefill_8k():
     assert_close(bits(kv[sel][:, C:]), ref_kv[:, C:], what="v, sampled rows")
     _, ref_g = oracle_gate(bits(h[sel]), ref_kv, bits(gh), bits(gk), 1e-6)
     assert np.max(np.abs(g[sel].cpu().numpy() - ref_g)) < 5e-4
+
+
+def test_kv_proj_gate_largest_hidden():
+    """hidden = 16384 (ple_gate's largest): 128 partial-sum blocks per row."""
+    M, E, C = 96, 64, 16384
+    emb, w, h, gh, gk = (t.cuda() for t in inputs(M, E, C, 17))
+    kv, g = run_fused(emb, w, h, gh, gk)
+    kv_ref = torch.empty_like(kv)
+    _lib.ple_kv_proj(emb, w, kv_ref)
+    u = torch.empty((M, C), dtype=torch.bfloat16, device="cuda")
+    g_ref = torch.empty((M,), dtype=torch.float32, device="cuda")
+    _lib.ple_gate(h, kv_ref, gh, gk, u, gate_out=g_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(kv[:, C:].view(torch.int16), kv_ref[:, C:].view(torch.int16))
+    assert float((g - g_ref).abs().max()) < 1e-5
+    _, ref_g = oracle_gate(bits(h), oracle_kv_proj(bits(emb), bits(w)), bits(gh), bits(gk), 1e-6)
+    assert np.max(np.abs(g.cpu().numpy() - ref_g)) < 5e-4

@@ -3,9 +3,9 @@ against the oracle (ids, carry-over and rows bit for bit) and against
 ple_ngram_ids followed by ple_lookup (the same bits): bf16 tables, fp8 tables
 with per-row and whole-table scales, the tiny / decode / 8k-prefill
 workloads (the last at full size in the launch configuration the benchmark
-times), many requests (boundaries searched outside shared memory), zero
-tokens, a missing ids output, invalid query_start_loc and a head partition
-outside the table."""
+times), many requests (boundaries searched outside shared memory), the
+largest head count (64), zero tokens, a missing ids output, invalid
+query_start_loc and a head partition outside the table."""
 
 import numpy as np
 import pytest
@@ -169,3 +169,35 @@ def test_invalid_query_start_loc_is_flagged_not_faulted():
         assert int(err.item()) & _lib.PLE_DEVERR_QSL
         got = ids.cpu().numpy()
         assert np.all((got >= O) & (got < np.add(O, V)))
+
+
+def test_largest_head_count():
+    """64 heads (2 n-gram orders x 32 heads each, the library's maximum) with
+    64-dim rows: the fused lookup equals ple_ngram_ids + ple_lookup and the
+    oracle."""
+    rng = np.random.default_rng(41)
+    L, hpn, D = 2, 32, 64
+    H = L * hpn
+    V = [int(v) for v in rng.integers(50, 120, size=H)]
+    O = [int(o) for o in np.concatenate([[0], np.cumsum(V)[:-1]])]
+    rows = int(sum(V))
+    table = (torch.randn((rows, D)) * 0.02).to(torch.bfloat16)
+    qsl = np.array([0, 40, 41, 100, 333], dtype=np.int32)
+    T = int(qsl[-1])
+    tokens = rng.integers(0, 60, size=T).astype(np.int32)
+    mult = [int(x) for x in (rng.integers(1 << 32, 1 << 62, size=L + 1) | 1)]
+    d_tok, d_qsl = torch.from_numpy(tokens).cuda(), torch.from_numpy(qsl).cuda()
+    tab = table.cuda()
+    out = torch.empty((T, H * D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, H), dtype=torch.int64, device="cuda")
+    _lib.ple_ngram_lookup(d_tok, d_qsl, None, mult, V, O, 2, hpn, tab, out, ids_out=ids)
+    ids2 = torch.empty_like(ids)
+    out2 = torch.empty_like(out)
+    _lib.ple_ngram_ids(d_tok, d_qsl, None, mult, V, O, 2, hpn, ids2)
+    _lib.ple_lookup(ids2, tab, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2) and torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    ref_ids, _ = oracle_ids(tokens, qsl, None, mult, V, O, 2, hpn, num_tokens=T)
+    ref_ids = np.asarray(ref_ids, dtype=np.int64).reshape(T, H)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.array_equal(bits(out), lookup_bf16(ref_ids, bits(table)))
