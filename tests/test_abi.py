@@ -189,3 +189,45 @@ def test_kv_proj_gate_host_checks(lib):
     # no tokens: nothing to do
     assert lib.ple_kv_proj_gate(None, None, 0, 64, 512, None, None, None, 1e-6, None, None,
                                 None, 0, None, None) == 0
+
+
+def _ngram_lookup(lib, **kw):
+    p = ctypes.c_void_p(256)  # never dereferenced: every case fails on the host first
+    args = dict(input_ids=p, T=4, qsl=p, R=1, ctx=None, ctx_len=2, mult=[1, 2, 3], V=[7, 11],
+                O=[0, 7], eos=2, hpn=1, table=p, rows=18, D=64, dtype=0, scale=None, loc=0,
+                out=p, ids_out=None, ctx_out=None)
+    args.update(kw)
+    I64P = ctypes.POINTER(ctypes.c_int64)
+    keep = [np.asarray(args[k], dtype=np.int64) for k in ("mult", "V", "O")]
+    return lib.ple_ngram_lookup(args["input_ids"], args["T"], args["qsl"], args["R"], args["ctx"],
+                                args["ctx_len"], *(a.ctypes.data_as(I64P) for a in keep),
+                                args["eos"], args["hpn"], args["table"], args["rows"], args["D"],
+                                args["dtype"], args["scale"], args["loc"], args["out"],
+                                args["ids_out"], args["ctx_out"], 0, None, None)
+
+
+def test_ngram_lookup_host_checks(lib):
+    assert _ngram_lookup(lib, hpn=0) == 1                      # empty head shard
+    assert b"empty head" in lib.ple_last_error()
+    assert _ngram_lookup(lib, O=[0, 8]) == 1                   # head 1's partition past row 18
+    assert b"outside" in lib.ple_last_error()
+    assert _ngram_lookup(lib, O=[-1, 7]) == 1
+    assert _ngram_lookup(lib, R=0) == 1                        # tokens but no request
+    assert _ngram_lookup(lib, T=-1) == 1
+    assert _ngram_lookup(lib, D=12) == 2                       # 24-byte rows
+    assert _ngram_lookup(lib, dtype=7) == 1                    # no such table type
+    assert _ngram_lookup(lib, dtype=1) == 1                    # fp8 without a scale
+    buf = (ctypes.c_int32 * 8)()
+    a = ctypes.addressof(buf)
+    assert _ngram_lookup(lib, ctx=a, ctx_out=a + 4, R=2, T=0) == 1
+    assert b"overlaps" in lib.ple_last_error()
+
+
+def test_gated_conv_host_checks(lib):
+    p = ctypes.c_void_p(256)
+    # K = 9 is above the largest filter; dilation 30 with K = 4 exceeds the halo
+    assert lib.ple_gated_conv(p, p, p, 1, 4, 64, p, 9, 1, None, None, p, None, None) == 1
+    assert lib.ple_gated_conv(p, p, p, 1, 4, 64, p, 4, 30, None, None, p, None, None) == 1
+    assert lib.ple_gated_conv(None, p, p, 1, 4, 64, p, 4, 3, None, None, p, None, None) == 1
+    assert lib.ple_gated_conv(p, None, p, 1, 4, 64, p, 4, 3, None, None, p, None, None) == 1
+    assert lib.ple_gated_conv(p, p, p, 1, 4, 12, p, 4, 3, None, None, p, None, None) == 1
