@@ -1,12 +1,16 @@
-// ple_kv_proj: the merged key/value projection kv = emb @ W^T on the
-// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
-// operands staged by TMA.
+// ple_kv_proj / ple_kv_proj_gate: the merged key/value projection
+// kv = emb @ W^T on the 5th-generation tensor cores (tcgen05.mma,
+// accumulators in tensor memory), operands staged by TMA; ple_kv_proj_gate
+// also reduces the gate's row sums from the key tiles in the epilogue.
 //
 // Source: PR#54517 report ("Fuse Qwen4Exp PLE kernels"), 实现拆解 item 1:
 // key_proj and value_proj merged into one MergedColumnParallelLinear, so one
 // GEMM [T, E] x [2C, E]^T produces k (columns [0, C)) and v ([C, 2C)).
 //
-// Design (dense contraction, tensor-bound at serving sizes):
+// Two kernels: the CTA-pair kernel further below (the default: cta_group::2
+// MMAs over 256 x 256 tiles) and the one-SM kernel described here (for at
+// most 128 rows, and the launch-shape variants). Design of the one-SM kernel
+// (dense contraction, tensor-bound at serving sizes):
 //   * CTA tile 128 x 256 (M x N), K step 64 = one 128-byte swizzle atom of
 //     bf16. A = emb and B = W are both K-major, exactly the canonical
 //     SWIZZLE_128B K-major layout TMA writes and tcgen05 reads, so no

@@ -1,6 +1,7 @@
-// ple_lookup / ple_lookup_prefetch: multi-head row gather from a PLE table in
-// HBM or in pinned host memory (UVA), bf16 rows or fp8 e4m3 rows with a
-// per-row float32 scale dequantised on the fly.
+// ple_lookup / ple_lookup_prefetch / ple_lookup_ordered / ple_ngram_lookup:
+// multi-head row gather from a PLE table in HBM or in pinned host memory
+// (UVA), bf16 rows or fp8 e4m3 rows with a per-row or whole-table float32
+// scale dequantised on the fly; ple_ngram_lookup also hashes the ids.
 //
 // Sources: PR#54371 report ("Support UVA PLE-offload ..."), 实现拆解 item 1 and
 // 关键源码片段 (Qwen4ExpPLEDeviceEmbedding / Qwen4ExpPLEPinnedHostEmbedding:
