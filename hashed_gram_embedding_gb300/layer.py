@@ -184,11 +184,24 @@ class PLEHostPipeline:
     The host output buffer of a step must not be read (or reused) before
     ``synchronize`` (or the step's ``done`` event). All arithmetic is in
     libple; the streams and events are PyTorch's.
+
+    With ``graphs`` (the default) a slot's layer calls are captured into a
+    CUDA graph the second time the slot runs with the same argument tensors
+    (the first run is launched directly and warms the library up) and
+    replayed from then on, so a step costs one graph launch on the host
+    instead of one launch per kernel: small steps (decode) are otherwise
+    bound by the host's launch rate. A change of argument tensors captures
+    another graph.
     """
 
-    def __init__(self, layer, num_tokens, num_reqs, device, depth=2):
+    def __init__(self, layer, num_tokens, num_reqs, device, depth=2, graphs=True):
         self.layer = layer
         self.device = torch.device(device)
+        self.graphs = bool(graphs)
+        self._graphs = {}   # (slot, argument tensors) -> CUDAGraph
+        self._seen = set()  # (slot, argument tensors) run once directly
+        self._capture = torch.cuda.Stream(self.device) if self.graphs else None
+        layer.buffers(num_tokens, self.device)  # allocated outside any capture
         self.copy_in = torch.cuda.Stream(self.device)
         self.compute = torch.cuda.Stream(self.device)
         self.copy_out = torch.cuda.Stream(self.device)
@@ -221,14 +234,37 @@ class PLEHostPipeline:
         # y may be overwritten once the previous user of the slot was read back
         self.compute.wait_event(s["loaded"])
         self.compute.wait_event(s["returned"])
-        self.layer.forward(s["ids"], s["qsl"], s["hidden"], stream=self.compute, out=s["y"],
-                           **forward_kwargs)
+        self._forward((self.k - 1) % len(self.slots), s, forward_kwargs)
         s["computed"].record(self.compute)
         self.copy_out.wait_event(s["computed"])
         with torch.cuda.stream(self.copy_out):
             h_out.copy_(s["y"], non_blocking=True)
         s["returned"].record(self.copy_out)
         return s["returned"]
+
+    def _forward(self, slot, s, kwargs):
+        def run(stream):
+            self.layer.forward(s["ids"], s["qsl"], s["hidden"], stream=stream, out=s["y"],
+                               **kwargs)
+        if not self.graphs:
+            run(self.compute)
+            return
+        key = (slot,) + tuple(sorted(
+            (name, v.data_ptr() if torch.is_tensor(v) else v) for name, v in kwargs.items()))
+        g = self._graphs.get(key)
+        if g is None and key not in self._seen:
+            self._seen.add(key)
+            run(self.compute)
+            return
+        if g is None:
+            # capture with nothing else in flight; the graph does not run now
+            torch.cuda.synchronize(self.device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self._capture):
+                run(self._capture)
+            self._graphs[key] = g
+        with torch.cuda.stream(self.compute):
+            g.replay()
 
     def synchronize(self):
         self.copy_out.synchronize()

@@ -236,17 +236,19 @@ def test_fp8_32k_layer_sampled():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("graphs", [True, False])
 @pytest.mark.parametrize("depth", [1, 2, 3])
-def test_host_pipeline_matches_layer(depth):
+def test_host_pipeline_matches_layer(depth, graphs):
     """PLEHostPipeline over pinned host buffers (transfers overlapping
     compute) gives, step by step, exactly what PLELayer.forward gives on the
-    same inputs; every step has its own tokens and hidden states."""
+    same inputs; every step has its own tokens and hidden states. With
+    graphs, each slot's steps after its first replay a captured graph."""
     from hashed_gram_embedding_gb300 import PLEHostPipeline
     w, host, dense, table, row_scale = tiny_case(wl.WORKLOADS["tiny"])
     d_dense = {k: v.cuda() for k, v in dense.items()}
     layer = build_layer(w, host, d_dense, table.cuda(), None)
     T, C = w.num_tokens, w.hidden
-    steps = 5
+    steps = 8
     rng = np.random.default_rng(3)
     g = torch.Generator().manual_seed(4)
     h_ids = [torch.from_numpy(rng.integers(0, w.token_vocab, T).astype(np.int32)).pin_memory()
@@ -255,7 +257,8 @@ def test_host_pipeline_matches_layer(depth):
     h_hidden = [torch.randn((T, C), generator=g).to(torch.bfloat16).pin_memory()
                 for _ in range(steps)]
     h_out = [torch.empty((T, C), dtype=torch.bfloat16).pin_memory() for _ in range(steps)]
-    pipe = PLEHostPipeline(layer, T, len(host["query_start_loc"]) - 1, "cuda", depth=depth)
+    pipe = PLEHostPipeline(layer, T, len(host["query_start_loc"]) - 1, "cuda", depth=depth,
+                           graphs=graphs)
     err = dev_err_word()
     for k in range(steps):
         pipe.submit(h_ids[k], h_qsl, h_hidden[k], h_out[k], dev_err=err)
