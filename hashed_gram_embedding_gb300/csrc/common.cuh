@@ -247,6 +247,19 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// lo += w.lo * x.lo, hi += w.hi * x.hi for two bf16 pair words, float32
+// accumulators (sm_100+ mixed-precision FMA: the bf16 operands are exact in
+// float32 and the product-sum is rounded once, so each lane equals fmaf on
+// the unpacked values).
+__device__ __forceinline__ void bf2_fma(uint32_t w, uint32_t x, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi) : "r"(w), "r"(x));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -21,12 +21,14 @@
 //     256-channel slice, stages its dilation window -- u of the tile and of
 //     the (K-1)*d tokens before it -- in shared memory as bf16 (u is a bf16
 //     value; 512 bytes per row), then each lane owns 8 channels (taps in
-//     registers as float pairs) and each warp walks tokens. A token whose
-//     taps all lie inside its own request (every token but the first (K-1)*d
-//     of a request) reads the K window rows and accumulates with packed
-//     two-wide FMAs; the others take the taps before their request's first
-//     token from the carry-over state. The CTA holding a request's last token
-//     writes the request's new state for its channels.
+//     registers as bf16 pairs, float32 accumulators, mixed-precision FMAs).
+//     When every token of the tile has all its taps inside its own request,
+//     each warp walks a block of tokens along its dilation chains with the
+//     K window rows of a token in a register ring (a row is read from shared
+//     memory once per chain, not once per tap); otherwise each warp walks
+//     tokens one by one, and a request's first (K-1)*d tokens take the taps
+//     before its start from the carry-over state. The CTA holding a
+//     request's last token writes the request's new state for its channels.
 // ple_conv is pass 2 on an ungated input; ple_gate is pass 1 plus u = g*v.
 #include "common.cuh"
 
@@ -343,7 +345,7 @@ __device__ void find_tile_requests(const int32_t* __restrict__ qsl, int R, int64
 }
 
 template <bool GATED, int K>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, K <= 4 ? 3 : 2)
 conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int tile_tokens) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int dil = a.dil;
@@ -371,8 +373,8 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   // Window row i <-> token t0 - W + i (rows of tokens before 0 are not
   // loaded; rows of an earlier request are loaded but never read). Each warp
   // takes every 8th row, kBatch rows' loads in flight per lane at a time (one
-  // batch covers a 64-token tile and its halo); warp 0 searches the tile's
-  // requests while its first batch is in flight.
+  // batch covers a 64-token tile and its halo, two a 112-token tile); warp 0
+  // searches the tile's requests while its first batch is in flight.
   {
     constexpr int kWarps = kConvThreads / 32;
     constexpr int kBatch = 10;
@@ -471,78 +473,79 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   if (!active) return;
 
   // taps of this lane's 8 channels: w[c..c+7][0..K-1] is 8*K contiguous bf16
-  // (K 16-byte loads), regrouped as float pairs wt[tap][pair]
-  uint64_t wt[K][4];
+  // (K 16-byte loads), regrouped as bf16 pair words wt[tap][pair] (channels
+  // 2*pair and 2*pair + 1, the layout of a window word)
+  uint32_t wt[K][4];
   {
-    float wf[K][8];
+    uint32_t h[8 * K];  // flat [8][K] bf16 values, one per word
     const uint4* wv = reinterpret_cast<const uint4*>(a.w + static_cast<int64_t>(c) * K);
 #pragma unroll
     for (int q = 0; q < K; ++q) {
-      float f[8];
-      unpack8(__ldg(wv + q), f);  // elements 8q .. 8q+7 of the [8][K] block
+      const uint4 b = __ldg(wv + q);
+      const uint32_t words[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int flat = 8 * q + e;
-        wf[flat % K][flat / K] = f[e];
+      for (int e = 0; e < 4; ++e) {
+        h[8 * q + 2 * e] = words[e] & 0xffffu;
+        h[8 * q + 2 * e + 1] = words[e] >> 16;
       }
     }
 #pragma unroll
     for (int i = 0; i < K; ++i)
 #pragma unroll
-      for (int p = 0; p < 4; ++p) wt[i][p] = f2(wf[i][2 * p], wf[i][2 * p + 1]);
+      for (int p = 0; p < 4; ++p) wt[i][p] = h[(2 * p) * K + i] | (h[(2 * p + 1) * K + i] << 16);
   }
 
-  // window row -> its 8 channels as four float pairs
-  auto row_pairs = [&](int row, uint64_t (&x)[4]) {
-    const uint4 b = s.win[row * 32 + lane];
-    x[0] = f2(bf_lo(b.x), bf_hi(b.x));
-    x[1] = f2(bf_lo(b.y), bf_hi(b.y));
-    x[2] = f2(bf_lo(b.z), bf_hi(b.z));
-    x[3] = f2(bf_lo(b.w), bf_hi(b.w));
+  // acc[0..7] += taps of tap i times the 8 channels of a bf16 window word
+  auto tap = [&](int i, uint4 b, float (&acc)[8]) {
+    bf2_fma(wt[i][0], b.x, acc[0], acc[1]);
+    bf2_fma(wt[i][1], b.y, acc[2], acc[3]);
+    bf2_fma(wt[i][2], b.z, acc[4], acc[5]);
+    bf2_fma(wt[i][3], b.w, acc[6], acc[7]);
+  };
+  auto store = [&](int64_t tok, const float (&acc)[8]) {
+    *reinterpret_cast<uint4*>(a.out + tok * C + c) =
+        make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
+                   pack2(acc[6], acc[7]));
   };
   if (all_fast) {
-    // no branches: two tokens per iteration so that one's shared-memory
-    // loads overlap the other's FMAs
+    // each warp takes a contiguous block of tokens and walks it along its
+    // dil chains (tokens tt, tt + d, tt + 2d, ...): consecutive tokens of a
+    // chain share K - 1 of their K window rows, so the rows stay in a
+    // register ring and each is read from shared memory once per chain
+    // (the ring is indexed at compile time: the walk is unrolled by K)
     constexpr int kWarps = kConvThreads / 32;
-    for (int tt = warp; tt < n_tok; tt += 2 * kWarps) {
-      const bool two = tt + kWarps < n_tok;
-      uint64_t acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    const int per = (n_tok + kWarps - 1) / kWarps;
+    const int b0 = warp * per;
+    const int b1 = min(n_tok, b0 + per);
+    for (int rho = 0; rho < dil && b0 + rho < b1; ++rho) {
+      int tt = b0 + rho;
+      uint4 ring[K];
 #pragma unroll
-      for (int i = 0; i < K; ++i) {
+      for (int i = 0; i < K - 1; ++i) ring[i] = s.win[(tt + i * dil) * 32 + lane];
+      bool more = true;
+      while (more) {
 #pragma unroll
-        for (int z = 0; z < 2; ++z) {
-          const int row = (z == 0 || two ? tt + z * kWarps : tt) + i * dil;
-          uint64_t x[4];
-          row_pairs(row, x);
+        for (int u = 0; u < K; ++u) {
+          if (more) {
+            ring[(u + K - 1) % K] = s.win[(tt + W) * 32 + lane];  // tap K-1: the token itself
+            float acc[8] = {};
 #pragma unroll
-          for (int p = 0; p < 4; ++p) acc[z][p] = f2_fma(wt[i][p], x[p], acc[z][p]);
+            for (int i = 0; i < K; ++i) tap(i, ring[(u + i) % K], acc);
+            store(t0 + tt, acc);
+            tt += dil;
+            more = tt < b1;
+          }
         }
-      }
-#pragma unroll
-      for (int z = 0; z < 2; ++z) {
-        if (z == 1 && !two) break;
-        uint4 y;
-        float lo, hi;
-        f2_split(acc[z][0], lo, hi); y.x = pack2(lo, hi);
-        f2_split(acc[z][1], lo, hi); y.y = pack2(lo, hi);
-        f2_split(acc[z][2], lo, hi); y.z = pack2(lo, hi);
-        f2_split(acc[z][3], lo, hi); y.w = pack2(lo, hi);
-        *reinterpret_cast<uint4*>(a.out + (t0 + tt + z * kWarps) * C + c) = y;
       }
     }
   } else
   for (int tt = warp; tt < n_tok; tt += kConvThreads / 32) {
     const int st = s.tok_start[tt];
-    uint64_t acc[4] = {0, 0, 0, 0};  // +0.0f pairs
+    float acc[8] = {};  // +0.0f
     if (tt - W >= st) {
       // all taps inside the request: window rows tt, tt + d, ..., tt + W
 #pragma unroll
-      for (int i = 0; i < K; ++i) {
-        uint64_t x[4];
-        row_pairs(tt + i * dil, x);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) acc[p] = f2_fma(wt[i][p], x[p], acc[p]);
-      }
+      for (int i = 0; i < K; ++i) tap(i, s.win[(tt + i * dil) * 32 + lane], acc);
     } else {
       // a request's first W tokens: taps before its start come from the
       // carry-over state (zeros without one); all state loads first
@@ -558,26 +561,10 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
 #pragma unroll
       for (int i = 0; i < K; ++i) {
         const int j = tt - (K - 1 - i) * dil;
-        uint64_t x[4];
-        if (j >= st) {
-          row_pairs(tt + i * dil, x);
-        } else {
-          x[0] = f2(bf_lo(hist[i].x), bf_hi(hist[i].x));
-          x[1] = f2(bf_lo(hist[i].y), bf_hi(hist[i].y));
-          x[2] = f2(bf_lo(hist[i].z), bf_hi(hist[i].z));
-          x[3] = f2(bf_lo(hist[i].w), bf_hi(hist[i].w));
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) acc[p] = f2_fma(wt[i][p], x[p], acc[p]);
+        tap(i, j >= st ? s.win[(tt + i * dil) * 32 + lane] : hist[i], acc);
       }
     }
-    uint4 y;
-    float lo, hi;
-    f2_split(acc[0], lo, hi); y.x = pack2(lo, hi);
-    f2_split(acc[1], lo, hi); y.y = pack2(lo, hi);
-    f2_split(acc[2], lo, hi); y.z = pack2(lo, hi);
-    f2_split(acc[3], lo, hi); y.w = pack2(lo, hi);
-    *reinterpret_cast<uint4*>(a.out + (t0 + tt) * C + c) = y;
+    store(t0 + tt, acc);
   }
 
   if (a.state_out == nullptr || W == 0) return;
@@ -909,12 +896,20 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   return PLE_OK;
 }
 
-// Tokens per conv tile: 64 (halo overhead (K-1)d/64) unless that leaves
-// fewer than ~4 CTAs per SM. PLE_CONV_TILE overrides (launch-shape sweeps).
+// Tokens per conv tile: 112 when that still gives ~4 CTAs per SM (each
+// CTA's fixed cost -- request search, one load round trip, two barriers --
+// spread over more tokens: 30.9 us at 8k prefill against 32.3 us for 64 and
+// 33.6 us for 128, measured); else 64, halved until ~4 CTAs per SM.
+// PLE_CONV_TILE overrides (launch-shape sweeps).
 int conv_tile_tokens(int64_t T, int C) {
   const int64_t slices = (C + kConvSlice - 1) / kConvSlice;
-  int tile = 64;
-  while (tile > 8 && ((T + tile - 1) / tile) * slices < 4 * static_cast<int64_t>(num_sms())) tile >>= 1;
+  const int64_t want = 4 * static_cast<int64_t>(num_sms());
+  auto ctas = [&](int tile) { return ((T + tile - 1) / tile) * slices; };
+  int tile = 112;
+  if (ctas(tile) < want) {
+    tile = 64;
+    while (tile > 8 && ctas(tile) < want) tile >>= 1;
+  }
   if (const char* e = getenv("PLE_CONV_TILE")) {
     const int v = atoi(e);
     if (v >= 1 && v <= 128) tile = v;

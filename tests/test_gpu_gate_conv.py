@@ -66,9 +66,11 @@ CONV_CASES = [
 ]
 
 
-# conv pass variants: the one-shot tiled kernel (default) and the streaming
-# kernel (default launch shape, one token range per slice, seven ranges)
-CONV_MODES = {"tile": {}, "stream": {"PLE_CONV_MODE": "stream"},
+# conv pass variants: the one-shot tiled kernel (default tile, the 112-token
+# tile of large steps, an odd 5-token tile) and the streaming kernel (default
+# launch shape, one token range per slice, seven ranges)
+CONV_MODES = {"tile": {}, "tile-112": {"PLE_CONV_TILE": "112"}, "tile-5": {"PLE_CONV_TILE": "5"},
+              "stream": {"PLE_CONV_MODE": "stream"},
               "stream-1range": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "1"},
               "stream-7ranges": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "7"}}
 
@@ -115,6 +117,40 @@ def test_conv_padding_tokens_join_last_request():
     ref_y, ref_st = oracle_conv(bits(x), q, bits(w), d, None, num_tokens=T)
     assert_close(bits(y), ref_y, what="conv y tail")
     assert np.array_equal(bits(st), ref_st)
+
+
+@pytest.mark.parametrize("tile", [None, "112", "5"])
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("case", CONV_CASES, ids=lambda c: f"{len(c[0])}req-C{c[1]}-K{c[2]}-d{c[3]}")
+def test_tiled_and_streaming_conv_same_bits(case, gated, tile, monkeypatch):
+    """The tiled kernel (taps and window as bf16 pairs, mixed-precision FMA)
+    and the streaming kernel (float32 ring, two-wide float32 FMA) take the
+    same taps in the same order with one rounding per tap: y and the
+    carry-over state agree bit for bit."""
+    lengths, C, K, d = case
+    q = qsl_of(lengths)
+    T, R, W = int(q[-1]), len(lengths), (K - 1) * d
+    src = rand_bf16((T, 2 * C if gated else C), 1.0, T + 7 * C)
+    w = rand_bf16((C, K), 0.5, K + 1).cuda()
+    state = rand_bf16((R, W, C), 0.3, 11).cuda()
+    g = torch.rand((T,), generator=torch.Generator().manual_seed(5)).cuda() if gated else None
+    outs = []
+    for env in ({} if tile is None else {"PLE_CONV_TILE": tile}, {"PLE_CONV_MODE": "stream"}):
+        monkeypatch.delenv("PLE_CONV_MODE", raising=False)
+        monkeypatch.delenv("PLE_CONV_TILE", raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        y = torch.full((T, C), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = torch.full((R, W, C), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if gated:
+            _lib.ple_gated_conv(src.cuda(), g, dev_qsl(q), w, d, y, conv_state=state,
+                                conv_state_out=st)
+        else:
+            _lib.ple_conv(src.cuda(), dev_qsl(q), w, d, y, conv_state=state, conv_state_out=st)
+        torch.cuda.synchronize()
+        outs.append((y.view(torch.int16).cpu(), st.view(torch.int16).cpu()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
 
 
 def _gate_conv_inputs(lengths, C, seed):
