@@ -14,6 +14,7 @@ namespace {
 thread_local char g_last_error[512] = "";
 constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices] = {0};
+int g_smem[kMaxDevices] = {0};
 }  // namespace
 
 ple_status fail(ple_status status, const char* fmt, ...) {
@@ -37,6 +38,16 @@ int num_sms() {
   int n = 1;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (dev >= 0 && dev < kMaxDevices) g_sms[dev] = n;
+  return n;
+}
+
+int smem_per_sm() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && g_smem[dev] > 0) return g_smem[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (dev >= 0 && dev < kMaxDevices) g_smem[dev] = n;
   return n;
 }
 

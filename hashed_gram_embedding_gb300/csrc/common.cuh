@@ -18,6 +18,8 @@ ple_status fail(ple_status status, const char* fmt, ...);
 ple_status check_cuda(cudaError_t err, const char* what);
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+// Shared memory per SM of the current device, bytes (cached per device).
+int smem_per_sm();
 // True if [a, a+na) and [b, b+nb) overlap (byte ranges).
 inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   auto pa = reinterpret_cast<uintptr_t>(a);

@@ -896,19 +896,36 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   return PLE_OK;
 }
 
-// Tokens per conv tile: 112 when that still gives ~4 CTAs per SM (each
-// CTA's fixed cost -- request search, one load round trip, two barriers --
-// spread over more tokens: 30.9 us at 8k prefill against 32.3 us for 64 and
-// 33.6 us for 128, measured); else 64, halved until ~4 CTAs per SM.
-// PLE_CONV_TILE overrides (launch-shape sweeps).
-int conv_tile_tokens(int64_t T, int C) {
+// Tokens per conv tile. A step small enough that a tile of 16..112 tokens
+// puts every CTA on the GPU at once takes the smallest such tile: one wave
+// (at 256 x 4 decode, 37-token tiles in 448 CTAs run the conv in 18.3 us
+// against 22.7 us for 16-token tiles in 1024 CTAs, measured). Otherwise 112
+// tokens when that still gives ~4 CTAs per SM (each CTA's fixed cost --
+// request search, one load round trip, two barriers -- spread over more
+// tokens: 30.9 us at 8k prefill against 32.3 us for 64 and 33.6 us for 128,
+// measured); else 64, halved until ~4 CTAs per SM. PLE_CONV_TILE overrides
+// (launch-shape sweeps).
+int conv_tile_tokens(int64_t T, int C, int K, int W) {
   const int64_t slices = (C + kConvSlice - 1) / kConvSlice;
   const int64_t want = 4 * static_cast<int64_t>(num_sms());
   auto ctas = [&](int tile) { return ((T + tile - 1) / tile) * slices; };
-  int tile = 112;
-  if (ctas(tile) < want) {
-    tile = 64;
-    while (tile > 8 && ctas(tile) < want) tile >>= 1;
+  // CTAs per SM: the register cap of the kernel (3 for K <= 4, else 2), or
+  // fewer when the shared memory of a 112-token tile does not fit
+  const int64_t by_smem = static_cast<int64_t>(smem_per_sm()) /
+                          static_cast<int64_t>(conv_smem_bytes(112, W) + 1024);
+  const int64_t per_sm = by_smem < (K <= 4 ? 3 : 2) ? by_smem : (K <= 4 ? 3 : 2);
+  const int64_t per_slice = per_sm * num_sms() / slices;  // tiles of one slice in one wave
+  int tile = 0;
+  if (per_slice >= 1) {
+    const int64_t one_wave = (T + per_slice - 1) / per_slice;
+    if (one_wave >= 16 && one_wave <= 112) tile = static_cast<int>(one_wave);
+  }
+  if (tile == 0) {
+    tile = 112;
+    if (ctas(tile) < want) {
+      tile = 64;
+      while (tile > 8 && ctas(tile) < want) tile >>= 1;
+    }
   }
   if (const char* e = getenv("PLE_CONV_TILE")) {
     const int v = atoi(e);
@@ -941,7 +958,7 @@ ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, c
   size_t smem = 0;
   dim3 grid;
   if (tiled) {
-    const int tile = conv_tile_tokens(a.T, a.C);
+    const int tile = conv_tile_tokens(a.T, a.C, a.K, W);
     param = tile;
     smem = conv_smem_bytes(tile, W);
     grid = dim3(static_cast<unsigned>((a.T + tile - 1) / tile), static_cast<unsigned>(slices));

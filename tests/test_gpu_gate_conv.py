@@ -119,7 +119,7 @@ def test_conv_padding_tokens_join_last_request():
     assert np.array_equal(bits(st), ref_st)
 
 
-@pytest.mark.parametrize("tile", [None, "112", "5"])
+@pytest.mark.parametrize("tile", [None, "112", "37", "5"])
 @pytest.mark.parametrize("gated", [False, True])
 @pytest.mark.parametrize("case", CONV_CASES, ids=lambda c: f"{len(c[0])}req-C{c[1]}-K{c[2]}-d{c[3]}")
 def test_tiled_and_streaming_conv_same_bits(case, gated, tile, monkeypatch):
