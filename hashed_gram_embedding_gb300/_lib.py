@@ -70,9 +70,25 @@ SIGNATURES = {
     "ple_host_table_map_file": [ctypes.c_char_p, ctypes.c_size_t, _I32,
                                 ctypes.POINTER(ctypes.c_void_p)],
     "ple_host_table_unmap": [ctypes.c_void_p, ctypes.c_size_t, _I32],
+    "ple_graph_begin": [_P],
+    "ple_graph_end": [_P, ctypes.POINTER(ctypes.c_void_p)],
+    "ple_graph_launch": [_P, _P],
+    "ple_graph_destroy": [_P],
+    "ple_event_create": [ctypes.POINTER(ctypes.c_void_p)],
+    "ple_event_destroy": [_P],
+    "ple_event_synchronize": [_P],
+    "ple_step_begin": [_P, _P, _P, _I32, _P, _P, _P],
+    "ple_step_end": [_P, _P, _P, _I32, _P, _P],
+    "ple_step": [_P, _P, _P, _P, _I32, _P, _P, _I32, _P, _P, _P],
     "ple_last_error": [],
     "ple_version": [],
 }
+_VOID = ("ple_graph_destroy", "ple_event_destroy")
+
+
+class PleCopy(ctypes.Structure):
+    """ple_copy: one host<->device copy of the step runtime."""
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
 class PleError(RuntimeError):
@@ -97,7 +113,8 @@ def lib():
             fn = getattr(handle, name)
             fn.argtypes = args
             fn.restype = (ctypes.c_char_p if name in ("ple_last_error", "ple_version") else
-                          ctypes.c_size_t if name.endswith("_workspace") else ctypes.c_int)
+                          ctypes.c_size_t if name.endswith("_workspace") else
+                          None if name in _VOID else ctypes.c_int)
         _lib = handle
     return _lib
 
@@ -370,3 +387,63 @@ class MappedHostTable:
 
 def ple_host_table_unlink_shared(name):
     return _check("ple_host_table_unlink_shared", lib().ple_host_table_unlink_shared(name.encode()))
+
+
+# ---- step runtime (graph capture, events, one step over three streams) ----
+
+def copies(items):
+    """PleCopy array of (dst, src, bytes) triples (pointers as ints)."""
+    arr = (PleCopy * max(len(items), 1))()
+    for i, (dst, src, nbytes) in enumerate(items):
+        arr[i].dst, arr[i].src, arr[i].bytes = dst, src, nbytes
+    return arr
+
+
+def ple_graph_begin(stream):
+    _check("ple_graph_begin", lib().ple_graph_begin(_stream(stream)))
+
+
+def ple_graph_end(stream):
+    """End the capture begun on ``stream``; returns the graph handle (int)."""
+    g = ctypes.c_void_p()
+    _check("ple_graph_end", lib().ple_graph_end(_stream(stream), ctypes.byref(g)))
+    return g.value
+
+
+def ple_graph_launch(graph, stream):
+    _check("ple_graph_launch", lib().ple_graph_launch(graph, _stream(stream)))
+
+
+def ple_graph_destroy(graph):
+    lib().ple_graph_destroy(graph)
+
+
+def ple_event_create():
+    ev = ctypes.c_void_p()
+    _check("ple_event_create", lib().ple_event_create(ctypes.byref(ev)))
+    return ev.value
+
+
+def ple_event_destroy(event):
+    lib().ple_event_destroy(event)
+
+
+def ple_event_synchronize(event):
+    _check("ple_event_synchronize", lib().ple_event_synchronize(event))
+
+
+def ple_step_begin(copy_in, compute, uploads, num_uploads, loaded, computed, returned):
+    _check("ple_step_begin", lib().ple_step_begin(_stream(copy_in), _stream(compute), uploads,
+                                                  num_uploads, loaded, computed, returned))
+
+
+def ple_step_end(compute, copy_out, downloads, num_downloads, computed, returned):
+    _check("ple_step_end", lib().ple_step_end(_stream(compute), _stream(copy_out), downloads,
+                                              num_downloads, computed, returned))
+
+
+def ple_step(copy_in, compute, copy_out, uploads, num_uploads, graph, downloads, num_downloads,
+             loaded, computed, returned):
+    _check("ple_step", lib().ple_step(_stream(copy_in), _stream(compute), _stream(copy_out),
+                                      uploads, num_uploads, graph, downloads, num_downloads,
+                                      loaded, computed, returned))

@@ -6,6 +6,8 @@ intermediate buffers (a table in host memory is gathered in table order). Device
 libple's kernels.
 """
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -182,92 +184,139 @@ class PLEHostPipeline:
     upload and step k-1's download run while step k-1 / k computes; a buffer
     set is reused only after the step that last used it has been read back.
     The host output buffer of a step must not be read (or reused) before
-    ``synchronize`` (or the step's ``done`` event). All arithmetic is in
-    libple; the streams and events are PyTorch's.
+    ``synchronize`` (or the ``synchronize()`` of the object ``submit``
+    returns). The streams are PyTorch's; the copies, the events ordering
+    them and the graph launches are issued by libple's step runtime
+    (ple_step_begin / ple_step_end / ple_step), all arithmetic is in libple.
 
     With ``graphs`` (the default) a slot's layer calls are captured into a
-    CUDA graph the second time the slot runs with the same argument tensors
-    (the first run is launched directly and warms the library up) and
-    replayed from then on, so a step costs one graph launch on the host
-    instead of one launch per kernel: small steps (decode) are otherwise
-    bound by the host's launch rate. A change of argument tensors captures
+    CUDA graph (ple_graph_begin / ple_graph_end) the second time the slot
+    runs with the same argument tensors (the first run is launched directly
+    and warms the library up); from then on a step is one ple_step call: its
+    uploads, the graph launch and its read-back with their event waits,
+    without a Python call per copy, wait or kernel. Small steps (decode) are
+    otherwise bound by the host. A change of argument tensors captures
     another graph.
     """
+
+    class Done:
+        """Completion of one submitted step (its read-back)."""
+
+        def __init__(self, event):
+            self.event = event
+
+        def synchronize(self):
+            _lib.ple_event_synchronize(self.event)
 
     def __init__(self, layer, num_tokens, num_reqs, device, depth=2, graphs=True):
         self.layer = layer
         self.device = torch.device(device)
         self.graphs = bool(graphs)
-        self._graphs = {}   # (slot, argument tensors) -> CUDAGraph
+        self._graphs = {}   # (slot, argument tensors) -> ple_graph handle
         self._seen = set()  # (slot, argument tensors) run once directly
         self._capture = torch.cuda.Stream(self.device) if self.graphs else None
         layer.buffers(num_tokens, self.device)  # allocated outside any capture
         self.copy_in = torch.cuda.Stream(self.device)
         self.compute = torch.cuda.Stream(self.device)
         self.copy_out = torch.cuda.Stream(self.device)
+        self._h = [ctypes.c_void_p(st.cuda_stream) for st in (self.copy_in, self.compute, self.copy_out)]
         C = layer.hidden
         self.slots = []
         for _ in range(depth):
-            self.slots.append({
+            s = {
                 "ids": torch.empty((num_tokens,), dtype=torch.int32, device=self.device),
                 "qsl": torch.empty((num_reqs + 1,), dtype=torch.int32, device=self.device),
                 "hidden": torch.empty((num_tokens, C), dtype=torch.bfloat16, device=self.device),
                 "y": torch.empty((num_tokens, C), dtype=torch.bfloat16, device=self.device),
-                "loaded": torch.cuda.Event(),    # inputs on the device
-                "computed": torch.cuda.Event(),  # the layer has read the inputs, written y
-                "returned": torch.cuda.Event(),  # y is back on the host
-            })
+            }
+            # events: inputs on the device / the layer read the inputs and wrote
+            # y / y back on the host
+            s["events"] = [ctypes.c_void_p(_lib.ple_event_create()) for _ in range(3)]
+            s["up"] = _lib.copies([(s[n].data_ptr(), None, s[n].numel() * s[n].element_size())
+                                   for n in ("ids", "qsl", "hidden")])
+            s["down"] = _lib.copies([(None, s["y"].data_ptr(),
+                                      s["y"].numel() * s["y"].element_size())])
+            s["done"] = PLEHostPipeline.Done(s["events"][2])
+            self.slots.append(s)
         self.k = 0
 
     def submit(self, h_input_ids, h_query_start_loc, h_hidden, h_out, **forward_kwargs):
         """Enqueue one step; ``forward_kwargs`` go to PLELayer.forward (device
-        carry-over buffers, dev_err). Returns the step's completion event."""
-        s = self.slots[self.k % len(self.slots)]
+        carry-over buffers, dev_err). Returns the step's completion (an
+        object with ``synchronize()``)."""
+        slot = self.k % len(self.slots)
+        s = self.slots[slot]
         self.k += 1
-        # inputs may be overwritten once the previous user of the slot computed
-        self.copy_in.wait_event(s["computed"])
-        with torch.cuda.stream(self.copy_in):
-            s["ids"].copy_(h_input_ids, non_blocking=True)
-            s["qsl"].copy_(h_query_start_loc, non_blocking=True)
-            s["hidden"].copy_(h_hidden, non_blocking=True)
-        s["loaded"].record(self.copy_in)
-        # y may be overwritten once the previous user of the slot was read back
-        self.compute.wait_event(s["loaded"])
-        self.compute.wait_event(s["returned"])
-        self._forward((self.k - 1) % len(self.slots), s, forward_kwargs)
-        s["computed"].record(self.compute)
-        self.copy_out.wait_event(s["computed"])
-        with torch.cuda.stream(self.copy_out):
-            h_out.copy_(s["y"], non_blocking=True)
-        s["returned"].record(self.copy_out)
-        return s["returned"]
+        up, down = s["up"], s["down"]
+        for i, (h, d) in enumerate(((h_input_ids, s["ids"]), (h_query_start_loc, s["qsl"]),
+                                    (h_hidden, s["hidden"]))):
+            if h.dtype != d.dtype or h.shape != d.shape or h.is_cuda:
+                raise ValueError(f"host input {i}: expected a host {d.dtype} tensor of shape "
+                                 f"{tuple(d.shape)}, got {h.dtype} {tuple(h.shape)} "
+                                 f"on {h.device}")
+            up[i].src = h.data_ptr()
+        y = s["y"]
+        if h_out.dtype != y.dtype or h_out.shape != y.shape or h_out.is_cuda:
+            raise ValueError(f"host output: expected a host {y.dtype} tensor of shape "
+                             f"{tuple(y.shape)}")
+        down[0].dst = h_out.data_ptr()
+        ci, cp, co = self._h
+        loaded, computed, returned = s["events"]
+        key = (slot,) + tuple((n, v.data_ptr() if torch.is_tensor(v) else v)
+                              for n, v in forward_kwargs.items())
+        g = self._graphs.get(key)
+        if g is not None:
+            _lib._check("ple_step", _lib.lib().ple_step(ci, cp, co, up, 3, g, down, 1,
+                                                        loaded, computed, returned))
+            return s["done"]
+        _lib._check("ple_step_begin", _lib.lib().ple_step_begin(ci, cp, up, 3, loaded, computed,
+                                                                returned))
+        self._forward(key, s, forward_kwargs)
+        _lib._check("ple_step_end", _lib.lib().ple_step_end(cp, co, down, 1, computed, returned))
+        return s["done"]
 
-    def _forward(self, slot, s, kwargs):
+    def _forward(self, key, s, kwargs):
         def run(stream):
             self.layer.forward(s["ids"], s["qsl"], s["hidden"], stream=stream, out=s["y"],
                                **kwargs)
-        if not self.graphs:
+        if not self.graphs or key not in self._seen:
+            if self.graphs:
+                self._seen.add(key)
             run(self.compute)
             return
-        key = (slot,) + tuple(sorted(
-            (name, v.data_ptr() if torch.is_tensor(v) else v) for name, v in kwargs.items()))
-        g = self._graphs.get(key)
-        if g is None and key not in self._seen:
-            self._seen.add(key)
-            run(self.compute)
-            return
-        if g is None:
-            # capture with nothing else in flight; the graph does not run now
-            torch.cuda.synchronize(self.device)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=self._capture):
-                run(self._capture)
-            self._graphs[key] = g
-        with torch.cuda.stream(self.compute):
-            g.replay()
+        # capture with nothing else in flight; the graph does not run now
+        torch.cuda.synchronize(self.device)
+        _lib.ple_graph_begin(self._capture)
+        try:
+            run(self._capture)
+        except BaseException:
+            _lib.ple_graph_destroy(_lib.ple_graph_end(self._capture))  # end the capture, drop it
+            raise
+        g = _lib.ple_graph_end(self._capture)
+        self._graphs[key] = g
+        _lib.ple_graph_launch(g, self.compute)
 
     def synchronize(self):
         self.copy_out.synchronize()
+
+    def close(self):
+        """Wait for every submitted step, then release the graphs and events."""
+        if not self.slots:
+            return
+        torch.cuda.synchronize(self.device)
+        for g in self._graphs.values():
+            _lib.ple_graph_destroy(g)
+        self._graphs.clear()
+        for s in self.slots:
+            for ev in s["events"]:
+                _lib.ple_event_destroy(ev)
+        self.slots = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library or CUDA may be gone
+            pass
 
 
 class PLEChain:

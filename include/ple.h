@@ -37,8 +37,9 @@
  *   - Calls are asynchronous on the given stream (0 = legacy default stream)
  *     and never synchronise it, except ple_wait with a host timeout.
  *   - The library allocates no device or host memory (except the explicit
- *     ple_host_table_alloc) and keeps no state between calls other than the
- *     thread-local error text.
+ *     ple_host_table_alloc, and the graph and event objects of the step
+ *     runtime, which the caller destroys) and keeps no state between calls
+ *     other than the thread-local error text.
  *   - bf16 data is passed as 16-bit containers (ple_bf16_t): IEEE binary32
  *     truncated to its high half, row-major.
  *   - A call returns PLE_OK when its work was enqueued. Argument errors found
@@ -486,6 +487,69 @@ ple_status ple_host_table_map_file(const char* path, size_t bytes, int32_t flags
 /* Undo ple_host_table_create_shared / _attach_shared / _map_file (the same
  * bytes and flags): unregister if registered, then unmap. */
 ple_status ple_host_table_unmap(void* host_ptr, size_t bytes, int32_t flags);
+
+/*
+ * Step runtime of the end-to-end host path (a layer run over host buffers):
+ * graph capture of a step's library calls, and one step enqueued across
+ * three caller-created streams so that neighbouring steps overlap --
+ *   copy_in   waits `computed`, uploads, records `loaded`;
+ *   compute   waits `loaded` and `returned`, runs the step, records `computed`;
+ *   copy_out  waits `computed`, reads back, records `returned`.
+ * With one set of device buffers and three events per pipeline slot, a
+ * slot's inputs are overwritten only after its previous step computed, and
+ * its device outputs only after they were read back; an event never
+ * recorded counts as complete, so a slot's first step waits for nothing.
+ * Host pointers of the copies must be pinned (or registered) for the copies
+ * to run asynchronously. Each copy is one cudaMemcpyAsync. (The pages run
+ * the layer from Python; this host path is an addition, needed because a
+ * small step's host-side launches and waits cost more than its kernels.)
+ * The graph and event objects below are the library's only allocations
+ * besides ple_host_table_alloc; the caller destroys them.
+ */
+typedef struct {
+  void* dst;        /* device (upload) or host (read-back) */
+  const void* src;  /* host (upload) or device (read-back) */
+  size_t bytes;     /* 0: skipped */
+} ple_copy;
+
+typedef struct ple_graph_s* ple_graph;
+
+/* ple_graph_begin / ple_graph_end -- capture the work the calling thread
+ * enqueues on `stream` between the two calls (thread-local capture mode:
+ * library calls only; nothing may allocate device memory meanwhile) into an
+ * instantiated graph. ple_graph_end always ends the capture; *graph is NULL
+ * on failure (a call in between that cannot be captured fails the end). */
+ple_status ple_graph_begin(cudaStream_t stream);
+ple_status ple_graph_end(cudaStream_t stream, ple_graph* graph);
+/* Launch a captured graph on `stream`; destroy one (NULL: no-op). */
+ple_status ple_graph_launch(ple_graph graph, cudaStream_t stream);
+void ple_graph_destroy(ple_graph graph);
+
+/* Events for the step runtime (timing disabled); ple_event_synchronize
+ * blocks the host until `event` completes. Destroy: NULL is a no-op. */
+ple_status ple_event_create(cudaEvent_t* event);
+void ple_event_destroy(cudaEvent_t event);
+ple_status ple_event_synchronize(cudaEvent_t event);
+
+/* ple_step_begin -- the copy-in half of a step (wait `computed`, uploads,
+ * record `loaded`) and the compute stream's waits on `loaded` and
+ * `returned`; the caller then enqueues the step's work on `compute`.
+ * ple_step_end -- record `computed` on `compute`, then the read-backs on
+ * `copy_out` after it, then record `returned`. Streams must be distinct and
+ * created (not the legacy default stream); null events, a negative copy
+ * count or a null pointer of a non-empty copy -> PLE_ERR_INVALID_ARG with
+ * nothing enqueued. */
+ple_status ple_step_begin(cudaStream_t copy_in, cudaStream_t compute, const ple_copy* uploads,
+                          int32_t num_uploads, cudaEvent_t loaded, cudaEvent_t computed,
+                          cudaEvent_t returned);
+ple_status ple_step_end(cudaStream_t compute, cudaStream_t copy_out, const ple_copy* downloads,
+                        int32_t num_downloads, cudaEvent_t computed, cudaEvent_t returned);
+/* ple_step -- ple_step_begin, the launch of `graph` on `compute`, then
+ * ple_step_end, in one call (same argument rules; `graph` non-NULL). */
+ple_status ple_step(cudaStream_t copy_in, cudaStream_t compute, cudaStream_t copy_out,
+                    const ple_copy* uploads, int32_t num_uploads, ple_graph graph,
+                    const ple_copy* downloads, int32_t num_downloads, cudaEvent_t loaded,
+                    cudaEvent_t computed, cudaEvent_t returned);
 
 /* Text of the last non-OK status on this host thread ("" if none). */
 const char* ple_last_error(void);

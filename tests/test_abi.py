@@ -231,3 +231,34 @@ def test_gated_conv_host_checks(lib):
     assert lib.ple_gated_conv(None, p, p, 1, 4, 64, p, 4, 3, None, None, p, None, None) == 1
     assert lib.ple_gated_conv(p, None, p, 1, 4, 64, p, 4, 3, None, None, p, None, None) == 1
     assert lib.ple_gated_conv(p, p, p, 1, 4, 12, p, 4, 3, None, None, p, None, None) == 1
+
+
+def test_step_runtime_host_checks(lib):
+    """The step runtime rejects missing or repeated streams, null events or
+    graphs and malformed copy lists before any CUDA call; destroying NULL
+    handles is a no-op."""
+    from hashed_gram_embedding_gb300 import _lib
+    s1, s2, s3, ev = (ctypes.c_void_p(v) for v in (16, 32, 48, 64))
+    up = _lib.copies([(256, 512, 64)])
+    bad = _lib.copies([(None, 512, 64)])
+    assert lib.ple_step(None, s2, s3, up, 1, ev, up, 1, ev, ev, ev) == 1   # legacy stream
+    assert lib.ple_step(s1, s1, s3, up, 1, ev, up, 1, ev, ev, ev) == 1    # repeated stream
+    assert lib.ple_step(s1, s2, s3, up, 1, None, up, 1, ev, ev, ev) == 1  # no graph
+    assert b"null graph" in lib.ple_last_error()
+    assert lib.ple_step(s1, s2, s3, up, 1, ev, up, 1, ev, None, ev) == 1  # null event
+    assert lib.ple_step(s1, s2, s3, bad, 1, ev, up, 1, ev, ev, ev) == 1   # null pointer
+    assert b"copy 0" in lib.ple_last_error()
+    assert lib.ple_step(s1, s2, s3, up, -1, ev, up, 1, ev, ev, ev) == 1   # negative count
+    assert lib.ple_step(s1, s2, s3, None, 1, ev, up, 1, ev, ev, ev) == 1  # missing list
+    assert lib.ple_step_begin(s1, s1, up, 1, ev, ev, ev) == 1
+    assert lib.ple_step_begin(s1, s2, bad, 1, ev, ev, ev) == 1
+    assert lib.ple_step_end(s2, s2, up, 1, ev, ev) == 1
+    assert lib.ple_step_end(s2, s3, up, 1, None, ev) == 1
+    assert lib.ple_step_end(s2, s3, bad, 1, ev, ev) == 1
+    assert lib.ple_graph_launch(None, s1) == 1
+    assert lib.ple_graph_begin(None) == 1
+    assert lib.ple_graph_end(None, None) == 1
+    assert lib.ple_event_create(None) == 1
+    assert lib.ple_event_synchronize(None) == 1
+    lib.ple_graph_destroy(None)
+    lib.ple_event_destroy(None)

@@ -271,6 +271,77 @@ def test_host_pipeline_matches_layer(depth, graphs):
         assert torch.equal(h_out[k].view(torch.int16), want.cpu().view(torch.int16)), f"step {k}"
 
 
+def test_host_pipeline_carry_over_ping_pong():
+    """Decode-style steps through PLEHostPipeline: the n-gram context and the
+    conv state alternate between two device buffers (step k reads set k % 2
+    and writes the other), so the argument tensors, and with them the
+    captured graphs, alternate too. From the fifth step on every step is one
+    native ple_step call replaying a graph. Step by step the host outputs and
+    the final carry-over equal sequential PLELayer.forward calls."""
+    from hashed_gram_embedding_gb300 import PLEHostPipeline
+    w, host, dense, table, _ = tiny_case(decode=True)
+    d_dense = {k: v.cuda() for k, v in dense.items()}
+    layer = build_layer(w, host, d_dense, table.cuda(), None)
+    T, C, R = w.num_tokens, w.hidden, w.num_reqs
+    steps = 10
+    rng = np.random.default_rng(8)
+    g = torch.Generator().manual_seed(9)
+    h_ids = [torch.from_numpy(rng.integers(0, w.token_vocab, T).astype(np.int32)).pin_memory()
+             for _ in range(steps)]
+    h_qsl = torch.from_numpy(host["query_start_loc"]).pin_memory()
+    h_hidden = [torch.randn((T, C), generator=g).to(torch.bfloat16).pin_memory()
+                for _ in range(steps)]
+    h_out = [torch.empty((T, C), dtype=torch.bfloat16).pin_memory() for _ in range(steps)]
+
+    def carry():
+        ctx0 = torch.from_numpy(host["ngram_context"]).cuda()
+        st0 = d_dense["conv_state"].clone()
+        return [ctx0, torch.empty_like(ctx0)], [st0, torch.empty_like(st0)]
+
+    ctx, st = carry()
+    pipe = PLEHostPipeline(layer, T, R, "cuda", depth=2)
+    err = dev_err_word()
+    done = None
+    for k in range(steps):
+        a, b = k % 2, (k + 1) % 2
+        done = pipe.submit(h_ids[k], h_qsl, h_hidden[k], h_out[k], ngram_context=ctx[a],
+                           ngram_context_out=ctx[b], conv_state=st[a], conv_state_out=st[b],
+                           dev_err=err)
+    done.synchronize()  # the last step's read-back
+    assert int(err.item()) == 0
+    assert len(pipe._graphs) == 2
+    rctx, rst = carry()
+    d_qsl = h_qsl.cuda()
+    for k in range(steps):
+        a, b = k % 2, (k + 1) % 2
+        want = layer.forward(h_ids[k].cuda(), d_qsl, h_hidden[k].cuda(), ngram_context=rctx[a],
+                             ngram_context_out=rctx[b], conv_state=rst[a],
+                             conv_state_out=rst[b]).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(h_out[k].view(torch.int16), want.cpu().view(torch.int16)), f"step {k}"
+    assert torch.equal(ctx[steps % 2], rctx[steps % 2])
+    assert torch.equal(st[steps % 2].view(torch.int16), rst[steps % 2].view(torch.int16))
+    pipe.close()
+
+
+def test_host_pipeline_rejects_mismatched_host_buffers():
+    from hashed_gram_embedding_gb300 import PLEHostPipeline
+    w, host, dense, table, _ = tiny_case()
+    layer = build_layer(w, host, {k: v.cuda() for k, v in dense.items()}, table.cuda(), None)
+    T, C = w.num_tokens, w.hidden
+    pipe = PLEHostPipeline(layer, T, w.num_reqs, "cuda", depth=1)
+    ids = torch.zeros((T,), dtype=torch.int32)
+    qsl = torch.from_numpy(host["query_start_loc"])
+    out = torch.empty((T, C), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="host input 2"):
+        pipe.submit(ids, qsl, torch.zeros((T, C), dtype=torch.float32), out)
+    with pytest.raises(ValueError, match="host input 0"):
+        pipe.submit(ids[:-1], qsl, torch.zeros((T, C), dtype=torch.bfloat16), out)
+    with pytest.raises(ValueError, match="host output"):
+        pipe.submit(ids, qsl, torch.zeros((T, C), dtype=torch.bfloat16), out.cuda())
+    pipe.close()
+
+
 @pytest.mark.parametrize("prefetch", [True, False])
 @pytest.mark.parametrize("on_host", [False, True])
 def test_chain_matches_layers(prefetch, on_host):
