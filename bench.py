@@ -398,7 +398,7 @@ def run_ours(args):
     layer = PLELayer(p0["table"], p0["row_scale"], p0["mult"], p0["host"]["V"], p0["host"]["O"],
                      w.eos_token_id, w.heads_per_ngram, p0["w_kv"], p0["gamma_h"], p0["gamma_k"],
                      p0["conv_w"], w.dilation, fuse_gate=fuse, fuse_ids=fuse_ids)
-    depth = 2
+    depth = args.e2e_depth
     pipe = PLEHostPipeline(layer, T, w.num_reqs, device, depth=depth)
     h_ids = torch.from_numpy(p0["host"]["input_ids"]).pin_memory()
     h_qsl = torch.from_numpy(p0["host"]["query_start_loc"]).pin_memory()
@@ -484,7 +484,8 @@ def run_ours(args):
                    {"gbs": kernels[KERNELS[0 if fuse_ids else 1]]["achieved"],
                     "frac_hbm": kernels[KERNELS[0 if fuse_ids else 1]]["frac"]}),
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "pipeline_depth": depth},
         "gpu_launches": launches_per_step(w, fuse, fuse_ids) * args.steps,
         "clocks": clocks,
     }
@@ -786,6 +787,8 @@ def main():
                     help="time ple_kv_proj + ple_gate_conv instead of the fused projection")
     ap.add_argument("--layer-sets", type=int, default=0,
                     help="layer parameter sets to rotate over (0 = workload default)")
+    ap.add_argument("--e2e-depth", type=int, default=3,
+                    help="device buffer sets rotating in the end-to-end pipeline")
     ap.add_argument("--vocab-start", type=int, default=0,
                     help="first per-head vocab prime (smaller table for profiling cases)")
     args = ap.parse_args()
