@@ -185,11 +185,13 @@ class PLEHostPipeline:
     set is reused only after the step that last used it has been read back.
     Three sets (the default) leave the transfers a step of slack: at 256 x 4
     decode the end-to-end rate is 15.6 M tokens/s/layer against 14.9 M with
-    two and 15.4 M with four (measured). The host output buffer of a step must not be read (or reused) before
-    ``synchronize`` (or the ``synchronize()`` of the object ``submit``
-    returns). The streams are PyTorch's; the copies, the events ordering
-    them and the graph launches are issued by libple's step runtime
-    (ple_step_begin / ple_step_end / ple_step), all arithmetic is in libple.
+    two and 15.4 M with four (measured). The copies run asynchronously: a
+    step's host inputs must not be changed, nor its host output read or
+    reused, before ``synchronize`` (or the ``synchronize()`` of the object
+    ``submit`` returns). The streams are PyTorch's; the copies, the events
+    ordering them and the graph launches are issued by libple's step
+    runtime (ple_step_begin / ple_step_end / ple_step); all arithmetic is in
+    libple.
 
     With ``graphs`` (the default) a slot's layer calls are captured into a
     CUDA graph (ple_graph_begin / ple_graph_end) the second time the slot
