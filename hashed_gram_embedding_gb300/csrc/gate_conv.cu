@@ -344,6 +344,9 @@ __device__ void find_tile_requests(const int32_t* __restrict__ qsl, int R, int64
   }
 }
 
+// 3 CTAs per SM for K <= 4 (80 registers: 10 staged rows in flight per lane;
+// a 4-CTA cap of 64 registers measured slower), 2 above (the taps and the
+// register ring of K rows grow with K).
 template <bool GATED, int K>
 __global__ void __launch_bounds__(kConvThreads, K <= 4 ? 3 : 2)
 conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int tile_tokens) {
