@@ -248,6 +248,8 @@ class PLEHostPipeline:
         """Enqueue one step; ``forward_kwargs`` go to PLELayer.forward (device
         carry-over buffers, dev_err). Returns the step's completion (an
         object with ``synchronize()``)."""
+        if not self.slots:
+            raise RuntimeError("PLEHostPipeline.submit after close()")
         slot = self.k % len(self.slots)
         s = self.slots[slot]
         self.k += 1

@@ -340,6 +340,8 @@ def test_host_pipeline_rejects_mismatched_host_buffers():
     with pytest.raises(ValueError, match="host output"):
         pipe.submit(ids, qsl, torch.zeros((T, C), dtype=torch.bfloat16), out.cuda())
     pipe.close()
+    with pytest.raises(RuntimeError, match="after close"):
+        pipe.submit(ids, qsl, torch.zeros((T, C), dtype=torch.bfloat16), out)
 
 
 @pytest.mark.parametrize("prefetch", [True, False])
