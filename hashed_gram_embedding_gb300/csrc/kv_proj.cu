@@ -68,17 +68,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset in every
-// CTA of ctaMask and completes bytes on the mbarrier at the same offset there.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      uint32_t bar, int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -126,15 +115,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Arrive (once the MMAs issued so far complete) on the mbarrier at the same
-// offset in every CTA of ctaMask.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -156,11 +136,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// CLUSTER = 2: the two CTAs of a cluster take vertically adjacent 128-row
-// tiles of the same 256 output columns, so they need the same W tile; each
-// loads half of it and multicasts that half to both, halving W's L2 reads.
-// A stage is then refilled only after both CTAs' MMAs released it.
-template <int CLUSTER>
+// One CTA per 128 x 256 tile (the kernel for at most 128 rows; the pair
+// kernel below takes everything larger).
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                ple_bf16_t* __restrict__ out, int M, int N, int K, int32_t* dev_err) {
@@ -181,22 +158,19 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = CLUSTER > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int cluster_id = blockIdx.x / CLUSTER;
-  const int num_clusters = gridDim.x / CLUSTER;
+  const int cluster_id = blockIdx.x;
+  const int num_clusters = gridDim.x;
   const int n_tiles = (N + BN - 1) / BN;
-  const int m_groups = ((M + BM - 1) / BM + CLUSTER - 1) / CLUSTER;
-  const int num_tiles = m_groups * n_tiles;  // tiles per CTA position in the cluster
+  const int num_tiles = ((M + BM - 1) / BM) * n_tiles;
   const int num_kb = (K + BK - 1) / BK;
-  constexpr uint16_t kAll = static_cast<uint16_t>((1u << CLUSTER) - 1);
-  // tile -> (m block, n block); the cluster's CTAs share the n block
-  auto m_block = [&](int tile) { return (tile / n_tiles) * CLUSTER + rank; };
+  // tile -> (m block, n block)
+  auto m_block = [&](int tile) { return tile / n_tiles; };
   auto n_block = [&](int tile) { return tile % n_tiles; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CLUSTER);  // released by every CTA's MMAs
+      mbar_init(empty_bar(s), 1);  // released by the MMAs' commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -215,7 +189,6 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   }
   tc_fence_before();
   __syncthreads();
-  if (CLUSTER > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // emb (A) comes from the previous kernel
@@ -237,13 +210,7 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
         tma_load_2d(smem_u32(a_smem + stage * A_STAGE), &map_a, full_bar(stage), kb * BK, m0);
-        if constexpr (CLUSTER == 1) {
-          tma_load_2d(smem_u32(b_smem + stage * B_STAGE), &map_b, full_bar(stage), kb * BK, n0);
-        } else {
-          constexpr int kPart = BN / CLUSTER;  // W rows this CTA loads for the cluster
-          tma_load_2d_multicast(smem_u32(b_smem + stage * B_STAGE + rank * kPart * BK * 2), &map_b,
-                                full_bar(stage), kb * BK, n0 + rank * kPart, kAll);
-        }
+        tma_load_2d(smem_u32(b_smem + stage * B_STAGE), &map_b, full_bar(stage), kb * BK, n0);
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -276,9 +243,8 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             const uint64_t koff = static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
             umma_bf16(d_tmem, a_desc + koff, b_desc + koff, (kb | kk) != 0 ? 1u : 0u);
           }
-          // frees the stage (in every CTA whose smem it fed) once these MMAs finish
-          if constexpr (CLUSTER == 1) umma_commit(empty_bar(stage));
-          else umma_commit_multicast(empty_bar(stage), kAll);
+          // frees the stage once these MMAs finish
+          umma_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -335,9 +301,6 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
-  // No CTA leaves while a peer may still multicast into its shared memory or
-  // arrive on its barriers.
-  if (CLUSTER > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -392,20 +355,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// Multicast variant: the box lands at the same shared-memory offset in every
-// CTA of ctaMask, and each landing completes on the mbarrier at offset `bar`
-// in that CTA's pair leader (bar: this CTA's own barrier address with the
-// pair bit, bit 24 of a shared::cluster address, cleared).
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           uint32_t bar, int x, int y,
-                                                           uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
 
@@ -560,9 +509,9 @@ __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int
   ge.gate_out[m] = gate_of(sh, sk, sd, ge.C, ge.eps);
 }
 
-// A work unit of the pair kernel: 256 rows from m_base, PAIRS x 256 columns
-// (this pair's from n_base), or -- units >= full_units, PAIRS == 1 only --
-// one 128-column half of a 256 x 256 tile. Splitting the last round's tiles
+// A work unit of the pair kernel: 256 rows from m_base, 256 columns from
+// n_base, or -- units >= full_units -- one 128-column half of a 256 x 256
+// tile. Splitting the last round's tiles
 // in halves lets twice as many CTA pairs share it when it would otherwise
 // leave more than half of them idle.
 struct PairUnit {
@@ -571,10 +520,9 @@ struct PairUnit {
   int cols;  // 256 or 128
 };
 
-template <int PAIRS>
-__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups, int pidx) {
+__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups) {
   PairUnit t;
-  if (PAIRS == 1 && u >= full_units) {
+  if (u >= full_units) {
     const int h = u - full_units;
     const int v = full_units + (h >> 1);
     t.m_base = (v / n_groups) * 2 * BM;
@@ -582,20 +530,16 @@ __device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_group
     t.cols = BN / 2;
   } else {
     t.m_base = (u / n_groups) * 2 * BM;
-    t.n_base = ((u % n_groups) * PAIRS + pidx) * BN;
+    t.n_base = (u % n_groups) * BN;
     t.cols = BN;
   }
   return t;
 }
 
-// PAIRS = CTA pairs per cluster. PAIRS = 2: the two pairs of a 4-CTA cluster
-// take adjacent 256-column tiles of the same 256 rows; CTAs 0/2 (and 1/3)
-// need the same 128 rows of A, so each loads 64 of them and multicasts them
-// to both, cutting each SM's A traffic in half; a stage may then be refilled
-// only after both pairs' MMAs released it.
-// Units [0, full_units) are full tiles; with PAIRS == 1 the units past them
-// are half tiles (2 per remaining tile; map_b_half loads 64 W rows per CTA).
-template <int PAIRS, bool GATE>
+// One CTA pair per cluster. Units [0, full_units) are full tiles; the units
+// past them are half tiles (2 per remaining tile; map_b_half loads 64 W rows
+// per CTA).
+template <bool GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
@@ -621,22 +565,20 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const uint32_t leader = rank & ~1u;       // even CTA of the pair: issues the MMAs
-  const int pidx = static_cast<int>(rank >> 1);  // pair within the cluster
-  const int cl = blockIdx.x / (2 * PAIRS);
-  const int num_cl = gridDim.x / (2 * PAIRS);
+  const int cl = blockIdx.x / 2;
+  const int num_cl = gridDim.x / 2;
   const int n_tiles = (N + BN - 1) / BN;
-  const int n_groups = (n_tiles + PAIRS - 1) / PAIRS;
+  const int n_groups = n_tiles;
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
-  const int base_units = m_tiles * n_groups;  // (256 rows, PAIRS x 256 columns) per cluster
-  const int num_units = PAIRS == 1 ? full_units + 2 * (base_units - full_units) : base_units;
+  const int base_units = m_tiles * n_groups;  // (256 rows, 256 columns) per cluster
+  const int num_units = full_units + 2 * (base_units - full_units);
   const int num_kb = (K + BK * P_ATOMS - 1) / (BK * P_ATOMS);
-  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << (2 * PAIRS)) - 1);
-  const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pidx));
+  constexpr uint16_t pair_mask = 3u;  // both CTAs of the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(full_bar(s), 1);      // the leader's expect_tx; bytes from both CTAs
-      mbar_init(empty_bar(s), PAIRS); // one commit of each pair's leader per use
+      mbar_init(empty_bar(s), 1);     // one commit of the pair leader per use
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -675,7 +617,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     bool ok = true;
     const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
     for (int u = cl; ok && u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit<PAIRS>(u, full_units, n_groups, pidx);
+      const PairUnit t = pair_unit(u, full_units, n_groups);
       const bool half = t.cols != BN;
       const int m0 = t.m_base + q * BM;
       const int n0 = t.n_base + q * (t.cols / 2);
@@ -691,15 +633,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         for (int at = 0; at < P_ATOMS; ++at) {
           const int kx = (kb * P_ATOMS + at) * BK;
-          if constexpr (PAIRS == 1) {
-            tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM), &map_a,
-                             leader_full, kx, m0);
-          } else {
-            tma_load_2d_pair_multicast(
-                smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM + pidx * (P_A_ATOM / 2)),
-                &map_a, leader_full, kx, m0 + pidx * (BM / 2),
-                static_cast<uint16_t>((1u << q) | (1u << (q + 2))));
-          }
+          tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM), &map_a,
+                           leader_full, kx, m0);
           tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE + at * P_B_ATOM),
                            half ? &map_b_half : &map_b, leader_full, kx, n0);
         }
@@ -720,7 +655,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       bool ok = true;
       for (int u = cl; ok && u < num_units; u += num_cl) {
         const uint32_t idesc =
-            pair_unit<PAIRS>(u, full_units, n_groups, pidx).cols == BN ? kIdescPair : kIdescPairHalf;
+            pair_unit(u, full_units, n_groups).cols == BN ? kIdescPair : kIdescPairHalf;
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -738,7 +673,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                              (kb | at | kk) != 0 ? 1u : 0u);
             }
           }
-          umma_commit_pair(empty_bar(stage), kClusterMask);  // frees the stage everywhere it fed
+          umma_commit_pair(empty_bar(stage), pair_mask);  // frees the stage in both CTAs
           if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -763,7 +698,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
         break;
       }
       tc_fence_after();
-      const PairUnit t = pair_unit<PAIRS>(u, full_units, n_groups, pidx);
+      const PairUnit t = pair_unit(u, full_units, n_groups);
       const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
       const int n_base = t.n_base;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
@@ -872,27 +807,22 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
                      const char* name) {
   // Kernel: the CTA-pair kernel when there are at least two 128-row blocks
   // (always, with the fused gate), else one CTA per tile.
-  // PLE_KVPROJ_MODE = quad | pair | cluster | single overrides (launch-shape
-  // sweeps and tests): quad = two CTA pairs per cluster sharing A by
-  // multicast; cluster = 2-CTA clusters that share the W tile by TMA
-  // multicast, each CTA with its own 1-SM MMAs. The fused gate takes pair or
-  // quad only.
-  enum { kSingle, kCluster, kPair, kQuad } mode = (M > BM || ge != nullptr) ? kPair : kSingle;
+  // PLE_KVPROJ_MODE = pair | single overrides that choice for the plain
+  // projection (launch-shape sweeps and tests); the fused gate is always
+  // the pair kernel.
+  bool paired = M > BM || ge != nullptr;
   if (const char* e = getenv("PLE_KVPROJ_MODE")) {
-    if (strcmp(e, "single") == 0) mode = kSingle;
-    else if (strcmp(e, "cluster") == 0) mode = kCluster;
-    else if (strcmp(e, "pair") == 0) mode = kPair;
-    else if (strcmp(e, "quad") == 0) mode = kQuad;
+    if (strcmp(e, "single") == 0) paired = false;
+    else if (strcmp(e, "pair") == 0) paired = true;
   }
-  if (ge != nullptr && mode != kQuad) mode = kPair;
-  const bool paired = mode == kPair || mode == kQuad;
-  const int cluster = mode == kSingle ? 1 : (mode == kQuad ? 4 : 2);
+  if (ge != nullptr) paired = true;
+  const int cluster = paired ? 2 : 1;
   CUtensorMap map_a, map_b, map_b_half;
-  ple_status s = make_map(&map_a, emb, M, K, mode == kQuad ? BM / 2 : BM);  // A rows a CTA loads
+  ple_status s = make_map(&map_a, emb, M, K, BM);  // A rows a CTA loads
   if (s != PLE_OK) return s;
-  s = make_map(&map_b, w, N, K, mode == kSingle ? BN : BN / 2);  // W rows one CTA loads per stage
+  s = make_map(&map_b, w, N, K, paired ? BN / 2 : BN);  // W rows one CTA loads per stage
   if (s != PLE_OK) return s;
-  if (mode == kPair) {
+  if (paired) {
     s = make_map(&map_b_half, w, N, K, BN / 4);  // a half tile's W rows per CTA
     if (s != PLE_OK) return s;
   } else {
@@ -901,28 +831,16 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int,
                           int32_t*, GateEpi);
   using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
-  PairFn pair_fn = nullptr;
-  TileFn tile_fn = nullptr;
-  if (paired) {
-    if (ge != nullptr) pair_fn = mode == kQuad ? kv_proj_pair_kernel<2, true> : kv_proj_pair_kernel<1, true>;
-    else pair_fn = mode == kQuad ? kv_proj_pair_kernel<2, false> : kv_proj_pair_kernel<1, false>;
-  } else {
-    tile_fn = mode == kCluster ? kv_proj_kernel<2> : kv_proj_kernel<1>;
-  }
+  const PairFn pair_fn = ge != nullptr ? kv_proj_pair_kernel<true> : kv_proj_pair_kernel<false>;
+  const TileFn tile_fn = kv_proj_kernel;
   const void* fn = paired ? reinterpret_cast<const void*>(pair_fn) : reinterpret_cast<const void*>(tile_fn);
   const size_t smem = paired ? kPairSmemBytes : kSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, "kv projection: smem attribute");
-  // work units per cluster: 256 rows x (pairs x 256 columns) for the pair
-  // kernels, else 128-row tiles per cluster position
-  int units;
-  if (paired) {
-    const int pairs = cluster / 2;
-    units = ((M + 2 * BM - 1) / (2 * BM)) * (((N + BN - 1) / BN + pairs - 1) / pairs);
-  } else {
-    units = ((M + BM * cluster - 1) / (BM * cluster)) * ((N + BN - 1) / BN);
-  }
+  // work units: 256 rows x 256 columns for the pair kernel, else 128 x 256 tiles
+  int units = paired ? ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN)
+                     : ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   // persistent grid: as many clusters as can be resident at once (a GPC may
   // not hold a whole number of clusters), no more than there are units
   int max_clusters = num_sms() / cluster;
@@ -944,12 +862,12 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
       max_clusters = active;
     cudaGetLastError();  // a failed query only leaves the SM-count bound
   }
-  // Last-round split (CTA pairs, one pair per cluster): when the tiles of
-  // the last round would keep at most half of the clusters busy, each of
-  // them becomes two 128-column halves, so the round ends in about half the
-  // time. PLE_KVPROJ_SPLIT=0 turns it off (launch-shape sweeps and tests).
+  // Last-round split (CTA pairs): when the tiles of the last round would
+  // keep at most half of the clusters busy, each of them becomes two
+  // 128-column halves, so the round ends in about half the time.
+  // PLE_KVPROJ_SPLIT=0 turns it off (launch-shape sweeps and tests).
   int full_units = units;
-  if (mode == kPair) {
+  if (paired) {
     const int rem = units % max_clusters;
     bool split = rem > 0 && 2 * rem <= max_clusters;
     if (const char* e = getenv("PLE_KVPROJ_SPLIT"))

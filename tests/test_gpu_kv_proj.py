@@ -70,15 +70,14 @@ def test_kv_proj_prefill_8k_shape():
     assert_close(bits(kv), bits(lib_ref), what="kv vs cuBLAS")
 
 
-@pytest.mark.parametrize("mode", ["single", "cluster", "pair", "pair-nosplit", "quad"])
+@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit"])
 @pytest.mark.parametrize("M,E,C", [(512, 512, 1024), (300, 2048, 4096), (129, 200, 48),
                                    (257, 72, 112), (1000, 128, 128)])
 def test_kv_proj_kernel_variants(M, E, C, mode, monkeypatch):
-    """Each kernel variant -- one CTA per 128 x 256 tile, 2-CTA clusters
-    sharing the W tile by multicast, CTA pairs with cta_group::2 MMAs over
-    256 x 256 tiles (with and without the last round split into 128-column
-    halves), two CTA pairs per cluster sharing A by multicast -- gives the
-    oracle's result, ragged edges included."""
+    """Each kernel variant -- one CTA per 128 x 256 tile, CTA pairs with
+    cta_group::2 MMAs over 256 x 256 tiles (with and without the last round
+    split into 128-column halves) -- gives the oracle's result, ragged edges
+    included."""
     monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
     monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
     emb = rand_bf16((M, E), 0.5, M + E)
@@ -91,7 +90,7 @@ def test_kv_proj_kernel_variants(M, E, C, mode, monkeypatch):
     assert_close(bits(kv), oracle_kv_proj(bits(emb), bits(w)), what=f"kv {mode} {M}x{E}x{2*C}")
 
 
-@pytest.mark.parametrize("mode", ["single", "cluster", "pair", "pair-nosplit", "quad"])
+@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit"])
 def test_kv_proj_variants_prefill_8k_against_cublas(mode, monkeypatch):
     monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
     monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
