@@ -1,19 +1,28 @@
 #!/usr/bin/env python
 """Benchmark of the per-layer n-gram embedding (PLE / Engram) path on GB300.
 
-One step = one pass of the whole hot path over one batch: n-gram ids ->
-row gather -> kv_proj -> gate + short conv (four libple launches), on the
-8192-token prefill workload (16 ragged requests, 16 heads x 128 over an 8.2 GB
-bf16 table in HBM, hidden 4096, kv_proj 2048 -> 2 x 4096, conv K=4 d=3).
-Metric: PLE tokens/sec/layer (one step processes one layer).
+One step = one pass of the whole hot path over one batch for one layer:
+n-gram ids -> row gather -> kv_proj (with the gate's reductions) -> gated
+short conv (libple launches only). Metric: PLE tokens/sec/layer.
 
-Steps rotate over 4 independent layer parameter sets (table, kv_proj weight,
+The default run measures every workload of the input recipe in one go and
+prints ONE JSON line: the headline is the largest workload, fp8x8 (8 layers,
+each with its own 8 GiB fp8 e4m3 table and per-row scales, 32768-token
+prefill over 64 ragged requests, Zipf tokens, hidden 4096; one step = one
+layer, rotating over the 8 layers), and "configs" holds the same figures for
+every workload: tiny (512 tokens), prefill8k (8192 tokens, 8.2 GB bf16 table
+in HBM), decode256x4 (256 x 4 decode tokens with carried context and conv
+state) and uva32g (8192 tokens over a 32 GiB bf16 table in pinned host
+memory read over the host link, reported against the measured link rate and
+the PCIe5 x16 nominal).
+
+Steps rotate over independent layer parameter sets (table, kv_proj weight,
 gammas, conv taps, hash multipliers, hidden states, token ids): one rotation
 touches far more than the 129 MB L2, so no step finds its inputs cached by an
 earlier one and no L2 flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill8k|decode256x4|tiny|uva32g|fp8x8]
+                  [--workload all|fp8x8|prefill8k|decode256x4|tiny|uva32g]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path has no exchange step on one node's replicas); rank 0 prints one
@@ -176,10 +185,11 @@ def source_hash(path):
     return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """dram bytes per launch from the committed ncu summary of ``kernel``,
-    or None when the summary is missing or the kernel source changed since."""
-    summary = os.path.join(ROOT, "profiles", f"{kernel}_prefill8k.md")
+def ncu_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu summary of ``kernel`` on
+    ``workload``, or None when the summary is missing or the kernel source
+    changed since."""
+    summary = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "hashed_gram_embedding_gb300", "csrc",
                        {"kv_proj": "kv_proj.cu", "kv_proj_gate": "kv_proj.cu",
                         "ngram_lookup": "lookup.cu",
@@ -249,12 +259,19 @@ def make_sets(torch, w, device, num_sets):
 # our arm
 # ---------------------------------------------------------------------------
 
+# The default run: the headline on the largest workload (8 fp8 layers, 32k
+# tokens), then every other workload measured in the same run and reported
+# under "configs" in the same line.
+HEADLINE = "fp8x8"
+ALL_WORKLOADS = ("fp8x8", "tiny", "prefill8k", "decode256x4", "uva32g")
+PCIE5_X16_GBS = 63.0  # nominal per direction, context for host-table gathers
+
+
 def run_ours(args):
+    import gc
     import torch
     from hashed_gram_embedding_gb300 import build as build_mod
     from hashed_gram_embedding_gb300 import _lib
-    from hashed_gram_embedding_gb300 import workloads as wl
-    from hashed_gram_embedding_gb300 import PLELayer
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
@@ -264,7 +281,50 @@ def run_ours(args):
         build_mod.build()
     barrier()
 
-    w = wl.WORKLOADS[args.workload]
+    names = ALL_WORKLOADS if args.workload == "all" else (args.workload,)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    lines = {}
+    for i, name in enumerate(names):
+        lines[name] = measure_workload(torch, args, name, device, rank, world, headline=i == 0)
+        gc.collect()  # host tables hold their owner in a reference cycle
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    if rank != 0:
+        return None
+    line = lines[names[0]]
+    line["clocks"] = clocks
+    if len(names) > 1:
+        line["configs"] = {n: config_summary(lines[n]) for n in names}
+    return line
+
+
+def config_summary(line):
+    """The per-workload figures reported side by side under "configs"."""
+    out = {"value": line["value"], "unit": line["unit"], "ms_per_step": line["ms_per_step"],
+           "mode": line["config"]["mode"], "num_tokens": line["config"]["num_tokens"],
+           "table_loc": line["config"]["table_loc"], "table_dtype": line["config"]["table_dtype"],
+           "e2e": line["e2e"]["value"], "gather": line["gather"],
+           "roofline": {k: line["roofline"][k] for k in ("kernel", "bound", "achieved", "unit",
+                                                         "frac")},
+           "kernels": {k: {"us": v["us"], "achieved": v["achieved"], "unit": v["unit"],
+                           "frac": v["frac"]} for k, v in line["kernels"].items()}}
+    if "chain" in line:
+        out["chain"] = line["chain"]
+    if "overlap" in line:
+        out["overlap"] = line["overlap"]
+    return out
+
+
+def measure_workload(torch, args, name, device, rank, world, headline):
+    """Set up one workload's layer sets, time its steps (per-kernel events,
+    then CUDA-graph replays), its end-to-end steps from pinned host buffers,
+    and return its JSON line (rank 0; None elsewhere)."""
+    from hashed_gram_embedding_gb300 import _lib
+    from hashed_gram_embedding_gb300 import workloads as wl
+    from hashed_gram_embedding_gb300 import PLELayer
+
+    w = wl.WORKLOADS[name]
     if args.vocab_start:
         w = wl.scaled(w, vocab_start=args.vocab_start)  # smaller table (profiling cases)
     # one step = one layer; multi-layer workloads rotate over their layers
@@ -337,13 +397,11 @@ def run_ours(args):
             if ev is not None:
                 ev[j + 1].record(st)
 
-    sampler = ClockSampler(local_rank)
-    sampler.start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+        raise RuntimeError(f"{name}: device error word {int(err.item())} during warm-up")
 
     # ---- eager steps with events between the kernels (per-kernel times) ----
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
@@ -361,14 +419,14 @@ def run_ours(args):
             per_kernel[k].append(ev[j].elapsed_time(ev[j + 1]))
     eager_ms = max_over_ranks(eager_ms, device)
     if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+        raise RuntimeError(f"{name}: device error word {int(err.item())} in the timed region")
 
     # ---- timed region: K steps replayed from CUDA graphs (one per layer
     # set, captured once), device events on the replay stream ----
     graphs, graph_error = capture_graphs(torch, step, num_sets, device)
     if graphs is not None:
-        for i in range(min(args.warmup, len(graphs))):
-            graphs[i].replay()
+        for i in range(max(args.warmup, len(graphs))):
+            graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
@@ -383,10 +441,11 @@ def run_ours(args):
         barrier()
         total_ms = max_over_ranks(g0.elapsed_time(g1), device)
         if int(err.item()) != 0:
-            raise RuntimeError(f"device error word {int(err.item())} in the graph replays")
+            raise RuntimeError(f"{name}: device error word {int(err.item())} in the graph replays")
         mode = "cuda_graph"
     else:
         total_ms, mode = eager_ms, "eager"
+    del graphs
 
     # ---- end to end through PLEHostPipeline with pinned host buffers ----
     # Every step uploads its inputs (token ids, query_start_loc, hidden) from
@@ -425,8 +484,15 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), device)
-    clocks = sampler.stop()
+    pipe.close()
+    del pipe, layer
 
+    extra = {}
+    if rank == 0 and w.table_loc == "host":
+        extra["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
+    chain_layers = args.chain_layers or (w.num_layers if w.num_layers > 1 else 0)
+    if chain_layers > 1:
+        extra["chain"] = chain_timing(torch, w, sets, device, err, fuse, chain_layers)
     if rank != 0:
         return None
     peaks, peak_kind = load_peaks()
@@ -455,51 +521,56 @@ def run_ours(args):
     dominant = max(KERNELS, key=lambda k: kernels[k]["us"])
     dk = kernels[dominant]
     bound, amount = work[dominant]
-    traffic = ncu_traffic(dominant) if args.workload == "prefill8k" else None
+    traffic = None if args.vocab_start else ncu_traffic(dominant, w.name)
     dpeak = {"tensor": peaks["bf16_tflops"], "link": link_gbs}.get(dk["bound"], peaks["hbm_gbs"])
     roofline = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
                 "peak": dpeak, "unit": dk["unit"], "frac": dk["frac"],
                 "peak_source": ("pinned host-to-device copy measured in this run"
-                                if dk["bound"] == "link" else peak_kind),
+                                if dk["bound"] == "link" else
+                                f"{peak_kind} ({'bf16 burst' if dk['bound'] == 'tensor' else 'HBM copy'})"),
                 "algorithmic_per_launch": amount, "traffic": traffic}
+    gk = "lookup" if not fuse_ids else "ngram_lookup"
+    if w.table_loc == "host":
+        gather_line = {"kernel": gk, "gbs": kernels[gk]["achieved"], "link_gbs": link_gbs,
+                       "frac_link": kernels[gk]["frac"],
+                       "pcie5_x16_nominal_gbs": PCIE5_X16_GBS,
+                       "frac_pcie5_x16_nominal": round(kernels[gk]["achieved"] / PCIE5_X16_GBS, 3)}
+    else:
+        gather_line = {"kernel": gk, "gbs": kernels[gk]["achieved"], "frac_hbm": kernels[gk]["frac"],
+                       "note": ("algorithmic bytes; Zipf tokens hit L2 for repeated rows"
+                                if w.token_dist == "zipf" else "algorithmic bytes")}
     value = world * args.steps * T / (total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.table_dtype == "bf16" else "fp8->bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded workload recipe; no dataset)",
         "config": {"workload": w.name, "mode": mode, "num_tokens": T, "num_reqs": w.num_reqs,
-                   "heads": H,
-                   "head_dim": w.head_dim, "table_rows": int(sets[0]["table"].shape[0]),
-                   "table_loc": w.table_loc, "table_dtype": w.table_dtype, "hidden": C,
-                   "conv_kernel": w.conv_k, "dilation": w.dilation,
-                   "fuse_gate": fuse, "fuse_ids": fuse_ids, "layer_sets": num_sets,
+                   "heads": H, "head_dim": w.head_dim,
+                   "table_rows": int(sets[0]["table"].shape[0]), "table_loc": w.table_loc,
+                   "table_dtype": ("fp8 e4m3 + float32 row scale" if w.table_dtype == "fp8"
+                                   else "bf16"),
+                   "hidden": C, "conv_kernel": w.conv_k, "dilation": w.dilation,
+                   "layers": w.num_layers, "fuse_gate": fuse, "fuse_ids": fuse_ids,
+                   "layer_sets": num_sets,
                    "l2": f"inputs rotate over {num_sets} layer sets (> 129 MB L2 per rotation); no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
         "kernels": kernels,
-        "gather": ({"gbs": kernels["lookup"]["achieved"], "link_gbs": link_gbs,
-                    "frac_link": kernels["lookup"]["frac"]} if w.table_loc == "host" else
-                   {"gbs": kernels[KERNELS[0 if fuse_ids else 1]]["achieved"],
-                    "frac_hbm": kernels[KERNELS[0 if fuse_ids else 1]]["frac"]}),
+        "gather": gather_line,
         "e2e": {"value": round(world * args.steps * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "pipeline_depth": depth},
         "gpu_launches": launches_per_step(w, fuse, fuse_ids) * args.steps,
-        "clocks": clocks,
     }
-    if w.table_loc == "host":
-        line["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
+    line.update(extra)
     line["eager"] = {"ms_per_step": round(eager_ms / args.steps, 4),
                      "value": round(world * args.steps * T / (eager_ms * 1e-3), 1),
                      "note": "same steps launched one by one, events between kernels"}
     if graph_error:
         line["eager"]["graph_capture_error"] = graph_error
-    chain_layers = args.chain_layers or (w.num_layers if w.num_layers > 1 else 0)
-    if chain_layers > 1:
-        line["chain"] = chain_timing(torch, w, sets, device, err, fuse, chain_layers)
-    if not args.no_cpu_baseline:
+    if headline and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, sets[0], budget_s=args.cpu_seconds)
     return line
 
@@ -738,7 +809,7 @@ def run_reference(args):
     if rank != 0:
         return None
     device = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
-    w = wl.WORKLOADS[args.workload]
+    w = wl.WORKLOADS[HEADLINE if args.workload == "all" else args.workload]
     p = make_sets(torch, w, device, 1)[0]
     qsl = p["host"]["query_start_loc"]
     max_tokens = args.ref_tokens
@@ -773,7 +844,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="prefill8k")
+    ap.add_argument("--workload", default="all",
+                    help="all (default: the fp8x8 headline, then every other workload under "
+                         "\"configs\") or one of " + ", ".join(ALL_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -1,12 +1,15 @@
 """Shared test utilities: bf16 bit conversions, tolerances, case builders.
 
 Tolerances (float stages; ids and gathered rows are compared bit for bit):
-  |gpu - ref| <= rtol * |ref| + atol_frac * rms(ref), elementwise,
-with rtol = atol_frac = 1e-2 for bf16 tables and 3e-2 for the fp8 chain.
-The absolute part is scaled by the data's rms because the synthetic
-activations are far below 1 (kv ~ 2e-2): a plain 1e-2 absolute bound would
-accept anything. One bf16 rounding step is 2^-8 relative, so an honest result
-sits well inside 1e-2.
+  |gpu - ref| <= rtol * |ref| + min(atol, atol_frac * rms(ref)), elementwise,
+with rtol = atol_frac = 1e-2 for bf16 tables and 3e-2 for the fp8 chain, and
+the absolute cap atol = 1e-2 (3e-2 with an fp8 table) -- the stated bound of
+1e-2 absolute / 1e-2 relative (3e-2 with fp8 tables). The absolute part is
+scaled by the data's rms because the synthetic activations are far below 1
+(kv ~ 2e-2), where a plain 1e-2 absolute bound would accept anything; the cap
+keeps it from ever being looser than that bound where the data's rms is above
+1 (unit-variance conv inputs). One bf16 rounding step is 2^-8 relative, so an
+honest result sits well inside 1e-2.
 
 Outputs downstream of kv_proj in the whole chain use CHAIN_ATOL_FRAC = 2e-2:
 the kernel's fp32-accumulated kv and the oracle's float64 kv may land one bf16
@@ -40,14 +43,18 @@ def bf16_values(a):
     return b.view(np.float32).astype(np.float64)
 
 
-def assert_close(gpu_bits, ref_bits, rtol=1e-2, atol_frac=1e-2, what=""):
+def assert_close(gpu_bits, ref_bits, rtol=1e-2, atol_frac=1e-2, atol=None, what=""):
+    """Elementwise |gpu - ref| <= rtol*|ref| + min(atol, atol_frac*rms(ref)).
+    atol defaults to 1e-2, or 3e-2 when rtol is the fp8 tolerance (>= 3e-2)."""
     g = bf16_values(gpu_bits)
     r = bf16_values(ref_bits)
     assert g.shape == r.shape, (what, g.shape, r.shape)
     if r.size == 0:
         return
+    if atol is None:
+        atol = 3e-2 if rtol >= 3e-2 else 1e-2
     rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
-    tol = rtol * np.abs(r) + atol_frac * max(rms, 1e-30)
+    tol = rtol * np.abs(r) + min(atol, atol_frac * max(rms, 1e-30))
     err = np.abs(g - r)
     bad = ~(err <= tol)
     if bad.any():

@@ -5,7 +5,9 @@ projection does the gate's reductions, ple_kv_proj_gate + ple_gated_conv
 (fuse_gate=False runs ple_kv_proj + ple_gate_conv)) against the oracle's layer_forward: the tiny workload with a
 bf16 and with an fp8 table (every token, both projections), the decode
 workload's carry-over outputs, and the 8k prefill at full size (sampled
-tokens with their conv windows)."""
+tokens with their conv windows); the four-layer chain (PLEChain, with and
+without cross-layer prefetch) and layers over host tables against the same
+oracle."""
 
 import numpy as np
 import pytest
@@ -440,3 +442,140 @@ def test_layer_in_cuda_graph_matches_eager(on_host):
         assert torch.equal(out.view(torch.int16), want.view(torch.int16)), f"replay {k}"
     if owner is not None:
         owner.close()
+
+
+@pytest.mark.parametrize("prefetch", [True, False])
+@pytest.mark.parametrize("on_host", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_chain_matches_oracle(prefetch, on_host, dtype):
+    """PLEChain over four layers against the oracle's layer_forward for each
+    layer (its own multipliers, table, weights, hidden state and conv state;
+    the n-gram context shared by all layers): ids of the carried context bit
+    for bit, every layer's y and conv-state carry-over within the chain
+    tolerance; next layers' gathers prefetched on a side stream or run in
+    line, tables in HBM or in pinned host memory (table-order gather)."""
+    from hashed_gram_embedding_gb300 import PLEChain, _lib
+    L = 4
+    tol = 1e-2 if dtype == "bf16" else 3e-2
+    w = wl.scaled(wl.WORKLOADS["tiny"], num_layers=L, decode=True, table_dtype=dtype)
+    layers, hiddens, states, owners, refs = [], [], [], [], []
+    host = None
+    for i in range(L):
+        _, host_i, dense, table, row_scale = tiny_case(w, seed_step=i)
+        host = host or host_i
+        d = {k: v.cuda() for k, v in dense.items()}
+        if on_host and dtype == "bf16":
+            owner = _lib.HostTable(table.shape[0], table.shape[1], torch.bfloat16)
+            owner.tensor.copy_(table)
+            owners.append(owner)
+            tab = owner.tensor
+        elif on_host:
+            tab = table.pin_memory()
+        else:
+            tab = table.cuda()
+        rs = None if row_scale is None else row_scale.cuda()
+        layers.append(PLELayer(tab, rs, host["multipliers"][i], host["V"], host["O"],
+                               w.eos_token_id, w.heads_per_ngram, d["w_kv"], d["gamma_h"],
+                               d["gamma_k"], d["conv_w"], w.dilation))
+        hiddens.append(d["hidden"])
+        states.append(d["conv_state"])
+        refs.append(oracle.layer_forward(
+            host["input_ids"], host["query_start_loc"], host["ngram_context"],
+            host["multipliers"][i], host["V"], host["O"], w.eos_token_id, w.heads_per_ngram,
+            bits(table) if row_scale is None else table.numpy(),
+            None if row_scale is None else row_scale.numpy(), bits(dense["hidden"]),
+            bits(dense["w_kv"]), bits(dense["gamma_h"]), bits(dense["gamma_k"]), 1e-6,
+            bits(dense["conv_w"]), w.dilation, bits(dense["conv_state"])))
+    T, C = w.num_tokens, w.hidden
+    ids = torch.from_numpy(host["input_ids"]).cuda()
+    qsl = torch.from_numpy(host["query_start_loc"]).cuda()
+    ctx = torch.from_numpy(host["ngram_context"]).cuda()
+    outs = [torch.empty((T, C), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    st_out = [torch.empty_like(s) for s in states]
+    ctx_out = torch.empty_like(ctx)
+    err = dev_err_word()
+    PLEChain(layers, prefetch=prefetch, prefetch_ctas=76).forward(
+        ids, qsl, hiddens, outs, ngram_context=ctx, ngram_context_out=ctx_out,
+        conv_states=states, conv_states_out=st_out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(ctx_out.cpu().numpy(), np.asarray(refs[0]["ngram_context_out"]))
+    for i in range(L):
+        assert_close(bits(outs[i]), refs[i]["y"], rtol=tol, atol_frac=max(tol, CHAIN_ATOL_FRAC),
+                     what=f"layer {i} y")
+        assert_close(bits(st_out[i]), refs[i]["conv_state_out"], rtol=tol,
+                     atol_frac=max(tol, CHAIN_ATOL_FRAC), what=f"layer {i} conv state")
+    for o in owners:
+        o.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_host_table_layer_every_token(dtype):
+    """PLELayer.forward over a table in pinned host memory (read over the
+    host link in table order) against the oracle's layer_forward: ids and
+    gathered rows bit for bit, y of every token in tolerance."""
+    from hashed_gram_embedding_gb300 import _lib
+    w = wl.scaled(wl.WORKLOADS["tiny"], table_dtype=dtype)
+    w, host, dense, table, row_scale = tiny_case(w)
+    d = {k: v.cuda() for k, v in dense.items()}
+    owner = None
+    if dtype == "bf16":
+        owner = _lib.HostTable(table.shape[0], table.shape[1], torch.bfloat16)
+        owner.tensor.copy_(table)
+        tab = owner.tensor
+    else:
+        tab = table.pin_memory()
+    layer = build_layer(w, host, d, tab, None if row_scale is None else row_scale.cuda())
+    err = dev_err_word()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(),
+                      torch.from_numpy(host["query_start_loc"]).cuda(), d["hidden"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.layer_forward(host["input_ids"], host["query_start_loc"], None,
+                               host["multipliers"][0], host["V"], host["O"], w.eos_token_id,
+                               w.heads_per_ngram,
+                               bits(table) if row_scale is None else table.numpy(),
+                               None if row_scale is None else row_scale.numpy(),
+                               bits(dense["hidden"]), bits(dense["w_kv"]), bits(dense["gamma_h"]),
+                               bits(dense["gamma_k"]), 1e-6, bits(dense["conv_w"]), w.dilation)
+    b = layer.buffers(w.num_tokens, y.device)
+    assert np.array_equal(b["ids"].cpu().numpy(), ref["ids"])
+    assert np.array_equal(bits(b["emb"]), ref["emb"])
+    tol = 1e-2 if dtype == "bf16" else 3e-2
+    assert_close(bits(y), ref["y"], rtol=tol, atol_frac=max(tol, CHAIN_ATOL_FRAC), what="y")
+    if owner is not None:
+        owner.close()
+
+
+def test_uva32g_layer_sampled():
+    """The host-table workload at full size (a 32 GiB bf16 table in pinned
+    host memory, 8192 tokens) through PLELayer.forward: every id bit for
+    bit, every gathered row of the sampled tokens bit for bit, and y against
+    the oracle on >= 2048 sampled tokens with their conv history."""
+    w = wl.WORKLOADS["uva32g"]
+    host = wl.host_inputs(w)
+    table, _ = wl.make_table(torch, w, "cuda")
+    assert not table.is_cuda
+    dense = wl.dense_inputs(torch, w, "cuda", random_gamma=True)
+    layer = build_layer(w, host, dense, table, None)
+    qsl = host["query_start_loc"]
+    err = dev_err_word()
+    y = layer.forward(torch.from_numpy(host["input_ids"]).cuda(), torch.from_numpy(qsl).cuda(),
+                      dense["hidden"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ids, _ = oracle.ngram_ids(host["input_ids"], qsl, None, host["multipliers"][0], host["V"],
+                              host["O"], w.eos_token_id, w.heads_per_ngram)
+    ids = np.asarray(ids, dtype=np.int64).reshape(w.num_tokens, -1)
+    b = layer.buffers(w.num_tokens, y.device)
+    assert np.array_equal(b["ids"].cpu().numpy(), ids)
+    blocks = sampled_blocks(qsl, w.num_tokens, (w.conv_k - 1) * w.dilation,
+                            np.random.default_rng(4))
+    rows = np.unique(np.concatenate([np.arange(lo, e) for lo, _, e in blocks]))
+    want = oracle.lookup_bf16(ids[rows], bits(table))
+    assert np.array_equal(bits(b["emb"])[rows], want)
+    n = check_chain_sampled(w, host, dense, lambda u: bits(table[torch.from_numpy(u)]), None, y,
+                            ids, blocks)
+    assert n >= 2048
+    del layer, b, table
+    torch.cuda.empty_cache()
