@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", "libple")
 LIB_PATH = os.path.join(PKG_DIR, "libple.so")
 
 SOURCES = ["common.cu", "ngram_ids.cu", "lookup.cu", "kv_proj.cu", "gate_conv.cu", "host_table.cu",
-           "pipeline.cu"]
+           "pipeline.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
           "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

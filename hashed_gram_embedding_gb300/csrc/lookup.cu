@@ -22,8 +22,7 @@
 // the items in table order (see the page-ordered walk below).
 #include "common.cuh"
 #include "ngram_hash.cuh"
-
-#include <cuda_fp8.h>
+#include "rows.cuh"
 
 #include <atomic>
 #include <cstdlib>
@@ -34,13 +33,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-
-__device__ __forceinline__ uint4 load_row_vec(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
 
 // bf16 rows: VPR = 16-byte vectors per row (template for the common sizes,
 // 0 = runtime value).
@@ -92,25 +84,7 @@ gather_bf16_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__
 }
 
 // fp8 rows: each work item is 16 codes (one 16-byte load) -> 16 bf16 values
-// (two 16-byte stores). VPR = code vectors per row.
-__device__ __forceinline__ uint32_t dequant_pair(uint16_t codes, float scale) {
-  const __half2 h2(__nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3));
-  const float2 f = __half22float2(h2);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
-__device__ __forceinline__ void dequant16(uint4 c, float s, uint4* lo, uint4* hi) {
-  lo->x = dequant_pair(static_cast<uint16_t>(c.x & 0xFFFF), s);
-  lo->y = dequant_pair(static_cast<uint16_t>(c.x >> 16), s);
-  lo->z = dequant_pair(static_cast<uint16_t>(c.y & 0xFFFF), s);
-  lo->w = dequant_pair(static_cast<uint16_t>(c.y >> 16), s);
-  hi->x = dequant_pair(static_cast<uint16_t>(c.z & 0xFFFF), s);
-  hi->y = dequant_pair(static_cast<uint16_t>(c.z >> 16), s);
-  hi->z = dequant_pair(static_cast<uint16_t>(c.w & 0xFFFF), s);
-  hi->w = dequant_pair(static_cast<uint16_t>(c.w >> 16), s);
-}
-
+// (two 16-byte stores, dequant16). VPR = code vectors per row.
 template <int VPR>
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ perm,

@@ -88,6 +88,9 @@ typedef enum {
  * single weight_scale). */
 typedef enum { PLE_BF16 = 0, PLE_FP8_E4M3 = 1, PLE_FP8_E4M3_TENSOR = 2 } ple_dtype;
 typedef enum { PLE_HBM = 0, PLE_HOST_UVA = 1 } ple_table_loc;
+/* How a table is split across the ranks of an exchange group
+ * (ple_lookup_shard): by heads, or by contiguous row ranges. */
+typedef enum { PLE_SHARD_HEADS = 0, PLE_SHARD_ROWS = 1 } ple_shard_kind;
 
 /* Limits of ple_ngram_ids (constants travel in the kernel's parameter block). */
 #define PLE_MAX_CTX_LEN 7     /* NGRAM_CONTEXT_LEN: n-gram orders 2 .. ctx_len + 1 */
@@ -245,6 +248,88 @@ ple_status ple_lookup_ordered_static(const int64_t* ids, int64_t num_tokens,
                                      ple_table_loc loc, ple_bf16_t* out,
                                      int32_t max_ctas, int32_t* dev_err,
                                      cudaStream_t stream);
+
+/*
+ * ple_lookup_shard -- one rank's part of a lookup whose table is split over
+ * the ranks of an exchange group, on ids already gathered from every
+ * replica of the group.
+ * (PR#56512 report, 执行摘要 and 实现拆解 3-4: heads sharded over the
+ * engram-DP group in TP-major order, hashes padded and all-gathered, each
+ * rank looking up its own heads for every gathered token. PR#54371 report,
+ * 实现拆解 3 and 关键源码片段 _get_dp_gather_slot / _gather_dp_ids: the table
+ * sharded over ETP = TP x DP ranks, rows combined by a parallel reduce, fp8
+ * rows reduced as an int8 view.)
+ *
+ * For token t < num_tokens and head j < num_heads, with the global row
+ * g = ids[t][head_begin + j] and the local row l = g - row_base:
+ *   PLE_SHARD_HEADS: the rank's table holds the rows of heads
+ *     [head_begin, head_begin + num_heads) of the concatenated table, its
+ *     row 0 being global row row_base. out[t][j*D + c] is ple_lookup's value
+ *     of local row l (bf16 out; fp8 dequantised with the row's or the
+ *     table's scale). l outside [0, table_rows) gives a zero row and
+ *     PLE_DEVERR_BOUNDS.
+ *   PLE_SHARD_ROWS: the rank's table holds global rows
+ *     [row_base, row_base + table_rows). out keeps the table's raw bytes:
+ *     bf16 rows as stored, fp8 rows as their e4m3 codes with the float32
+ *     scale of row l in scale_out[t][j] (the table's one scale for
+ *     PLE_FP8_E4M3_TENSOR). l outside the rank's rows is not an error: the
+ *     row's bytes and scale are zero, so adding the ranks' outputs as 8-bit
+ *     integers (one nonzero contributor per byte) rebuilds every row exactly.
+ *
+ *   ids        [num_tokens][ids_heads] int64 device; the columns
+ *              [head_begin, head_begin + num_heads) are read.
+ *   table      [table_rows][head_dim] (bf16, or uint8 e4m3 codes); device
+ *              memory (PLE_HBM) or pinned / registered host memory
+ *              (PLE_HOST_UVA), 16-byte aligned.
+ *   row_scale  float32 device: [table_rows] (PLE_FP8_E4M3), [1]
+ *              (PLE_FP8_E4M3_TENSOR), NULL for bf16.
+ *   out        16-byte aligned device: PLE_SHARD_HEADS: [num_tokens]
+ *              [num_heads * head_dim] bf16; PLE_SHARD_ROWS: the same shape
+ *              in the table's element type (bf16 bits or e4m3 codes).
+ *   scale_out  [num_tokens][num_heads] float32 device, required for an fp8
+ *              table with PLE_SHARD_ROWS; ignored otherwise.
+ *   max_ctas   as in ple_lookup.
+ * Errors: bad sizes, head range outside [0, ids_heads), unknown dtype /
+ * kind / location, a missing scale -> PLE_ERR_INVALID_ARG; a row that is not
+ * a multiple of 16 bytes -> PLE_ERR_UNSUPPORTED. num_tokens == 0 is a no-op.
+ */
+ple_status ple_lookup_shard(const int64_t* ids, int64_t num_tokens, int32_t ids_heads,
+                            int32_t head_begin, int32_t num_heads, const void* table,
+                            int64_t table_rows, int64_t row_base, int32_t head_dim,
+                            ple_dtype dtype, const float* row_scale, ple_table_loc loc,
+                            ple_shard_kind kind, void* out, float* scale_out,
+                            int32_t max_ctas, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * ple_select_rows -- this replica's token window out of the buffer the
+ * group exchanged, heads back in head order, fp8 codes dequantised.
+ * (PR#56512 report, 实现拆解 4: _engram_select_rows takes the token window
+ * from the rank-major gathered buffer; PR#54371 report, 实现拆解 3:
+ * _select_embeddings returns the DP-local rows.)
+ *
+ *   out[t][h*D + c] = src[p][row_begin + t][k*D + c]                  (bf16)
+ *   out[t][h*D + c] = bf16_rn(float(e4m3(src[p][row_begin + t][k*D + c]))
+ *                             * src_scale[p][row_begin + t][k])      (fp8)
+ * with p = part_of_head[h], k = col_of_head[h], t < num_tokens.
+ *
+ *   src          [num_parts][part_rows][part_heads * head_dim] device, bf16
+ *                (PLE_BF16) or e4m3 codes (either fp8 dtype), 16-byte
+ *                aligned: e.g. the all-gathered head-shard outputs of the
+ *                group (part = group rank), or the reduced row-shard
+ *                outputs (one part).
+ *   src_scale    [num_parts][part_rows][part_heads] float32 device (fp8).
+ *   part_of_head, col_of_head  host arrays [num_heads]: where head h sits.
+ *   out          [num_tokens][num_heads * head_dim] bf16 device, 16-byte
+ *                aligned.
+ * Errors: a window outside [0, part_rows), a head mapped outside the parts
+ * or columns -> PLE_ERR_INVALID_ARG; more than PLE_MAX_HEADS heads, a row
+ * that is not a multiple of 16 bytes -> PLE_ERR_UNSUPPORTED.
+ */
+ple_status ple_select_rows(const void* src, int32_t num_parts, int64_t part_rows,
+                           int32_t part_heads, const float* src_scale, int64_t row_begin,
+                           int64_t num_tokens, int32_t num_heads, const int32_t* part_of_head,
+                           const int32_t* col_of_head, int32_t head_dim, ple_dtype dtype,
+                           ple_bf16_t* out, cudaStream_t stream);
 
 /*
  * ple_wait -- make `consumer` wait for `done`.
