@@ -31,6 +31,8 @@ PLE_FP8_E4M3 = 1
 PLE_FP8_E4M3_TENSOR = 2
 PLE_HBM = 0
 PLE_HOST_UVA = 1
+PLE_SHARD_HEADS = 0
+PLE_SHARD_ROWS = 1
 PLE_HOST_TABLE_REGISTER = 1
 
 # Every entry point of include/ple.h with its ctypes signature.
@@ -39,6 +41,7 @@ _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _F32 = ctypes.c_float
 _I64P = ctypes.POINTER(ctypes.c_int64)
+_I32P = ctypes.POINTER(ctypes.c_int32)
 SIGNATURES = {
     "ple_ngram_ids": [_P, _I64, _P, _I32, _P, _I32, _I64P, _I64P, _I64P, _I32, _I32, _P, _P, _P, _P],
     "ple_lookup": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P, _I32, _P, _P],
@@ -51,6 +54,10 @@ SIGNATURES = {
                            _P, ctypes.c_size_t, _P, _P],
     "ple_lookup_ordered_static": [_P, _I64, _I32, _P, _I64, _I32, ctypes.c_int, _P, ctypes.c_int, _P,
                                   _I32, _P, _P],
+    "ple_lookup_shard": [_P, _I64, _I32, _I32, _I32, _P, _I64, _I64, _I32, ctypes.c_int, _P,
+                         ctypes.c_int, ctypes.c_int, _P, _P, _I32, _P, _P],
+    "ple_select_rows": [_P, _I32, _I64, _I32, _P, _I64, _I64, _I32, _I32P, _I32P, _I32,
+                        ctypes.c_int, _P, _P],
     "ple_wait": [_P, _P, _I32],
     "ple_kv_proj": [_P, _P, _I64, _I32, _I32, _P, _P, _P],
     "ple_kv_proj_gate_workspace": [_I64, _I32],
@@ -225,6 +232,46 @@ def ple_lookup_ordered_static(ids, table, out, row_scale=None, max_ctas=0, dev_e
     workspace, no allocation); calls in flight at once must not overlap."""
     return _check("ple_lookup_ordered_static", lib().ple_lookup_ordered_static(
         *_lookup_args(ids, table, row_scale, out, max_ctas, dev_err, loc), _stream(stream)))
+
+
+def ple_lookup_shard(ids, table, out, kind, head_begin=0, num_heads=None, row_base=0,
+                     row_scale=None, scale_out=None, max_ctas=0, dev_err=None, loc=None,
+                     stream=None):
+    """One rank's lookup in a table split over an exchange group.
+
+    ids int64 [T, ids_heads] (global rows); the heads [head_begin,
+    head_begin + num_heads) are looked up in ``table`` [rows, D], whose row 0
+    is global row ``row_base``. kind PLE_SHARD_HEADS: out bf16 [T, heads*D]
+    (fp8 dequantised). kind PLE_SHARD_ROWS: out holds the raw rows (bf16, or
+    uint8 e4m3 codes with scale_out float32 [T, heads]); rows owned by other
+    ranks are zero."""
+    T, ids_heads = ids.shape
+    if num_heads is None:
+        num_heads = ids_heads - head_begin
+    if loc is None:
+        loc = PLE_HBM if table.is_cuda else PLE_HOST_UVA
+    return _check("ple_lookup_shard", lib().ple_lookup_shard(
+        _ptr(ids), T, ids_heads, int(head_begin), int(num_heads), _ptr(table), table.shape[0],
+        int(row_base), table.shape[1], _fp8_dtype(row_scale), _ptr(row_scale), loc, int(kind),
+        _ptr(out), _ptr(scale_out), int(max_ctas), _ptr(dev_err), _stream(stream)))
+
+
+def ple_select_rows(src, row_begin, num_tokens, part_of_head, col_of_head, out, src_scale=None,
+                    fp8_dtype=PLE_FP8_E4M3, stream=None):
+    """out bf16 [num_tokens, H*D] <- rows [row_begin, row_begin + num_tokens)
+    of src [parts, rows, part_heads*D] (bf16, or uint8 e4m3 codes with
+    src_scale float32 [parts, rows, part_heads]), head h taken from part
+    part_of_head[h], column col_of_head[h]."""
+    parts, rows, width = src.shape
+    H = len(part_of_head)
+    D = out.shape[1] // H
+    fp8 = src_scale is not None
+    P = np.ascontiguousarray(np.asarray(part_of_head, dtype=np.int32))
+    K = np.ascontiguousarray(np.asarray(col_of_head, dtype=np.int32))
+    return _check("ple_select_rows", lib().ple_select_rows(
+        _ptr(src), parts, rows, width // D, _ptr(src_scale), int(row_begin), int(num_tokens), H,
+        P.ctypes.data_as(_I32P), K.ctypes.data_as(_I32P), D, fp8_dtype if fp8 else PLE_BF16,
+        _ptr(out), _stream(stream)))
 
 
 def _event_handle(event, stream):

@@ -262,3 +262,47 @@ def test_step_runtime_host_checks(lib):
     assert lib.ple_event_synchronize(None) == 1
     lib.ple_graph_destroy(None)
     lib.ple_event_destroy(None)
+
+
+def test_lookup_shard_host_checks(lib):
+    P = ctypes.c_void_p(16)
+    # head range outside the ids' columns, empty head range, negative base
+    assert lib.ple_lookup_shard(P, 4, 8, 6, 4, P, 10, 0, 64, 0, None, 0, 0, P, None, 0, None,
+                                None) == 1
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 0, P, 10, 0, 64, 0, None, 0, 0, P, None, 0, None,
+                                None) == 1
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 8, P, 10, -1, 64, 0, None, 0, 0, P, None, 0, None,
+                                None) == 1
+    # unknown shard kind; 24-byte rows
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 8, P, 10, 0, 64, 0, None, 0, 5, P, None, 0, None,
+                                None) == 1
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 8, P, 10, 0, 12, 0, None, 0, 0, P, None, 0, None,
+                                None) == 2
+    # fp8 without a scale; an fp8 row shard without scale_out
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 8, P, 10, 0, 64, 1, None, 0, 0, P, None, 0, None,
+                                None) == 1
+    assert lib.ple_lookup_shard(P, 4, 8, 0, 8, P, 10, 0, 64, 1, P, 0, 1, P, None, 0, None,
+                                None) == 1
+    assert b"scale_out" in lib.ple_last_error()
+    # no tokens: nothing to do
+    assert lib.ple_lookup_shard(None, 0, 8, 0, 8, None, 10, 0, 64, 0, None, 0, 0, None, None, 0,
+                                None, None) == 0
+
+
+def test_select_rows_host_checks(lib):
+    I32P = ctypes.POINTER(ctypes.c_int32)
+
+    def call(T=4, H=2, part=(0, 1), col=(0, 1), r0=0, rows=10, parts=2, ph=2, D=64, dtype=0):
+        p = np.asarray(part, dtype=np.int32)
+        c = np.asarray(col, dtype=np.int32)
+        return lib.ple_select_rows(ctypes.c_void_p(16), parts, rows, ph, None, r0, T, H,
+                                   p.ctypes.data_as(I32P), c.ctypes.data_as(I32P), D, dtype,
+                                   ctypes.c_void_p(16), None)
+
+    assert call(r0=8) == 1                      # window past the rows
+    assert call(part=(0, 2)) == 1               # part outside
+    assert call(col=(0, 2)) == 1                # column outside
+    assert call(H=65, part=[0] * 65, col=[0] * 65) == 2   # too many heads
+    assert call(D=12) == 2                      # 24-byte bf16 rows
+    assert call(dtype=1) == 1                   # fp8 without scales
+    assert call(T=0) == 0                       # no tokens
