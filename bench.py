@@ -362,8 +362,8 @@ def measure_workload(torch, args, name, device, rank, world, headline):
             _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err,
                             stream=st)
 
-    def step(s, ev=None, st=None):
-        st = stream if st is None else st
+    def stages_of(s, st):
+        """The step's libple calls for layer set s, one callable per kernel."""
         p = sets[s % num_sets]
         ctx_o = ctx_out if w.decode else None
         stages = []
@@ -390,6 +390,11 @@ def measure_workload(torch, args, name, device, rank, world, headline):
                 p["hidden"], kv, p["gamma_h"], p["gamma_k"], p["qsl"], p["conv_w"], w.dilation, y,
                 conv_state=p.get("conv_state"), conv_state_out=st_out, gate_out=gate, dev_err=err,
                 stream=st))
+        return stages
+
+    def step(s, ev=None, st=None):
+        st = stream if st is None else st
+        stages = stages_of(s, st)
         if ev is not None:
             ev[0].record(st)
         for j, run in enumerate(stages):
@@ -420,6 +425,39 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     eager_ms = max_over_ranks(eager_ms, device)
     if int(err.item()) != 0:
         raise RuntimeError(f"{name}: device error word {int(err.item())} in the timed region")
+
+    # ---- each kernel alone: K back-to-back launches over the rotating layer
+    # sets between two events on the launching stream, so that a short
+    # kernel's launch latency overlaps the previous launch (the events
+    # between the kernels of the eager steps above add it to every kernel);
+    # the per-launch average is the kernel's duration for the roofline ----
+    # (the K launches are replayed from one CUDA graph, so that the host's
+    # submission rate does not bound the short kernels)
+    alone = {}
+    for j, k in enumerate(KERNELS):
+        def launches(st, j=j):
+            for i in range(args.steps):
+                stages_of(i, st)[j]()
+        g_alone, why = capture_graphs(torch, lambda s, st=None: launches(st), 1, device)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        if g_alone is not None:
+            g_alone[0].replay()
+            torch.cuda.synchronize()
+            a0.record(stream)
+            g_alone[0].replay()
+            a1.record(stream)
+        else:
+            launches(stream)
+            torch.cuda.synchronize()
+            a0.record(stream)
+            launches(stream)
+            a1.record(stream)
+        torch.cuda.synchronize()
+        alone[k] = a0.elapsed_time(a1) / args.steps
+        del g_alone
+    if int(err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(err.item())} in the per-kernel timing")
 
     # ---- timed region: K steps replayed from CUDA graphs (one per layer
     # set, captured once), device events on the replay stream ----
@@ -499,8 +537,10 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     link_gbs = measure_link_gbs(torch, device) if w.table_loc == "host" else None
     work = algorithmic_work(w)
     kernels = {}
+    step_kernels_ms = float(np.mean([sum(per_kernel[x][i] for x in KERNELS)
+                                     for i in range(args.steps)]))
     for k in KERNELS:
-        avg_ms = float(np.mean(per_kernel[k]))
+        avg_ms = alone[k]
         bound, amount = work[k]
         if bound == "tensor":
             achieved = amount / (avg_ms * 1e-3) / 1e12
@@ -514,10 +554,11 @@ def measure_workload(torch, args, name, device, rank, world, headline):
             achieved = amount / (avg_ms * 1e-3) / 1e9
             peak = peaks["hbm_gbs"]
             unit = "GB/s"
+        in_step_ms = float(np.mean(per_kernel[k]))
         kernels[k] = {"us": round(avg_ms * 1e3, 2), "bound": bound, "achieved": round(achieved, 1),
                       "unit": unit, "frac": round(achieved / peak, 4),
-                      "share": round(avg_ms / float(np.mean([sum(per_kernel[x][i] for x in KERNELS)
-                                                           for i in range(args.steps)])), 4)}
+                      "us_in_step": round(in_step_ms * 1e3, 2),
+                      "share": round(in_step_ms / step_kernels_ms, 4)}
     dominant = max(KERNELS, key=lambda k: kernels[k]["us"])
     dk = kernels[dominant]
     bound, amount = work[dominant]
@@ -567,7 +608,9 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     line.update(extra)
     line["eager"] = {"ms_per_step": round(eager_ms / args.steps, 4),
                      "value": round(world * args.steps * T / (eager_ms * 1e-3), 1),
-                     "note": "same steps launched one by one, events between kernels"}
+                     "note": "same steps launched one by one, events between kernels "
+                             "(kernels.*.us_in_step and share); kernels.*.us: each kernel alone, "
+                             f"{args.steps} back-to-back launches over the rotating layer sets"}
     if graph_error:
         line["eager"]["graph_capture_error"] = graph_error
     if headline and not args.no_cpu_baseline:

@@ -138,6 +138,84 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Token-major gather (the default for a table in HBM): a warp takes tpw
+// tokens at a time (tpw * H <= 32). Lane l loads id l of the group (one
+// coalesced load for all of the group's heads), then every lane issues all of
+// its row-vector loads -- vector j = lane + 32 i of the group's tpw*H*VPR
+// vectors, so the 16 (8) lanes of a half (quarter) warp read one whole
+// 256-byte (128-byte) row -- before any store. The group's rows are thus in
+// flight after one id round trip instead of one round trip per vector (the
+// vector-strided kernel above), and the next group's ids are loaded while
+// they fly. fp8 rows: each lane reads its row's scale beside the codes.
+// ---------------------------------------------------------------------------
+constexpr int kTokLoads = 8;  // row vectors in flight per lane
+
+template <int VPR, bool FP8>
+__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 4)
+gather_tok_kernel(const int64_t* __restrict__ ids, int64_t T, int H, int tpw,
+                  const uint4* __restrict__ table, const float* __restrict__ row_scale,
+                  int scale_stride, int64_t table_rows, uint4* __restrict__ out,
+                  int32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (kThreads / 32) * tpw;
+  auto group_id = [&](int64_t t0) {  // id of item `lane` of the group at t0 (-1: none)
+    const int64_t n = (T - t0 < tpw ? T - t0 : tpw) * H;
+    return lane < n ? __ldg(ids + t0 * H + lane) : int64_t(-1);
+  };
+  int64_t t0 = warp * tpw;
+  int64_t idn = t0 < T ? group_id(t0) : -1;
+  for (; t0 < T; t0 += step) {
+    const int64_t my_id = idn;
+    const int nv = static_cast<int>((T - t0 < tpw ? T - t0 : tpw) * H * VPR);
+    if (lane < nv / VPR && static_cast<uint64_t>(my_id) >= static_cast<uint64_t>(table_rows))
+      set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // that row is written as zeros
+    uint4 v[kTokLoads];
+    float sc[kTokLoads];
+#pragma unroll
+    for (int i = 0; i < kTokLoads; ++i) {
+      const int j = lane + 32 * i;
+      const int item = j / VPR;
+      const int64_t id = __shfl_sync(0xffffffffu, my_id, item & 31);
+      v[i] = make_uint4(0, 0, 0, 0);
+      sc[i] = 0.f;
+      if (j < nv && static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
+        v[i] = load_row_vec(table + id * VPR + (j - item * VPR));
+        if constexpr (FP8) sc[i] = __ldg(row_scale + id * scale_stride);
+      }
+    }
+    if (t0 + step < T) idn = group_id(t0 + step);  // next group's ids, while the rows fly
+    const int64_t o0 = t0 * H * VPR;
+#pragma unroll
+    for (int i = 0; i < kTokLoads; ++i) {
+      const int j = lane + 32 * i;
+      if (j >= nv) continue;
+      if constexpr (FP8) {
+        uint4 lo, hi;
+        dequant16(v[i], sc[i], &lo, &hi);
+        out[2 * (o0 + j)] = lo;
+        out[2 * (o0 + j) + 1] = hi;
+      } else {
+        out[o0 + j] = v[i];
+      }
+    }
+  }
+}
+
+// Tokens per warp group for the token-major gather, or 0 when the shape does
+// not fit it (more than 32 heads, or more than 32 * kTokLoads row vectors per
+// token).
+int tok_group(int H, int vpr) {
+  if (H < 1 || H > 32 || H * vpr > 32 * kTokLoads) return 0;
+  int tpw = 32 / H;
+  const int by_loads = 32 * kTokLoads / (H * vpr);
+  return tpw < by_loads ? tpw : by_loads;
+}
+
 // ---------------------------------------------------------------------------
 // ple_ngram_lookup: the n-gram ids and the row gather in one kernel. Each work
 // item (one 16-byte table vector of one (token, head) row) hashes its row's
@@ -620,6 +698,38 @@ ple_status launch_gather(const int64_t* ids, int64_t num_tokens, int32_t num_hea
                         smem, stream, 1, ids, num_tokens, static_cast<int>(num_heads),
                         g.row_bytes, reinterpret_cast<const uint8_t*>(g.table), table_rows,
                         reinterpret_cast<uint8_t*>(g.out), dev_err);
+    if (err != cudaSuccess) return check_cuda(err, name);
+    return check_cuda(cudaGetLastError(), name);
+  }
+  // Default: the token-major kernel when the shape fits it (PLE_GATHER_MODE=
+  // vector keeps the vector-strided kernel: sweeps and tests).
+  const int tpw = tok_group(num_heads, g.vpr);
+  const bool vector_mode = mode != nullptr && strcmp(mode, "vector") == 0;
+  if (tpw > 0 && !vector_mode && loc == PLE_HBM && (g.vpr == 8 || g.vpr == 16)) {
+    const int64_t groups = (num_tokens + tpw - 1) / tpw;
+    int64_t blocks = (groups + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t full = static_cast<int64_t>(num_sms()) * (dtype == PLE_BF16 ? 4 : 3);
+    if (blocks > full) blocks = full;
+    if (max_ctas > 0 && blocks > max_ctas) blocks = max_ctas;
+    const dim3 grid(static_cast<unsigned>(blocks < 1 ? 1 : blocks));
+    const int sstride = dtype == PLE_FP8_E4M3 ? 1 : 0;
+    cudaError_t err;
+    if (dtype == PLE_BF16)
+      err = g.vpr == 16
+                ? launch_kernel(gather_tok_kernel<16, false>, grid, dim3(kThreads), 0, stream, 1,
+                                ids, num_tokens, static_cast<int>(num_heads), tpw, g.table,
+                                row_scale, sstride, table_rows, g.out, dev_err)
+                : launch_kernel(gather_tok_kernel<8, false>, grid, dim3(kThreads), 0, stream, 1,
+                                ids, num_tokens, static_cast<int>(num_heads), tpw, g.table,
+                                row_scale, sstride, table_rows, g.out, dev_err);
+    else
+      err = g.vpr == 16
+                ? launch_kernel(gather_tok_kernel<16, true>, grid, dim3(kThreads), 0, stream, 1,
+                                ids, num_tokens, static_cast<int>(num_heads), tpw, g.table,
+                                row_scale, sstride, table_rows, g.out, dev_err)
+                : launch_kernel(gather_tok_kernel<8, true>, grid, dim3(kThreads), 0, stream, 1,
+                                ids, num_tokens, static_cast<int>(num_heads), tpw, g.table,
+                                row_scale, sstride, table_rows, g.out, dev_err);
     if (err != cudaSuccess) return check_cuda(err, name);
     return check_cuda(cudaGetLastError(), name);
   }

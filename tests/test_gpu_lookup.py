@@ -29,11 +29,12 @@ def to_dev_bf16(a, pinned=False):
     return t.cuda()
 
 
-@pytest.fixture(params=["lsu", "bulk"])
+@pytest.fixture(params=["tok", "vector", "bulk"])
 def gather_mode(request, monkeypatch):
-    """bf16 HBM gathers: the register-fed kernel (default) and the copy-engine one."""
-    if request.param == "bulk":
-        monkeypatch.setenv("PLE_GATHER_MODE", "bulk")
+    """HBM gathers: the token-major kernel (default where the shape fits it),
+    the vector-strided kernel, and the copy-engine one (bf16)."""
+    if request.param != "tok":
+        monkeypatch.setenv("PLE_GATHER_MODE", request.param)
     return request.param
 
 
@@ -410,3 +411,50 @@ def test_gather_from_shared_and_file_backed_tables(kind, tmp_path):
         t.close()
         if kind == "shared":
             _lib.ple_host_table_unlink_shared(name)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "fp8_tensor"])
+@pytest.mark.parametrize("T,H,D", [(1, 1, 64), (3, 3, 128), (201, 16, 128), (1025, 5, 64),
+                                   (77, 12, 64), (64, 32, 64), (40, 2, 128), (9, 16, 64)])
+def test_token_major_gather_equals_vector_gather_and_oracle(T, H, D, dtype, monkeypatch):
+    """The token-major kernel (ragged last group, heads not dividing 32, ids
+    outside the table) writes exactly what the vector-strided kernel writes,
+    and the oracle's rows."""
+    rng = np.random.default_rng(T * 13 + H * 7 + D)
+    rows = 3001
+    ids = rng.integers(0, rows, size=(T, H))
+    ids[T // 2, H - 1] = rows + 5
+    ids[0, 0] = -3
+    if dtype == "bf16":
+        table_np = random_table_bits(rng, rows, D)
+        table = to_dev_bf16(table_np)
+        scale = None
+    else:
+        codes = rng.integers(0, 256, size=(rows, D)).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0
+        table = torch.from_numpy(codes).cuda()
+        sc = (rng.random(rows if dtype == "fp8" else 1) * 1e-2 + 1e-4).astype(np.float32)
+        scale = torch.from_numpy(sc).cuda()
+    outs, errs = [], []
+    for mode in ("tok", "vector"):
+        if mode == "vector":
+            monkeypatch.setenv("PLE_GATHER_MODE", "vector")
+        out = torch.full((T, H * D), 3.0, dtype=torch.bfloat16, device="cuda")
+        err = dev_err_word()
+        _lib.ple_lookup(torch.from_numpy(ids).cuda(), table, out, row_scale=scale, dev_err=err)
+        torch.cuda.synchronize()
+        outs.append(bits(out))
+        errs.append(int(err.item()))
+    assert errs == [_lib.PLE_DEVERR_BOUNDS] * 2
+    assert np.array_equal(outs[0], outs[1])
+    ok = ids.copy()
+    ok[T // 2, H - 1] = 0
+    ok[0, 0] = 0
+    if dtype == "bf16":
+        ref = lookup_bf16(ok, table_np)
+    else:
+        full = np.full(rows, sc[0], dtype=np.float32) if sc.size == 1 else sc
+        ref = lookup_fp8(ok, codes, full)
+    ref[T // 2, (H - 1) * D:] = 0
+    ref[0, :D] = 0
+    assert np.array_equal(outs[0], ref)
