@@ -340,13 +340,17 @@ def measure_workload(torch, args, name, device, rank, world, headline):
                (("kv_proj_gate", "conv") if fuse else ("kv_proj", "gate_conv")))
     gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
                            device=device) if fuse else None)
-    ids = torch.empty((T, H), dtype=torch.int64, device=device)
-    emb = torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device)
-    kv = torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device)
-    y = torch.empty((T, C), dtype=torch.bfloat16, device=device)
-    ctx_out = torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device)
-    st_out = (torch.empty_like(sets[0]["conv_state"]) if w.decode else None)
-    gate = torch.empty((T,), dtype=torch.float32, device=device)
+    # intermediate buffers per layer set, so that a kernel timed alone over
+    # the rotating sets reads what that set's own step produced (cold in L2)
+    bufs = [{"ids": torch.empty((T, H), dtype=torch.int64, device=device),
+             "emb": torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device),
+             "kv": torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device),
+             "y": torch.empty((T, C), dtype=torch.bfloat16, device=device),
+             "gate": torch.empty((T,), dtype=torch.float32, device=device),
+             "ctx_out": torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device),
+             "st_out": torch.empty_like(sets[0]["conv_state"]) if w.decode else None}
+            for _ in range(num_sets)]
+    ids, emb, ctx_out, st_out = (bufs[0][k] for k in ("ids", "emb", "ctx_out", "st_out"))
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
     order_ws = None
@@ -354,18 +358,21 @@ def measure_workload(torch, args, name, device, rank, world, headline):
         order_ws = torch.empty((_lib.ple_lookup_ordered_workspace(
             T, H, sets[0]["table"], sets[0]["row_scale"]),), dtype=torch.uint8, device=device)
 
-    def gather(p, st):
+    def gather(p, b, st):
         if order_ws is not None:
-            _lib.ple_lookup_ordered(ids, p["table"], emb, order_ws, row_scale=p["row_scale"],
-                                    dev_err=err, stream=st)
+            _lib.ple_lookup_ordered(b["ids"], p["table"], b["emb"], order_ws,
+                                    row_scale=p["row_scale"], dev_err=err, stream=st)
         else:
-            _lib.ple_lookup(ids, p["table"], emb, row_scale=p["row_scale"], dev_err=err,
+            _lib.ple_lookup(b["ids"], p["table"], b["emb"], row_scale=p["row_scale"], dev_err=err,
                             stream=st)
 
     def stages_of(s, st):
         """The step's libple calls for layer set s, one callable per kernel."""
         p = sets[s % num_sets]
-        ctx_o = ctx_out if w.decode else None
+        b = bufs[s % num_sets]
+        ids, emb, kv, y, gate = (b[k] for k in ("ids", "emb", "kv", "y", "gate"))
+        st_out = b["st_out"]
+        ctx_o = b["ctx_out"] if w.decode else None
         stages = []
         if fuse_ids:
             stages.append(lambda: _lib.ple_ngram_lookup(
@@ -376,7 +383,7 @@ def measure_workload(torch, args, name, device, rank, world, headline):
             stages.append(lambda: _lib.ple_ngram_ids(
                 p["input_ids"], p["qsl"], p["ctx"], p["mult"], p["host"]["V"], p["host"]["O"],
                 w.eos_token_id, w.heads_per_ngram, ids, ctx_o, err, st))
-            stages.append(lambda: gather(p, st))
+            stages.append(lambda: gather(p, b, st))
         if fuse:
             stages.append(lambda: _lib.ple_kv_proj_gate(
                 emb, p["w_kv"], p["hidden"], p["gamma_h"], p["gamma_k"], kv, gate, gate_ws,
@@ -402,7 +409,7 @@ def measure_workload(torch, args, name, device, rank, world, headline):
             if ev is not None:
                 ev[j + 1].record(st)
 
-    for i in range(args.warmup):
+    for i in range(max(args.warmup, num_sets)):  # every set's buffers hold its step's results
         step(i)
     torch.cuda.synchronize()
     if int(err.item()) != 0:

@@ -148,7 +148,7 @@ gather_fp8_kernel(const int64_t* __restrict__ ids, const uint32_t* __restrict__ 
 // 256-byte (128-byte) row -- before any store. The group's rows are thus in
 // flight after one id round trip instead of one round trip per vector (the
 // vector-strided kernel above), and the next group's ids are loaded while
-// they fly. fp8 rows: each lane reads its row's scale beside the codes.
+// they fly. fp8 rows: lane l reads the scale of item l, shared by shuffle.
 // ---------------------------------------------------------------------------
 constexpr int kTokLoads = 8;  // row vectors in flight per lane
 
@@ -175,31 +175,33 @@ gather_tok_kernel(const int64_t* __restrict__ ids, int64_t T, int H, int tpw,
     if (lane < nv / VPR && static_cast<uint64_t>(my_id) >= static_cast<uint64_t>(table_rows))
       set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // that row is written as zeros
     uint4 v[kTokLoads];
-    float sc[kTokLoads];
 #pragma unroll
     for (int i = 0; i < kTokLoads; ++i) {
       const int j = lane + 32 * i;
       const int item = j / VPR;
       const int64_t id = __shfl_sync(0xffffffffu, my_id, item & 31);
       v[i] = make_uint4(0, 0, 0, 0);
-      sc[i] = 0.f;
-      if (j < nv && static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows)) {
+      if (j < nv && static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows))
         v[i] = load_row_vec(table + id * VPR + (j - item * VPR));
-        if constexpr (FP8) sc[i] = __ldg(row_scale + id * scale_stride);
-      }
     }
+    // fp8: lane l reads the scale of item l once; the vectors take it by shuffle
+    float my_sc = 0.f;
+    if (FP8 && static_cast<uint64_t>(my_id) < static_cast<uint64_t>(table_rows))
+      my_sc = __ldg(row_scale + my_id * scale_stride);
     if (t0 + step < T) idn = group_id(t0 + step);  // next group's ids, while the rows fly
     const int64_t o0 = t0 * H * VPR;
 #pragma unroll
     for (int i = 0; i < kTokLoads; ++i) {
       const int j = lane + 32 * i;
-      if (j >= nv) continue;
       if constexpr (FP8) {
+        const float sc = __shfl_sync(0xffffffffu, my_sc, (j / VPR) & 31);
+        if (j >= nv) continue;
         uint4 lo, hi;
-        dequant16(v[i], sc[i], &lo, &hi);
+        dequant16(v[i], sc, &lo, &hi);
         out[2 * (o0 + j)] = lo;
         out[2 * (o0 + j) + 1] = hi;
       } else {
+        if (j >= nv) continue;
         out[o0 + j] = v[i];
       }
     }
@@ -349,6 +351,105 @@ ngram_gather_kernel(const __grid_constant__ NgramArgs na, const __grid_constant_
         out[2 * static_cast<size_t>(idx) + 1] = hi;
       } else {
         out[idx] = c[u];
+      }
+    }
+  }
+}
+
+
+// Token-major ple_ngram_lookup (the default where the shape fits it, as
+// gather_tok_kernel): lane l of a warp group hashes the id of item l of the
+// group's tpw tokens (ngram_id, request found in the staged boundaries) and
+// the group's rows are then loaded as in gather_tok_kernel; the next group's
+// ids are hashed while the rows fly.
+template <int VPR, bool FP8>
+__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 4)
+ngram_tok_kernel(const __grid_constant__ NgramArgs na, const __grid_constant__ NgramConsts k,
+                 int tpw, const uint4* __restrict__ table, const float* __restrict__ row_scale,
+                 int scale_stride, int64_t table_rows, uint4* __restrict__ out,
+                 int32_t* dev_err) {
+  __shared__ int32_t qsl_s[kStagedBounds];
+  __shared__ NgramHeadsSmem hs;
+  const int R = na.num_reqs;
+  const int H = na.num_heads;
+  const int64_t T = na.num_tokens;
+  const bool staged = R < kStagedBounds;
+  stage_ngram_heads(k, H, hs);
+  pdl_wait();
+  pdl_trigger();
+  if (staged)
+    for (int r = threadIdx.x; r <= R; r += kThreads) qsl_s[r] = __ldg(na.qsl + r);
+  __syncthreads();
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const int64_t gsize = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t i = gid; i <= R; i += gsize) check_qsl(na.qsl, R, T, i, dev_err);
+  if (na.ctx_out != nullptr)
+    for (int64_t i = gid; i < static_cast<int64_t>(R) * na.ctx_len; i += gsize)
+      ngram_carry(na.input_ids, T, na.qsl, R, na.ctx, na.ctx_len, na.eos, i, na.ctx_out);
+
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = gid >> 5;
+  const int64_t step = (gsize >> 5) * tpw;
+  auto group_id = [&](int64_t t0) -> int64_t {  // hashed id of item `lane` of the group
+    const int64_t n = (T - t0 < tpw ? T - t0 : tpw) * H;
+    if (lane >= n) return -1;
+    const int64_t t = t0 + lane / H;
+    const int h = lane - (lane / H) * H;
+    int r;
+    int64_t start;
+    if (staged) {
+      int lo = 0, hi = R + 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(qsl_s[mid]) <= t) lo = mid + 1; else hi = mid;
+      }
+      r = lo - 1 < 0 ? 0 : (lo - 1 >= R ? R - 1 : lo - 1);
+      start = qsl_s[r];
+    } else {
+      r = find_request(na.qsl, R, t);
+      start = __ldg(na.qsl + r);
+    }
+    const int64_t id = ngram_id(na.input_ids, na.ctx, na.ctx_len, na.eos, t, t - start, r, h,
+                                na.heads_per_ngram, k, hs);
+    if (na.ids_out != nullptr) na.ids_out[t0 * H + lane] = id;
+    return id;
+  };
+  int64_t t0 = warp * tpw;
+  int64_t idn = t0 < T ? group_id(t0) : -1;
+  for (; t0 < T; t0 += step) {
+    const int64_t my_id = idn;
+    const int nv = static_cast<int>((T - t0 < tpw ? T - t0 : tpw) * H * VPR);
+    if (lane < nv / VPR && static_cast<uint64_t>(my_id) >= static_cast<uint64_t>(table_rows))
+      set_dev_err(dev_err, PLE_DEVERR_BOUNDS);  // that row is written as zeros
+    uint4 v[kTokLoads];
+#pragma unroll
+    for (int i = 0; i < kTokLoads; ++i) {
+      const int j = lane + 32 * i;
+      const int item = j / VPR;
+      const int64_t id = __shfl_sync(0xffffffffu, my_id, item & 31);
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (j < nv && static_cast<uint64_t>(id) < static_cast<uint64_t>(table_rows))
+        v[i] = load_row_vec(table + id * VPR + (j - item * VPR));
+    }
+    // fp8: lane l reads the scale of item l once; the vectors take it by shuffle
+    float my_sc = 0.f;
+    if (FP8 && static_cast<uint64_t>(my_id) < static_cast<uint64_t>(table_rows))
+      my_sc = __ldg(row_scale + my_id * scale_stride);
+    if (t0 + step < T) idn = group_id(t0 + step);  // next group's ids, while the rows fly
+    const int64_t o0 = t0 * H * VPR;
+#pragma unroll
+    for (int i = 0; i < kTokLoads; ++i) {
+      const int j = lane + 32 * i;
+      if constexpr (FP8) {
+        const float sc = __shfl_sync(0xffffffffu, my_sc, (j / VPR) & 31);
+        if (j >= nv) continue;
+        uint4 lo, hi;
+        dequant16(v[i], sc, &lo, &hi);
+        out[2 * (o0 + j)] = lo;
+        out[2 * (o0 + j) + 1] = hi;
+      } else {
+        if (j >= nv) continue;
+        out[o0 + j] = v[i];
       }
     }
   }
@@ -964,6 +1065,35 @@ PLE_EXPORT ple_status ple_ngram_lookup(const int32_t* input_ids, int64_t num_tok
   na.ids_out = ids_out;
   const int scale_stride = dtype == PLE_FP8_E4M3 ? 1 : 0;
   cudaError_t err;
+  // Token-major kernel where the shape fits it (PLE_GATHER_MODE=vector keeps
+  // the vector-strided one: sweeps and tests).
+  const int tpw = tok_group(num_heads, g.vpr);
+  const char* mode = getenv("PLE_GATHER_MODE");
+  const bool vector_mode = mode != nullptr && strcmp(mode, "vector") == 0;
+  if (tpw > 0 && !vector_mode && (g.vpr == 8 || g.vpr == 16)) {
+    const int64_t groups = (num_tokens + tpw - 1) / tpw;
+    int64_t blocks = (groups + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t full = static_cast<int64_t>(num_sms()) * (dtype == PLE_BF16 ? 4 : 3);
+    if (blocks > full) blocks = full;
+    if (max_ctas > 0 && blocks > max_ctas) blocks = max_ctas;
+    const dim3 grid(static_cast<unsigned>(blocks < 1 ? 1 : blocks));
+    if (dtype == PLE_BF16)
+      err = g.vpr == 16 ? launch_kernel(ngram_tok_kernel<16, false>, grid, dim3(kThreads), 0,
+                                        stream, 1, na, k, tpw, g.table, g.row_scale, 0,
+                                        g.table_rows, g.out, dev_err)
+                        : launch_kernel(ngram_tok_kernel<8, false>, grid, dim3(kThreads), 0,
+                                        stream, 1, na, k, tpw, g.table, g.row_scale, 0,
+                                        g.table_rows, g.out, dev_err);
+    else
+      err = g.vpr == 16 ? launch_kernel(ngram_tok_kernel<16, true>, grid, dim3(kThreads), 0,
+                                        stream, 1, na, k, tpw, g.table, g.row_scale,
+                                        scale_stride, g.table_rows, g.out, dev_err)
+                        : launch_kernel(ngram_tok_kernel<8, true>, grid, dim3(kThreads), 0,
+                                        stream, 1, na, k, tpw, g.table, g.row_scale,
+                                        scale_stride, g.table_rows, g.out, dev_err);
+    if (err != cudaSuccess) return check_cuda(err, name);
+    return check_cuda(cudaGetLastError(), name);
+  }
   if (dtype == PLE_BF16) {
     err = g.vpr == 16
               ? launch_kernel(ngram_gather_kernel<16, false>, dim3(g.grid), dim3(kThreads), 0,

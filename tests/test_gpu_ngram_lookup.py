@@ -71,10 +71,22 @@ def assert_same(res):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+@pytest.fixture(params=["tok", "vector"])
+def gather_mode(request, monkeypatch):
+    """The token-major kernels (default where the shape fits) and the
+    vector-strided ones."""
+    if request.param == "vector":
+        monkeypatch.setenv("PLE_GATHER_MODE", "vector")
+    return request.param
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp8-row", "fp8-tensor"])
-@pytest.mark.parametrize("workload", ["tiny", "decode256x4"])
-def test_matches_oracle_and_separate_kernels(workload, dtype):
-    w = wl.WORKLOADS[workload]
+@pytest.mark.parametrize("workload", ["tiny", "decode256x4", "fp8x8-small"])
+def test_matches_oracle_and_separate_kernels(workload, dtype, gather_mode):
+    if workload == "fp8x8-small":  # 2000 Zipf tokens over 64 ragged requests
+        w = wl.scaled(wl.WORKLOADS["fp8x8"], vocab_start=5003, num_tokens=2000)
+    else:
+        w = wl.WORKLOADS[workload]
     if workload == "decode256x4":  # a small table with the workload's ids and context
         w = wl.scaled(w, vocab_start=5003)
     h = wl.host_inputs(w)
@@ -110,7 +122,20 @@ def test_prefill_8k_full_size_against_separate_kernels():
     assert np.all((ids >= h["O"]) & (ids < h["O"] + h["V"]))
 
 
-def test_many_requests_and_no_ids_output():
+def test_fp8_32k_full_size_against_separate_kernels():
+    """One layer of the 32k-token fp8 workload with its 8 GiB table, in the
+    benchmark's launch configuration: the same ids and rows as the two-kernel
+    path."""
+    w = wl.WORKLOADS["fp8x8"]
+    h = wl.host_inputs(w)
+    table, scale = wl.make_table(torch, w, "cuda", layer=2)
+    res = run_both(h, w, 2, table, scale)
+    assert_same(res)
+    del table, scale, res
+    torch.cuda.empty_cache()
+
+
+def test_many_requests_and_no_ids_output(gather_mode):
     # more request boundaries than the kernel stages in shared memory; no ids output
     rng = np.random.default_rng(12)
     lengths = rng.integers(0, 4, size=5000)
