@@ -340,15 +340,16 @@ def measure_workload(torch, args, name, device, rank, world, headline):
                (("kv_proj_gate", "conv") if fuse else ("kv_proj", "gate_conv")))
     gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
                            device=device) if fuse else None)
-    # intermediate buffers per layer set, so that a kernel timed alone over
-    # the rotating sets reads what that set's own step produced (cold in L2)
-    bufs = [{"ids": torch.empty((T, H), dtype=torch.int64, device=device),
-             "emb": torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device),
-             "kv": torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device),
-             "y": torch.empty((T, C), dtype=torch.bfloat16, device=device),
-             "gate": torch.empty((T,), dtype=torch.float32, device=device),
-             "ctx_out": torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device),
-             "st_out": torch.empty_like(sets[0]["conv_state"]) if w.decode else None}
+    # activation buffers shared by the steps (as an engine reuses them), except
+    # the ids: one buffer per layer set, so that the gather timed alone over
+    # the rotating sets reads each set's own rows (cold in L2)
+    shared = {"emb": torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device),
+              "kv": torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device),
+              "y": torch.empty((T, C), dtype=torch.bfloat16, device=device),
+              "gate": torch.empty((T,), dtype=torch.float32, device=device),
+              "ctx_out": torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device),
+              "st_out": torch.empty_like(sets[0]["conv_state"]) if w.decode else None}
+    bufs = [dict(shared, ids=torch.empty((T, H), dtype=torch.int64, device=device))
             for _ in range(num_sets)]
     ids, emb, ctx_out, st_out = (bufs[0][k] for k in ("ids", "emb", "ctx_out", "st_out"))
     err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -674,27 +675,45 @@ def chain_timing(torch, w, sets, device, err, fuse, L, reps=10):
     outs = [torch.empty((T, C), dtype=torch.bfloat16, device=device) for _ in range(L)]
     stream = torch.cuda.current_stream(device)
     res = {"layers": L}
-    variants = [("prefetch", True, 0), ("inline", False, 0)]
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    variants = [("prefetch", True, 0), ("prefetch_one_cta_per_sm", True, sms),
+                ("inline", False, 0)]
     if w.table_loc == "host":  # the pages cap the side-stream gather at half the SMs
-        half = torch.cuda.get_device_properties(device).multi_processor_count // 2
-        variants.insert(1, ("prefetch_half_grid", True, half))
-    for name, prefetch, ctas in variants:
-        chain = PLEChain(layers, prefetch=prefetch, prefetch_ctas=ctas)
-        for _ in range(2):
-            chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
-                          dev_err=err, stream=stream)
-        torch.cuda.synchronize()
+        variants.insert(1, ("prefetch_half_grid", True, sms // 2))
+
+    def timed(run):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(reps):
-            chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
-                          dev_err=err, stream=stream)
+            run()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        return e0.elapsed_time(e1) / reps
+
+    for name, prefetch, ctas in variants:
+        chain = PLEChain(layers, prefetch=prefetch, prefetch_ctas=ctas)
+
+        def fwd(st=stream, chain=chain):
+            chain.forward(p0["input_ids"], p0["qsl"], hiddens, outs, ngram_context=p0["ctx"],
+                          dev_err=err, stream=st)
+        for _ in range(2):
+            fwd()
+        ms = timed(fwd)
         res[f"{name}_ms"] = round(ms, 4)
         res[f"{name}_tokens_per_s_per_layer"] = round(T * L / (ms * 1e-3), 1)
+        # the same chain captured once into a CUDA graph (side stream forked
+        # and joined inside the capture) and replayed
+        graphs, why = capture_graphs(torch, lambda s, st=None: fwd(st), 1, device)
+        if graphs is not None:
+            graphs[0].replay()
+            gms = timed(graphs[0].replay)
+            res[f"{name}_graph_ms"] = round(gms, 4)
+            res[f"{name}_graph_tokens_per_s_per_layer"] = round(T * L / (gms * 1e-3), 1)
+            del graphs
+        else:
+            res[f"{name}_graph_error"] = why
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the chain timing")
     return res
