@@ -341,15 +341,16 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     gate_ws = (torch.zeros((_lib.ple_kv_proj_gate_workspace(T, C),), dtype=torch.uint8,
                            device=device) if fuse else None)
     # activation buffers shared by the steps (as an engine reuses them), except
-    # the ids: one buffer per layer set, so that the gather timed alone over
-    # the rotating sets reads each set's own rows (cold in L2)
-    shared = {"emb": torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device),
-              "kv": torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device),
+    # the gather's ids and rows: one buffer each per layer set, so that the
+    # gather timed alone over the rotating sets reads each set's own rows and
+    # writes its own output (cold in L2, as in a step)
+    shared = {"kv": torch.empty((T, 2 * C), dtype=torch.bfloat16, device=device),
               "y": torch.empty((T, C), dtype=torch.bfloat16, device=device),
               "gate": torch.empty((T,), dtype=torch.float32, device=device),
               "ctx_out": torch.empty((w.num_reqs, w.ctx_len), dtype=torch.int32, device=device),
               "st_out": torch.empty_like(sets[0]["conv_state"]) if w.decode else None}
-    bufs = [dict(shared, ids=torch.empty((T, H), dtype=torch.int64, device=device))
+    bufs = [dict(shared, ids=torch.empty((T, H), dtype=torch.int64, device=device),
+                 emb=torch.empty((T, w.emb_dim), dtype=torch.bfloat16, device=device))
             for _ in range(num_sets)]
     ids, emb, ctx_out, st_out = (bufs[0][k] for k in ("ids", "emb", "ctx_out", "st_out"))
     err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -434,8 +435,35 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     if int(err.item()) != 0:
         raise RuntimeError(f"{name}: device error word {int(err.item())} in the timed region")
 
-    # ---- each kernel alone: K back-to-back launches over the rotating layer
-    # sets between two events on the launching stream, so that a short
+    # ---- timed region: K steps replayed from CUDA graphs (one per layer
+    # set, captured once), device events on the replay stream ----
+    graphs, graph_error = capture_graphs(torch, step, num_sets, device)
+    if graphs is not None:
+        for i in range(max(args.warmup, len(graphs))):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        replay = torch.cuda.current_stream(device)
+        barrier()
+        torch.cuda.synchronize()
+        g0.record(replay)
+        for i in range(args.steps):
+            graphs[i % num_sets].replay()
+        g1.record(replay)
+        torch.cuda.synchronize()
+        barrier()
+        total_ms = max_over_ranks(g0.elapsed_time(g1), device)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"{name}: device error word {int(err.item())} in the graph replays")
+        mode = "cuda_graph"
+    else:
+        total_ms, mode = eager_ms, "eager"
+    del graphs
+
+    # ---- each kernel alone (after the timed region, so that its extra GPU
+    # work does not warm the board before it): K back-to-back launches over
+    # the rotating layer sets between two events on the launching stream, so that a short
     # kernel's launch latency overlaps the previous launch (the events
     # between the kernels of the eager steps above add it to every kernel);
     # the per-launch average is the kernel's duration for the roofline ----
@@ -466,32 +494,6 @@ def measure_workload(torch, args, name, device, rank, world, headline):
         del g_alone
     if int(err.item()) != 0:
         raise RuntimeError(f"{name}: device error word {int(err.item())} in the per-kernel timing")
-
-    # ---- timed region: K steps replayed from CUDA graphs (one per layer
-    # set, captured once), device events on the replay stream ----
-    graphs, graph_error = capture_graphs(torch, step, num_sets, device)
-    if graphs is not None:
-        for i in range(max(args.warmup, len(graphs))):
-            graphs[i % len(graphs)].replay()
-        torch.cuda.synchronize()
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        replay = torch.cuda.current_stream(device)
-        barrier()
-        torch.cuda.synchronize()
-        g0.record(replay)
-        for i in range(args.steps):
-            graphs[i % num_sets].replay()
-        g1.record(replay)
-        torch.cuda.synchronize()
-        barrier()
-        total_ms = max_over_ranks(g0.elapsed_time(g1), device)
-        if int(err.item()) != 0:
-            raise RuntimeError(f"{name}: device error word {int(err.item())} in the graph replays")
-        mode = "cuda_graph"
-    else:
-        total_ms, mode = eager_ms, "eager"
-    del graphs
 
     # ---- end to end through PLEHostPipeline with pinned host buffers ----
     # Every step uploads its inputs (token ids, query_start_loc, hidden) from
@@ -676,7 +678,7 @@ def chain_timing(torch, w, sets, device, err, fuse, L, reps=10):
     stream = torch.cuda.current_stream(device)
     res = {"layers": L}
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    variants = [("prefetch", True, 0), ("prefetch_one_cta_per_sm", True, sms),
+    variants = [("prefetch", True, None), ("prefetch_full_grid", True, 0),
                 ("inline", False, 0)]
     if w.table_loc == "host":  # the pages cap the side-stream gather at half the SMs
         variants.insert(1, ("prefetch_half_grid", True, sms // 2))

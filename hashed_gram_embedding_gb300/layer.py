@@ -332,14 +332,24 @@ class PLEChain:
     Layer i+1's ids and gather (its embed stage) only need the tokens, so
     they run on a side stream into one of two staging buffers while layer i's
     kv_proj, gate and conv (its mix stage) run on the main stream; a staging
-    buffer is refilled once the kv_proj that read it has finished. With
-    ``prefetch=False`` the layers run one after the other on the main
-    stream. Results are the same either way.
+    buffer is refilled once the layer that read it has finished, so the
+    gather overlaps the next layer's projection. With ``prefetch=False`` the
+    layers run one after the other on the main stream. Results are the same
+    either way.
+
+    prefetch_ctas caps the side-stream gathers' grid: None = one CTA per SM
+    for tables in HBM (a gather CTA fits beside the projection's CTA on the
+    same SM, so the two run together) and the full grid for host tables; 0 =
+    the full grid.
     """
 
-    def __init__(self, layers, prefetch=True, prefetch_ctas=0):
+    def __init__(self, layers, prefetch=True, prefetch_ctas=None):
         self.layers = list(layers)
         self.prefetch = bool(prefetch)
+        if prefetch_ctas is None:
+            on_device = all(l.table.is_cuda for l in self.layers)
+            prefetch_ctas = (torch.cuda.get_device_properties(
+                torch.cuda.current_device()).multi_processor_count if on_device else 0)
         self.prefetch_ctas = int(prefetch_ctas)
         self._bufs = {}
         self._side = {}
@@ -407,12 +417,16 @@ class PLEChain:
             main.wait_event(slot["ready"])
             layer = self.layers[i]
             layer.project(slot["emb"], hiddens[i], dev_err=dev_err, stream=main)
+            layer.convolve(hiddens[i], query_start_loc, outs[i], conv_state=cs[i],
+                           conv_state_out=cso[i], dev_err=dev_err, stream=main)
+            # The projection has read this staging buffer; refill it with layer
+            # i+2's rows once the conv is done too, so that the gather runs
+            # beside layer i+1's projection (tensor-bound, one CTA per SM)
+            # rather than beside this layer's conv (memory-bound, SMs full).
             slot["free"].record(main)
-            if i + 2 < L:  # refill this staging buffer with layer i+2's rows
+            if i + 2 < L:
                 side.wait_event(slot["free"])
                 embed(i + 2, side)
                 slot["ready"].record(side)
-            layer.convolve(hiddens[i], query_start_loc, outs[i], conv_state=cs[i],
-                           conv_state_out=cso[i], dev_err=dev_err, stream=main)
         main.wait_stream(side)
         return outs
