@@ -3,9 +3,10 @@
 The compute path is libple.so (hand-written CUDA for sm_103a, C ABI in
 include/ple.h); this package holds its build script, a ctypes binding with
 the C names, the PLELayer convenience wrapper (and PLEHostPipeline, which
-runs it over pinned host buffers with transfers overlapping compute) and the
-seeded synthetic
-workloads used by the tests and the benchmark.
+runs it over pinned host buffers with transfers overlapping compute; PLEChain,
+several layers with the next layers' lookups prefetched), the sharded lookups
+over a group of ranks (HeadShardedLookup, RowShardedLookup) and the seeded
+synthetic workloads used by the tests and the benchmark.
 """
 
 from ._lib import (  # noqa: F401
@@ -21,11 +22,16 @@ from ._lib import (  # noqa: F401
     ple_gate,
     ple_conv,
     ple_gate_conv,
+    ple_lookup_shard,
+    ple_select_rows,
     ple_version,
     PLE_DEVERR_BOUNDS,
     PLE_DEVERR_QSL,
     PLE_DEVERR_TIMEOUT,
     PLE_HBM,
     PLE_HOST_UVA,
+    PLE_SHARD_HEADS,
+    PLE_SHARD_ROWS,
 )
 from .layer import PLELayer, PLEHostPipeline, PLEChain  # noqa: F401
+from .sharded import HeadShardedLookup, RowShardedLookup  # noqa: F401
