@@ -220,6 +220,8 @@ def algorithmic_work(w):
     """Bytes (or flops) one launch of each kernel must move (or do)."""
     T, H, D, C, E = w.num_tokens, w.num_heads, w.head_dim, w.hidden, w.emb_dim
     elem = 1 if w.table_dtype == "fp8" else 2
+    # decode steps also read and write every request's conv state [(K-1)d, C]
+    state = 2 * w.num_reqs * (w.conv_k - 1) * w.dilation * C * 2 if w.decode else 0
     row_read = H * D * elem + (H * 4 if w.table_dtype == "fp8" else 0)
     lookup = (("link", T * row_read) if w.table_loc == "host"
               else ("hbm", T * (H * 8 + row_read + H * D * 2)))
@@ -229,11 +231,11 @@ def algorithmic_work(w):
         "ngram_lookup": ("hbm", T * (4 + row_read + H * D * 2 + H * 8)),
         "lookup": lookup,
         "kv_proj": ("tensor", 2.0 * T * E * 2 * C),
-        "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2)),
+        "gate_conv": ("hbm", T * (C * 2 + 2 * C * 2 + C * 2) + state),
         # the gate reductions ride in the projection's epilogue: tensor-bound
         "kv_proj_gate": ("tensor", 2.0 * T * E * 2 * C),
-        # v and g in, y out
-        "conv": ("hbm", T * (C * 2 + 4 + C * 2)),
+        # v and g in, y out (+ the carried conv state)
+        "conv": ("hbm", T * (C * 2 + 4 + C * 2) + state),
     }
 
 

@@ -62,3 +62,12 @@ def test_algorithmic_work_of_the_prefill_workload():
     assert work["lookup"] == ("hbm", 8192 * (128 + 4096 + 4096))
     assert work["kv_proj"] == ("tensor", 2.0 * 8192 * 2048 * 8192)
     assert work["gate_conv"] == ("hbm", 8192 * (8192 + 16384 + 8192))
+
+
+def test_algorithmic_work_counts_the_decode_conv_state():
+    import bench
+    from hashed_gram_embedding_gb300 import workloads as wl
+    w = wl.WORKLOADS["decode256x4"]
+    work = bench.algorithmic_work(w)
+    # 1024 tokens x (v 8 KB + g 4 B + y 8 KB) + 256 requests x 9 rows x 4096 x 2 B, in and out
+    assert work["conv"] == ("hbm", 1024 * (8192 + 4 + 8192) + 2 * 256 * 9 * 4096 * 2)
