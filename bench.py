@@ -551,6 +551,7 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     kernels = {}
     step_kernels_ms = float(np.mean([sum(per_kernel[x][i] for x in KERNELS)
                                      for i in range(args.steps)]))
+    alone_total = sum(alone[x] for x in KERNELS)
     for k in KERNELS:
         avg_ms = alone[k]
         bound, amount = work[k]
@@ -570,7 +571,8 @@ def measure_workload(torch, args, name, device, rank, world, headline):
         kernels[k] = {"us": round(avg_ms * 1e3, 2), "bound": bound, "achieved": round(achieved, 1),
                       "unit": unit, "frac": round(achieved / peak, 4),
                       "us_in_step": round(in_step_ms * 1e3, 2),
-                      "share": round(in_step_ms / step_kernels_ms, 4)}
+                      "share": round(avg_ms / alone_total, 4),
+                      "share_in_step": round(in_step_ms / step_kernels_ms, 4)}
     dominant = max(KERNELS, key=lambda k: kernels[k]["us"])
     dk = kernels[dominant]
     bound, amount = work[dominant]
@@ -621,7 +623,8 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     line["eager"] = {"ms_per_step": round(eager_ms / args.steps, 4),
                      "value": round(world * args.steps * T / (eager_ms * 1e-3), 1),
                      "note": "same steps launched one by one, events between kernels "
-                             "(kernels.*.us_in_step and share); kernels.*.us: each kernel alone, "
+                             "(kernels.*.us_in_step, share_in_step: these also time the host's "
+                             "submission); kernels.*.us and share: each kernel alone, "
                              f"{args.steps} back-to-back launches over the rotating layer sets"}
     if graph_error:
         line["eager"]["graph_capture_error"] = graph_error
