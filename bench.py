@@ -315,6 +315,8 @@ def config_summary(line):
         out["chain"] = line["chain"]
     if "overlap" in line:
         out["overlap"] = line["overlap"]
+    if "sharded" in line:
+        out["sharded"] = line["sharded"]
     return out
 
 
@@ -540,6 +542,8 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     extra = {}
     if rank == 0 and w.table_loc == "host":
         extra["overlap"] = uva_overlap(torch, _lib, sets[0], ids, emb, w, device, order_ws)
+    if rank == 0 and w.name == "prefill8k" and w.table_loc == "hbm" and not args.vocab_start:
+        extra["sharded"] = sharded_timing(torch, _lib, w, sets[0], bufs[0]["ids"], device)
     chain_layers = args.chain_layers or (w.num_layers if w.num_layers > 1 else 0)
     if chain_layers > 1:
         extra["chain"] = chain_timing(torch, w, sets, device, err, fuse, chain_layers)
@@ -742,6 +746,81 @@ def measure_link_gbs(torch, device, nbytes=512 << 20, reps=5):
     e1.record(stream)
     torch.cuda.synchronize()
     return round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+
+
+def sharded_timing(torch, _lib, w, p, ids, device, tp=2, dp=2, reps=20):
+    """The per-rank kernels of a sharded lookup, for a tp x dp group emulated
+    on this GPU over the workload's table and ids (the step's tokens split
+    into dp replicas): each rank's head-shard gather (its H / (tp dp) heads
+    for every gathered token) and the select of one replica's window; and for
+    a row-sharded table, one rank's raw-row gather (its row range, zeros
+    elsewhere) and the select. Collectives are not timed (one GPU). Checks
+    that the emulated group rebuilds the plain lookup's rows bit for bit."""
+    from hashed_gram_embedding_gb300 import sharded
+    T, H, D = w.num_tokens, w.num_heads, w.head_dim
+    G = tp * dp
+    table = p["table"]
+    V, O = p["host"]["V"], p["host"]["O"]
+    stream = torch.cuda.current_stream(device)
+
+    def timed(fn):
+        """us per call of fn: reps calls replayed from one CUDA graph (so that
+        the host's submission does not bound these short kernels)."""
+        fn()
+        torch.cuda.synchronize()
+        graphs, _ = capture_graphs(torch, lambda s_, st=None: [fn() for _ in range(reps)], 1,
+                                   device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if graphs is not None:
+            graphs[0].replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            graphs[0].replay()
+            e1.record(stream)
+        else:
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us
+
+    slot = T // dp
+    heads = {}
+    for r in range(G):
+        d, t = divmod(r, tp)
+        _, hb, n = sharded.head_shard(H, tp, t, dp, d)
+        r0, r1 = sharded.head_rows(V, O, hb, n)
+        heads[r] = sharded.HeadShardedLookup(table[r0:r1], None, V, O, tp, t, dp, d)
+    rows_out = torch.stack([heads[r].gather(ids) for r in range(G)])
+    out = heads[0].select(rows_out, slot, slot)
+    ref = torch.empty((T, H * D), dtype=torch.bfloat16, device=device)
+    _lib.ple_lookup(ids, table, ref)
+    ok_heads = bool(torch.equal(out.view(torch.int16), ref[:slot].view(torch.int16)))
+    hs = heads[G - 1]
+    g_us = timed(lambda: hs.gather(ids))
+    s_us = timed(lambda: heads[0].select(rows_out, slot, slot, out=out))
+    # row shards of the same table
+    r0, r1 = sharded.row_shard(table.shape[0], G, 1)
+    rl = sharded.RowShardedLookup(table[r0:r1], None, r0, H, dp, 0)
+    raw, _ = rl.gather(ids)
+    rg_us = timed(lambda: rl.gather(ids))
+    rs_us = timed(lambda: rl.select(raw, None, slot, slot, out=out))
+    n = H // G
+    peak = load_peaks()[0]["hbm_gbs"]
+    # bytes: head shard: T x n ids read, T x n rows read + written; select: slot x H rows
+    # read + written; row shard: T x H ids, the owned rows read (~1/G), T x H rows written
+    gb = {"head_gather": T * n * (8 + 2 * D * 2), "select": slot * H * D * 2 * 2,
+          "row_gather": T * H * (8 + D * 2) + T * H * D * 2 // G}
+    us = {"head_gather": g_us, "select": s_us, "row_gather": rg_us, "row_select": rs_us}
+    gb["row_select"] = gb["select"]
+    res = {"group": f"tp{tp} x dp{dp} emulated on one GPU (collectives not timed)",
+           "tokens": T, "heads_per_shard": n, "rows_equal_plain_lookup": ok_heads}
+    for k, v in us.items():
+        ach = gb[k] / (v * 1e-6) / 1e9
+        res[k] = {"us": round(v, 2), "gbs": round(ach, 1), "frac_hbm": round(ach / peak, 4)}
+    return res
 
 
 def uva_overlap(torch, _lib, p, ids, emb, w, device, order_ws, reps=10):

@@ -111,6 +111,15 @@ select_rows_kernel(const uint4* __restrict__ src, int64_t part_vecs, int64_t row
                    const float* __restrict__ src_scale, int64_t scale_part, int part_heads,
                    int64_t row_begin, uint32_t total_vecs, int num_heads, int vpr,
                    const __grid_constant__ SelectMap map, uint4* __restrict__ out) {
+  // the head map in shared memory: the lanes of a warp index different heads,
+  // and a lane-varying index into the parameter block would serialise on the
+  // constant cache
+  __shared__ int32_t part_s[kMaxSelectHeads], col_s[kMaxSelectHeads];
+  for (int h = threadIdx.x; h < num_heads; h += kThreads) {
+    part_s[h] = map.part[h];
+    col_s[h] = map.col[h];
+  }
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   const uint32_t step = gridDim.x * kThreads;
@@ -130,8 +139,8 @@ select_rows_kernel(const uint4* __restrict__ src, int64_t part_vecs, int64_t row
         const uint32_t k = idx - p * vpr;
         const uint32_t t = p / num_heads;
         const uint32_t h = p - t * num_heads;
-        const int part = map.part[h];
-        const int col = map.col[h];
+        const int part = part_s[h];
+        const int col = col_s[h];
         const int64_t row = row_begin + t;
         o[u] = idx;
         v[u] = __ldg(src + part * part_vecs + row * row_vecs + static_cast<int64_t>(col) * vpr + k);
