@@ -9,9 +9,9 @@
 // semantics).
 //
 // Design: one thread per (token, head) output, so the int64 stores of a warp
-// are contiguous. Request boundaries are staged in shared memory once per
-// block, the block's first token is searched once and every thread steps
-// forward from there; the hash itself is ngram_id (ngram_hash.cuh).
+// are contiguous. Each thread searches query_start_loc for its token's
+// request (cached loads); the heads' constants are staged in shared memory;
+// the hash itself is ngram_id (ngram_hash.cuh).
 #include "ngram_hash.cuh"
 
 namespace ple {
@@ -28,36 +28,16 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t work = static_cast<uint32_t>(num_tokens) * static_cast<uint32_t>(num_heads);
 
-  // Request boundaries staged once per block (one coalesced load); the
-  // block's first token is searched once, every thread then steps forward
-  // from there (a block spans 256 / num_heads consecutive tokens).
-  __shared__ int32_t qsl_s[kStagedBounds];
-  __shared__ int r_first_s;
+  // The heads' constants are staged in shared memory (lanes index different
+  // heads); every thread then finds its token's request itself with a
+  // binary search of query_start_loc (a few dependent loads that hit L1:
+  // the whole array is a few hundred bytes), so the block waits at one
+  // barrier only.
   __shared__ NgramHeadsSmem hs;
-  const bool staged = num_reqs < kStagedBounds;
   stage_ngram_heads(k, num_heads, hs);
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  if (staged)
-    for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) qsl_s[r] = __ldg(qsl + r);
-  __syncthreads();
-  const uint32_t i_first = blockIdx.x * blockDim.x;
-  if (threadIdx.x == 0 && i_first < work) {
-    const int64_t t_first = i_first / static_cast<uint32_t>(num_heads);
-    int r;
-    if (staged) {
-      int lo = 0, hi = num_reqs + 1;  // count of boundaries <= t_first
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (static_cast<int64_t>(qsl_s[mid]) <= t_first) lo = mid + 1; else hi = mid;
-      }
-      r = lo - 1 < 0 ? 0 : (lo - 1 >= num_reqs ? num_reqs - 1 : lo - 1);
-    } else {
-      r = find_request(qsl, num_reqs, t_first);
-    }
-    r_first_s = r;
-  }
-  __syncthreads();
 
   check_qsl(qsl, num_reqs, num_tokens, i, dev_err);
 
@@ -71,16 +51,9 @@ ngram_ids_kernel(const int32_t* __restrict__ input_ids, int64_t num_tokens,
   const int64_t t = t32;
 
   // Last request whose start is <= t (the right-sided search of the pages'
-  // CPU branch, clamped): step forward from the block's first request.
-  int r = r_first_s;
-  int64_t start;
-  if (staged) {
-    while (r + 1 < num_reqs && static_cast<int64_t>(qsl_s[r + 1]) <= t) ++r;
-    start = qsl_s[r];
-  } else {
-    r = find_request(qsl, num_reqs, t);
-    start = __ldg(qsl + r);
-  }
+  // CPU branch, clamped).
+  const int r = find_request(qsl, num_reqs, t);
+  const int64_t start = __ldg(qsl + r);
   const int64_t pos = t - start;  // position inside the request
 
   out[i] = ngram_id(input_ids, ctx, ctx_len, eos, t, pos, r, h, heads_per_ngram, k, hs);
