@@ -332,7 +332,16 @@ constexpr int P_B_STAGE = P_ATOMS * P_B_ATOM;
 constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
 constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
-constexpr int kEpilogueWarps = kEpilogueThreads / 32;
+// Epilogue warps: 4 (one per TMEM lane quadrant, each draining all columns
+// of a tile) or 8 (two per quadrant, each draining one 128-column half).
+// With few tiles per CTA the last tile's epilogue, which nothing hides, is a
+// large share of the launch and 8 warps halve it (29.5 against 30.7 us for
+// 1024 x 2048 -> 8192 with the fused gate on a GB300); with many tiles the
+// epilogues are hidden behind the MMAs and the extra warps only compete
+// with the issuing warps (1 % slower at 32768 rows).
+template <int EW>
+constexpr int pair_threads() { return 64 + 32 * EW; }
+constexpr int kFewRounds = 4;  // at most this many tiles per CTA pair: 8 epilogue warps
 // kind::f16 instruction descriptors for M = 256 (two SMs) x N = 256, and
 // x N = 128 (the half tiles of the last round).
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -539,8 +548,8 @@ __device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_group
 // One CTA pair per cluster. Units [0, full_units) are full tiles; the units
 // past them are half tiles (2 per remaining tile; map_b_half loads 64 W rows
 // per CTA).
-template <bool GATE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATE, int EW>
+__global__ void __launch_bounds__(pair_threads<EW>(), 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_b_half, ple_bf16_t* __restrict__ out,
@@ -582,7 +591,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 2 * kEpilogueWarps);  // every epilogue warp of the pair
+      mbar_init(acce_bar(b), 2 * EW);  // every epilogue warp of the pair
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -687,7 +696,12 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     __syncwarp();
   } else if (warp >= 2) {
     // ---------------- epilogue (both CTAs): this SM's 128 rows ----------------
+    // Warp w reads TMEM lanes 32 (w % 4) .. +31 (its quadrant). With 8
+    // warps, w and w + 4 split a tile's columns in halves, h = (w - 2) / 4;
+    // of a half tile's key block (128 channels) warp h = 0 alone sums it, so
+    // that every 128-channel block is one warp's, as in full tiles.
     const int quad = warp & 3;
+    const int hsel = EW == 8 ? (warp - 2) >> 2 : 0;
     const int row_in_tile = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -700,22 +714,33 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_after();
       const PairUnit t = pair_unit(u, full_units, n_groups);
       const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
-      const int n_base = t.n_base;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+      const uint32_t tlane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * ACC_COLS);
+      // this warp's columns of the tile: [col0, col0 + wcols)
+      const int wcols = EW == 8 ? t.cols / 2 : t.cols;
+      const int col0 = hsel * wcols;
       if constexpr (GATE) {
-        if (n_base < ge.C) {
-          gate_tile(ge, taddr, m, M, n_base, t.cols, lane, leader, acce_bar(acc));
+        if (t.n_base < ge.C) {
+          if (EW == 4 || t.cols == BN || hsel == 0) {
+            const int kcols = EW == 8 ? kGateBlock : t.cols;
+            const int kc0 = hsel * kGateBlock;
+            gate_tile(ge, tlane + static_cast<uint32_t>(kc0), m, M, t.n_base + kc0, kcols, lane,
+                      leader, acce_bar(acc));
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(acc), leader));
+          }
           if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
           continue;
         }
       }
       ple_bf16_t* row_out = out + static_cast<int64_t>(m) * N;
 #pragma unroll 1
-      for (int chunk = 0; chunk < t.cols / 32; ++chunk) {
+      for (int chunk = 0; chunk < wcols / 32; ++chunk) {
         uint32_t r[32];
-        tmem_ld32(taddr + static_cast<uint32_t>(chunk * 32), r);
-        const int n = n_base + chunk * 32;
+        tmem_ld32(tlane + static_cast<uint32_t>(col0 + chunk * 32), r);
+        const int n = t.n_base + col0 + chunk * 32;
         if (m < M && n < N) {
           uint4* dst = reinterpret_cast<uint4*>(row_out + n);
 #pragma unroll
@@ -830,8 +855,9 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   }
   using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int,
                           int32_t*, GateEpi);
+  // the 4-warp instantiation sizes the grid (the occupancy of both is one CTA per SM)
   using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
-  const PairFn pair_fn = ge != nullptr ? kv_proj_pair_kernel<true> : kv_proj_pair_kernel<false>;
+  PairFn pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 4> : kv_proj_pair_kernel<false, 4>;
   const TileFn tile_fn = kv_proj_kernel;
   const void* fn = paired ? reinterpret_cast<const void*>(pair_fn) : reinterpret_cast<const void*>(tile_fn);
   const size_t smem = paired ? kPairSmemBytes : kSmemBytes;
@@ -847,7 +873,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   if (cluster > 1) {
     cudaLaunchConfig_t qcfg{};
     qcfg.gridDim = dim3(static_cast<unsigned>(max_clusters * cluster));
-    qcfg.blockDim = dim3(kThreads);
+    qcfg.blockDim = dim3(paired ? pair_threads<4>() : kThreads);
     qcfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute qattr[1];
     qattr[0].id = cudaLaunchAttributeClusterDimension;
@@ -879,8 +905,21 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   }
   const int clusters = units < max_clusters ? units : max_clusters;
   const dim3 grid(static_cast<unsigned>(clusters * cluster));
+  // few tiles per CTA pair: the 8-warp epilogue (PLE_KVPROJ_EPI = 4 | 8 forces one)
+  int epi_warps = (units + clusters - 1) / clusters <= kFewRounds ? 8 : 4;
+  if (const char* e = getenv("PLE_KVPROJ_EPI")) {
+    if (atoi(e) == 4) epi_warps = 4;
+    else if (atoi(e) == 8) epi_warps = 8;
+  }
+  if (paired && epi_warps == 8) {
+    pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 8> : kv_proj_pair_kernel<false, 8>;
+    err = cudaFuncSetAttribute(pair_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return check_cuda(err, "kv projection: smem attribute");
+  }
   if (paired)
-    err = launch_kernel(pair_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
+    err = launch_kernel(pair_fn, grid, dim3(epi_warps == 8 ? pair_threads<8>() : pair_threads<4>()),
+                        smem, stream, static_cast<unsigned>(cluster),
                         map_a, map_b, map_b_half, kv, M, N, K, full_units, dev_err,
                         ge != nullptr ? *ge : GateEpi{});
   else

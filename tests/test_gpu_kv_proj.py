@@ -70,16 +70,18 @@ def test_kv_proj_prefill_8k_shape():
     assert_close(bits(kv), bits(lib_ref), what="kv vs cuBLAS")
 
 
-@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit"])
+@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit", "pair-epi4", "pair-epi8"])
 @pytest.mark.parametrize("M,E,C", [(512, 512, 1024), (300, 2048, 4096), (129, 200, 48),
                                    (257, 72, 112), (1000, 128, 128)])
 def test_kv_proj_kernel_variants(M, E, C, mode, monkeypatch):
     """Each kernel variant -- one CTA per 128 x 256 tile, CTA pairs with
     cta_group::2 MMAs over 256 x 256 tiles (with and without the last round
-    split into 128-column halves) -- gives the oracle's result, ragged edges
-    included."""
+    split into 128-column halves; with 4 or 8 epilogue warps) -- gives the
+    oracle's result, ragged edges included."""
     monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
     monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
+    if "epi" in mode:
+        monkeypatch.setenv("PLE_KVPROJ_EPI", mode[-1])
     emb = rand_bf16((M, E), 0.5, M + E)
     w = rand_bf16((2 * C, E), 0.05, C + 7)
     kv = torch.full((M, 2 * C), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -90,10 +92,12 @@ def test_kv_proj_kernel_variants(M, E, C, mode, monkeypatch):
     assert_close(bits(kv), oracle_kv_proj(bits(emb), bits(w)), what=f"kv {mode} {M}x{E}x{2*C}")
 
 
-@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit"])
+@pytest.mark.parametrize("mode", ["single", "pair", "pair-nosplit", "pair-epi8"])
 def test_kv_proj_variants_prefill_8k_against_cublas(mode, monkeypatch):
     monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
     monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
+    if "epi" in mode:
+        monkeypatch.setenv("PLE_KVPROJ_EPI", mode[-1])
     M, E, C = 8192, 2048, 4096
     g = torch.Generator(device="cuda").manual_seed(12)
     emb = (torch.randn((M, E), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
