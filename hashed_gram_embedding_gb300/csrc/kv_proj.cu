@@ -342,6 +342,7 @@ constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
 template <int EW>
 constexpr int pair_threads() { return 64 + 32 * EW; }
 constexpr int kFewRounds = 4;  // at most this many tiles per CTA pair: 8 epilogue warps
+constexpr size_t kKeyFirstMaxA = size_t(64) << 20;  // bytes of A for the key-first order
 // kind::f16 instruction descriptors for M = 256 (two SMs) x N = 256, and
 // x N = 128 (the half tiles of the last round).
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -425,6 +426,9 @@ struct GateEpi {
   int C;
 };
 
+__device__ __forceinline__ void gate_publish(const GateEpi& ge, int m, int M, int lane, int blk0,
+                                             int nb, float4 part0, float4 part1);
+
 // One key tile (cols = 256 or 128 channels from n_base) of the fused gate
 // epilogue for this thread's row m (one warp = 32 consecutive rows). taddr:
 // the warp's lane quadrant of the accumulator. Releases the accumulator to
@@ -486,9 +490,15 @@ __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar, leader));
+  gate_publish(ge, m, M, lane, n_base / kGateBlock, cols / kGateBlock, part0, part1);
+}
 
-  const int blk0 = n_base / kGateBlock;
-  const int nb = cols / kGateBlock;
+// Publishes a warp's block sums (nb = 1 or 2 blocks from blk0) for its rows
+// and, in the warp that delivers the last block of its 32 rows, writes
+// their gate scalars.
+__device__ __forceinline__ void gate_publish(const GateEpi& ge, int m, int M, int lane, int blk0,
+                                             int nb, float4 part0, float4 part1) {
+  const bool row_ok = m < M;
   const int n_blk = ge.C / kGateBlock;
   if (row_ok) {
     ge.partial[static_cast<int64_t>(blk0) * M + m] = part0;
@@ -518,6 +528,73 @@ __device__ __forceinline__ void gate_tile(const GateEpi& ge, uint32_t taddr, int
   ge.gate_out[m] = gate_of(sh, sk, sd, ge.C, ge.eps);
 }
 
+// The 8-warp epilogue's key block (128 channels from n_base, one per warp):
+// all of the row's h and the block's gammas are loaded before the block's
+// accumulator is ready (behind the MMAs), so the reduction waits on tensor
+// memory alone. Lane l < 16 holds gamma_h of channels n_base + 8l .. + 7 and
+// lane 16 + l gamma_k of the same channels; the chunks take them by shuffle.
+struct GateBlockIn {
+  uint4 h[kGateBlock / 32][4];
+  uint4 gam;
+};
+
+__device__ __forceinline__ void gate_block_load(const GateEpi& ge, int m, int M, int n_base,
+                                                int lane, GateBlockIn& in) {
+  const bool row_ok = m < M;
+  const ple_bf16_t* hrow = ge.hidden + static_cast<int64_t>(row_ok ? m : 0) * ge.C + n_base;
+#pragma unroll
+  for (int c = 0; c < kGateBlock / 32; ++c)
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      in.h[c][q] = row_ok ? ldg16(hrow + c * 32 + q * 8) : make_uint4(0, 0, 0, 0);
+  in.gam = ldg16((lane < 16 ? ge.gamma_h : ge.gamma_k) + n_base + 8 * (lane & 15));
+}
+
+// The same sums, in the same order, as gate_tile over one block.
+__device__ __forceinline__ void gate_block(const GateEpi& ge, uint32_t taddr, int m, int M,
+                                           int n_base, int lane, uint32_t leader,
+                                           uint32_t acce_bar, const GateBlockIn& in) {
+  uint64_t sh2 = 0, sk2 = 0, sd2 = 0;  // (+0.0f, +0.0f) pairs
+#pragma unroll
+  for (int chunk = 0; chunk < kGateBlock / 32; ++chunk) {
+    uint32_t r[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(chunk * 32), r);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int src = chunk * 4 + q;  // the lane holding these 8 channels' gamma_h
+      const uint32_t aw[4] = {__shfl_sync(0xffffffffu, in.gam.x, src),
+                              __shfl_sync(0xffffffffu, in.gam.y, src),
+                              __shfl_sync(0xffffffffu, in.gam.z, src),
+                              __shfl_sync(0xffffffffu, in.gam.w, src)};
+      const uint32_t bw[4] = {__shfl_sync(0xffffffffu, in.gam.x, src + 16),
+                              __shfl_sync(0xffffffffu, in.gam.y, src + 16),
+                              __shfl_sync(0xffffffffu, in.gam.z, src + 16),
+                              __shfl_sync(0xffffffffu, in.gam.w, src + 16)};
+      const uint32_t hw[4] = {in.h[chunk][q].x, in.h[chunk][q].y, in.h[chunk][q].z,
+                              in.h[chunk][q].w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t kb = pack_bf16x2(r[8 * q + 2 * p], r[8 * q + 2 * p + 1]);
+        const uint64_t k2 = f2(bf_lo(kb), bf_hi(kb));
+        const uint64_t h2 = f2(bf_lo(hw[p]), bf_hi(hw[p]));
+        const uint64_t gg = f2_mul(f2(bf_lo(aw[p]), bf_hi(aw[p])), f2(bf_lo(bw[p]), bf_hi(bw[p])));
+        sh2 = f2_fma(h2, h2, sh2);
+        sk2 = f2_fma(k2, k2, sk2);
+        sd2 = f2_fma(f2_mul(h2, k2), gg, sd2);
+      }
+    }
+  }
+  float a0, a1, b0, b1, d0, d1;
+  f2_split(sh2, a0, a1);
+  f2_split(sk2, b0, b1);
+  f2_split(sd2, d0, d1);
+  const float4 part = make_float4(a0 + a1, b0 + b1, d0 + d1, 0.f);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar, leader));
+  gate_publish(ge, m, M, lane, n_base / kGateBlock, 1, part, part);
+}
+
 // A work unit of the pair kernel: 256 rows from m_base, 256 columns from
 // n_base, or -- units >= full_units -- one 128-column half of a 256 x 256
 // tile. Splitting the last round's tiles
@@ -529,17 +606,44 @@ struct PairUnit {
   int cols;  // 256 or 128
 };
 
-__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups) {
+// Tile v of the launch's tile order -> its 256-row block mb and 256-column
+// group g. The natural order walks each row block's column groups in turn
+// (consecutive CTA pairs share A rows). With key_groups > 0 (the fused gate's
+// C / 256 key groups; used when each CTA pair has few tiles) every key tile
+// comes first and every value tile after: the last round then holds value
+// tiles, whose epilogue is a plain store, and the gate's completion of each
+// row group runs behind the value tiles' MMAs instead of after them.
+__device__ __forceinline__ void tile_of(int v, int n_groups, int key_groups, int m_tiles, int& mb,
+                                        int& g) {
+  if (key_groups == 0) {
+    mb = v / n_groups;
+    g = v % n_groups;
+    return;
+  }
+  const int n_key = m_tiles * key_groups;
+  if (v < n_key) {
+    mb = v / key_groups;
+    g = v % key_groups;
+  } else {
+    const int value_groups = n_groups - key_groups;
+    mb = (v - n_key) / value_groups;
+    g = key_groups + (v - n_key) % value_groups;
+  }
+}
+
+__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups, int key_groups,
+                                              int m_tiles) {
   PairUnit t;
+  const int h = u - full_units;
+  const int v = u >= full_units ? full_units + (h >> 1) : u;
+  int mb, g;
+  tile_of(v, n_groups, key_groups, m_tiles, mb, g);
+  t.m_base = mb * 2 * BM;
   if (u >= full_units) {
-    const int h = u - full_units;
-    const int v = full_units + (h >> 1);
-    t.m_base = (v / n_groups) * 2 * BM;
-    t.n_base = (v % n_groups) * BN + (h & 1) * (BN / 2);
+    t.n_base = g * BN + (h & 1) * (BN / 2);
     t.cols = BN / 2;
   } else {
-    t.m_base = (u / n_groups) * 2 * BM;
-    t.n_base = (u % n_groups) * BN;
+    t.n_base = g * BN;
     t.cols = BN;
   }
   return t;
@@ -547,13 +651,15 @@ __device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_group
 
 // One CTA pair per cluster. Units [0, full_units) are full tiles; the units
 // past them are half tiles (2 per remaining tile; map_b_half loads 64 W rows
-// per CTA).
+// per CTA). Tiles follow tile_of's order (key_groups > 0: key tiles first).
+// Warps: 0 the TMA producer, 1 the MMA issuer (tensor memory owner), 2 .. 1 +
+// EW the epilogue.
 template <bool GATE, int EW>
 __global__ void __launch_bounds__(pair_threads<EW>(), 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_b_half, ple_bf16_t* __restrict__ out,
-                    int M, int N, int K, int full_units, int32_t* dev_err,
+                    int M, int N, int K, int full_units, int key_groups, int32_t* dev_err,
                     const __grid_constant__ GateEpi ge) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -626,7 +732,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     bool ok = true;
     const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
     for (int u = cl; ok && u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit(u, full_units, n_groups);
+      const PairUnit t = pair_unit(u, full_units, n_groups, key_groups, m_tiles);
       const bool half = t.cols != BN;
       const int m0 = t.m_base + q * BM;
       const int n0 = t.n_base + q * (t.cols / 2);
@@ -664,7 +770,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       bool ok = true;
       for (int u = cl; ok && u < num_units; u += num_cl) {
         const uint32_t idesc =
-            pair_unit(u, full_units, n_groups).cols == BN ? kIdescPair : kIdescPairHalf;
+            pair_unit(u, full_units, n_groups, key_groups, m_tiles).cols == BN ? kIdescPair : kIdescPairHalf;
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -706,14 +812,19 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cl; u < num_units; u += num_cl) {
+      const PairUnit t = pair_unit(u, full_units, n_groups, key_groups, m_tiles);
+      const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
+      // 8 warps: a key block's h and gammas are loaded before its MMAs end
+      const bool key_block8 =
+          GATE && EW == 8 && t.n_base < ge.C && (t.cols == BN || hsel == 0);
+      GateBlockIn gin;
+      if (key_block8) gate_block_load(ge, m, M, t.n_base + hsel * kGateBlock, lane, gin);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag));
       if (!ok) {
         if (lane == 0) { *abort_flag = 1; set_dev_err(dev_err, PLE_DEVERR_TIMEOUT); }
         break;
       }
       tc_fence_after();
-      const PairUnit t = pair_unit(u, full_units, n_groups);
-      const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
       const uint32_t tlane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * ACC_COLS);
       // this warp's columns of the tile: [col0, col0 + wcols)
@@ -721,11 +832,12 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       const int col0 = hsel * wcols;
       if constexpr (GATE) {
         if (t.n_base < ge.C) {
-          if (EW == 4 || t.cols == BN || hsel == 0) {
-            const int kcols = EW == 8 ? kGateBlock : t.cols;
+          if (key_block8) {
             const int kc0 = hsel * kGateBlock;
-            gate_tile(ge, tlane + static_cast<uint32_t>(kc0), m, M, t.n_base + kc0, kcols, lane,
-                      leader, acce_bar(acc));
+            gate_block(ge, tlane + static_cast<uint32_t>(kc0), m, M, t.n_base + kc0, lane, leader,
+                       acce_bar(acc), gin);
+          } else if (EW == 4) {
+            gate_tile(ge, tlane, m, M, t.n_base, t.cols, lane, leader, acce_bar(acc));
           } else {
             tc_fence_before();
             __syncwarp();
@@ -854,7 +966,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
     map_b_half = map_b;  // not read
   }
   using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int,
-                          int32_t*, GateEpi);
+                          int, int32_t*, GateEpi);
   // the 4-warp instantiation sizes the grid (the occupancy of both is one CTA per SM)
   using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
   PairFn pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 4> : kv_proj_pair_kernel<false, 4>;
@@ -905,12 +1017,25 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   }
   const int clusters = units < max_clusters ? units : max_clusters;
   const dim3 grid(static_cast<unsigned>(clusters * cluster));
-  // few tiles per CTA pair: the 8-warp epilogue (PLE_KVPROJ_EPI = 4 | 8 forces one)
-  int epi_warps = (units + clusters - 1) / clusters <= kFewRounds ? 8 : 4;
+  // Few tiles per CTA pair: the 8-warp epilogue. With the fused gate, key
+  // tiles first while A (emb) fits in half of L2, so that the second pass
+  // over its rows (for the value tiles) reads L2, not HBM: 1024, 4096 and
+  // 8192 x 2048 -> 8192 take 25.9, 77.7 and 160.1 us against 29.1, 79.9 and
+  // 162.9 in the natural order on a GB300; at 32768 rows (128 MB of A) the
+  // natural order is 2 % faster. PLE_KVPROJ_EPI = 4 | 8 and
+  // PLE_KVPROJ_ORDER = natural | keyfirst force either choice.
+  const bool few = (units + clusters - 1) / clusters <= kFewRounds;
+  int epi_warps = few ? 8 : 4;
   if (const char* e = getenv("PLE_KVPROJ_EPI")) {
     if (atoi(e) == 4) epi_warps = 4;
     else if (atoi(e) == 8) epi_warps = 8;
   }
+  bool key_first = ge != nullptr && static_cast<size_t>(M) * K * 2 <= kKeyFirstMaxA;
+  if (const char* e = getenv("PLE_KVPROJ_ORDER")) {
+    if (strcmp(e, "natural") == 0) key_first = false;
+    else if (strcmp(e, "keyfirst") == 0) key_first = ge != nullptr;
+  }
+  const int key_groups = key_first ? ge->C / BN : 0;
   if (paired && epi_warps == 8) {
     pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 8> : kv_proj_pair_kernel<false, 8>;
     err = cudaFuncSetAttribute(pair_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -920,7 +1045,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   if (paired)
     err = launch_kernel(pair_fn, grid, dim3(epi_warps == 8 ? pair_threads<8>() : pair_threads<4>()),
                         smem, stream, static_cast<unsigned>(cluster),
-                        map_a, map_b, map_b_half, kv, M, N, K, full_units, dev_err,
+                        map_a, map_b, map_b_half, kv, M, N, K, full_units, key_groups, dev_err,
                         ge != nullptr ? *ge : GateEpi{});
   else
     err = launch_kernel(tile_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),

@@ -8,8 +8,8 @@ scalars agree with ple_gate run on ple_kv_proj's kv (same bf16 k; only the
 float32 summation order differs), and ple_gated_conv on ple_gate's scalars
 equals ple_gate_conv bit for bit. Shapes cover ragged row counts (a partial
 32-row group, M = 1), several key-tile counts, both CTA-pair kernels with 4
-and 8 epilogue warps, and the 8k-prefill shape in the launch configuration
-the benchmark times."""
+and 8 epilogue warps and both tile orders, and the 8k-prefill shape in the
+launch configuration the benchmark times."""
 
 import numpy as np
 import pytest
@@ -70,20 +70,24 @@ CASES = [(512, 512, 1024), (1, 64, 256), (129, 200, 256), (300, 2048, 4096), (10
          (257, 72, 768), (33, 64, 512)]
 
 
-@pytest.mark.parametrize("epi", ["4", "8"])
+@pytest.mark.parametrize("epi,order", [("4", "natural"), ("8", "natural"), ("4", "keyfirst"),
+                                       ("8", "keyfirst")])
 @pytest.mark.parametrize("mode", ["pair", "pair-nosplit"])
 @pytest.mark.parametrize("M,E,C", CASES)
-def test_kv_proj_gate_matches_oracle_and_unfused(M, E, C, mode, epi, monkeypatch):
+def test_kv_proj_gate_matches_oracle_and_unfused(M, E, C, mode, epi, order, monkeypatch):
     """The CTA-pair kernel; "pair" splits the last round's tiles into
     128-column halves where that shortens it (every case here but 300 x 4096
-    and 1000 x 512), "pair-nosplit" never does; epi: 4 or 8 epilogue warps
-    (the gate scalars and v are the same bits with either)."""
+    and 1000 x 512), "pair-nosplit" never does; epi: 4 or 8 epilogue warps;
+    order: row blocks in turn, or every key tile before the value tiles. The
+    gate scalars and v are the same bits with every epilogue width and order."""
     monkeypatch.setenv("PLE_KVPROJ_MODE", mode.split("-")[0])
     monkeypatch.setenv("PLE_KVPROJ_SPLIT", "0" if mode.endswith("nosplit") else "1")
     monkeypatch.setenv("PLE_KVPROJ_EPI", "8" if epi == "4" else "4")
+    monkeypatch.setenv("PLE_KVPROJ_ORDER", "keyfirst" if order == "natural" else "natural")
     emb, w, h, gh, gk = (t.cuda() for t in inputs(M, E, C, M + C))
     kv_other, g_other = run_fused(emb, w, h, gh, gk)
     monkeypatch.setenv("PLE_KVPROJ_EPI", epi)
+    monkeypatch.setenv("PLE_KVPROJ_ORDER", order)
     kv, g = run_fused(emb, w, h, gh, gk)
     assert torch.equal(g.view(torch.int32), g_other.view(torch.int32))
     assert torch.equal(kv[:, C:].view(torch.int16), kv_other[:, C:].view(torch.int16))
