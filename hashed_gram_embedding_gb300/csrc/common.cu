@@ -1,5 +1,6 @@
-// Status text, device-property cache, event wait, version.
+// Status text, device-property cache, event wait, version, tensor-map encoder.
 #include "common.cuh"
+#include "tma.cuh"
 
 #include <cstdlib>
 
@@ -39,6 +40,19 @@ int num_sms() {
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (dev >= 0 && dev < kMaxDevices) g_sms[dev] = n;
   return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
 }
 
 int smem_per_sm() {

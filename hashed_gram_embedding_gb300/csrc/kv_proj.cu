@@ -28,9 +28,7 @@
 //     kernel raises PLE_DEVERR_TIMEOUT, stops issuing, waits (bounded) for its
 //     own TMA copies and MMAs in flight, frees TMEM and returns.
 #include "common.cuh"
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "tma.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -58,15 +56,6 @@ constexpr size_t kSmemBytes = size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 25
 // M >> 4 at 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -884,19 +873,6 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                  "r"(TMEM_COLS)
                  : "memory");
   }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
 }
 
 // 2-D K-major bf16 matrix [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.

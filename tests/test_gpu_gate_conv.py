@@ -63,6 +63,12 @@ CONV_CASES = [
     ([0] * 40 + [5] + [0] * 300 + [7, 0, 0, 3], 48, 3, 2),
     # one long request over many token tiles
     ([2000], 72, 4, 3),
+    # several 256-channel slices
+    ([64, 100, 150, 198], 512, 4, 3),
+    # the largest window (W = 63 rows before each tile)
+    ([70, 2, 33], 256, 8, 9),
+    # a ragged last slice (C % 256 = 64) and empty requests
+    ([5, 0, 17, 1, 0, 40], 320, 3, 2),
 ]
 
 
@@ -149,8 +155,9 @@ def test_tiled_and_streaming_conv_same_bits(case, gated, tile, monkeypatch):
             _lib.ple_conv(src.cuda(), dev_qsl(q), w, d, y, conv_state=state, conv_state_out=st)
         torch.cuda.synchronize()
         outs.append((y.view(torch.int16).cpu(), st.view(torch.int16).cpu()))
-    assert torch.equal(outs[0][0], outs[1][0])
-    assert torch.equal(outs[0][1], outs[1][1])
+    for y, st in outs[1:]:
+        assert torch.equal(outs[0][0], y)
+        assert torch.equal(outs[0][1], st)
 
 
 def _gate_conv_inputs(lengths, C, seed):
