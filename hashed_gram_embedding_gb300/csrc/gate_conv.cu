@@ -20,8 +20,10 @@
 //   pass 2 (conv_kernel<GATED=true>): a CTA takes a tile of tokens and a
 //     256-channel slice, stages its dilation window -- u of the tile and of
 //     the (K-1)*d tokens before it -- in shared memory as bf16 (u is a bf16
-//     value; 512 bytes per row), then each lane owns 8 channels (taps in
-//     registers as bf16 pairs, float32 accumulators, mixed-precision FMAs).
+//     value; 512 bytes per row; for large steps one TMA copy of the raw v
+//     rows, then u = bf16(g*v) in place; for small ones per-lane loads),
+//     then each lane owns 8 channels (taps in registers as bf16 pairs,
+//     float32 accumulators, mixed-precision FMAs).
 //     When every token of the tile has all its taps inside its own request,
 //     each warp walks a block of tokens along its dilation chains with the
 //     K window rows of a token in a register ring (a row is read from shared
@@ -31,6 +33,7 @@
 //     request's last token writes the request's new state for its channels.
 // ple_conv is pass 2 on an ungated input; ple_gate is pass 1 plus u = g*v.
 #include "common.cuh"
+#include "tma.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -272,10 +275,15 @@ struct ConvSmem {
   int* req_r;
   int* counts;     // [0] requests listed, [1] requests ending in the tile
   int* end_k;      // [tile] list positions of the requests ending in the tile
+  float* gs;       // [tile + W] gate scalars of the window rows (TMA staging)
+  uint64_t* bar;   // the window copy's mbarrier (TMA staging)
 };
 
+// Window, lists, gate scalars and mbarrier, plus room to align the window
+// to 128 bytes (a TMA destination).
 __host__ __device__ inline size_t conv_smem_bytes(int tile, int W) {
-  return static_cast<size_t>(tile + W) * kConvSlice * 2 + static_cast<size_t>(tile) * 6 * 4 + 16;
+  return static_cast<size_t>(tile + W) * kConvSlice * 2 + static_cast<size_t>(tile) * 6 * 4 + 16 +
+         static_cast<size_t>(tile + W) * 4 + 8 + 128;
 }
 
 __device__ __forceinline__ ConvSmem conv_smem(uint8_t* base, int tile, int W) {
@@ -289,6 +297,9 @@ __device__ __forceinline__ ConvSmem conv_smem(uint8_t* base, int tile, int W) {
   s.req_r = p + 4 * tile;
   s.end_k = p + 5 * tile;
   s.counts = p + 6 * tile;
+  s.gs = reinterpret_cast<float*>(p + 6 * tile + 4);
+  s.bar = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(s.gs + tile + W) + 7) & ~static_cast<uintptr_t>(7));
   return s;
 }
 
@@ -344,13 +355,21 @@ __device__ void find_tile_requests(const int32_t* __restrict__ qsl, int R, int64
   }
 }
 
-// 3 CTAs per SM for K <= 4 (80 registers: 10 staged rows in flight per lane;
-// a 4-CTA cap of 64 registers measured slower), 2 above (the taps and the
-// register ring of K rows grow with K).
-template <bool GATED, int K>
-__global__ void __launch_bounds__(kConvThreads, K <= 4 ? 3 : 2)
-conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int tile_tokens) {
-  extern __shared__ __align__(16) uint8_t smem[];
+// CTAs per SM the register cap allows. Per-lane staging: 3 for K <= 4 (80
+// registers: 10 staged rows in flight per lane; a 4-CTA cap of 64 registers
+// measured slower), 2 above (the taps and the register ring of K rows grow
+// with K). TMA staging holds no rows in registers: 4 for K <= 4 (64
+// registers, no spills; the shared memory of an 88-token tile).
+__host__ __device__ constexpr int conv_ctas_per_sm(int K, bool tma) {
+  return K <= 4 ? (tma ? 4 : 3) : 2;
+}
+template <bool GATED, int K, bool TMA>
+__global__ void __launch_bounds__(kConvThreads, conv_ctas_per_sm(K, TMA))
+conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int tile_tokens,
+            const __grid_constant__ CUtensorMap map_src, int tma_col0) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
   const int dil = a.dil;
   const int W = (K - 1) * dil;
   const int C = a.C;
@@ -367,65 +386,119 @@ conv_kernel(const __grid_constant__ ConvArgs a, const float* __restrict__ g, int
   const ConvSmem s = conv_smem(smem, tile_tokens, W);
   const int64_t src_pitch = GATED ? 2 * static_cast<int64_t>(C) : C;
   const ple_bf16_t* src = a.src + (GATED ? C : 0) + c;
+  constexpr bool use_tma = TMA;
+  const uint32_t bar = smem_u32(s.bar);
+  if (use_tma && tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  if (use_tma) __syncthreads();
   pdl_wait();  // v and g come from the previous kernels
   pdl_trigger();
 
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = tid; i < R + 1; i += kConvThreads) check_qsl(a.qsl, R, T, i, a.dev_err);
 
-  // Window row i <-> token t0 - W + i (rows of tokens before 0 are not
-  // loaded; rows of an earlier request are loaded but never read). Each warp
-  // takes every 8th row, kBatch rows' loads in flight per lane at a time (one
-  // batch covers a 64-token tile and its halo, two a 112-token tile); warp 0
-  // searches the tile's requests while its first batch is in flight.
-  {
-    constexpr int kWarps = kConvThreads / 32;
-    constexpr int kBatch = 10;
-    const int i0 = t0 >= W ? 0 : static_cast<int>(W - t0);
-    const int rows = n_tok + W;
-    uint4 v[kBatch];
-    float gv[kBatch];
-    auto load = [&](int first) {
+  if constexpr (TMA) {
+    // One TMA copy of the window (rows t0 - W .. t0 + tile - 1 of the slice,
+    // 512 bytes each; rows outside [0, T) read as zeros) while the gate
+    // scalars of its rows go to shared memory and warp 0 finds the tile's
+    // requests; then each warp forms u = bf16(g * v) in place for every 8th
+    // row (gated).
+    const int rows = tile_tokens + W;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * kConvSlice * 2);
+      tma_load_2d(smem_u32(s.win), &map_src, bar, tma_col0 + c0, static_cast<int>(t0 - W));
+    }
+    if constexpr (GATED) {
+      for (int i = tid; i < rows; i += kConvThreads) {
+        const int64_t tok = t0 - W + i;
+        s.gs[i] = tok >= 0 && tok < T ? __ldg(g + tok) : 0.f;
+      }
+    }
+    if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
+    if (!__syncthreads_and(mbar_wait(bar, 0, nullptr))) {
+      // not within the wait limit: report, and do not leave with the copy in flight
+      if (tid == 0) {
+        set_dev_err(a.dev_err, PLE_DEVERR_TIMEOUT);
+        mbar_wait(bar, 0, nullptr);
+      }
+      __syncthreads();
+      return;
+    }
+    if constexpr (GATED) {
+      __syncthreads();  // the gate scalars
+      if (active) {
+        for (int i = warp; i < rows; i += kConvThreads / 32) {
+          const float gx = s.gs[i];
+          const uint4 v = s.win[i * 32 + lane];
+          const uint64_t gg = f2(gx, gx);
+          uint32_t u4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int i = first + q * kWarps;
-        v[q] = make_uint4(0, 0, 0, 0);
-        gv[q] = 0.f;
-        if (active && i < rows) {
-          const int64_t tok = t0 - W + i;
-          v[q] = ldg16(src + tok * src_pitch);
-          if constexpr (GATED) gv[q] = __ldg(g + tok);
+          for (int p = 0; p < 4; ++p) {
+            float lo, hi;
+            f2_split(f2_mul(f2(bf_lo(u4[p]), bf_hi(u4[p])), gg), lo, hi);
+            u4[p] = pack2(lo, hi);  // u = bf16(g * v)
+          }
+          s.win[i * 32 + lane] = make_uint4(u4[0], u4[1], u4[2], u4[3]);
         }
       }
-    };
-    auto stage = [&](int first) {
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int i = first + q * kWarps;
-        if (active && i < rows) {
-          if constexpr (GATED) {
-            const uint64_t gg = f2(gv[q], gv[q]);
-            uint32_t u4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              float lo, hi;
-              f2_split(f2_mul(f2(bf_lo(u4[p]), bf_hi(u4[p])), gg), lo, hi);
-              u4[p] = pack2(lo, hi);  // u = bf16(g * v)
-            }
-            s.win[i * 32 + lane] = make_uint4(u4[0], u4[1], u4[2], u4[3]);
-          } else {
-            s.win[i * 32 + lane] = v[q];
+    }
+  } else {
+    // Window row i <-> token t0 - W + i (rows of tokens before 0 are not
+    // loaded; rows of an earlier request are loaded but never read). Each warp
+    // takes every 8th row, kBatch rows' loads in flight per lane at a time (one
+    // batch covers a 64-token tile and its halo, two a 112-token tile); warp 0
+    // searches the tile's requests while its first batch is in flight.
+    {
+      constexpr int kWarps = kConvThreads / 32;
+      constexpr int kBatch = 10;
+      const int i0 = t0 >= W ? 0 : static_cast<int>(W - t0);
+      const int rows = n_tok + W;
+      uint4 v[kBatch];
+      float gv[kBatch];
+      auto load = [&](int first) {
+  #pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = first + q * kWarps;
+          v[q] = make_uint4(0, 0, 0, 0);
+          gv[q] = 0.f;
+          if (active && i < rows) {
+            const int64_t tok = t0 - W + i;
+            v[q] = ldg16(src + tok * src_pitch);
+            if constexpr (GATED) gv[q] = __ldg(g + tok);
           }
         }
-      }
-    };
-    int first = i0 + warp;
-    load(first);
-    if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
-    stage(first);
-    for (first += kWarps * kBatch; first < rows; first += kWarps * kBatch) {
+      };
+      auto stage = [&](int first) {
+  #pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = first + q * kWarps;
+          if (active && i < rows) {
+            if constexpr (GATED) {
+              const uint64_t gg = f2(gv[q], gv[q]);
+              uint32_t u4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+  #pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                float lo, hi;
+                f2_split(f2_mul(f2(bf_lo(u4[p]), bf_hi(u4[p])), gg), lo, hi);
+                u4[p] = pack2(lo, hi);  // u = bf16(g * v)
+              }
+              s.win[i * 32 + lane] = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+            } else {
+              s.win[i * 32 + lane] = v[q];
+            }
+          }
+        }
+      };
+      int first = i0 + warp;
       load(first);
+      if (warp == 0) find_tile_requests(a.qsl, R, T, t0, n_tok, tile_tokens, s, lane);
       stage(first);
+      for (first += kWarps * kBatch; first < rows; first += kWarps * kBatch) {
+        load(first);
+        stage(first);
+      }
     }
   }
   __syncthreads();
@@ -899,42 +972,65 @@ ple_status validate_conv(const int32_t* qsl, int32_t num_reqs, int64_t T, int32_
   return PLE_OK;
 }
 
-// Tokens per conv tile. A step small enough that a tile of 16..112 tokens
-// puts every CTA on the GPU at once takes the smallest such tile: one wave
-// (at 256 x 4 decode, 37-token tiles in 448 CTAs run the conv in 18.3 us
-// against 22.7 us for 16-token tiles in 1024 CTAs, measured). Otherwise 112
-// tokens when that still gives ~4 CTAs per SM (each CTA's fixed cost --
-// request search, one load round trip, two barriers -- spread over more
-// tokens: 30.9 us at 8k prefill against 32.3 us for 64 and 33.6 us for 128,
-// measured); else 64, halved until ~4 CTAs per SM. PLE_CONV_TILE overrides
-// (launch-shape sweeps).
-int conv_tile_tokens(int64_t T, int C, int K, int W) {
+// Tile of the tiled conv and how its window is staged. A step small enough
+// that a tile of 16..112 tokens puts every CTA on the GPU at once takes the
+// smallest such tile (one wave: at 256 x 4 decode, 37-token tiles in 448
+// CTAs run the conv in 18.3 us against 22.7 us for 16-token tiles in 1024
+// CTAs) with per-lane staging (12.5 us against 12.8 us with the TMA copy).
+// Otherwise, where the window is one TMA box inside the source tensor, the
+// TMA copy with 88-token tiles at 4 CTAs per SM (88.6 us at 32k tokens and
+// 28.7 us at 8k against 101.8 and 30.1 us for per-lane staging with
+// 112-token tiles at 3 per SM; 112-token TMA tiles at 3 per SM 89.8 and
+// 29.5 us); else per-lane staging with 112 tokens when that still gives ~4
+// CTAs per SM (each CTA's fixed cost -- request search, one load round
+// trip, two barriers -- spread over more tokens: 30.9 us at 8k prefill
+// against 32.3 us for 64 and 33.6 us for 128), else 64, halved until ~4 CTAs
+// per SM. Measured on a GB300. PLE_CONV_TILE overrides the tile and
+// PLE_CONV_TMA = 0 | 1 the staging (launch-shape sweeps and tests).
+struct ConvTile {
+  int tile;
+  bool tma;
+};
+
+ConvTile conv_tile(int64_t T, int C, int K, int W, int64_t src_cols) {
   const int64_t slices = (C + kConvSlice - 1) / kConvSlice;
   const int64_t want = 4 * static_cast<int64_t>(num_sms());
   auto ctas = [&](int tile) { return ((T + tile - 1) / tile) * slices; };
-  // CTAs per SM: the register cap of the kernel (3 for K <= 4, else 2), or
-  // fewer when the shared memory of a 112-token tile does not fit
+  auto tma_fits = [&](int tile) {
+    return src_cols >= kConvSlice && T >= tile + W && tile + W <= 256;
+  };
+  // CTAs per SM of per-lane staging: the register cap of the kernel (3 for
+  // K <= 4, else 2), or fewer when the shared memory of a 112-token tile
+  // does not fit
   const int64_t by_smem = static_cast<int64_t>(smem_per_sm()) /
                           static_cast<int64_t>(conv_smem_bytes(112, W) + 1024);
   const int64_t per_sm = by_smem < (K <= 4 ? 3 : 2) ? by_smem : (K <= 4 ? 3 : 2);
   const int64_t per_slice = per_sm * num_sms() / slices;  // tiles of one slice in one wave
-  int tile = 0;
+  ConvTile t{0, false};
   if (per_slice >= 1) {
     const int64_t one_wave = (T + per_slice - 1) / per_slice;
-    if (one_wave >= 16 && one_wave <= 112) tile = static_cast<int>(one_wave);
+    if (one_wave >= 16 && one_wave <= 112) t.tile = static_cast<int>(one_wave);
   }
-  if (tile == 0) {
-    tile = 112;
-    if (ctas(tile) < want) {
-      tile = 64;
-      while (tile > 8 && ctas(tile) < want) tile >>= 1;
+  if (t.tile == 0) {
+    if (K <= 4 && tma_fits(88)) {
+      t = {88, true};
+    } else if (tma_fits(112)) {
+      t = {112, true};
+    } else {
+      t.tile = 112;
+      if (ctas(t.tile) < want) {
+        t.tile = 64;
+        while (t.tile > 8 && ctas(t.tile) < want) t.tile >>= 1;
+      }
     }
   }
   if (const char* e = getenv("PLE_CONV_TILE")) {
     const int v = atoi(e);
-    if (v >= 1 && v <= 128) tile = v;
+    if (v >= 1 && v <= 128) t.tile = v;
   }
-  return tile;
+  if (const char* e = getenv("PLE_CONV_TMA")) t.tma = atoi(e) != 0;
+  if (t.tma && !tma_fits(t.tile)) t.tma = false;
+  return t;
 }
 
 template <bool GATED>
@@ -946,25 +1042,20 @@ ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, c
   // sweeps and tests: both give the same bits).
   const char* mode = getenv("PLE_CONV_MODE");
   const bool tiled = !(mode != nullptr && strcmp(mode, "stream") == 0);
-  void (*kernel)(ConvArgs, const float*, int) = nullptr;
-  switch (a.K) {
-    case 1: kernel = tiled ? conv_kernel<GATED, 1> : conv_stream_kernel<GATED, 1>; break;
-    case 2: kernel = tiled ? conv_kernel<GATED, 2> : conv_stream_kernel<GATED, 2>; break;
-    case 3: kernel = tiled ? conv_kernel<GATED, 3> : conv_stream_kernel<GATED, 3>; break;
-    case 4: kernel = tiled ? conv_kernel<GATED, 4> : conv_stream_kernel<GATED, 4>; break;
-    case 5: kernel = tiled ? conv_kernel<GATED, 5> : conv_stream_kernel<GATED, 5>; break;
-    case 6: kernel = tiled ? conv_kernel<GATED, 6> : conv_stream_kernel<GATED, 6>; break;
-    case 7: kernel = tiled ? conv_kernel<GATED, 7> : conv_stream_kernel<GATED, 7>; break;
-    default: kernel = tiled ? conv_kernel<GATED, 8> : conv_stream_kernel<GATED, 8>; break;
-  }
   int param = 0;
   size_t smem = 0;
   dim3 grid;
+  // The tiled kernel's window is one TMA copy (conv_tile: where the box of
+  // 256 columns x tile + W rows lies inside the source tensor, kv's value
+  // half for the gated pass, x otherwise) or per-lane loads.
+  bool use_tma = false;
+  const int64_t cols = GATED ? 2 * static_cast<int64_t>(a.C) : a.C;
   if (tiled) {
-    const int tile = conv_tile_tokens(a.T, a.C, a.K, W);
-    param = tile;
-    smem = conv_smem_bytes(tile, W);
-    grid = dim3(static_cast<unsigned>((a.T + tile - 1) / tile), static_cast<unsigned>(slices));
+    const ConvTile ct = conv_tile(a.T, a.C, a.K, W, cols);
+    param = ct.tile;
+    use_tma = ct.tma;
+    smem = conv_smem_bytes(ct.tile, W);
+    grid = dim3(static_cast<unsigned>((a.T + ct.tile - 1) / ct.tile), static_cast<unsigned>(slices));
   } else {
     const int CH = conv_stream_chunk(W);
     param = CH;
@@ -980,10 +1071,57 @@ ple_status launch_conv(const ConvArgs& a, const float* g, cudaStream_t stream, c
     }
     grid = dim3(static_cast<unsigned>(ranges), static_cast<unsigned>(slices));
   }
+  using TiledFn = void (*)(ConvArgs, const float*, int, CUtensorMap, int);
+  using StreamFn = void (*)(ConvArgs, const float*, int);
+  TiledFn tiled_fn = nullptr;
+  StreamFn stream_fn = nullptr;
+#define PLE_CONV_CASE(KK)                                                                    \
+  case KK:                                                                                   \
+    tiled_fn = use_tma ? conv_kernel<GATED, KK, true> : conv_kernel<GATED, KK, false>;      \
+    stream_fn = conv_stream_kernel<GATED, KK>;                                               \
+    break;
+  switch (a.K) {
+    PLE_CONV_CASE(1)
+    PLE_CONV_CASE(2)
+    PLE_CONV_CASE(3)
+    PLE_CONV_CASE(4)
+    PLE_CONV_CASE(5)
+    PLE_CONV_CASE(6)
+    PLE_CONV_CASE(7)
+    default:
+    PLE_CONV_CASE(8)
+  }
+#undef PLE_CONV_CASE
+  const void* kernel = tiled ? reinterpret_cast<const void*>(tiled_fn)
+                             : reinterpret_cast<const void*>(stream_fn);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return check_cuda(err, name);
-  err = launch_kernel(kernel, grid, dim3(kConvThreads), smem, stream, 1, a, g, param);
+  if (tiled) {
+    CUtensorMap map{};
+    int tma_col0 = -1;
+    if (use_tma) {
+      const int rows = param + W;
+      auto encode = tensor_map_encoder();
+      if (encode == nullptr) return fail(PLE_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", name);
+      cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(a.T)};
+      cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+      cuuint32_t box[2] = {static_cast<cuuint32_t>(kConvSlice), static_cast<cuuint32_t>(rows)};
+      cuuint32_t elem_strides[2] = {1, 1};
+      CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<ple_bf16_t*>(a.src), dims, strides, box, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS)
+        return fail(PLE_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", name,
+                    static_cast<int>(r));
+      tma_col0 = GATED ? a.C : 0;
+    }
+    err = launch_kernel(tiled_fn, grid, dim3(kConvThreads), smem, stream, 1, a, g, param, map,
+                        tma_col0);
+  } else {
+    err = launch_kernel(stream_fn, grid, dim3(kConvThreads), smem, stream, 1, a, g, param);
+  }
   if (err != cudaSuccess) return check_cuda(err, name);
   return check_cuda(cudaGetLastError(), name);
 }

@@ -73,9 +73,12 @@ CONV_CASES = [
 
 
 # conv pass variants: the one-shot tiled kernel (default tile, the 112-token
-# tile of large steps, an odd 5-token tile) and the streaming kernel (default
-# launch shape, one token range per slice, seven ranges)
+# tile of large steps, an odd 5-token tile; the window staged as the default
+# chooses, by per-lane loads, and by one TMA copy wherever that fits the
+# source tensor) and the streaming kernel (default launch shape, one token
+# range per slice, seven ranges)
 CONV_MODES = {"tile": {}, "tile-112": {"PLE_CONV_TILE": "112"}, "tile-5": {"PLE_CONV_TILE": "5"},
+              "tile-noTMA": {"PLE_CONV_TMA": "0"}, "tile-TMA": {"PLE_CONV_TMA": "1"},
               "stream": {"PLE_CONV_MODE": "stream"},
               "stream-1range": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "1"},
               "stream-7ranges": {"PLE_CONV_MODE": "stream", "PLE_CONV_RANGES": "7"}}
@@ -129,10 +132,11 @@ def test_conv_padding_tokens_join_last_request():
 @pytest.mark.parametrize("gated", [False, True])
 @pytest.mark.parametrize("case", CONV_CASES, ids=lambda c: f"{len(c[0])}req-C{c[1]}-K{c[2]}-d{c[3]}")
 def test_tiled_and_streaming_conv_same_bits(case, gated, tile, monkeypatch):
-    """The tiled kernel (taps and window as bf16 pairs, mixed-precision FMA)
-    and the streaming kernel (float32 ring, two-wide float32 FMA) take the
-    same taps in the same order with one rounding per tap: y and the
-    carry-over state agree bit for bit."""
+    """The tiled kernel (taps and window as bf16 pairs, mixed-precision FMA;
+    window staged by TMA where it fits, and by per-lane loads) and the
+    streaming kernel (float32 ring, two-wide float32 FMA) take the same taps
+    in the same order with one rounding per tap: y and the carry-over state
+    agree bit for bit."""
     lengths, C, K, d = case
     q = qsl_of(lengths)
     T, R, W = int(q[-1]), len(lengths), (K - 1) * d
@@ -141,7 +145,9 @@ def test_tiled_and_streaming_conv_same_bits(case, gated, tile, monkeypatch):
     state = rand_bf16((R, W, C), 0.3, 11).cuda()
     g = torch.rand((T,), generator=torch.Generator().manual_seed(5)).cuda() if gated else None
     outs = []
-    for env in ({} if tile is None else {"PLE_CONV_TILE": tile}, {"PLE_CONV_MODE": "stream"}):
+    tile_env = {} if tile is None else {"PLE_CONV_TILE": tile}
+    for env in (tile_env, {**tile_env, "PLE_CONV_TMA": "0"}, {**tile_env, "PLE_CONV_TMA": "1"},
+                {"PLE_CONV_MODE": "stream"}):
         monkeypatch.delenv("PLE_CONV_MODE", raising=False)
         monkeypatch.delenv("PLE_CONV_TILE", raising=False)
         for k, v in env.items():
