@@ -332,13 +332,13 @@ template <int EW>
 constexpr int pair_threads() { return 64 + 32 * EW; }
 constexpr int kFewRounds = 4;  // at most this many tiles per CTA pair: 8 epilogue warps
 constexpr size_t kKeyFirstMaxA = size_t(64) << 20;  // bytes of A for the key-first order
-// kind::f16 instruction descriptors for M = 256 (two SMs) x N = 256, and
-// x N = 128 (the half tiles of the last round).
-constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) |
-                                (uint32_t(BN >> 3) << 17) | (uint32_t((2 * BM) >> 4) << 24);
-constexpr uint32_t kIdescPairHalf = (1u << 4) | (1u << 7) | (1u << 10) |
-                                    (uint32_t((BN / 2) >> 3) << 17) |
-                                    (uint32_t((2 * BM) >> 4) << 24);
+// kind::f16 instruction descriptor for M = 256 (two SMs) x N = cols (a
+// multiple of 16 up to 256: the full, half and value-strip tiles): D f32, A
+// and B bf16, both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_pair(int cols) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(cols >> 3) << 17) |
+         (uint32_t((2 * BM) >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -584,15 +584,29 @@ __device__ __forceinline__ void gate_block(const GateEpi& ge, uint32_t taddr, in
   gate_publish(ge, m, M, lane, n_base / kGateBlock, 1, part, part);
 }
 
-// A work unit of the pair kernel: 256 rows from m_base, 256 columns from
-// n_base, or -- units >= full_units -- one 128-column half of a 256 x 256
-// tile. Splitting the last round's tiles
-// in halves lets twice as many CTA pairs share it when it would otherwise
-// leave more than half of them idle.
+// A work unit of the pair kernel: 256 rows from m_base, `cols` columns from
+// n_base. Default schedule: 256 x 256 tiles, and -- units >= full_units --
+// 128-column halves of the last round's tiles (they let twice as many CTA
+// pairs share that round when it would otherwise leave more than half of
+// them idle). Strip schedule (vn > 0, the fused gate with key tiles first):
+// the value half in strips of vn columns, the narrower strips left over at
+// the end of each row block's value half (rem columns) first, then every key
+// tile, then the vn-column strips: with units dealt to the pairs in turn, the
+// host picks vn so that no pair gets much more than its share of columns
+// (1024 x 2048 -> 8192 on 74 pairs: at most 1.75 tiles' columns per pair
+// with vn = 192, against 2 tiles with 256-column tiles).
 struct PairUnit {
   int m_base;
   int n_base;
-  int cols;  // 256 or 128
+  int cols;  // 256, 128, vn or rem
+};
+
+struct PairSched {
+  int full_units;  // default schedule: units past it are half tiles
+  int key_groups;  // > 0: key tiles first (C / 256 key groups)
+  int vn;          // > 0: strip schedule
+  int rem;         // strip schedule: columns left over per row block (0: none)
+  int num_units;
 };
 
 // Tile v of the launch's tile order -> its 256-row block mb and 256-column
@@ -620,9 +634,35 @@ __device__ __forceinline__ void tile_of(int v, int n_groups, int key_groups, int
   }
 }
 
-__device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_groups, int key_groups,
+__device__ __forceinline__ PairUnit pair_unit(int u, const PairSched& sc, int n_groups,
                                               int m_tiles) {
   PairUnit t;
+  if (sc.vn > 0) {
+    const int C = sc.key_groups * BN;
+    const int strips = (C - sc.rem) / sc.vn;  // full strips per row block
+    const int n_rem = sc.rem > 0 ? m_tiles : 0;
+    const int n_key = m_tiles * sc.key_groups;
+    int mb;
+    if (u < n_rem) {
+      mb = u;
+      t.n_base = C + strips * sc.vn;
+      t.cols = sc.rem;
+    } else if (u - n_rem < n_key) {
+      const int v = u - n_rem;
+      mb = v / sc.key_groups;
+      t.n_base = (v % sc.key_groups) * BN;
+      t.cols = BN;
+    } else {
+      const int v = u - n_rem - n_key;
+      mb = v / strips;
+      t.n_base = C + (v % strips) * sc.vn;
+      t.cols = sc.vn;
+    }
+    t.m_base = mb * 2 * BM;
+    return t;
+  }
+  const int full_units = sc.full_units;
+  const int key_groups = sc.key_groups;
   const int h = u - full_units;
   const int v = u >= full_units ? full_units + (h >> 1) : u;
   int mb, g;
@@ -638,17 +678,20 @@ __device__ __forceinline__ PairUnit pair_unit(int u, int full_units, int n_group
   return t;
 }
 
-// One CTA pair per cluster. Units [0, full_units) are full tiles; the units
-// past them are half tiles (2 per remaining tile; map_b_half loads 64 W rows
-// per CTA). Tiles follow tile_of's order (key_groups > 0: key tiles first).
+// One CTA pair per cluster, dealt units cl, cl + clusters, ... of the
+// schedule (pair_unit). A unit of `cols` columns loads cols / 2 W rows per
+// CTA: map_b (128 rows), map_b_half (64), map_b_v (vn / 2) or map_b_r
+// (rem / 2).
 // Warps: 0 the TMA producer, 1 the MMA issuer (tensor memory owner), 2 .. 1 +
 // EW the epilogue.
 template <bool GATE, int EW>
 __global__ void __launch_bounds__(pair_threads<EW>(), 1)
 kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b,
-                    const __grid_constant__ CUtensorMap map_b_half, ple_bf16_t* __restrict__ out,
-                    int M, int N, int K, int full_units, int key_groups, int32_t* dev_err,
+                    const __grid_constant__ CUtensorMap map_b_half,
+                    const __grid_constant__ CUtensorMap map_b_v,
+                    const __grid_constant__ CUtensorMap map_b_r, ple_bf16_t* __restrict__ out,
+                    int M, int N, int K, const PairSched sc, int32_t* dev_err,
                     const __grid_constant__ GateEpi ge) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -674,8 +717,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   const int n_tiles = (N + BN - 1) / BN;
   const int n_groups = n_tiles;
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
-  const int base_units = m_tiles * n_groups;  // (256 rows, 256 columns) per cluster
-  const int num_units = full_units + 2 * (base_units - full_units);
+  const int num_units = sc.num_units;
   const int num_kb = (K + BK * P_ATOMS - 1) / (BK * P_ATOMS);
   constexpr uint16_t pair_mask = 3u;  // both CTAs of the pair
 
@@ -712,21 +754,30 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     // ---------------- TMA producer (both CTAs) ----------------
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
-    if (num_units > base_units)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_half))
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_half))
+                 : "memory");
+    if (sc.vn > 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_v))
                    : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_r))
+                   : "memory");
+    }
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
     const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
     for (int u = cl; ok && u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit(u, full_units, n_groups, key_groups, m_tiles);
-      const bool half = t.cols != BN;
+      const PairUnit t = pair_unit(u, sc, n_groups, m_tiles);
+      const CUtensorMap* wmap = t.cols == BN       ? &map_b
+                                : t.cols == sc.vn  ? &map_b_v
+                                : t.cols == BN / 2 ? &map_b_half
+                                                   : &map_b_r;
       const int m0 = t.m_base + q * BM;
       const int n0 = t.n_base + q * (t.cols / 2);
       // both CTAs' A rows and W rows of one stage
-      const uint32_t stage_tx = 2u * (P_A_STAGE + (half ? P_B_STAGE / 2 : P_B_STAGE));
+      const uint32_t stage_tx =
+          2u * (P_A_STAGE + static_cast<uint32_t>(P_B_STAGE / BN) * static_cast<uint32_t>(t.cols));
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t leader_full = map_to_rank(full_bar(stage), leader);
@@ -739,8 +790,8 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
           const int kx = (kb * P_ATOMS + at) * BK;
           tma_load_2d_pair(smem_u32(a_smem + stage * P_A_STAGE + at * P_A_ATOM), &map_a,
                            leader_full, kx, m0);
-          tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE + at * P_B_ATOM),
-                           half ? &map_b_half : &map_b, leader_full, kx, n0);
+          tma_load_2d_pair(smem_u32(b_smem + stage * P_B_STAGE + at * P_B_ATOM), wmap,
+                           leader_full, kx, n0);
         }
         if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -758,8 +809,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = cl; ok && u < num_units; u += num_cl) {
-        const uint32_t idesc =
-            pair_unit(u, full_units, n_groups, key_groups, m_tiles).cols == BN ? kIdescPair : kIdescPairHalf;
+        const uint32_t idesc = idesc_pair(pair_unit(u, sc, n_groups, m_tiles).cols);
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -801,7 +851,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cl; u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit(u, full_units, n_groups, key_groups, m_tiles);
+      const PairUnit t = pair_unit(u, sc, n_groups, m_tiles);
       const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
       // 8 warps: a key block's h and gammas are loaded before its MMAs end
       const bool key_block8 =
@@ -930,7 +980,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   }
   if (ge != nullptr) paired = true;
   const int cluster = paired ? 2 : 1;
-  CUtensorMap map_a, map_b, map_b_half;
+  CUtensorMap map_a, map_b, map_b_half, map_b_v, map_b_r;
   ple_status s = make_map(&map_a, emb, M, K, BM);  // A rows a CTA loads
   if (s != PLE_OK) return s;
   s = make_map(&map_b, w, N, K, paired ? BN / 2 : BN);  // W rows one CTA loads per stage
@@ -941,8 +991,8 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   } else {
     map_b_half = map_b;  // not read
   }
-  using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int,
-                          int, int32_t*, GateEpi);
+  using PairFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                          ple_bf16_t*, int, int, int, PairSched, int32_t*, GateEpi);
   // the 4-warp instantiation sizes the grid (the occupancy of both is one CTA per SM)
   using TileFn = void (*)(CUtensorMap, CUtensorMap, ple_bf16_t*, int, int, int, int32_t*);
   PairFn pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 4> : kv_proj_pair_kernel<false, 4>;
@@ -1012,6 +1062,61 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
     else if (strcmp(e, "keyfirst") == 0) key_first = ge != nullptr;
   }
   const int key_groups = key_first ? ge->C / BN : 0;
+  PairSched sc{full_units, key_groups, 0, 0, units};
+  map_b_v = map_b_r = map_b;  // not read by the default schedule
+  if (paired && key_groups > 0 && few) {
+    // Strip schedule: value strips of vn columns when, with units dealt to
+    // the pairs in turn, the busiest pair then gets fewer columns (plus a
+    // per-unit cost) than with the default schedule. PLE_KVPROJ_VN = 0
+    // keeps the default; 128 or 192 forces that strip width.
+    const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
+    const int C = ge->C;
+    constexpr int64_t kUnitCost = 32;  // columns' worth of a unit's fixed cost
+    auto busiest = [&](int n_units, auto cols_of) {
+      const int P = n_units < max_clusters ? n_units : max_clusters;
+      int64_t load[512] = {};
+      if (P > 512) return int64_t(1) << 62;
+      for (int u = 0; u < n_units; ++u) load[u % P] += cols_of(u) + kUnitCost;
+      int64_t mx = 0;
+      for (int p = 0; p < P; ++p) mx = load[p] > mx ? load[p] : mx;
+      return mx;
+    };
+    auto strip_units = [&](int vn) {
+      const int rem = C % vn;
+      return (rem > 0 ? m_tiles : 0) + m_tiles * key_groups + m_tiles * ((C - rem) / vn);
+    };
+    auto strip_cols = [&](int vn) {
+      const int rem = C % vn;
+      const int n_rem = rem > 0 ? m_tiles : 0;
+      const int n_key = m_tiles * key_groups;
+      return [=](int u) { return u < n_rem ? rem : u < n_rem + n_key ? BN : vn; };
+    };
+    int64_t best = busiest(units, [&](int u) { return u < full_units ? BN : BN / 2; });
+    int vn = 0;
+    int forced = -1;
+    if (const char* e = getenv("PLE_KVPROJ_VN")) forced = atoi(e);
+    for (int cand : {192, 128}) {
+      if (forced >= 0 && forced != cand) continue;
+      const int64_t b = busiest(strip_units(cand), strip_cols(cand));
+      if (forced == cand || b < best) {
+        best = b;
+        vn = cand;
+      }
+    }
+    if (vn > 0) {
+      sc.vn = vn;
+      sc.rem = C % vn;
+      sc.num_units = strip_units(vn);
+      s = make_map(&map_b_v, w, N, K, vn / 2);  // a strip's W rows per CTA
+      if (s != PLE_OK) return s;
+      if (sc.rem > 0) {
+        s = make_map(&map_b_r, w, N, K, sc.rem / 2);
+        if (s != PLE_OK) return s;
+      }
+    }
+  }
+  const int launch_clusters = sc.num_units < max_clusters ? sc.num_units : max_clusters;
+  const dim3 launch_grid(static_cast<unsigned>(launch_clusters * cluster));
   if (paired && epi_warps == 8) {
     pair_fn = ge != nullptr ? kv_proj_pair_kernel<true, 8> : kv_proj_pair_kernel<false, 8>;
     err = cudaFuncSetAttribute(pair_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1019,10 +1124,10 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
     if (err != cudaSuccess) return check_cuda(err, "kv projection: smem attribute");
   }
   if (paired)
-    err = launch_kernel(pair_fn, grid, dim3(epi_warps == 8 ? pair_threads<8>() : pair_threads<4>()),
-                        smem, stream, static_cast<unsigned>(cluster),
-                        map_a, map_b, map_b_half, kv, M, N, K, full_units, key_groups, dev_err,
-                        ge != nullptr ? *ge : GateEpi{});
+    err = launch_kernel(pair_fn, launch_grid,
+                        dim3(epi_warps == 8 ? pair_threads<8>() : pair_threads<4>()), smem, stream,
+                        static_cast<unsigned>(cluster), map_a, map_b, map_b_half, map_b_v, map_b_r,
+                        kv, M, N, K, sc, dev_err, ge != nullptr ? *ge : GateEpi{});
   else
     err = launch_kernel(tile_fn, grid, dim3(kThreads), smem, stream, static_cast<unsigned>(cluster),
                         map_a, map_b, kv, M, N, K, dev_err);

@@ -114,6 +114,25 @@ def test_kv_proj_gate_matches_oracle_and_unfused(M, E, C, mode, epi, order, monk
     assert np.max(np.abs(gg - ref_g)) < 5e-4
 
 
+@pytest.mark.parametrize("vn", ["192", "128"])
+@pytest.mark.parametrize("M,E,C", CASES + [(1024, 256, 4096), (2000, 64, 1024)])
+def test_kv_proj_gate_strip_schedule_same_bits(M, E, C, vn, monkeypatch):
+    """The strip schedule (value half in vn-column strips, the narrower
+    remainder strips first, then the key tiles) gives the default schedule's
+    v and gate scalars bit for bit, and the oracle's within tolerance."""
+    monkeypatch.setenv("PLE_KVPROJ_ORDER", "keyfirst")
+    monkeypatch.setenv("PLE_KVPROJ_VN", "0")
+    emb, w, h, gh, gk = (t.cuda() for t in inputs(M, E, C, M + 3 * C))
+    kv_ref, g_ref = run_fused(emb, w, h, gh, gk)
+    monkeypatch.setenv("PLE_KVPROJ_VN", vn)
+    kv, g = run_fused(emb, w, h, gh, gk)
+    assert torch.equal(g.view(torch.int32), g_ref.view(torch.int32))
+    assert torch.equal(kv[:, C:].view(torch.int16), kv_ref[:, C:].view(torch.int16))
+    assert torch.isnan(kv[:, :C].float()).all()
+    ref_kv = oracle_kv_proj(bits(emb), bits(w))
+    assert_close(bits(kv[:, C:]), ref_kv[:, C:], what=f"v strips {vn} {M}x{E}x{2 * C}")
+
+
 def test_kv_proj_gate_is_deterministic_with_a_reused_workspace():
     M, E, C = 700, 256, 512
     emb, w, h, gh, gk = (t.cuda() for t in inputs(M, E, C, 5))
