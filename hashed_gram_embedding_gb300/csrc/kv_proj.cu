@@ -634,10 +634,13 @@ __device__ __forceinline__ void tile_of(int v, int n_groups, int key_groups, int
   }
 }
 
+// STRIPS: the kernel can run the strip schedule (the 8-warp kernels only:
+// the host uses it for launches of few tiles per pair).
+template <bool STRIPS>
 __device__ __forceinline__ PairUnit pair_unit(int u, const PairSched& sc, int n_groups,
                                               int m_tiles) {
   PairUnit t;
-  if (sc.vn > 0) {
+  if (STRIPS && sc.vn > 0) {
     const int C = sc.key_groups * BN;
     const int strips = (C - sc.rem) / sc.vn;  // full strips per row block
     const int n_rem = sc.rem > 0 ? m_tiles : 0;
@@ -718,6 +721,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
   const int n_groups = n_tiles;
   const int m_tiles = (M + 2 * BM - 1) / (2 * BM);
   const int num_units = sc.num_units;
+  constexpr bool kStrips = EW == 8;
   const int num_kb = (K + BK * P_ATOMS - 1) / (BK * P_ATOMS);
   constexpr uint16_t pair_mask = 3u;  // both CTAs of the pair
 
@@ -756,7 +760,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_half))
                  : "memory");
-    if (sc.vn > 0) {
+    if (kStrips && sc.vn > 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_v))
                    : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b_r))
@@ -768,16 +772,18 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     bool ok = true;
     const int q = static_cast<int>(rank & 1u);  // half of the pair's rows / W tile
     for (int u = cl; ok && u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit(u, sc, n_groups, m_tiles);
-      const CUtensorMap* wmap = t.cols == BN       ? &map_b
-                                : t.cols == sc.vn  ? &map_b_v
-                                : t.cols == BN / 2 ? &map_b_half
-                                                   : &map_b_r;
+      const PairUnit t = pair_unit<kStrips>(u, sc, n_groups, m_tiles);
+      const CUtensorMap* wmap = t.cols == BN                   ? &map_b
+                                : kStrips && t.cols == sc.vn ? &map_b_v
+                                : t.cols == BN / 2           ? &map_b_half
+                                                             : &map_b_r;
       const int m0 = t.m_base + q * BM;
       const int n0 = t.n_base + q * (t.cols / 2);
       // both CTAs' A rows and W rows of one stage
       const uint32_t stage_tx =
-          2u * (P_A_STAGE + static_cast<uint32_t>(P_B_STAGE / BN) * static_cast<uint32_t>(t.cols));
+          kStrips ? 2u * (P_A_STAGE + static_cast<uint32_t>(P_B_STAGE / BN) *
+                                          static_cast<uint32_t>(t.cols))
+                  : 2u * (P_A_STAGE + (t.cols != BN ? P_B_STAGE / 2 : P_B_STAGE));
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t leader_full = map_to_rank(full_bar(stage), leader);
@@ -809,7 +815,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = cl; ok && u < num_units; u += num_cl) {
-        const uint32_t idesc = idesc_pair(pair_unit(u, sc, n_groups, m_tiles).cols);
+        const uint32_t idesc = idesc_pair(pair_unit<kStrips>(u, sc, n_groups, m_tiles).cols);
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
@@ -851,7 +857,7 @@ kv_proj_pair_kernel(const __grid_constant__ CUtensorMap map_a,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cl; u < num_units; u += num_cl) {
-      const PairUnit t = pair_unit(u, sc, n_groups, m_tiles);
+      const PairUnit t = pair_unit<kStrips>(u, sc, n_groups, m_tiles);
       const int m = t.m_base + static_cast<int>(rank & 1u) * BM + row_in_tile;
       // 8 warps: a key block's h and gammas are loaded before its MMAs end
       const bool key_block8 =
@@ -1064,7 +1070,7 @@ ple_status launch_kv(const ple_bf16_t* emb, const ple_bf16_t* w, int M, int K, i
   const int key_groups = key_first ? ge->C / BN : 0;
   PairSched sc{full_units, key_groups, 0, 0, units};
   map_b_v = map_b_r = map_b;  // not read by the default schedule
-  if (paired && key_groups > 0 && few) {
+  if (paired && key_groups > 0 && few && epi_warps == 8) {
     // Strip schedule: value strips of vn columns when, with units dealt to
     // the pairs in turn, the busiest pair then gets fewer columns (plus a
     // per-unit cost) than with the default schedule. PLE_KVPROJ_VN = 0
