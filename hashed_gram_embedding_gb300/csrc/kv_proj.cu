@@ -300,7 +300,8 @@ kv_proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
 // ---------------------------------------------------------------------------
 // CTA-pair kernel: tcgen05.mma.cta_group::2, M = 256 (128 rows per SM) x
-// N = 256. Each CTA of a cluster pair stages its own 128 rows of A and its own
+// N = 256 (128, 192 or 64 for the narrower units of pair_unit's schedules).
+// Each CTA of a cluster pair stages its own 128 rows of A and its own
 // half (128 rows) of the W tile; the pair's tensor cores read both halves of
 // W, so each SM reads 32 KB of operands from shared memory per K step of 64
 // instead of 48 KB. The even CTA (leader) issues the MMAs; TMA copies of both CTAs
@@ -322,7 +323,7 @@ constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
 constexpr size_t kPairSmemBytes = size_t(P_STAGES) * P_STAGE_BYTES + 1024 + 256;
 // Epilogue warps: 4 (one per TMEM lane quadrant, each draining all columns
-// of a tile) or 8 (two per quadrant, each draining one 128-column half).
+// of a unit) or 8 (two per quadrant, each draining one half of them).
 // With few tiles per CTA the last tile's epilogue, which nothing hides, is a
 // large share of the launch and 8 warps halve it (29.5 against 30.7 us for
 // 1024 x 2048 -> 8192 with the fused gate on a GB300); with many tiles the
