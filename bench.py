@@ -186,10 +186,11 @@ def source_hash(path):
     return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload):
-    """dram bytes per launch from the committed ncu summary of ``kernel`` on
-    ``workload``, or None when the summary is missing or the kernel source
-    changed since."""
+def ncu_traffic(kernel, workload, field="dram_bytes_per_launch"):
+    """bytes per launch (``field``: DRAM bytes, or for a kernel bound by the
+    host link the bytes L2 read from host memory) from the committed ncu
+    summary of ``kernel`` on ``workload``, or None when the summary is
+    missing or the kernel source changed since."""
     summary = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "hashed_gram_embedding_gb300", "csrc",
                        {"kv_proj": "kv_proj.cu", "kv_proj_gate": "kv_proj.cu",
@@ -202,13 +203,13 @@ def ncu_traffic(kernel, workload):
         return None
     fields = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("source_sha256", "dram_bytes_per_launch")):
+        if ":" in line and line.strip().startswith(("source_sha256", field)):
             k, _, v = line.strip().partition(":")
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("source_sha256") != source_hash(src):
         return None
     try:
-        return float(fields["dram_bytes_per_launch"])
+        return float(fields[field])
     except (KeyError, ValueError):
         return None
 
@@ -592,7 +593,9 @@ def measure_workload(torch, args, name, device, rank, world, headline):
     dominant = max(KERNELS, key=lambda k: kernels[k]["us"])
     dk = kernels[dominant]
     bound, amount = work[dominant]
-    traffic = None if args.vocab_start else ncu_traffic(dominant, w.name)
+    traffic = None if args.vocab_start else ncu_traffic(
+        dominant, w.name, "link_bytes_per_launch" if dk["bound"] == "link" else
+        "dram_bytes_per_launch")
     dpeak = {"tensor": tensor_peak(alone[dominant])[0],
              "link": link_gbs}.get(dk["bound"], peaks["hbm_gbs"])
     roofline = {"bound": dk["bound"], "kernel": dominant, "achieved": dk["achieved"],
@@ -600,7 +603,10 @@ def measure_workload(torch, args, name, device, rank, world, headline):
                 "peak_source": ("pinned host-to-device copy measured in this run"
                                 if dk["bound"] == "link" else
                                 f"{peak_kind} ({tensor_peak(alone[dominant])[1] if dk['bound'] == 'tensor' else 'HBM copy'})"),
-                "algorithmic_per_launch": amount, "traffic": traffic}
+                "algorithmic_per_launch": amount, "traffic": traffic,
+                "traffic_counters": ("syslts__t_sectors_aperture_sysmem_op_read x 32 B"
+                                     if dk["bound"] == "link" else
+                                     "dram__bytes_read + dram__bytes_write")}
     gk = "lookup" if not fuse_ids else "ngram_lookup"
     if w.table_loc == "host":
         gather_line = {"kernel": gk, "gbs": kernels[gk]["achieved"], "link_gbs": link_gbs,
