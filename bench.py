@@ -309,8 +309,9 @@ def config_summary(line):
            "mode": line["config"]["mode"], "num_tokens": line["config"]["num_tokens"],
            "table_loc": line["config"]["table_loc"], "table_dtype": line["config"]["table_dtype"],
            "e2e": line["e2e"]["value"], "gather": line["gather"],
-           "roofline": {k: line["roofline"][k] for k in ("kernel", "bound", "achieved", "unit",
-                                                         "frac")},
+           "roofline": {k: line["roofline"][k] for k in ("kernel", "bound", "achieved", "peak",
+                                                         "unit", "frac", "traffic",
+                                                         "traffic_counters")},
            "kernels": {k: {"us": v["us"], "achieved": v["achieved"], "unit": v["unit"],
                            "peak": v["peak"], "frac": v["frac"]}
                        for k, v in line["kernels"].items()}}
